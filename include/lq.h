@@ -1,0 +1,178 @@
+/*
+ * lq.h -- C ABI of liblq: per-tile randomized Hadamard transform (RHT) plus
+ * nearest-point lattice vector quantization of weight matrices, and the
+ * products y = W^ x computed straight from the lattice codes, on one
+ * sm_103a GPU.
+ *
+ * Method source: HyperQuant (github release page of moonmath-ai/HyperQuant),
+ * sections "Key algorithmic ingredients" (per-tile RHT, E8/D4/A2/Z1 lattice VQ),
+ * the mma="int8" paragraph (codes decoded into int8; RHT of the activation on
+ * every forward; no bf16 weight written), the mma="bf16" paragraph (decode
+ * straight into partial dot products) and "Hadamard block size" (tile rule).
+ * Nearest-point algorithms: Conway & Sloane, Sphere Packings, Lattices and
+ * Groups, ch. 20.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All matrices are row-major.  W is [rows x cols] (rows = out_features,
+ *   cols = in_features).  A tile is a run of `tile` consecutive columns of
+ *   one row; `cols % tile == 0`.
+ * - Pointers named *_dev are device pointers owned by the caller; the library
+ *   never allocates, frees or retains them.  Device pointers must be 16-byte
+ *   aligned.  `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *   default stream).  Every call only enqueues work on `stream` and returns.
+ * - Argument errors are returned synchronously, before anything is launched.
+ *   Data-dependent problems (non-finite input, a code outside int8, a wait
+ *   that gave up) are OR-ed as LQ_DEV_* bits into the caller's int32 status
+ *   word `dev_status_dev` (may be NULL to ignore them); read it after the
+ *   stream has synchronised.  No kernel traps or spins without a bound.
+ * - Lattice codes are int8 "doubled coordinates": code = 2 p for a lattice
+ *   point p (E8, D4, Z1), and (2x, 2y/sqrt(3)) for an A2 point (x, y).  Codes
+ *   are stored [rows x cols], the block of lattice dimension n of tile t at
+ *   columns t*tile + n*j ... n*j + n - 1.
+ * - Scales are float32 [rows x cols/tile]: s = beta * RMS(tile), the RMS of
+ *   the tile before or after the (orthonormal) rotation.
+ * - Signs are int8 +1/-1 [cols], one per column, shared by all rows; the
+ *   rotation of a tile is w~ = H D w / sqrt(tile) (H Sylvester Hadamard in
+ *   natural order, D = diag(signs)).
+ */
+#ifndef LQ_H
+#define LQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Synchronous status returned by every entry point. */
+typedef enum {
+    LQ_OK = 0,
+    LQ_ERR_ARG = 1,         /* null pointer, bad enum value, misaligned pointer */
+    LQ_ERR_SHAPE = 2,       /* sizes inconsistent or out of the supported range */
+    LQ_ERR_DTYPE = 3,       /* unsupported element type */
+    LQ_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, ...) */
+    LQ_ERR_UNSUPPORTED = 5  /* valid request that this build does not implement */
+} lq_status;
+
+/* Bits OR-ed into the device status word by the kernels. */
+enum {
+    LQ_DEV_NONFINITE = 1,   /* a tile held NaN or Inf: that tile's codes are unspecified */
+    LQ_DEV_RANGE = 2,       /* some |code| > 127 (or an fp16 activation overflowed) */
+    LQ_DEV_TIMEOUT = 4      /* a bounded wait on an mbarrier expired; outputs unspecified */
+};
+
+typedef enum { LQ_Z1 = 1, LQ_A2 = 2, LQ_D4 = 4, LQ_E8 = 8 } lq_lattice;
+typedef enum { LQ_F32 = 0, LQ_BF16 = 1 } lq_dtype;
+
+/* Human-readable name of a status code (static string). */
+const char* lq_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int lq_version(void);
+
+/*
+ * Tile-size rule (HyperQuant page, "Hadamard block size"): the largest tile in
+ * {256, 512, 1024, 2048} that is <= `requested` and divides `cols`; 0 when
+ * none does.  Pure host function.
+ */
+int lq_pick_tile(int64_t cols, int requested);
+
+/*
+ * Rademacher signs of the RHT (HyperQuant page, "Key algorithmic
+ * ingredients": randomized Hadamard).  signs_dev[k] = -1 when the top bit of
+ * output k of SplitMix64 started from state `seed` is set (output k mixes
+ * seed + (k+1) * 0x9E3779B97F4A7C15), else +1.  signs_dev: int8 [cols].
+ */
+lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_dev, void* stream);
+
+/*
+ * Quantize W (HyperQuant page, "Key algorithmic ingredients"; Conway & Sloane
+ * ch. 20).  For every tile of every row: sign flip by D, Hadamard, s = beta *
+ * RMS, y = w~ / s (s == 0 gives y = 0), nearest lattice point of every
+ * n-block of y (E8: the closer of the D8 and D8+1/2 decodes, D8 kept on equal
+ * distance; D_n: round, fix parity on the worst coordinate, lowest index on
+ * ties; ties of rounding go to even), codes = doubled coordinates.
+ *
+ *   lattice   LQ_E8 / LQ_D4 / LQ_A2 / LQ_Z1
+ *   W_dev     [rows x ldw] elements of type wdtype (LQ_BF16 or LQ_F32);
+ *             ldw >= cols and ldw * sizeof(elem) % 16 == 0
+ *   tile      128, 256 or 512 (cols % tile == 0)
+ *   seed      signs are generated from it into signs_dev (int8 [cols], written)
+ *   beta      > 0
+ *   codes_dev int8 [rows x cols] (written, row stride cols)
+ *   scales_dev float32 [rows x cols/tile] (written)
+ *   dev_status_dev  int32 status word or NULL (LQ_DEV_NONFINITE, LQ_DEV_RANGE)
+ * Limits: rows >= 0, 0 < cols <= 2^20, rows * cols < 2^40.
+ */
+lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
+                      int64_t ldw, int tile, uint64_t seed, float beta,
+                      int8_t* codes_dev, float* scales_dev, int8_t* signs_dev,
+                      int32_t* dev_status_dev, void* stream);
+
+/*
+ * Reconstruct W^ = D H (s * p) / sqrt(tile) per tile, the inverse of the
+ * rotation applied to the scaled lattice points (HyperQuant page, mma="int8"
+ * paragraph: the codes are decoded, never stored as a weight).
+ *   codes_dev int8 [rows x cols], scales_dev float32 [rows x cols/tile],
+ *   signs_dev int8 [cols]; What_dev [rows x cols] of type out_dtype (written).
+ */
+lq_status lq_dequantize(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                        const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                        void* What_dev, int out_dtype, void* stream);
+
+/*
+ * Workspace bytes lq_gemv needs for `batch` activation rows of length `cols`
+ * with tile `tile` (the rotated activation split into two fp16 halves plus one
+ * float per (row, tile)).
+ */
+size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile);
+
+/*
+ * Decode-side product y = W^ x from the codes (HyperQuant page, mma="bf16"
+ * paragraph: decoding straight into partial dot products; mma="int8"
+ * paragraph: the activation goes through the RHT on every forward):
+ *     y[b, r] = sum_t s[r, t] * sum_i p[r, t, i] * x~[b, t, i],
+ *     x~ = H D x / sqrt(tile) per tile.
+ *   x_dev     [batch x cols] of type xdtype (LQ_BF16 or LQ_F32), row stride cols
+ *   batch     1 .. 16
+ *   y_dev     float32 [batch x rows] (overwritten)
+ *   workspace_dev  lq_gemv_workspace_size(batch, cols, tile) bytes, 16-byte aligned
+ *   dev_status_dev  int32 status word or NULL (LQ_DEV_RANGE if a rotated
+ *             activation does not fit the fp16 split)
+ * Two kernels run on `stream`: the activation rotation, then the product.
+ */
+lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                  const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                  const void* x_dev, int xdtype, int batch, float* y_dev,
+                  void* workspace_dev, int32_t* dev_status_dev, void* stream);
+
+/*
+ * Workspace bytes lq_gemm needs: the rotated activations X~ as fp16 [M x K]
+ * plus one float per row.
+ */
+size_t lq_gemm_workspace_size(int64_t M, int64_t K);
+
+/*
+ * Prefill product Y[M x N] = X W^T from E8 codes of W [N x K] (HyperQuant
+ * page, mma="int8" paragraph: best for prefill / large batch, decoded weights
+ * never written to memory):
+ *     Y[m, n] = sum_t s[n, t] * (X~_t[m] . p[n, t]).
+ * X~ is rounded to fp16 (after a per-row power-of-two range scaling) and the
+ * decoded weights s * p are formed as fp16 on chip; tensor cores (tcgen05)
+ * accumulate in fp32.
+ *   X_dev     bf16 [M x K];  Y_dev float32 [M x N] (written)
+ *   tile      256;  N % 128 == 0;  K % 256 == 0;  M >= 1
+ *   workspace_dev  lq_gemm_workspace_size(M, K) bytes
+ *   dev_status_dev  int32 status word or NULL (LQ_DEV_TIMEOUT)
+ */
+lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                  const int8_t* signs_dev, int64_t N, int64_t K, int tile,
+                  const uint16_t* X_dev, int64_t M, float* Y_dev,
+                  void* workspace_dev, int32_t* dev_status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LQ_H */

@@ -1,0 +1,213 @@
+"""Thin Python binding of liblq (include/lq.h): argument marshalling only.
+
+Every step of quantization and of the code-based products runs in the CUDA
+kernels of ``liblq.so``; this module only turns torch tensors into pointers,
+sizes and the current CUDA stream, and raises :class:`LQError` on a non-OK
+status.  There is no fallback: if the library is missing, importing the
+binding's entry points raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liblq.so")
+
+LQ_OK, LQ_ERR_ARG, LQ_ERR_SHAPE, LQ_ERR_DTYPE, LQ_ERR_CUDA, LQ_ERR_UNSUPPORTED = range(6)
+LQ_DEV_NONFINITE, LQ_DEV_RANGE, LQ_DEV_TIMEOUT = 1, 2, 4
+LQ_Z1, LQ_A2, LQ_D4, LQ_E8 = 1, 2, 4, 8
+LQ_F32, LQ_BF16 = 0, 1
+LATTICE_IDS = {"z1": LQ_Z1, "a2": LQ_A2, "d4": LQ_D4, "e8": LQ_E8}
+LATTICE_DIM = {"z1": 1, "a2": 2, "d4": 4, "e8": 8}
+
+# (name, restype, argtypes) of every entry point declared in include/lq.h
+_P, _I64, _U64, _I32, _F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "lq_status_string": (ctypes.c_char_p, [_I32]),
+    "lq_version": (_I32, []),
+    "lq_pick_tile": (_I32, [_I64, _I32]),
+    "lq_make_signs": (_I32, [_U64, _I64, _P, _P]),
+    "lq_quantize": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _F32, _P, _P, _P, _P, _P]),
+    "lq_dequantize": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _P]),
+    "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
+    "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
+    "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+    "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
+}
+
+
+class LQError(RuntimeError):
+    """A liblq entry point returned a status other than LQ_OK."""
+
+    def __init__(self, name: str, status: int):
+        super().__init__(f"{name} failed: status {status} ({status_string(status)})")
+        self.status = status
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"liblq.so is not built ({LIB_PATH}); run `python -m lattice_vq_weight_gb300.build` "
+            "or __graft_entry__.build()")
+    dll = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(dll, name)
+        fn.restype = res
+        fn.argtypes = args
+    return dll
+
+
+_LIB = None
+
+
+def _get_lib():
+    global _LIB
+    if _LIB is None:
+        _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _get_lib()
+    raise AttributeError(name)
+
+
+def status_string(status: int) -> str:
+    return _get_lib().lq_status_string(int(status)).decode()
+
+
+def _check(name: str, status: int) -> None:
+    if status != LQ_OK:
+        raise LQError(name, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is not None:
+        return ctypes.c_void_p(int(stream))
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _lattice_id(lattice) -> int:
+    return LATTICE_IDS[lattice] if isinstance(lattice, str) else int(lattice)
+
+
+def _dtype_id(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return LQ_BF16
+    if t.dtype == torch.float32:
+        return LQ_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+# ------------------------------------------------------------------ C-ABI calls
+def lq_version() -> int:
+    return _get_lib().lq_version()
+
+
+def lq_pick_tile(cols: int, requested: int) -> int:
+    return _get_lib().lq_pick_tile(int(cols), int(requested))
+
+
+def lq_make_signs(seed: int, signs, stream=None) -> None:
+    _check("lq_make_signs", _get_lib().lq_make_signs(int(seed), signs.numel(), _ptr(signs), _stream(stream)))
+
+
+def lq_quantize(lattice, W, tile: int, seed: int, beta: float, codes, scales, signs,
+                dev_status=None, stream=None) -> None:
+    """W [rows x cols] (row stride W.stride(0)) -> codes, scales, signs (all preallocated)."""
+    rows, cols = W.shape
+    assert W.stride(1) == 1
+    _check("lq_quantize", _get_lib().lq_quantize(
+        _lattice_id(lattice), _ptr(W), _dtype_id(W), rows, cols, W.stride(0), int(tile), int(seed),
+        float(beta), _ptr(codes), _ptr(scales), _ptr(signs), _ptr(dev_status), _stream(stream)))
+
+
+def lq_dequantize(lattice, codes, scales, signs, tile: int, W_hat, stream=None) -> None:
+    rows, cols = codes.shape
+    _check("lq_dequantize", _get_lib().lq_dequantize(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), rows, cols, int(tile),
+        _ptr(W_hat), _dtype_id(W_hat), _stream(stream)))
+
+
+def lq_gemv_workspace_size(batch: int, cols: int, tile: int) -> int:
+    return int(_get_lib().lq_gemv_workspace_size(int(batch), int(cols), int(tile)))
+
+
+def lq_gemv(lattice, codes, scales, signs, tile: int, x, y, workspace, dev_status=None,
+            stream=None) -> None:
+    """y[b, r] = sum_t s[r,t] p[r,t,:] . x~[b,t,:]; x [batch x cols], y float32 [batch x rows]."""
+    rows, cols = codes.shape
+    batch = x.shape[0]
+    _check("lq_gemv", _get_lib().lq_gemv(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), rows, cols, int(tile),
+        _ptr(x), _dtype_id(x), batch, _ptr(y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def lq_gemm_workspace_size(M: int, K: int) -> int:
+    return int(_get_lib().lq_gemm_workspace_size(int(M), int(K)))
+
+
+def lq_gemm(lattice, codes, scales, signs, tile: int, X, Y, workspace, dev_status=None,
+            stream=None) -> None:
+    """Y [M x N] float32 = X~ . (s p)^T from E8 codes [N x K]; X bf16 [M x K]."""
+    N, K = codes.shape
+    M = X.shape[0]
+    _check("lq_gemm", _get_lib().lq_gemm(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), N, K, int(tile), _ptr(X), M,
+        _ptr(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+# ------------------------------------------------------------------ allocating helpers
+def quantize(W, lattice: str = "e8", tile: int = 256, seed: int = 0, beta: float = 0.25,
+             dev_status=None, stream=None):
+    """Allocate outputs with torch on W's device and call :func:`lq_quantize`.
+
+    Returns (codes int8 [rows x cols], scales float32 [rows x cols/tile], signs int8 [cols]).
+    """
+    import torch
+    rows, cols = W.shape
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=W.device)
+    scales = torch.empty((rows, cols // tile), dtype=torch.float32, device=W.device)
+    signs = torch.empty((cols,), dtype=torch.int8, device=W.device)
+    lq_quantize(lattice, W, tile, seed, beta, codes, scales, signs, dev_status, stream)
+    return codes, scales, signs
+
+
+def dequantize(codes, scales, signs, lattice: str = "e8", tile: int = 256, dtype=None, stream=None):
+    import torch
+    dtype = torch.float32 if dtype is None else dtype
+    out = torch.empty(codes.shape, dtype=dtype, device=codes.device)
+    lq_dequantize(lattice, codes, scales, signs, tile, out, stream)
+    return out
+
+
+def gemv(codes, scales, signs, x, lattice: str = "e8", tile: int = 256, workspace=None,
+         dev_status=None, stream=None):
+    import torch
+    rows, cols = codes.shape
+    y = torch.empty((x.shape[0], rows), dtype=torch.float32, device=codes.device)
+    if workspace is None:
+        workspace = torch.empty(lq_gemv_workspace_size(x.shape[0], cols, tile), dtype=torch.uint8,
+                                device=codes.device)
+    lq_gemv(lattice, codes, scales, signs, tile, x, y, workspace, dev_status, stream)
+    return y
+
+
+def gemm(codes, scales, signs, X, lattice: str = "e8", tile: int = 256, workspace=None,
+         dev_status=None, stream=None):
+    import torch
+    N, K = codes.shape
+    M = X.shape[0]
+    Y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
+    if workspace is None:
+        workspace = torch.empty(lq_gemm_workspace_size(M, K), dtype=torch.uint8, device=codes.device)
+    lq_gemm(lattice, codes, scales, signs, tile, X, Y, workspace, dev_status, stream)
+    return Y

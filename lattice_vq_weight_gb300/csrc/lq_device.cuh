@@ -1,0 +1,333 @@
+// Device building blocks shared by the liblq kernels: packed fp32 pair
+// arithmetic, the per-lane/ cross-lane fast Walsh-Hadamard transform, and the
+// nearest-point decoders of the E8, D4, A2 and Z1 lattices.
+//
+// Data layout used by every kernel that rotates a 2048-column chunk of a row:
+// lane l of a warp owns the 64 consecutive columns [64 l, 64 l + 64) of the
+// chunk, held as float2 p[32] (p[j] = columns 2j, 2j+1).  A tile of T columns
+// is spread over T/64 consecutive lanes, so the Hadamard index bits 0..5 live
+// in registers and bits 6.. in the lane index.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "lq.h"
+
+namespace lq {
+
+constexpr int kWarp = 32;
+constexpr int kLaneElems = 64;                  // columns owned by one lane
+constexpr int kChunkCols = kWarp * kLaneElems;  // 2048 columns per warp unit
+
+// x + 1.5 * 2^23 rounds x (|x| < 2^22) to the nearest integer, ties to even,
+// and leaves that integer in the low mantissa bits: bits = 0x4B400000 + rint(x).
+constexpr float kRoundMagic = 12582912.0f;
+constexpr uint32_t kRoundMagicBits = 0x4B400000u;
+
+// ---------------------------------------------------------------- f32x2 ops
+// sm_100+ packed fp32 pair arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ unsigned long long as_u64(float2 a) {
+  return *reinterpret_cast<unsigned long long*>(&a);
+}
+__device__ __forceinline__ float2 as_f2(unsigned long long a) {
+  return *reinterpret_cast<float2*>(&a);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(r);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)));
+  return as_f2(r);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(as_u64(a)), "l"(as_u64(b)), "l"(as_u64(c)));
+  return as_f2(r);
+}
+
+// ---------------------------------------------------------------- status word
+__device__ __forceinline__ void raise_flag(int32_t* status, int32_t bit) {
+  if (status != nullptr) atomicOr(status, bit);
+}
+
+// ---------------------------------------------------------------- FWHT
+// Unnormalised Walsh-Hadamard transform (Sylvester order, entry
+// (-1)^popcount(i & j)) of the 64 register-resident columns: 6 butterfly
+// stages, the first inside each float2, the rest between float2 pairs.
+__device__ __forceinline__ void fwht64_local(float2 (&p)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float a = p[j].x, b = p[j].y;
+    p[j] = make_float2(a + b, a - b);
+  }
+#pragma unroll
+  for (int hp = 1; hp < 32; hp <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if ((j & hp) == 0) {
+        const float2 a = p[j], b = p[j + hp];
+        p[j] = add2(a, b);
+        p[j + hp] = sub2(a, b);
+      }
+    }
+  }
+}
+
+// Remaining butterfly stages across the lanes of one tile: the partner of lane
+// l in the stage for index bit 6 + log2(m) is lane l ^ m.  The lane whose bit
+// is clear keeps a + b, the other keeps a - b (a = lower index).
+__device__ __forceinline__ void fwht_cross_lanes(float2 (&p)[32], int lanes_per_tile, int lane) {
+  for (int m = 1; m < lanes_per_tile; m <<= 1) {
+    const float sg = (lane & m) ? -1.0f : 1.0f;
+    const float2 sg2 = make_float2(sg, sg);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float2 q;
+      q.x = __shfl_xor_sync(0xffffffffu, p[j].x, m);
+      q.y = __shfl_xor_sync(0xffffffffu, p[j].y, m);
+      p[j] = fma2(p[j], sg2, q);
+    }
+  }
+}
+
+// Sum over the lanes of one tile (lanes_per_tile is a power of two <= 32).
+__device__ __forceinline__ float tile_lane_sum(float v, int lanes_per_tile) {
+  for (int m = 1; m < lanes_per_tile; m <<= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+  return v;
+}
+__device__ __forceinline__ float tile_lane_max(float v, int lanes_per_tile) {
+  for (int m = 1; m < lanes_per_tile; m <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+  return v;
+}
+
+// ---------------------------------------------------------------- code packing
+// Low bytes of four ints into one word (byte i = low byte of ci).
+__device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {
+  return __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
+}
+
+// Add `step` (+-2) to byte k (0..7) of the code pair (w0: bytes 0-3, w1: 4-7)
+// when `fix` is set.  Bytes are moved to offset binary first so that the add
+// cannot carry into a neighbour unless the code itself leaves int8, which the
+// range check reports.
+__device__ __forceinline__ void add_to_byte(uint32_t& w0, uint32_t& w1, bool fix, int k, int step) {
+  const uint32_t delta = fix ? (uint32_t)(step * (1 << (8 * (k & 3)))) : 0u;
+  const uint32_t d0 = (k < 4) ? delta : 0u;
+  const uint32_t d1 = (k < 4) ? 0u : delta;
+  w0 = ((w0 ^ 0x80808080u) + d0) ^ 0x80808080u;
+  w1 = ((w1 ^ 0x80808080u) + d1) ^ 0x80808080u;
+}
+
+// ---------------------------------------------------------------- decoders
+// Each decoder takes the scaled coordinates y of one lattice block and writes
+// the int8 codes (doubled coordinates).  Rounding is x + kRoundMagic, which is
+// round-half-even; for f = rint(y), e = y - f is exact and bits(t) - 0x4B400000
+// is f as an integer.
+//
+// Worst-coordinate search packs (|e|, index, sign) into one integer key:
+// rotl(bits(e), 1) moves the sign to bit 0 and keeps |e| monotone in bits
+// 4..31 (|e| <= 1/2, so the top bit is clear); bits 1..3 hold the index,
+// ordered so that ties of |e| (to 2^-20 relative) go to the lowest index.
+//
+// Range: a code is 2 rint(y) plus at most 3 in magnitude, so a block whose
+// coordinates all satisfy |y| < 62.5 cannot leave int8.  Blocks above that
+// recompute their codes as 32-bit integers and report |code| > 127.
+
+struct BlockCodes8 { uint32_t w0, w1; };
+
+__device__ __forceinline__ int rint_int(uint32_t tbits) { return (int)(tbits - kRoundMagicBits); }
+
+// E8 = D8 u (D8 + 1/2).  Coset D8: f = rint(y), parity of sum(f), fix the
+// coordinate with the largest |e| when odd.  Coset D8 + 1/2 shares the
+// rounding: rint(y - 1/2) + 1/2 = f + copysign(1/2, e), residual
+// e' = e - copysign(1/2, e), |e'| = 1/2 - |e|, and its parity differs from
+// sum(f) by the number of negative e.  So
+//   dA = sum e^2              (+ 1 - 2 max|e| when sum f is odd)
+//   dB = sum e^2 + 2 - sum|e| (+ 2 min|e|     when sum f + #neg is odd)
+// and the D8 candidate is kept when dA <= dB.
+__device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& range) {
+  const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
+  float2 t[4], e[4];
+  float2 sq = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    t[j] = add2(y[j], M2);
+    e[j] = sub2(y[j], sub2(t[j], M2));
+    sq = fma2(e[j], e[j], sq);
+  }
+  const float dA0 = sq.x + sq.y;
+  uint32_t px = 0, sx = 0, keyA = 0, keyB = 0xFFFFFFFFu;
+  float sabs = 0.f, bmax = 0.f;
+  uint32_t tb[8], eb[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float ei = (i & 1) ? e[i >> 1].y : e[i >> 1].x;
+    const float yi = (i & 1) ? y[i >> 1].y : y[i >> 1].x;
+    tb[i] = __float_as_uint((i & 1) ? t[i >> 1].y : t[i >> 1].x);
+    eb[i] = __float_as_uint(ei);
+    px ^= tb[i];
+    sx ^= eb[i];
+    sabs += fabsf(ei);
+    bmax = fmaxf(bmax, fabsf(yi));
+    const uint32_t rot = __funnelshift_l(eb[i], eb[i], 1);
+    keyA = max(keyA, (rot & 0xFFFFFFF1u) | (uint32_t)((7 - i) << 1));
+    keyB = min(keyB, (rot & 0xFFFFFFF1u) | (uint32_t)(i << 1));
+  }
+  const bool oddA = (px & 1u) != 0;
+  const bool oddB = ((px ^ (sx >> 31)) & 1u) != 0;
+  const float maxe = __uint_as_float((keyA >> 1) & 0x7FFFFFF8u);
+  const float mine = __uint_as_float((keyB >> 1) & 0x7FFFFFF8u);
+  const float dA = oddA ? dA0 + fmaf(-2.f, maxe, 1.f) : dA0;
+  const float dB = (dA0 + 2.f - sabs) + (oddB ? 2.f * mine : 0.f);
+  const bool takeB = dB < dA;
+  // codes: 2 f (low byte of 2 * bits(t)), plus +-1 toward y for the half coset
+  const uint32_t bmask = takeB ? 0xFFFFFFFFu : 0u;
+  uint32_t c[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t adj = ((uint32_t)((int32_t)eb[i] >> 31) | 1u) & bmask;
+    c[i] = tb[i] + tb[i] + adj;
+  }
+  BlockCodes8 r;
+  r.w0 = pack4(c[0], c[1], c[2], c[3]);
+  r.w1 = pack4(c[4], c[5], c[6], c[7]);
+  // parity fix of the chosen coset
+  const uint32_t key = takeB ? keyB : keyA;
+  const int k = takeB ? (int)((keyB >> 1) & 7u) : 7 - (int)((keyA >> 1) & 7u);
+  const bool neg = (key & 1u) != 0;
+  // D8: rounding the other way moves toward y, +1 when e >= 0.
+  // D8 + 1/2: e' = e - copysign(1/2, e) has the opposite sign of e.
+  const int step = takeB ? (neg ? 2 : -2) : (neg ? -2 : 2);
+  const bool fix = takeB ? oddB : oddA;
+  add_to_byte(r.w0, r.w1, fix, k, step);
+  if (!(bmax < 62.5f)) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int adj = takeB ? (((int32_t)eb[i] >> 31) | 1) : 0;
+      const int ci = 2 * rint_int(tb[i]) + adj + ((fix && i == k) ? step : 0);
+      range |= (ci > 127) || (ci < -127);
+    }
+  }
+  return r;
+}
+
+// D4 = {x in Z^4 : sum even}: round, fix the worst coordinate when odd.
+__device__ __forceinline__ uint32_t decode_d4(const float2 (&y)[2], bool& range) {
+  const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
+  uint32_t tb[4], px = 0, keyA = 0;
+  float bmax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float2 t = add2(y[j], M2);
+    const float2 e = sub2(y[j], sub2(t, M2));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 2 * j + h;
+      tb[i] = __float_as_uint(h ? t.y : t.x);
+      const uint32_t eb = __float_as_uint(h ? e.y : e.x);
+      px ^= tb[i];
+      bmax = fmaxf(bmax, fabsf(h ? y[j].y : y[j].x));
+      const uint32_t rot = __funnelshift_l(eb, eb, 1);
+      keyA = max(keyA, (rot & 0xFFFFFFF1u) | (uint32_t)((7 - i) << 1));
+    }
+  }
+  uint32_t w = pack4(tb[0] + tb[0], tb[1] + tb[1], tb[2] + tb[2], tb[3] + tb[3]);
+  uint32_t unused = 0;
+  const int k = 7 - (int)((keyA >> 1) & 7u);
+  const int step = (keyA & 1u) ? -2 : 2;
+  const bool fix = (px & 1u) != 0;
+  add_to_byte(w, unused, fix, k, step);
+  if (!(bmax < 62.5f)) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int ci = 2 * rint_int(tb[i]) + ((fix && i == k) ? step : 0);
+      range |= (ci > 127) || (ci < -127);
+    }
+  }
+  return w;
+}
+
+// A2 = R u (R + (1/2, sqrt3/2)), R = Z x sqrt3 Z.  In the coordinates
+// (y0, z = y1/sqrt3) both cosets are integer grids: squared distance
+// e0^2 + 3 ez^2 for R, (1/2-|e0|)^2 + 3 (1/2-|ez|)^2 for the shifted coset
+// (R kept on equal distance).  Codes (2x, 2y/sqrt3) = (2 f0, 2 fz) or
+// (2 f0 +- 1, 2 fz +- 1), the +-1 toward the coordinate.  Returns 2 bytes.
+__device__ __forceinline__ uint32_t decode_a2_pair(float2 y, bool& range) {
+  const float z = y.y * 0.57735026918962576f;  // 1/sqrt(3)
+  const float2 v = make_float2(y.x, z);
+  const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
+  const float2 t = add2(v, M2);
+  const float2 e = sub2(v, sub2(t, M2));
+  const float a0 = fabsf(e.x), a1 = fabsf(e.y);
+  const float dA = fmaf(3.f * e.y, e.y, e.x * e.x);
+  const float b0 = 0.5f - a0, b1 = 0.5f - a1;
+  const float dB = fmaf(3.f * b1, b1, b0 * b0);
+  const bool takeB = dB < dA;
+  const uint32_t bmask = takeB ? 0xFFFFFFFFu : 0u;
+  const uint32_t t0 = __float_as_uint(t.x), t1 = __float_as_uint(t.y);
+  const uint32_t s0 = ((uint32_t)((int32_t)__float_as_uint(e.x) >> 31) | 1u) & bmask;
+  const uint32_t s1 = ((uint32_t)((int32_t)__float_as_uint(e.y) >> 31) | 1u) & bmask;
+  const uint32_t c0 = t0 + t0 + s0;
+  const uint32_t c1 = t1 + t1 + s1;
+  if (!(fmaxf(fabsf(y.x), fabsf(z)) < 62.5f)) {
+    const int i0 = 2 * rint_int(t0) + (int)s0, i1 = 2 * rint_int(t1) + (int)s1;
+    range |= (i0 > 127) || (i0 < -127) || (i1 > 127) || (i1 < -127);
+  }
+  return (c0 & 0xFFu) | ((c1 & 0xFFu) << 8);
+}
+
+// Z: c = 2 rint(y) for four coordinates.
+__device__ __forceinline__ uint32_t decode_z1_quad(float2 a, float2 b, bool& range) {
+  const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
+  const float2 t0 = add2(a, M2), t1 = add2(b, M2);
+  const uint32_t u0 = __float_as_uint(t0.x), u1 = __float_as_uint(t0.y);
+  const uint32_t u2 = __float_as_uint(t1.x), u3 = __float_as_uint(t1.y);
+  const float m = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+  if (!(m < 62.5f)) {
+    const int mx = max(max(abs(rint_int(u0)), abs(rint_int(u1))), max(abs(rint_int(u2)), abs(rint_int(u3))));
+    range |= (2 * mx > 127);
+  }
+  return pack4(u0 + u0, u1 + u1, u2 + u2, u3 + u3);
+}
+
+// Decode the 64 register-resident coordinates of one lane into 16 code words
+// (word w = columns 4w .. 4w+3).
+template <int LAT>
+__device__ __forceinline__ void decode_lane(const float2 (&p)[32], uint32_t (&w)[16], bool& range) {
+  if constexpr (LAT == LQ_E8) {
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const float2 y[4] = {p[4 * b], p[4 * b + 1], p[4 * b + 2], p[4 * b + 3]};
+      const BlockCodes8 r = decode_e8(y, range);
+      w[2 * b] = r.w0;
+      w[2 * b + 1] = r.w1;
+    }
+  } else if constexpr (LAT == LQ_D4) {
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const float2 y[2] = {p[2 * b], p[2 * b + 1]};
+      w[b] = decode_d4(y, range);
+    }
+  } else if constexpr (LAT == LQ_A2) {
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const uint32_t lo = decode_a2_pair(p[2 * b], range);
+      const uint32_t hi = decode_a2_pair(p[2 * b + 1], range);
+      w[b] = lo | (hi << 16);
+    }
+  } else {
+#pragma unroll
+    for (int b = 0; b < 16; ++b) w[b] = decode_z1_quad(p[2 * b], p[2 * b + 1], range);
+  }
+}
+
+}  // namespace lq

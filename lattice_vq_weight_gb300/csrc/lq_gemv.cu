@@ -1,0 +1,426 @@
+// Decode-side GEMV: y = W^ x computed from the lattice codes.
+//
+// HyperQuant page, mma="bf16" paragraph: the product decodes the stored weight
+// straight into partial dot products (no decoded weight in memory); mma="int8"
+// paragraph: the activation goes through the RHT on every forward.
+//
+//   y[b, r] = sum_t s[r, t] * sum_i p[r, t, i] * x~[b, t, i],  x~ = H D x / sqrt(T).
+//
+// Two kernels:
+//  1. rotate_activation_kernel: x~ per tile, times 1/2 (codes are 2p) and, for
+//     A2, sqrt(3) on odd coordinates (the second A2 code is 2y/sqrt3); each
+//     (row, tile) is scaled by a power of two into [2^14, 2^15) and split into
+//     two fp16 halves hi + lo (22 significant bits).  It also zeroes y.
+//  2. gemv_kernel: warps stream 16-row groups of int8 codes with 16-byte loads,
+//     turn them into exact fp16 values (magic-number conversion: the fp16 with
+//     bits 0x6400 | u is 1024 + u), and run m16n8k16 fp16 MMAs with fp32
+//     accumulation against hi and lo.  One accumulator per tile is scaled by
+//     s[r, t] * 2^-e[b, t] and summed; warps that split a row's tiles combine
+//     with fp32 atomics.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "lq_device.cuh"
+#include "lq_host.h"
+
+namespace lq {
+
+struct RotateArgs {
+  const void* x;
+  const int8_t* signs;
+  int64_t cols;
+  int batch, tile, lanes_per_tile, tiles_per_row, chunks_per_row;
+  float post_scale;    // 1 / (2 sqrt(T))
+  int a2;              // multiply odd coordinates by sqrt(3)
+  __half* xh;
+  __half* xl;
+  float* xs;           // [batch x tiles] = 2^-e
+  float* y;
+  int64_t y_elems;
+  int32_t* status;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256, 1) rotate_activation_kernel(RotateArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = gtid; i < a.y_elems; i += nthreads) a.y[i] = 0.f;
+
+  const int64_t warp0 = gtid >> 5, nwarps = nthreads >> 5;
+  const int64_t units = (int64_t)a.batch * a.chunks_per_row;
+  bool bad = false;
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int64_t b = u / a.chunks_per_row;
+    const int chunk = (int)(u % a.chunks_per_row);
+    const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
+    const bool active = col0 < a.cols;
+    float2 p[32];
+    if (active) {
+      uint4 sw[4];
+      const uint4* ss = reinterpret_cast<const uint4*>(a.signs + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sw[q] = __ldg(ss + q);
+      if constexpr (BF16) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = __ldg(src + i);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+          }
+        }
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 v = __ldg(src + i);
+          p[2 * i] = make_float2(v.x, v.y);
+          p[2 * i + 1] = make_float2(v.z, v.w);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w[4] = {sw[q].x, sw[q].y, sw[q].z, sw[q].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = 16 * q + 4 * h + c;
+            const uint32_t sb = ((w[h] >> (8 * c + 7)) & 1u) << 31;
+            float& v = (col & 1) ? p[col >> 1].y : p[col >> 1].x;
+            v = __uint_as_float(__float_as_uint(v) ^ sb);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) p[j] = make_float2(0.f, 0.f);
+    }
+    fwht64_local(p);
+    fwht_cross_lanes(p, a.lanes_per_tile, lane);
+    const float sc = a.post_scale;
+    const float2 sc2 = make_float2(sc, a.a2 ? sc * 1.7320508075688772f : sc);
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      p[j] = mul2(p[j], sc2);
+      m = fmaxf(m, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
+    }
+    m = tile_lane_max(m, a.lanes_per_tile);
+    float f = 1.f;
+    if (!isfinite(m)) {
+      bad = active;
+    } else if (m > 0.f) {
+      const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;  // m in [2^(E-1), 2^E)
+      const int ex = max(-126, min(127, 15 - E));
+      f = __uint_as_float((uint32_t)(ex + 127) << 23);
+    }
+    if (!active) continue;
+    const float2 f2 = make_float2(f, f);
+    uint32_t hw[32], lw[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 v = mul2(p[j], f2);
+      const __half2 h = __floats2half2_rn(v.x, v.y);
+      const float2 hf = __half22float2(h);
+      const __half2 l = __floats2half2_rn(v.x - hf.x, v.y - hf.y);
+      hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+      lw[j] = *reinterpret_cast<const uint32_t*>(&l);
+    }
+    uint4* dh = reinterpret_cast<uint4*>(a.xh + b * a.cols + col0);
+    uint4* dl = reinterpret_cast<uint4*>(a.xl + b * a.cols + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      dh[q] = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
+      dl[q] = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
+    }
+    if ((lane & (a.lanes_per_tile - 1)) == 0) a.xs[b * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
+}
+
+struct GemvArgs {
+  const int8_t* codes;
+  const float* scales;
+  int64_t rows, cols;
+  int tile, tiles_per_row, batch;
+  const __half* xh;
+  const __half* xl;
+  const float* xs;
+  float* y;
+  int splits, tiles_per_split;
+  int64_t tasks;
+};
+
+// int8 codes (4 per word) -> two f16x2 words holding the exact values.
+__device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;  // c + 128 as unsigned bytes
+  const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);
+  const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
+  const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+  const __half2 lv = __hsub2(*reinterpret_cast<const __half2*>(&l), off);
+  const __half2 hv = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
+  lo = *reinterpret_cast<const uint32_t*>(&lv);
+  hi = *reinterpret_cast<const uint32_t*>(&hv);
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One warp: RG groups of 16 rows x the tiles [t0, t1) of one split.
+// Fragment mapping (g = lane/4, q4 = lane%4): within a 64-column step the
+// thread loads 16 code bytes of rows g and g+8 at columns 16 q4 .. 16 q4 + 15;
+// MMA k-chunk c uses bytes 4c .. 4c+3, i.e. k-slots (2 q4, 2 q4+1, 2 q4+8,
+// 2 q4+9) hold columns 16 q4 + 4c + (0, 1, 2, 3).  The activation fragment of
+// column n = g uses the same permutation, so the dot products are unchanged.
+template <int NB, int RG>
+__global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, q4 = lane & 3;
+  const int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (task >= a.tasks) return;
+  const int64_t rgrp = task / a.splits;
+  const int ks = (int)(task % a.splits);
+  const int t0 = ks * a.tiles_per_split;
+  const int t1 = min(a.tiles_per_row, t0 + a.tiles_per_split);
+  if (t0 >= t1) return;
+  const int64_t row0 = rgrp * 16 * RG;
+  const int steps = a.tile >> 6;
+
+  float yacc[RG][NB][4];
+#pragma unroll
+  for (int i = 0; i < RG; ++i)
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) yacc[i][n][c] = 0.f;
+
+  const int8_t* rowp[RG][2];
+  bool rowok[RG][2];
+#pragma unroll
+  for (int i = 0; i < RG; ++i)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int64_t r = row0 + 16 * i + 8 * h + g;
+      rowok[i][h] = r < a.rows;
+      rowp[i][h] = a.codes + (rowok[i][h] ? r : 0) * a.cols + 16 * q4;
+    }
+  const __half* xhp[NB];
+  const __half* xlp[NB];
+  bool xok[NB];
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int bb = n * 8 + g;
+    xok[n] = bb < a.batch;
+    xhp[n] = a.xh + (int64_t)(xok[n] ? bb : 0) * a.cols + 16 * q4;
+    xlp[n] = a.xl + (int64_t)(xok[n] ? bb : 0) * a.cols + 16 * q4;
+  }
+
+  for (int t = t0; t < t1; ++t) {
+    float acc[RG][NB][4];
+#pragma unroll
+    for (int i = 0; i < RG; ++i)
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+
+    for (int st = 0; st < steps; ++st) {
+      const int64_t k0 = (int64_t)t * a.tile + st * 64;
+      uint4 cw[RG][2];
+#pragma unroll
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          cw[i][h] = rowok[i][h] ? __ldg(reinterpret_cast<const uint4*>(rowp[i][h] + k0)) : make_uint4(0, 0, 0, 0);
+      uint4 xhv[NB][2], xlv[NB][2];
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        if (xok[n]) {
+          const uint4* ph = reinterpret_cast<const uint4*>(xhp[n] + k0);
+          const uint4* pl = reinterpret_cast<const uint4*>(xlp[n] + k0);
+          xhv[n][0] = __ldg(ph); xhv[n][1] = __ldg(ph + 1);
+          xlv[n][0] = __ldg(pl); xlv[n][1] = __ldg(pl + 1);
+        } else {
+          xhv[n][0] = xhv[n][1] = xlv[n][0] = xlv[n][1] = make_uint4(0, 0, 0, 0);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t bh[NB][2], bl[NB][2];
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          const uint4& H = xhv[n][c >> 1];
+          const uint4& L = xlv[n][c >> 1];
+          bh[n][0] = (c & 1) ? H.z : H.x;
+          bh[n][1] = (c & 1) ? H.w : H.y;
+          bl[n][0] = (c & 1) ? L.z : L.x;
+          bl[n][1] = (c & 1) ? L.w : L.y;
+        }
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+          const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
+          const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
+          uint32_t a0, a2, a1, a3;
+          codes_to_f16x2(wa, a0, a2);
+          codes_to_f16x2(wb, a1, a3);
+#pragma unroll
+          for (int n = 0; n < NB; ++n) {
+            mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
+            mma16816(acc[i][n], a0, a1, a2, a3, bl[n][0], bl[n][1]);
+          }
+        }
+      }
+    }
+    // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
+    float fx[NB][2];
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int bb = n * 8 + 2 * q4 + h;
+        fx[n][h] = (bb < a.batch) ? __ldg(a.xs + (int64_t)bb * a.tiles_per_row + t) : 0.f;
+      }
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+      float sr[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t r = row0 + 16 * i + 8 * h + g;
+        sr[h] = rowok[i][h] ? __ldg(a.scales + r * a.tiles_per_row + t) : 0.f;
+      }
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        yacc[i][n][0] = fmaf(acc[i][n][0], sr[0] * fx[n][0], yacc[i][n][0]);
+        yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
+        yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
+        yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
+      }
+    }
+  }
+  const bool single = (a.splits == 1);
+#pragma unroll
+  for (int i = 0; i < RG; ++i)
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int h = c >> 1;
+        const int64_t r = row0 + 16 * i + 8 * h + g;
+        const int bb = n * 8 + 2 * q4 + (c & 1);
+        if (r < a.rows && bb < a.batch) {
+          float* dst = a.y + (int64_t)bb * a.rows + r;
+          if (single) *dst = yacc[i][n][c]; else atomicAdd(dst, yacc[i][n][c]);
+        }
+      }
+}
+
+}  // namespace lq
+
+using namespace lq;
+
+namespace {
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct GemvWorkspace {
+  size_t xh, xl, xs, total;
+};
+
+GemvWorkspace gemv_workspace_layout(int batch, int64_t cols, int tile) {
+  GemvWorkspace w;
+  const size_t half_bytes = align256((size_t)batch * (size_t)cols * 2);
+  w.xh = 0;
+  w.xl = half_bytes;
+  w.xs = 2 * half_bytes;
+  w.total = w.xs + align256((size_t)batch * (size_t)(cols / tile) * 4);
+  return w;
+}
+
+template <int NB, int RG>
+lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
+  GemvArgs a = a0;
+  static int per_sm = 0;
+  if (per_sm == 0) per_sm = occupancy_per_sm(gemv_kernel<NB, RG>, 256);
+  const int sms = device_sm_count();
+  if (sms <= 0) return LQ_ERR_CUDA;
+  const int64_t groups = (a.rows + 16 * RG - 1) / (16 * RG);
+  const int64_t target = (int64_t)sms * per_sm * 8;  // one warp per task, one wave
+  int64_t splits = (target + groups - 1) / groups;
+  if (splits > a.tiles_per_row) splits = a.tiles_per_row;
+  if (splits < 1) splits = 1;
+  a.tiles_per_split = (int)((a.tiles_per_row + splits - 1) / splits);
+  a.splits = (int)((a.tiles_per_row + a.tiles_per_split - 1) / a.tiles_per_split);
+  a.tasks = groups * a.splits;
+  const int64_t grid = (a.tasks + 7) / 8;
+  gemv_kernel<NB, RG><<<(unsigned)grid, 256, 0, st>>>(a);
+  return check_launch();
+}
+
+}  // namespace
+
+extern "C" size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile) {
+  if (batch <= 0 || cols <= 0 || tile <= 0) return 0;
+  return gemv_workspace_layout(batch, cols, tile).total;
+}
+
+extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                             const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                             const void* x_dev, int xdtype, int batch, float* y_dev,
+                             void* workspace_dev, int32_t* dev_status_dev, void* stream) {
+  lq_status st = validate_common(lattice, rows, cols, tile);
+  if (st != LQ_OK) return st;
+  if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
+  if (batch < 1 || batch > 16) return LQ_ERR_SHAPE;
+  if (rows == 0) return LQ_OK;
+  if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || x_dev == nullptr ||
+      y_dev == nullptr || workspace_dev == nullptr)
+    return LQ_ERR_ARG;
+  if (!aligned16(codes_dev) || !aligned16(signs_dev) || !aligned16(x_dev) || !aligned16(workspace_dev) ||
+      !aligned4(scales_dev) || !aligned4(y_dev) || (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
+    return LQ_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const GemvWorkspace lay = gemv_workspace_layout(batch, cols, tile);
+  char* ws = reinterpret_cast<char*>(workspace_dev);
+
+  RotateArgs r;
+  r.x = x_dev; r.signs = signs_dev; r.cols = cols; r.batch = batch; r.tile = tile;
+  r.lanes_per_tile = tile / kLaneElems; r.tiles_per_row = (int)(cols / tile);
+  r.chunks_per_row = (int)((cols + kChunkCols - 1) / kChunkCols);
+  r.post_scale = (float)(0.5 / sqrt((double)tile));
+  r.a2 = (lattice == LQ_A2);
+  r.xh = reinterpret_cast<__half*>(ws + lay.xh);
+  r.xl = reinterpret_cast<__half*>(ws + lay.xl);
+  r.xs = reinterpret_cast<float*>(ws + lay.xs);
+  r.y = y_dev; r.y_elems = (int64_t)batch * rows; r.status = dev_status_dev;
+  const int64_t units = (int64_t)batch * r.chunks_per_row;
+  const int sms = device_sm_count();
+  if (sms <= 0) return LQ_ERR_CUDA;
+  int64_t rgrid = (units + 7) / 8;
+  const int64_t zgrid = (r.y_elems + 255) / 256;
+  if (rgrid < zgrid) rgrid = zgrid < sms ? zgrid : sms;
+  if (rgrid < 1) rgrid = 1;
+  if (xdtype == LQ_BF16) rotate_activation_kernel<true><<<(unsigned)rgrid, 256, 0, s>>>(r);
+  else rotate_activation_kernel<false><<<(unsigned)rgrid, 256, 0, s>>>(r);
+  st = check_launch();
+  if (st != LQ_OK) return st;
+
+  GemvArgs g;
+  g.codes = codes_dev; g.scales = scales_dev; g.rows = rows; g.cols = cols; g.tile = tile;
+  g.tiles_per_row = (int)(cols / tile); g.batch = batch;
+  g.xh = r.xh; g.xl = r.xl; g.xs = r.xs; g.y = y_dev;
+  g.splits = 1; g.tiles_per_split = g.tiles_per_row; g.tasks = 0;
+  if (batch <= 8) return launch_gemv<1, 2>(g, s);
+  return launch_gemv<2, 2>(g, s);
+}

@@ -1,0 +1,87 @@
+"""CPU-side checks of the C-ABI library: it builds, loads, exports every
+symbol declared in include/lq.h, and rejects bad arguments before launching
+anything (these calls never reach the GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lattice_vq_weight_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "lq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_covers_every_declared_symbol():
+    import lattice_vq_weight_gb300 as L
+    assert set(declared_functions()) == set(L.SIGNATURES)
+
+
+def test_pick_tile_matches_oracle_rule(golden_dir):
+    import json
+    import lattice_vq_weight_gb300 as L
+    f = json.load(open(os.path.join(golden_dir, "pages_figures.json")))["hadamard_tile_sizes"]
+    for c in f["cases"]:
+        assert L.lq_pick_tile(c["cols"], c["requested"]) == c["expect"]
+    for cols in (128, 256, 768, 1000, 3584, 4096, 14336, 28672, 8192, 5120, 2048 * 3):
+        for req in (128, 256, 512, 1024, 2048, 4096):
+            assert L.lq_pick_tile(cols, req) == O.pick_tile(cols, req), (cols, req)
+
+
+def test_status_strings_and_version():
+    import lattice_vq_weight_gb300 as L
+    assert L.status_string(0) == "ok"
+    for s in range(1, 6):
+        assert len(L.status_string(s)) > 5
+    assert L.status_string(99) == "unknown status"
+    assert L.lq_version() >= 100
+
+
+def test_argument_errors_are_synchronous():
+    import lattice_vq_weight_gb300 as L
+    lib = L.lib
+    P = ctypes.c_void_p
+    good = P(0x10000)        # aligned stand-in pointer, never dereferenced
+    odd = P(0x10004)
+    nul = P(0)
+    s = P(0)
+    q = lambda lat, W, wdt, rows, cols, ldw, tile, beta, codes, scales, signs: lib.lq_quantize(
+        lat, W, wdt, rows, cols, ldw, tile, 0, beta, codes, scales, signs, nul, s)
+    assert q(3, good, 1, 4, 256, 256, 256, 0.25, good, good, good) == L.LQ_ERR_ARG        # lattice
+    assert q(8, good, 1, 4, 256, 256, 100, 0.25, good, good, good) == L.LQ_ERR_UNSUPPORTED  # tile
+    assert q(8, good, 1, 4, 384, 384, 256, 0.25, good, good, good) == L.LQ_ERR_SHAPE   # cols % tile
+    assert q(8, good, 7, 4, 256, 256, 256, 0.25, good, good, good) == L.LQ_ERR_DTYPE
+    assert q(8, good, 1, 4, 256, 256, 256, -1.0, good, good, good) == L.LQ_ERR_ARG     # beta
+    assert q(8, good, 1, 4, 256, 128, 256, 0.25, good, good, good) == L.LQ_ERR_SHAPE   # ldw < cols
+    assert q(8, good, 1, 4, 256, 260, 256, 0.25, good, good, good) == L.LQ_ERR_SHAPE   # ldw*2 % 16
+    assert q(8, nul, 1, 4, 256, 256, 256, 0.25, good, good, good) == L.LQ_ERR_ARG
+    assert q(8, odd, 1, 4, 256, 256, 256, 0.25, good, good, good) == L.LQ_ERR_ARG
+    assert q(8, good, 1, -1, 256, 256, 256, 0.25, good, good, good) == L.LQ_ERR_SHAPE
+    g = lambda batch, tile=256, cols=256: lib.lq_gemv(
+        8, good, good, good, 4, cols, tile, good, 1, batch, good, good, nul, s)
+    assert g(0) == L.LQ_ERR_SHAPE and g(17) == L.LQ_ERR_SHAPE
+    assert g(1, tile=64) == L.LQ_ERR_UNSUPPORTED
+    assert lib.lq_dequantize(8, good, good, good, 4, 256, 256, good, 5, s) == L.LQ_ERR_DTYPE
+    assert lib.lq_make_signs(0, -1, good, s) == L.LQ_ERR_SHAPE
+    assert L.lq_gemv_workspace_size(1, 4096, 256) >= 4096 * 4
+    assert L.lq_gemv_workspace_size(0, 4096, 256) == 0

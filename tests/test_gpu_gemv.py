@@ -1,0 +1,102 @@
+"""GPU GEMV from lattice codes against the float64 oracle (codes from the oracle)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from synthetic import gaussian_matrix, gaussian_vectors, small_fp32_case
+from tests._parity import normwise_rel
+from tests.gpu_util import cuda, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-3   # normwise relative error of y against the float64 oracle on the same codes
+
+
+def gpu_gemv(torch, L, q, d, x, lattice, tile, xdtype):
+    xd = to_dev_bf16(torch, x) if xdtype == "bf16" else to_dev(torch, x)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    y = L.gemv(to_dev(torch, q.codes), to_dev(torch, q.scales), to_dev(torch, d), xd,
+               lattice=lattice, tile=tile, dev_status=status)
+    torch.cuda.synchronize()
+    return y.cpu().numpy(), int(status.item())
+
+
+def test_small_fp32_case_gemv():
+    torch, L = cuda()
+    W, x = small_fp32_case(0)
+    d = O.splitmix64_signs(0, 1024)
+    q = O.quantize(W, "e8", 256, d, 0.25)
+    y, st = gpu_gemv(torch, L, q, d, x, "e8", 256, "fp32")
+    ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
+    assert st == 0
+    assert normwise_rel(y, ref) < TOL
+    assert normwise_rel(y, ref) < 1e-5      # the fp16 hi/lo split keeps ~22 bits
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+@pytest.mark.parametrize("tile", [128, 256, 512])
+@pytest.mark.parametrize("batch", [1, 3, 8, 16])
+def test_gemv_parity(lattice, tile, batch):
+    torch, L = cuda()
+    rows, cols = 75, 2048 + 2 * tile       # ragged rows and a partial column chunk
+    W = gaussian_matrix(rows, cols, 0.02, 300 + tile, dtype="bf16")
+    d = O.splitmix64_signs(11, cols)
+    q = O.quantize(W, lattice, tile, d, 0.25)
+    x = gaussian_vectors(batch, cols, 400 + batch, dtype="bf16")
+    y, st = gpu_gemv(torch, L, q, d, x, lattice, tile, "bf16")
+    ref = O.gemv(q.codes, q.scales, d, tile, lattice, x)
+    assert st == 0
+    rel = normwise_rel(y, ref)
+    assert rel < TOL, rel
+    assert np.max(np.abs(y - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-12
+
+
+def test_gemv_extreme_activation_scales():
+    """Per-tile power-of-two scaling keeps the fp16 split accurate for tiny and huge x."""
+    torch, L = cuda()
+    W = gaussian_matrix(64, 1024, 0.02, 5, dtype="bf16")
+    d = O.splitmix64_signs(2, 1024)
+    q = O.quantize(W, "e8", 256, d, 0.25)
+    x = gaussian_vectors(4, 1024, 6, dtype="fp32")
+    x[1] *= 1e-12
+    x[2] *= 1e12
+    x[3, :256] = 0.0
+    y, st = gpu_gemv(torch, L, q, d, x, "e8", 256, "fp32")
+    ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
+    assert st == 0
+    for b in range(4):
+        assert normwise_rel(y[b], ref[b]) < 1e-5
+
+
+def test_gemv_nonfinite_activation_flag():
+    torch, L = cuda()
+    W = gaussian_matrix(16, 512, 0.02, 5, dtype="bf16")
+    d = O.splitmix64_signs(2, 512)
+    q = O.quantize(W, "e8", 256, d, 0.25)
+    x = gaussian_vectors(1, 512, 6, dtype="fp32")
+    x[0, 10] = np.inf
+    _, st = gpu_gemv(torch, L, q, d, x, "e8", 256, "fp32")
+    assert st & L.LQ_DEV_NONFINITE
+
+
+@pytest.mark.parametrize("batch", [1, 4, 16])
+def test_full_size_down_matrix_sampled_rows(batch):
+    """down_proj 4096 x 14336 (E8, tile 256) in the launch shape the bench times: the
+    codes of 64 sampled rows come from the oracle, the rest from the GPU quantizer."""
+    torch, L = cuda()
+    R, C = 4096, 14336
+    W = gaussian_matrix(R, C, 0.02, 1006, dtype="bf16")
+    Wd = to_dev_bf16(torch, W)
+    codes, scales, signs = L.quantize(Wd, lattice="e8", tile=256, seed=1006, beta=0.25)
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(R, 64, replace=False))
+    d = O.splitmix64_signs(1006, C)
+    q = O.quantize(W[rows], "e8", 256, d, 0.25)
+    ridx = torch.from_numpy(rows).to("cuda")
+    codes[ridx] = to_dev(torch, q.codes)
+    scales[ridx] = to_dev(torch, q.scales)
+    x = gaussian_vectors(batch, C, 2000 + batch, dtype="bf16")
+    y = L.gemv(codes, scales, signs, to_dev_bf16(torch, x), lattice="e8", tile=256)
+    torch.cuda.synchronize()
+    ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
+    assert normwise_rel(y.cpu().numpy()[:, rows], ref) < TOL

@@ -1,0 +1,158 @@
+"""GPU quantize / dequantize / signs against the float64 oracle (through the C ABI)."""
+import numpy as np
+import pytest
+
+import oracle as O
+from synthetic import gaussian_matrix, small_fp32_case
+from tests._parity import compare_codes, normwise_rel
+from tests.gpu_util import cuda, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def run_quantize(torch, L, W_np, dtype, lattice, tile, seed, beta, ldw_pad=0):
+    rows, cols = W_np.shape
+    if dtype == "bf16":
+        full = np.zeros((rows, cols + ldw_pad), dtype=np.float32)
+        full[:, :cols] = W_np
+        Wd = to_dev_bf16(torch, full)[:, :cols]
+    else:
+        full = np.zeros((rows, cols + ldw_pad), dtype=np.float32)
+        full[:, :cols] = W_np
+        Wd = to_dev(torch, full)[:, :cols]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, signs = L.quantize(Wd, lattice=lattice, tile=tile, seed=seed, beta=beta, dev_status=status)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy(), signs.cpu().numpy(), int(status.item())
+
+
+def test_signs_match_oracle():
+    torch, L = cuda()
+    for seed, n in ((0, 1024), (12345, 14336), (2**63 + 7, 4096)):
+        s = torch.empty(n, dtype=torch.int8, device="cuda")
+        L.lq_make_signs(seed, s)
+        np.testing.assert_array_equal(s.cpu().numpy(), O.splitmix64_signs(seed, n))
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+@pytest.mark.parametrize("tile", [128, 256, 512])
+def test_quantize_parity_ragged(lattice, tile):
+    torch, L = cuda()
+    rows, cols = 37, 3 * 512 if tile == 512 else 5 * tile   # not a multiple of the 2048-column chunk
+    W = gaussian_matrix(rows, cols, 0.02, 100 + tile, outlier_frac=0.002, dtype="bf16")
+    for beta in (0.125, 0.25, 0.5):
+        codes, scales, signs, st = run_quantize(torch, L, W, "bf16", lattice, tile, 77, beta)
+        d = O.splitmix64_signs(77, cols)
+        np.testing.assert_array_equal(signs, d)
+        q = O.quantize(W, lattice, tile, d, beta)
+        assert st == (2 if q.range_error else 0), st
+        np.testing.assert_allclose(scales, q.scales, rtol=1e-6, atol=0)
+        compare_codes(codes, q, lattice)
+
+
+def test_small_fp32_case_e8():
+    """256 x 1024 fp32 with 0.1 % x20 outliers, tile 256, beta 0.25, seed 0."""
+    torch, L = cuda()
+    W, _ = small_fp32_case(0)
+    codes, scales, signs, st = run_quantize(torch, L, W, "fp32", "e8", 256, 0, 0.25)
+    d = O.splitmix64_signs(0, 1024)
+    q = O.quantize(W, "e8", 256, d, 0.25)
+    assert st == (2 if q.range_error else 0)
+    np.testing.assert_allclose(scales, q.scales, rtol=1e-6)
+    compare_codes(codes, q, "e8")
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+def test_fp32_multi_chunk(lattice):
+    torch, L = cuda()
+    W = gaussian_matrix(24, 6144, 0.05, 9, outlier_frac=0.001, dtype="fp32")
+    codes, scales, _, st = run_quantize(torch, L, W, "fp32", lattice, 256, 5, 0.25)
+    q = O.quantize(W, lattice, 256, O.splitmix64_signs(5, 6144), 0.25)
+    np.testing.assert_allclose(scales, q.scales, rtol=1e-6)
+    compare_codes(codes, q, lattice)
+
+
+def test_strided_rows():
+    torch, L = cuda()
+    W = gaussian_matrix(19, 2048, 0.02, 3, dtype="bf16")
+    codes, scales, _, _ = run_quantize(torch, L, W, "bf16", "e8", 256, 1, 0.25, ldw_pad=8 * 5)
+    q = O.quantize(W, "e8", 256, O.splitmix64_signs(1, 2048), 0.25)
+    np.testing.assert_allclose(scales, q.scales, rtol=1e-6)
+    compare_codes(codes, q, "e8")
+
+
+def test_exact_lattice_points_and_zero_tiles():
+    """Unit spikes give y = +-1/beta exactly (codes +-8 at beta 1/4); zero tiles give zeros."""
+    torch, L = cuda()
+    T, C = 256, 1024
+    W = np.zeros((6, C), dtype=np.float32)
+    W[0, 5] = 1.0
+    W[1, 300] = -2.0
+    W[2, 0] = 0.5
+    W[2, 1023] = 0.5
+    W[4, 700] = 3.0
+    codes, scales, signs, st = run_quantize(torch, L, W, "bf16", "e8", T, 9, 0.25)
+    q = O.quantize(W, "e8", T, O.splitmix64_signs(9, C), 0.25)
+    assert st == 0
+    np.testing.assert_array_equal(codes, q.codes)
+    np.testing.assert_array_equal(scales, q.scales)
+    assert np.all(codes[3] == 0) and np.all(scales[3] == 0)
+
+
+def test_nonfinite_and_range_flags():
+    torch, L = cuda()
+    W = gaussian_matrix(4, 512, 0.02, 1, dtype="fp32")
+    W[1, 7] = np.nan
+    W[2, 300] = np.inf
+    _, _, _, st = run_quantize(torch, L, W, "fp32", "e8", 256, 0, 0.25)
+    assert st & L.LQ_DEV_NONFINITE
+    S = np.zeros((2, 256), dtype=np.float32)
+    S[0, 3] = 1.0           # spike: code 2/beta = 200 at beta 0.01
+    _, _, _, st = run_quantize(torch, L, S, "fp32", "e8", 256, 0, 0.01)
+    assert st == L.LQ_DEV_RANGE
+    q = O.quantize(S, "e8", 256, O.splitmix64_signs(0, 256), 0.01)
+    assert q.range_error
+    _, _, _, st = run_quantize(torch, L, S, "fp32", "e8", 256, 0, 0.05)   # code 40: in range
+    assert st == 0
+
+
+def test_empty_rows_is_noop():
+    torch, L = cuda()
+    W = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
+    codes, scales, signs = L.quantize(W, tile=256)
+    torch.cuda.synchronize()
+    assert codes.shape == (0, 512)
+    np.testing.assert_array_equal(signs.cpu().numpy(), O.splitmix64_signs(0, 512))
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+@pytest.mark.parametrize("tile", [128, 256, 512])
+def test_dequantize_parity(lattice, tile):
+    torch, L = cuda()
+    rows, cols = 21, 2 * 2048 + 2 * tile
+    W = gaussian_matrix(rows, cols, 0.02, 200 + tile, dtype="bf16")
+    d = O.splitmix64_signs(3, cols)
+    q = O.quantize(W, lattice, tile, d, 0.25)
+    What = L.dequantize(to_dev(torch, q.codes), to_dev(torch, q.scales), to_dev(torch, d),
+                        lattice=lattice, tile=tile)
+    ref = O.dequantize(q.codes, q.scales, d, tile, lattice)
+    got = What.cpu().numpy()
+    assert normwise_rel(got, ref) < 1e-6
+    bf = L.dequantize(to_dev(torch, q.codes), to_dev(torch, q.scales), to_dev(torch, d),
+                      lattice=lattice, tile=tile, dtype=torch.bfloat16).float().cpu().numpy()
+    assert normwise_rel(bf, ref) < 4e-3     # bf16 output rounding (2^-9 relative)
+
+
+def test_full_size_gate_matrix_sampled():
+    """Llama-3-8B gate_proj 14336 x 4096 bf16, E8, tile 256, beta 0.25, in one launch;
+    oracle on 96 sampled rows; lattice membership of every block."""
+    torch, L = cuda()
+    W = gaussian_matrix(14336, 4096, 0.02, 1004, dtype="bf16")
+    codes, scales, signs, st = run_quantize(torch, L, W, "bf16", "e8", 256, 1004, 0.25)
+    assert st == 0
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([[0, 14335], rng.choice(14336, 94, replace=False)]))
+    q = O.quantize(W[rows], "e8", 256, O.splitmix64_signs(1004, 4096), 0.25)
+    np.testing.assert_allclose(scales[rows], q.scales, rtol=1e-6)
+    compare_codes(codes[rows], q, "e8")
+    assert np.all(O.code_membership_ok("e8", codes.reshape(-1, 8).astype(np.int64)))
