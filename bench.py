@@ -1,0 +1,533 @@
+#!/usr/bin/env python
+"""Benchmark of the lattice weight-quantization hot path on GB300.
+
+One step = the whole path over one Llama-3-8B decoder layer (q, k, v, o,
+gate, up, down; bf16 N(0, 0.02^2) weights, seeds 1000..1006):
+  quantize every matrix to E8 codes (tile 256, beta 0.25; signs, RHT, scale,
+  nearest point, int8 codes + fp32 scales), then the decode GEMV y = W^ x from
+  the codes at batch 1, 4 and 16 (x ~ N(0, 1) bf16) over every matrix.
+The step is captured once as a CUDA graph and replayed; the timed region is
+exactly K replays between barriers and device synchronisations.
+
+value  = algorithmic bytes of the step / step time (GB/s, whole job over all ranks)
+e2e    = the same bytes / time of a step that also copies the layer's weights
+         and activations from pinned host memory and reads codes, scales and
+         y back to the host
+parts  = quantize GB/s, GEMV GB/s per batch, and (when available) the prefill
+         GEMM TFLOP/s on the Llama-3-70B MLP shapes
+roofline = the quantize kernel (largest share of the step) against the measured
+         HBM copy bandwidth
+
+--impl reference times the float64 CPU oracle on the same metric over a bounded
+row sample of the same layer (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+TILE, BETA, LATTICE = 256, 0.25, "e8"
+BATCHES = (1, 4, 16)
+FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS = 6800.0, 1900.0
+METRIC = "quantize GB/s + lattice-GEMV GB/s (frac of HBM peak); prefill GEMM TFLOPS"
+
+
+def layer_shapes():
+    from synthetic import LLAMA3_8B_LAYER
+    return [(n, r, c, 1000 + i) for i, (n, r, c) in enumerate(LLAMA3_8B_LAYER)]
+
+
+def quantize_bytes(rows, cols, in_bytes=2):
+    return rows * cols * (in_bytes + 1 + 4.0 / TILE) + cols
+
+
+def gemv_bytes(rows, cols, b, x_bytes=2):
+    return rows * cols * (1 + 4.0 / TILE) + cols + b * cols * x_bytes + b * rows * 4
+
+
+def step_bytes(shapes, frac_rows=1.0):
+    q = g = 0.0
+    per_b = {}
+    for _, r, c, _ in shapes:
+        rr = max(1, int(r * frac_rows))
+        q += quantize_bytes(rr, c)
+    for b in BATCHES:
+        per_b[b] = sum(gemv_bytes(max(1, int(r * frac_rows)), c, b) for _, r, c, _ in shapes)
+        g += per_b[b]
+    return q, per_b, q + g
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return json.load(open(p)), "measured"
+        except Exception:
+            pass
+    return None, "fallback"
+
+
+def hbm_peak(kind="burst"):
+    peaks, src = measured_peaks()
+    if peaks:
+        for key in (("hbm_gbs_" + kind), "hbm_gbs", "hbm_gbs_burst", "hbm_gbs_sustained"):
+            v = peaks.get(key)
+            if isinstance(v, (int, float)) and v > 0:
+                return float(v), "of measured"
+            if isinstance(v, dict):
+                for kk in ("gbs", "value", kind):
+                    if isinstance(v.get(kk), (int, float)):
+                        return float(v[kk]), "of measured"
+    return FALLBACK_HBM_GBS, "of fallback"
+
+
+def bf16_peak(kind="burst"):
+    peaks, _ = measured_peaks()
+    if peaks:
+        for key in ("bf16_tflops" if kind == "burst" else "bf16_tflops_sustained", "bf16_tflops"):
+            v = peaks.get(key)
+            if isinstance(v, (int, float)) and v > 0:
+                return float(v), "of measured"
+    return FALLBACK_BF16_TFLOPS, "of fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="lq_clocks_", suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def cpu_oracle_sample(frac_rows: float, repeats: int = 1) -> dict:
+    """Time the float64 oracle on the first frac_rows of every layer matrix."""
+    import numpy as np
+    import oracle as O
+    from synthetic import gaussian_matrix, gaussian_vectors
+    shapes = layer_shapes()
+    mats, xs = [], {}
+    for n, r, c, seed in shapes:
+        rr = max(1, int(r * frac_rows))
+        mats.append((n, gaussian_matrix(rr, c, 0.02, seed, dtype="bf16"), c, seed))
+    for b in BATCHES:
+        for c in sorted({c for _, _, c, _ in shapes}):
+            xs[(b, c)] = gaussian_vectors(b, c, 5000 + b, dtype="bf16")
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        for n, W, c, seed in mats:
+            d = O.splitmix64_signs(seed, c)
+            q = O.quantize(W, LATTICE, TILE, d, BETA)
+            for b in BATCHES:
+                O.gemv(q.codes, q.scales, d, TILE, LATTICE, xs[(b, c)])
+        times.append(time.perf_counter() - t0)
+    _, _, total = step_bytes(shapes, frac_rows)
+    return {"seconds": times, "bytes": total}
+
+
+def run_cpu_baseline(frac_rows: float, repeats: int) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_oracle_sample(%r, %d)))" % (ROOT, frac_rows, repeats))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError("CPU oracle leg failed:\n" + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("LQ_DIST_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, value, device):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- reference arm
+def reference_arm(args, ws, rank):
+    if rank != 0:
+        return
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"      # the oracle runs on one host core
+    shapes = layer_shapes()
+    frac = args.reference_frac
+    for _ in range(args.warmup):
+        cpu_oracle_sample(frac, 1)
+    t0 = time.perf_counter()
+    res = cpu_oracle_sample(frac, args.steps)
+    total = time.perf_counter() - t0
+    step_s = statistics.mean(res["seconds"])
+    value = res["bytes"] / step_s / 1e9
+    sample = (f"first {frac:.4g} of the rows of each Llama-3-8B layer matrix per step "
+              f"(quantize + GEMV b=1,4,16), float64 NumPy oracle")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6),
+        "unit": "GB/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "llama3-8b-layer e8 tile256 beta0.25 quantize+gemv(b=1,4,16)",
+                   "sample_rows_fraction": frac},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(total, 3),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def gpu_arm(args, ws, rank, local):
+    import numpy as np
+    import torch
+
+    from lattice_vq_weight_gb300 import build as _build
+    _build.build()
+    import lattice_vq_weight_gb300 as L
+    from synthetic import bf16_bits_to_f32, f32_to_bf16_bits, gaussian_matrix, gaussian_vectors  # noqa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    shapes = layer_shapes()
+
+    # ---- inputs: host (pinned) copies for the end-to-end leg, device copies for the kernel leg
+    host_w, dev_w = [], []
+    for n, r, c, seed in shapes:
+        w = gaussian_matrix(r, c, 0.02, seed, dtype="bf16")
+        hw = torch.from_numpy(f32_to_bf16_bits(w).view(np.int16)).view(torch.bfloat16).pin_memory()
+        host_w.append(hw)
+        dev_w.append(hw.to(dev, non_blocking=False))
+    host_x = {}
+    dev_x = {}
+    for b in BATCHES:
+        for c in sorted({c for _, _, c, _ in shapes}):
+            x = gaussian_vectors(b, c, 5000 + b, dtype="bf16")
+            hx = torch.from_numpy(f32_to_bf16_bits(x).view(np.int16)).view(torch.bfloat16).pin_memory()
+            host_x[(b, c)] = hx
+            dev_x[(b, c)] = hx.to(dev)
+    codes = [torch.empty((r, c), dtype=torch.int8, device=dev) for _, r, c, _ in shapes]
+    scales = [torch.empty((r, c // TILE), dtype=torch.float32, device=dev) for _, r, c, _ in shapes]
+    signs = [torch.empty((c,), dtype=torch.int8, device=dev) for _, _, c, _ in shapes]
+    ys = {(b, i): torch.empty((b, r), dtype=torch.float32, device=dev)
+          for b in BATCHES for i, (_, r, _, _) in enumerate(shapes)}
+    ws_bytes = max(L.lq_gemv_workspace_size(b, c, TILE) for b in BATCHES for _, _, c, _ in shapes)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def quantize_all():
+        for i, (n, r, c, seed) in enumerate(shapes):
+            L.lq_quantize(LATTICE, dev_w[i], TILE, seed, BETA, codes[i], scales[i], signs[i], status)
+
+    def gemv_all(b):
+        for i, (n, r, c, seed) in enumerate(shapes):
+            L.lq_gemv(LATTICE, codes[i], scales[i], signs[i], TILE, dev_x[(b, c)], ys[(b, i)], work, status)
+
+    def step():
+        quantize_all()
+        for b in BATCHES:
+            gemv_all(b)
+
+    launches_per_step = 2 * len(shapes) + 2 * len(shapes) * len(BATCHES)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    g_step = capture(step)
+    g_quant = capture(quantize_all)
+    g_gemv = {b: capture(lambda b=b: gemv_all(b)) for b in BATCHES}
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize(dev)
+
+    def time_graph(g, reps):
+        with torch.cuda.stream(stream):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    # ---- timed region: exactly K steps
+    clocks = ClockSampler(torch.cuda.current_device() if local is None else local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g_step.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    ms_step_local = e0.elapsed_time(e1) / args.steps
+    ms_step = max_over_ranks(ws, ms_step_local, dev)
+    qb, gb_per_b, total_bytes = step_bytes(shapes)
+    value = total_bytes * ws / (ms_step * 1e-3) / 1e9
+
+    # ---- per-part timings (quantize kernel = roofline kernel; GEMV per batch)
+    reps = max(3, args.steps)
+    ms_quant = time_graph(g_quant, reps)
+    ms_gemv = {b: time_graph(g_gemv[b], reps) for b in BATCHES}
+    quant_gbs = qb / (ms_quant * 1e-3) / 1e9
+    parts = {"quantize_gbs": round(quant_gbs, 1)}
+    for b in BATCHES:
+        parts[f"gemv_b{b}_gbs"] = round(gb_per_b[b] / (ms_gemv[b] * 1e-3) / 1e9, 1)
+    parts["quantize_ms"] = round(ms_quant, 4)
+    parts.update({f"gemv_b{b}_ms": round(ms_gemv[b], 4) for b in BATCHES})
+
+    # ---- end-to-end through the public API with host buffers
+    h_codes = [torch.empty(cd.shape, dtype=torch.int8).pin_memory() for cd in codes]
+    h_scales = [torch.empty(s.shape, dtype=torch.float32).pin_memory() for s in scales]
+    h_ys = {k: torch.empty(v.shape, dtype=torch.float32).pin_memory() for k, v in ys.items()}
+    h2d = sum(w.numel() * 2 for w in host_w) + sum(x.numel() * 2 for x in host_x.values())
+    d2h = sum(c.numel() for c in codes) + sum(s.numel() * 4 for s in scales) + sum(v.numel() * 4 for v in ys.values())
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for i in range(len(shapes)):
+                dev_w[i].copy_(host_w[i], non_blocking=True)
+            for k in host_x:
+                dev_x[k].copy_(host_x[k], non_blocking=True)
+            g_step.replay()
+            for i in range(len(shapes)):
+                h_codes[i].copy_(codes[i], non_blocking=True)
+                h_scales[i].copy_(scales[i], non_blocking=True)
+            for k in ys:
+                h_ys[k].copy_(ys[k], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e2e_ms = max_over_ranks(ws, (time.perf_counter() - t0) * 1e3 / args.steps, dev)
+    e2e_val = total_bytes * ws / (e2e_ms * 1e-3) / 1e9
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed region")
+
+    # ---- prefill GEMM (Llama-3-70B MLP shapes), when the library provides it
+    gemm = None
+    if not args.no_gemm:
+        gemm = gemm_part(L, torch, dev, stream, reps=max(3, min(args.steps, 10)))
+
+    peak, peak_src = hbm_peak("burst")
+    roof_achieved = quant_gbs
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get("quantize_layer_bytes")
+        except Exception:
+            traffic = None
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->int8 (fp32 compute)",
+        "data": "synthetic",
+        "config": {"workload": "llama3-8b-layer e8 tile256 beta0.25 quantize+gemv(b=1,4,16)",
+                   "matrices": [f"{n} {r}x{c}" for n, r, c, _ in shapes], "lattice": LATTICE, "tile": TILE,
+                   "beta": BETA, "batches": list(BATCHES), "parallelism": f"replicas{ws}",
+                   "l2": "inputs larger than L2 (436 MB bf16 weights, 218 MB codes per step); no flush",
+                   "graph": "step captured as one CUDA graph"},
+        "gpu_launches": launches_per_step * args.steps,
+        "parts": parts,
+        "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 3)},
+        "roofline": {"kernel": "quantize_kernel (all 7 matrices of the layer)", "bound": "hbm",
+                     "achieved": round(roof_achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(roof_achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": traffic},
+        "clocks": clk,
+    }
+    if gemm is not None:
+        line["parts"].update(gemm)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            cb = run_cpu_baseline(args.cpu_frac, 1)
+            secs = cb["seconds"][0]
+            line["cpu_baseline"] = {
+                "value": round(cb["bytes"] / secs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                "sample": (f"first {args.cpu_frac:.4g} of the rows of each layer matrix, quantize + GEMV "
+                           f"b=1,4,16, float64 NumPy, 1 thread, {secs:.1f} s")}
+        except Exception as exc:  # reported, not fatal for the GPU number
+            line["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def gemm_part(L, torch, dev, stream, reps):
+    """Prefill GEMM TFLOP/s on Llama-3-70B MLP shapes (E8 codes, X bf16 M x K)."""
+    from synthetic import LLAMA3_70B_MLP
+    out = {}
+    for name, N, K in LLAMA3_70B_MLP:
+        W = (torch.randn((N, K), device=dev, generator=torch.Generator(device=dev).manual_seed(4000))
+             * 0.015).to(torch.bfloat16)
+        codes, scales, signs = L.quantize(W, lattice="e8", tile=TILE, seed=4000, beta=BETA)
+        del W
+        for M in (256, 2048):
+            X = torch.randn((M, K), device=dev, generator=torch.Generator(device=dev).manual_seed(4100 + M)
+                            ).to(torch.bfloat16)
+            Y = torch.empty((M, N), dtype=torch.float32, device=dev)
+            wsz = torch.empty(L.lq_gemm_workspace_size(M, K), dtype=torch.uint8, device=dev)
+            try:
+                with torch.cuda.stream(stream):
+                    L.lq_gemm("e8", codes, scales, signs, TILE, X, Y, wsz)
+            except L.LQError as e:
+                if e.status == L.LQ_ERR_UNSUPPORTED:
+                    return None
+                raise
+            torch.cuda.synchronize(dev)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                L.lq_gemm("e8", codes, scales, signs, TILE, X, Y, wsz)
+            for _ in range(2):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            with torch.cuda.stream(stream):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            out[f"gemm_{name}_M{M}_tflops"] = round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1)
+            out[f"gemm_{name}_M{M}_ms"] = round(ms, 4)
+        del codes, scales, signs
+    pk, src = bf16_peak("burst")
+    best = max(v for k, v in out.items() if k.endswith("_tflops"))
+    out["gemm_peak_tflops"] = pk
+    out["gemm_best_frac"] = round(best / pk, 4)
+    out["gemm_peak_source"] = src
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("lq", "reference"), default="lq")
+    ap.add_argument("--no-gemm", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-frac", type=float, default=0.25)
+    ap.add_argument("--reference-frac", type=float, default=1.0 / 64)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_setup(args)
+    try:
+        if args.impl == "reference":
+            reference_arm(args, ws, rank)
+        else:
+            gpu_arm(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
