@@ -149,6 +149,33 @@ lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,
                   void* workspace_dev, int32_t* dev_status_dev, void* stream);
 
 /*
+ * lq_gemv without a caller-provided workspace (the method's pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory).  Such callers include inference-engine plug-ins whose host engine
+ * owns every device allocation through its own pool and forbids allocation at
+ * run time, and latency-critical decode loops where an allocation's implicit
+ * device synchronisation is not acceptable.
+ *
+ * Same arguments and result as lq_gemv minus the workspace.  The workspace is
+ * a fixed array of LQ_GEMV_NOALLOC_MAX_WORKSPACE bytes inside the library's
+ * device image: every GPU that loads the library holds it until the process
+ * exits.  Requests whose lq_gemv_workspace_size(batch, cols, tile) exceeds that
+ * size return LQ_ERR_SHAPE before anything is launched (for example batch 16
+ * with cols up to 65536 fits).  The first call on a device looks the array's
+ * device address up (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Nothing is allocated by this call.  All calls share the one
+ * array, so calls that may overlap on the GPU (different streams without
+ * ordering between them) race and must not be issued; calls on one stream are
+ * ordered and safe.  The array keeps the previous call's contents; the call
+ * rewrites every part it reads.
+ */
+#define LQ_GEMV_NOALLOC_MAX_WORKSPACE ((size_t)4 * 1024 * 1024 + (size_t)64 * 1024)
+lq_status lq_gemv_noalloc(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                          const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                          const void* x_dev, int xdtype, int batch, float* y_dev,
+                          int32_t* dev_status_dev, void* stream);
+
+/*
  * Workspace bytes lq_gemm needs: the rotated activations X~ as fp16 [M x K]
  * plus one float per row.
  */

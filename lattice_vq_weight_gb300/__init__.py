@@ -32,6 +32,7 @@ SIGNATURES = {
     "lq_dequantize": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _P]),
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
     "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
+    "lq_gemv_noalloc": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P]),
     "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
     "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
 }
@@ -149,6 +150,19 @@ def lq_gemv(lattice, codes, scales, signs, tile: int, x, y, workspace, dev_statu
     _check("lq_gemv", _get_lib().lq_gemv(
         _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), rows, cols, int(tile),
         _ptr(x), _dtype_id(x), batch, _ptr(y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+# Largest workspace lq_gemv_noalloc can serve (LQ_GEMV_NOALLOC_MAX_WORKSPACE in lq.h)
+LQ_GEMV_NOALLOC_MAX_WORKSPACE = 4 * 1024 * 1024 + 64 * 1024
+
+
+def lq_gemv_noalloc(lattice, codes, scales, signs, tile: int, x, y, dev_status=None, stream=None) -> None:
+    """lq_gemv using the library's fixed device scratch instead of a caller workspace."""
+    rows, cols = codes.shape
+    batch = x.shape[0]
+    _check("lq_gemv_noalloc", _get_lib().lq_gemv_noalloc(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), rows, cols, int(tile),
+        _ptr(x), _dtype_id(x), batch, _ptr(y), _ptr(dev_status), _stream(stream)))
 
 
 def lq_gemm_workspace_size(M: int, K: int) -> int:

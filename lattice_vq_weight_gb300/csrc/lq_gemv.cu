@@ -17,6 +17,8 @@
 //     accumulation against hi and lo.  One accumulator per tile is scaled by
 //     s[r, t] * 2^-e[b, t] and summed; warps that split a row's tiles combine
 //     with fp32 atomics.
+#include <mutex>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -423,4 +425,57 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   g.splits = 1; g.tiles_per_split = g.tiles_per_row; g.tasks = 0;
   if (batch <= 8) return launch_gemv<1, 2>(g, s);
   return launch_gemv<2, 2>(g, s);
+}
+
+// ---------------------------------------------------------------------------
+// lq_gemv_noalloc: the same product for callers that cannot allocate device
+// memory themselves.  Its workspace is a fixed array in this library's device
+// image (allocated once per GPU when the library's module is loaded and kept
+// until the process exits).  Host code must not use the array's name as a
+// device address; the address is looked up per device with
+// cudaGetSymbolAddress the first time a device is used.
+static __device__ __align__(256) unsigned char g_gemv_noalloc_scratch[LQ_GEMV_NOALLOC_MAX_WORKSPACE];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once).
+lq_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return LQ_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_gemv_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return LQ_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return LQ_OK;
+}
+
+}  // namespace
+
+extern "C" lq_status lq_gemv_noalloc(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                                     const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                                     const void* x_dev, int xdtype, int batch, float* y_dev,
+                                     int32_t* dev_status_dev, void* stream) {
+  lq_status st = validate_common(lattice, rows, cols, tile);
+  if (st != LQ_OK) return st;
+  if (batch < 1 || batch > 16) return LQ_ERR_SHAPE;
+  if (lq_gemv_workspace_size(batch, cols, tile) > (size_t)LQ_GEMV_NOALLOC_MAX_WORKSPACE) return LQ_ERR_SHAPE;
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != LQ_OK) return st;
+  return lq_gemv(lattice, codes_dev, scales_dev, signs_dev, rows, cols, tile, x_dev, xdtype, batch, y_dev,
+                 scratch, dev_status_dev, stream);
 }
