@@ -469,7 +469,7 @@ def gemm_part(L, torch, dev, stream, reps):
             X = torch.randn((M, K), device=dev, generator=torch.Generator(device=dev).manual_seed(4100 + M)
                             ).to(torch.bfloat16)
             Y = torch.empty((M, N), dtype=torch.float32, device=dev)
-            wsz = torch.empty(L.lq_gemm_workspace_size(M, K), dtype=torch.uint8, device=dev)
+            wsz = torch.empty(L.lq_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
             try:
                 with torch.cuda.stream(stream):
                     L.lq_gemm("e8", codes, scales, signs, TILE, X, Y, wsz)

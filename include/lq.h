@@ -176,23 +176,30 @@ lq_status lq_gemv_noalloc(int lattice, const int8_t* codes_dev, const float* sca
                           int32_t* dev_status_dev, void* stream);
 
 /*
- * Workspace bytes lq_gemm needs: the rotated activations X~ as fp16 [M x K]
- * plus one float per row.
+ * Workspace bytes lq_gemm needs: the rotated activations X~ as fp16 [M x K],
+ * one float per token row and one float per weight row.
  */
-size_t lq_gemm_workspace_size(int64_t M, int64_t K);
+size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
- * Prefill product Y[M x N] = X W^T from E8 codes of W [N x K] (HyperQuant
- * page, mma="int8" paragraph: best for prefill / large batch, decoded weights
- * never written to memory):
- *     Y[m, n] = sum_t s[n, t] * (X~_t[m] . p[n, t]).
- * X~ is rounded to fp16 (after a per-row power-of-two range scaling) and the
- * decoded weights s * p are formed as fp16 on chip; tensor cores (tcgen05)
- * accumulate in fp32.
- *   X_dev     bf16 [M x K];  Y_dev float32 [M x N] (written)
- *   tile      256;  N % 128 == 0;  K % 256 == 0;  M >= 1
- *   workspace_dev  lq_gemm_workspace_size(M, K) bytes
- *   dev_status_dev  int32 status word or NULL (LQ_DEV_TIMEOUT)
+ * Prefill product Y[M x N] = X W^T from the lattice codes of W [N x K]
+ * (HyperQuant page, mma="int8" paragraph: tensor-core GEMM on the decoded
+ * codes, the activation rotated on every forward, no decoded weight written
+ * to memory; best for prefill / large batch):
+ *     Y[m, n] = sum_t s[n, t] * sum_i p[n, t, i] * X~[m, t, i],
+ *     X~ = H D X / sqrt(tile) per tile.
+ * On chip the decoded weights p s are formed in fp16 (times a per-row power of
+ * two) and X~ is rounded to fp16 (times a per-token-row power of two); the
+ * tcgen05 tensor cores accumulate in fp32.
+ *   codes_dev int8 [N x K], scales_dev float32 [N x K/tile], signs_dev int8 [K]
+ *   X_dev     bf16 [M x K] (raw 16-bit patterns), row stride K
+ *   tile      128, 256 or 512;  N % 128 == 0;  K % tile == 0;  M >= 0
+ *   Y_dev     float32 [M x N] (overwritten)
+ *   workspace_dev  lq_gemm_workspace_size(M, N, K) bytes, 256-byte aligned
+ *   dev_status_dev  int32 status word or NULL (LQ_DEV_NONFINITE for a
+ *             non-finite activation row, LQ_DEV_TIMEOUT if a pipeline wait
+ *             gave up -- Y is then unspecified)
+ * Two kernels run on `stream`: the activation rotation, then the GEMM.
  */
 lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
                   const int8_t* signs_dev, int64_t N, int64_t K, int tile,

@@ -33,7 +33,7 @@ SIGNATURES = {
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
     "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "lq_gemv_noalloc": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P]),
-    "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64]),
+    "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
 }
 
@@ -165,13 +165,13 @@ def lq_gemv_noalloc(lattice, codes, scales, signs, tile: int, x, y, dev_status=N
         _ptr(x), _dtype_id(x), batch, _ptr(y), _ptr(dev_status), _stream(stream)))
 
 
-def lq_gemm_workspace_size(M: int, K: int) -> int:
-    return int(_get_lib().lq_gemm_workspace_size(int(M), int(K)))
+def lq_gemm_workspace_size(M: int, N: int, K: int) -> int:
+    return int(_get_lib().lq_gemm_workspace_size(int(M), int(N), int(K)))
 
 
 def lq_gemm(lattice, codes, scales, signs, tile: int, X, Y, workspace, dev_status=None,
             stream=None) -> None:
-    """Y [M x N] float32 = X~ . (s p)^T from E8 codes [N x K]; X bf16 [M x K]."""
+    """Y [M x N] float32 = X~ . (s p)^T from the codes [N x K]; X bf16 [M x K]."""
     N, K = codes.shape
     M = X.shape[0]
     _check("lq_gemm", _get_lib().lq_gemm(
@@ -222,6 +222,6 @@ def gemm(codes, scales, signs, X, lattice: str = "e8", tile: int = 256, workspac
     M = X.shape[0]
     Y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
     if workspace is None:
-        workspace = torch.empty(lq_gemm_workspace_size(M, K), dtype=torch.uint8, device=codes.device)
+        workspace = torch.empty(lq_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=codes.device)
     lq_gemm(lattice, codes, scales, signs, tile, X, Y, workspace, dev_status, stream)
     return Y

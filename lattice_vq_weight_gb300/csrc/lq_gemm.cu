@@ -1,19 +1,654 @@
-// Prefill GEMM from E8 codes (tcgen05).  Placeholder until the kernel lands.
-#include <cstddef>
+// Prefill GEMM from lattice codes on the 5th-generation tensor cores (tcgen05).
+//
+// HyperQuant page, mma="int8" paragraph: the decoded codes feed a tensor-core
+// GEMM on every forward, the activation is rotated first, and no decoded
+// weight is ever written to memory -- best for prefill / large batch.
+//
+//   Y[m, n] = sum_t s[n, t] * (X~_t[m] . p[n, t]),   X~ = H D X / sqrt(T).
+//
+// Two kernels:
+//  1. gemm_prep_kernel:  X~ as fp16 (each token row scaled by a power of two
+//     g_m so that |X~ g_m| < 2^15; A2 odd coordinates times sqrt 3), one
+//     power-of-two factor f_n per weight row so that |p s f_n| < 2^15, and a
+//     zeroed Y when several CTAs add into the same output.
+//  2. gemm_kernel: persistent, warp-specialised CTA (one per SM) computing a
+//     128 (weight rows) x 256 (tokens) output tile with
+//       tcgen05.mma.cta_group::1.kind::f16  (A = decoded weights, B = X~, D fp32 in TMEM)
+//     warp 0      TMA producer: int8 code tile [128 x 64] and X~ tile [256 x 64]
+//     warp 1      allocates TMEM, one lane issues the MMAs
+//     warps 2..5  decoders: codes -> fp16 (c * s[n,t] * f_n / 2) written to
+//                 shared memory in the 128-byte-swizzled K-major layout
+//     warps 6..9  epilogue: tcgen05.ld of the accumulator, Y = D / (f_n g_m)
+//   Shared memory holds 3 stages; TMEM holds two 256-column accumulators so
+//   the epilogue of one tile overlaps the main loop of the next.  Every
+//   mbarrier wait is bounded (about a second of clock cycles); on expiry the
+//   kernel records LQ_DEV_TIMEOUT and winds down.
 #include <cstdint>
+#include <cstring>
+#include <mutex>
 
-#include "lq.h"
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
-extern "C" size_t lq_gemm_workspace_size(int64_t M, int64_t K) {
-  if (M <= 0 || K <= 0) return 0;
-  return (size_t)M * (size_t)K * 2 + (size_t)M * 4 + 512;
+#include "lq_device.cuh"
+#include "lq_host.h"
+
+namespace lq {
+namespace gemm {
+
+constexpr int BM = 128;            // weight rows per tile (MMA M)
+constexpr int BN = 256;            // tokens per tile (MMA N)
+constexpr int BK = 64;             // K per pipeline stage
+constexpr int kStages = 3;
+constexpr int kCodeBytes = BM * BK;          // int8 codes per stage:   8 KB
+constexpr int kABytes = BM * BK * 2;         // fp16 decoded weights:   16 KB
+constexpr int kXBytes = BN * BK * 2;         // fp16 activations:       32 KB
+constexpr int kThreads = 320;                // 10 warps
+constexpr int kDecodeThreads = 128;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
+constexpr long long kWaitCycles = 2000000000ll;  // about one second
+
+struct Smem;
+struct Smem {
+  // stage buffers come first and are 1024-byte aligned (128-byte swizzle atoms)
+  alignas(1024) uint8_t x[kStages][kXBytes];
+  alignas(1024) uint8_t a[kStages][kABytes];
+  alignas(1024) uint8_t codes[kStages][kCodeBytes];
+  alignas(8) uint64_t full[kStages];      // TMA bytes landed (codes + X~)
+  alignas(8) uint64_t decoded[kStages];   // decoders wrote A
+  alignas(8) uint64_t empty[kStages];     // MMAs finished reading the stage
+  alignas(8) uint64_t tmem_full[2];       // accumulator ready for the epilogue
+  alignas(8) uint64_t tmem_empty[2];      // epilogue drained the accumulator
+  alignas(8) uint64_t drain;              // all issued MMAs complete (teardown)
+  uint32_t tmem_base;
+  int timeout;
+};
+
+struct Args {
+  int64_t M, N, K;
+  int tile, tiles_per_row;
+  int n_tiles, m_tiles, splits, stages_per_split, k_stages;
+  int64_t units;
+  const float* scales;    // [N x K/T]
+  const float* f;         // [N]   row factors 2^e
+  const float* inv_g;     // [M]   1 / g_m
+  float* Y;               // [M x N]
+  int32_t* status;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the limit expired (the caller records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* timeout_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*timeout_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *timeout_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05: K-major, 128-byte swizzle,
+// 8-row atoms of 1024 bytes (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr >> 4) & 0x3FFFu);          // start address
+  d |= (uint64_t)1u << 16;                          // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024u >> 4) << 32;                // stride byte offset
+  d |= (uint64_t)1u << 46;                          // descriptor version
+  d |= (uint64_t)2u << 61;                          // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: D f32, A/B f16, both K-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+      ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// int8 codes (4 per word) -> f16x2 words (exact), then times the fp16 scale.
+__device__ __forceinline__ uint32_t code_pair_f16(uint32_t u, uint32_t sel, __half2 sf) {
+  const uint32_t h = __byte_perm(u, 0x64646464u, sel);
+  const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+  const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&h), off), sf);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x, Args a) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile int* timeout = &sm.timeout;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.decoded[s], kDecodeThreads);
+      mbar_init(&sm.empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.tmem_full[i], 1);
+      mbar_init(&sm.tmem_empty[i], kEpiThreads);
+    }
+    mbar_init(&sm.drain, 1);
+    sm.timeout = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&sm.tmem_base)), "r"(kTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int64_t issued = 0;
+      for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x) {
+        const int nt = (int)(u % a.n_tiles);
+        const int64_t rest = u / a.n_tiles;
+        const int mt = (int)(rest % a.m_tiles);
+        const int sp = (int)(rest / a.m_tiles);
+        const int k0 = sp * a.stages_per_split;
+        const int k1 = min(a.k_stages, k0 + a.stages_per_split);
+        for (int ks = k0; ks < k1; ++ks) {
+          if (!mbar_wait(&sm.empty[s], ph ^ 1, timeout)) break;
+          mbar_arrive_expect_tx(&sm.full[s], kCodeBytes + kXBytes);
+          tma_load_2d(sm.codes[s], &map_codes, &sm.full[s], ks * BK, nt * BM);
+          tma_load_2d(sm.x[s], &map_x, &sm.full[s], ks * BK, mt * BN);
+          ++issued;
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+      if (*timeout) {
+        // let the copies already in flight land before the CTA exits (bounded)
+        for (int i = 0; i < kStages && i < issued; ++i) {
+          if (--s < 0) { s = kStages - 1; ph ^= 1; }
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&sm.full[s], ph) && clock64() - t0 < kWaitCycles) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      int it = 0;
+      for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x, ++it) {
+        const int64_t rest = u / a.n_tiles;
+        const int sp = (int)(rest / a.m_tiles);
+        const int k0 = sp * a.stages_per_split;
+        const int k1 = min(a.k_stages, k0 + a.stages_per_split);
+        const int acc = it & 1;
+        const uint32_t acc_ph = (uint32_t)((it >> 1) & 1);
+        if (!mbar_wait(&sm.tmem_empty[acc], acc_ph ^ 1, timeout)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int ks = k0; ks < k1; ++ks) {
+          if (!mbar_wait(&sm.decoded[s], ph, timeout)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sm.a[s]);
+          const uint32_t x_addr = smem_u32(sm.x[s]);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            mma_f16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(x_addr + kk * 32),
+                    (ks > k0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sm.empty[s]);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+        if (!ok) break;
+        mma_commit(&sm.tmem_full[acc]);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ decoders
+    const int d = threadIdx.x - 64;          // 0..127
+    const int rsub = d >> 2;                 // row within a 32-row pass
+    const int c4 = d & 3;                    // 16-code chunk within the 64-code stage row
+    int s = 0;
+    uint32_t ph = 0;
+    for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x) {
+      const int nt = (int)(u % a.n_tiles);
+      const int64_t rest = u / a.n_tiles;
+      const int sp = (int)(rest / a.m_tiles);
+      const int k0 = sp * a.stages_per_split;
+      const int k1 = min(a.k_stages, k0 + a.stages_per_split);
+      float fr[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) fr[p] = 0.5f * __ldg(a.f + (int64_t)nt * BM + 32 * p + rsub);
+      __half2 sf[4];
+      int cur_t = -1;
+      for (int ks = k0; ks < k1; ++ks) {
+        if (!mbar_wait(&sm.full[s], ph, timeout)) break;
+        const int t = (ks * BK) / a.tile;
+        if (t != cur_t) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const int64_t row = (int64_t)nt * BM + 32 * p + rsub;
+            sf[p] = __float2half2_rn(__ldg(a.scales + row * a.tiles_per_row + t) * fr[p]);
+          }
+          cur_t = t;
+        }
+        const uint8_t* cbase = sm.codes[s];
+        uint8_t* abase = sm.a[s];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const int r = 32 * p + rsub;
+          const uint4 cw = *reinterpret_cast<const uint4*>(cbase + r * BK + 16 * c4);
+          const uint32_t w[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u, cw.w ^ 0x80808080u};
+          uint32_t o[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            o[2 * q] = code_pair_f16(w[q], 0x4140, sf[p]);
+            o[2 * q + 1] = code_pair_f16(w[q], 0x4342, sf[p]);
+          }
+          // 128-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ (r & 7)
+          const int j0 = 2 * c4, j1 = 2 * c4 + 1;
+          *reinterpret_cast<uint4*>(abase + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(abase + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&sm.decoded[s]);
+        if (++s == kStages) { s = 0; ph ^= 1; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quarter = warp & 3;            // TMEM lane quarter this warp may access
+    const int row_in_tile = quarter * 32 + lane;
+    int it = 0;
+    for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
+      if (__any_sync(0xffffffffu, *timeout != 0)) break;
+      const int nt = (int)(u % a.n_tiles);
+      const int64_t rest = u / a.n_tiles;
+      const int mt = (int)(rest % a.m_tiles);
+      const int acc = it & 1;
+      const uint32_t acc_ph = (uint32_t)((it >> 1) & 1);
+      const bool ready = mbar_wait(&sm.tmem_full[acc], acc_ph, timeout);
+      if (!__all_sync(0xffffffffu, ready)) break;
+      tc_fence_after();
+      const int64_t n = (int64_t)nt * BM + row_in_tile;
+      const float inv_f = 1.0f / __ldg(a.f + n);
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
+      float* yrow = a.Y + n;
+      const bool atomic = a.splits > 1;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + (uint32_t)c0, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int64_t m = (int64_t)mt * BN + c0 + j;
+          if (m < a.M) {
+            const float v = __uint_as_float(r[j]) * inv_f * __ldg(a.inv_g + m);
+            if (atomic) atomicAdd(yrow + m * a.N, v); else yrow[m * a.N] = v;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.tmem_empty[acc]);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      // every MMA this thread issued has completed once this commit arrives
+      mma_commit(&sm.drain);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(&sm.drain, 0) && clock64() - t0 < kWaitCycles) {
+      }
+    }
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+  }
+  if (threadIdx.x == 0 && sm.timeout) raise_flag(a.status, LQ_DEV_TIMEOUT);
+}
+
+// ---------------------------------------------------------------- prep kernel
+struct PrepArgs {
+  const __nv_bfloat16* X;    // [M x K]
+  const int8_t* signs;       // [K]
+  int64_t M, N, K;
+  int tile, lanes_per_tile, tiles_per_row, chunks_per_row;
+  float inv_sqrt_tile;
+  int a2;
+  __half* Xt;                // [M x K]
+  float* inv_g;              // [M]
+  const float* scales;       // [N x K/T]
+  float* f;                  // [N]
+  float* Y;                  // zeroed when zero_y
+  int zero_y;
+  int32_t* status;
+};
+
+// Blocks [0, M): one token row each.  Blocks [M, M + ceil(N/256)): weight-row
+// factors, one thread per row.
+__global__ void __launch_bounds__(256, 1) gemm_prep_kernel(PrepArgs a) {
+  __shared__ float red[8];
+  __shared__ float row_g;
+  if (blockIdx.x >= a.M) {
+    const int64_t n = (int64_t)(blockIdx.x - a.M) * 256 + threadIdx.x;
+    if (n >= a.N) return;
+    float mx = 0.f;
+    for (int t = 0; t < a.tiles_per_row; ++t) mx = fmaxf(mx, __ldg(a.scales + n * a.tiles_per_row + t));
+    // |p s| <= 63.5 s; choose f = 2^e with 63.5 * max(s) * f in [2^14, 2^15)
+    float fv = 1.f;
+    if (mx > 0.f && isfinite(mx)) {
+      const float top = 63.5f * mx;
+      const int E = (int)((__float_as_uint(top) >> 23) & 0xFFu) - 126;  // top in [2^(E-1), 2^E)
+      const int ex = max(-126, min(127, 15 - E));
+      fv = __uint_as_float((uint32_t)(ex + 127) << 23);
+    }
+    a.f[n] = fv;
+    return;
+  }
+  const int64_t m = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const __nv_bfloat16* xr = a.X + m * a.K;
+  // pass 1: max |x| over the row
+  float mx = 0.f;
+  for (int64_t i = (int64_t)threadIdx.x * 8; i < a.K; i += 256 * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + i));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[h] << 16)), fabsf(__uint_as_float(w[h] & 0xFFFF0000u))));
+  }
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = 0.f;
+    for (int i = 0; i < 8; ++i) v = fmaxf(v, red[i]);
+    // |x~| <= sqrt(T) max|x| (times sqrt 3 for A2): g = 2^e with that bound in [2^13, 2^14]
+    float gv = 1.f;
+    if (!isfinite(v)) {
+      raise_flag(a.status, LQ_DEV_NONFINITE);
+    } else if (v > 0.f) {
+      const float top = v * (1.0f / a.inv_sqrt_tile) * (a.a2 ? 1.7320508f : 1.f);
+      const int E = (int)((__float_as_uint(top) >> 23) & 0xFFu) - 126;
+      const int ex = max(-126, min(127, 14 - E));
+      gv = __uint_as_float((uint32_t)(ex + 127) << 23);
+    }
+    row_g = gv;
+    a.inv_g[m] = 1.0f / gv;
+  }
+  __syncthreads();
+  const float g = row_g;
+  if (a.zero_y) {
+    for (int64_t i = threadIdx.x; i < a.N; i += 256) a.Y[m * a.N + i] = 0.f;
+  }
+  // pass 2: rotate 2048-column chunks, one warp per chunk
+  for (int chunk = warp; chunk < a.chunks_per_row; chunk += 8) {
+    const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
+    const bool active = col0 < a.K;
+    float2 p[32];
+    if (active) {
+      const uint4* src = reinterpret_cast<const uint4*>(xr + col0);
+      const uint4* ss = reinterpret_cast<const uint4*>(a.signs + col0);
+      uint4 sw[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sw[q] = __ldg(ss + q);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(src + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w[4] = {sw[q].x, sw[q].y, sw[q].z, sw[q].w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int col = 16 * q + 4 * h + c;
+            const uint32_t sbit = ((w[h] >> (8 * c + 7)) & 1u) << 31;
+            float& v = (col & 1) ? p[col >> 1].y : p[col >> 1].x;
+            v = __uint_as_float(__float_as_uint(v) ^ sbit);
+          }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) p[j] = make_float2(0.f, 0.f);
+    }
+    fwht64_local(p);
+    fwht_cross_lanes(p, a.lanes_per_tile, lane);
+    if (!active) continue;
+    const float sc = a.inv_sqrt_tile * g;
+    const float2 sc2 = make_float2(sc, a.a2 ? sc * 1.7320508075688772f : sc);
+    uint32_t hw[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float2 v = mul2(p[j], sc2);
+      const __half2 h = __floats2half2_rn(v.x, v.y);
+      hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.Xt + m * a.K + col0);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) dst[q] = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
+  }
+}
+
+}  // namespace gemm
+}  // namespace lq
+
+using namespace lq;
+using namespace lq::gemm;
+
+namespace {
+
+constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+struct GemmWorkspace {
+  size_t xt, inv_g, f, total;
+};
+
+GemmWorkspace gemm_layout(int64_t M, int64_t N, int64_t K) {
+  GemmWorkspace w;
+  w.xt = 0;
+  w.inv_g = align256((size_t)M * (size_t)K * 2);
+  w.f = w.inv_g + align256((size_t)M * 4);
+  w.total = w.f + align256((size_t)N * 4);
+  return w;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, size_t esize, const void* base, uint64_t inner,
+                 uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * esize};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Split K so that the work units fill the GPU without a long tail.
+int choose_splits(int64_t tiles, int k_stages, int sms) {
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 8; ++s) {
+    if (k_stages / s < 8) break;
+    const int64_t units = tiles * s;
+    const double waves = (double)units / sms;
+    const double eff = waves / (double)((units + sms - 1) / sms) - 0.03 * (s - 1);
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
+  }
+  return best;
+}
+
+}  // namespace
+
+extern "C" size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return gemm_layout(M, N, K).total;
 }
 
 extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
                              const int8_t* signs_dev, int64_t N, int64_t K, int tile,
                              const uint16_t* X_dev, int64_t M, float* Y_dev, void* workspace_dev,
                              int32_t* dev_status_dev, void* stream) {
-  (void)lattice; (void)codes_dev; (void)scales_dev; (void)signs_dev; (void)N; (void)K; (void)tile;
-  (void)X_dev; (void)M; (void)Y_dev; (void)workspace_dev; (void)dev_status_dev; (void)stream;
-  return LQ_ERR_UNSUPPORTED;
+  lq_status st = validate_common(lattice, N, K, tile);
+  if (st != LQ_OK) return st;
+  if (M < 0) return LQ_ERR_SHAPE;
+  if (N % BM != 0 || K % BK != 0) return LQ_ERR_SHAPE;
+  if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31)) return LQ_ERR_SHAPE;
+  if (M == 0 || N == 0) return LQ_OK;
+  if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || X_dev == nullptr ||
+      Y_dev == nullptr || workspace_dev == nullptr)
+    return LQ_ERR_ARG;
+  if (!aligned16(codes_dev) || !aligned16(signs_dev) || !aligned16(X_dev) || !aligned16(Y_dev) ||
+      (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0 || !aligned4(scales_dev) ||
+      (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
+    return LQ_ERR_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int sms = device_sm_count();
+  if (sms <= 0) return LQ_ERR_CUDA;
+
+  const GemmWorkspace lay = gemm_layout(M, N, K);
+  char* ws = reinterpret_cast<char*>(workspace_dev);
+  __half* Xt = reinterpret_cast<__half*>(ws + lay.xt);
+  float* inv_g = reinterpret_cast<float*>(ws + lay.inv_g);
+  float* f = reinterpret_cast<float*>(ws + lay.f);
+
+  Args a;
+  a.M = M; a.N = N; a.K = K; a.tile = tile; a.tiles_per_row = (int)(K / tile);
+  a.n_tiles = (int)(N / BM);
+  a.m_tiles = (int)((M + BN - 1) / BN);
+  a.k_stages = (int)(K / BK);
+  a.splits = choose_splits((int64_t)a.n_tiles * a.m_tiles, a.k_stages, sms);
+  a.stages_per_split = (a.k_stages + a.splits - 1) / a.splits;
+  a.splits = (a.k_stages + a.stages_per_split - 1) / a.stages_per_split;
+  a.units = (int64_t)a.n_tiles * a.m_tiles * a.splits;
+  a.scales = scales_dev; a.f = f; a.inv_g = inv_g; a.Y = Y_dev; a.status = dev_status_dev;
+
+  PrepArgs p;
+  p.X = reinterpret_cast<const __nv_bfloat16*>(X_dev); p.signs = signs_dev; p.M = M; p.N = N; p.K = K;
+  p.tile = tile; p.lanes_per_tile = tile / kLaneElems; p.tiles_per_row = (int)(K / tile);
+  p.chunks_per_row = (int)((K + kChunkCols - 1) / kChunkCols);
+  p.inv_sqrt_tile = (float)(1.0 / sqrt((double)tile));
+  p.a2 = (lattice == LQ_A2);
+  p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.f = f; p.Y = Y_dev; p.zero_y = a.splits > 1;
+  p.status = dev_status_dev;
+  const int64_t prep_blocks = M + (N + 255) / 256;
+  gemm_prep_kernel<<<(unsigned)prep_blocks, 256, 0, s>>>(p);
+  st = check_launch();
+  if (st != LQ_OK) return st;
+
+  CUtensorMap map_codes, map_x;
+  if (!make_map_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, codes_dev, (uint64_t)K, (uint64_t)N, BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+    return LQ_ERR_CUDA;
+  if (!make_map_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, Xt, (uint64_t)K, (uint64_t)M, BK, BN,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+    return LQ_ERR_CUDA;
+
+  const size_t smem = sizeof(Smem) + 1024;
+  static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory budget");
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+      cudaGetLastError();
+      return LQ_ERR_CUDA;
+    }
+    attr_set = true;
+  }
+  const int64_t grid = a.units < sms ? a.units : sms;
+  gemm_kernel<<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
+  return check_launch();
 }

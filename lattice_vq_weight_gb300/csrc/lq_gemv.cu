@@ -229,86 +229,104 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
     xlp[n] = a.xl + (int64_t)(xok[n] ? bb : 0) * a.cols + 16 * q4;
   }
 
-  for (int t = t0; t < t1; ++t) {
-    float acc[RG][NB][4];
+  // Flattened (tile, step) loop with the loads of the next step issued before
+  // the MMAs of the current one (one step of software pipelining).
+  const int n_it = (t1 - t0) * steps;
+  uint4 cw[RG][2], xhv[NB][2], xlv[NB][2];
+  uint4 ncw[RG][2], nxh[NB][2], nxl[NB][2];
+  auto load_step = [&](int it, uint4 (&c)[RG][2], uint4 (&h)[NB][2], uint4 (&l)[NB][2]) {
+    const int t = t0 + it / steps;
+    const int64_t k0 = (int64_t)t * a.tile + (it % steps) * 64;
 #pragma unroll
     for (int i = 0; i < RG; ++i)
 #pragma unroll
-      for (int n = 0; n < NB; ++n)
+      for (int hh = 0; hh < 2; ++hh)
+        c[i][hh] = rowok[i][hh] ? __ldg(reinterpret_cast<const uint4*>(rowp[i][hh] + k0)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-
-    for (int st = 0; st < steps; ++st) {
-      const int64_t k0 = (int64_t)t * a.tile + st * 64;
-      uint4 cw[RG][2];
+    for (int n = 0; n < NB; ++n) {
+      if (xok[n]) {
+        const uint4* ph = reinterpret_cast<const uint4*>(xhp[n] + k0);
+        const uint4* pl = reinterpret_cast<const uint4*>(xlp[n] + k0);
+        h[n][0] = __ldg(ph); h[n][1] = __ldg(ph + 1);
+        l[n][0] = __ldg(pl); l[n][1] = __ldg(pl + 1);
+      } else {
+        h[n][0] = h[n][1] = l[n][0] = l[n][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  load_step(0, cw, xhv, xlv);
+  float acc[RG][NB][4];
+  for (int it = 0; it < n_it; ++it) {
+    const int st = it % steps;
+    const int t = t0 + it / steps;
+    if (it + 1 < n_it) load_step(it + 1, ncw, nxh, nxl);
+    if (st == 0) {
 #pragma unroll
       for (int i = 0; i < RG; ++i)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          cw[i][h] = rowok[i][h] ? __ldg(reinterpret_cast<const uint4*>(rowp[i][h] + k0)) : make_uint4(0, 0, 0, 0);
-      uint4 xhv[NB][2], xlv[NB][2];
+        for (int n = 0; n < NB; ++n)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t bh[NB][2], bl[NB][2];
 #pragma unroll
       for (int n = 0; n < NB; ++n) {
-        if (xok[n]) {
-          const uint4* ph = reinterpret_cast<const uint4*>(xhp[n] + k0);
-          const uint4* pl = reinterpret_cast<const uint4*>(xlp[n] + k0);
-          xhv[n][0] = __ldg(ph); xhv[n][1] = __ldg(ph + 1);
-          xlv[n][0] = __ldg(pl); xlv[n][1] = __ldg(pl + 1);
-        } else {
-          xhv[n][0] = xhv[n][1] = xlv[n][0] = xlv[n][1] = make_uint4(0, 0, 0, 0);
-        }
+        const uint4& H = xhv[n][c >> 1];
+        const uint4& Lw = xlv[n][c >> 1];
+        bh[n][0] = (c & 1) ? H.z : H.x;
+        bh[n][1] = (c & 1) ? H.w : H.y;
+        bl[n][0] = (c & 1) ? Lw.z : Lw.x;
+        bl[n][1] = (c & 1) ? Lw.w : Lw.y;
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t bh[NB][2], bl[NB][2];
+      for (int i = 0; i < RG; ++i) {
+        const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
+        const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
+        uint32_t a0, a2, a1, a3;
+        codes_to_f16x2(wa, a0, a2);
+        codes_to_f16x2(wb, a1, a3);
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
-          const uint4& H = xhv[n][c >> 1];
-          const uint4& L = xlv[n][c >> 1];
-          bh[n][0] = (c & 1) ? H.z : H.x;
-          bh[n][1] = (c & 1) ? H.w : H.y;
-          bl[n][0] = (c & 1) ? L.z : L.x;
-          bl[n][1] = (c & 1) ? L.w : L.y;
-        }
-#pragma unroll
-        for (int i = 0; i < RG; ++i) {
-          const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
-          const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
-          uint32_t a0, a2, a1, a3;
-          codes_to_f16x2(wa, a0, a2);
-          codes_to_f16x2(wb, a1, a3);
-#pragma unroll
-          for (int n = 0; n < NB; ++n) {
-            mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
-            mma16816(acc[i][n], a0, a1, a2, a3, bl[n][0], bl[n][1]);
-          }
+          mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
+          mma16816(acc[i][n], a0, a1, a2, a3, bl[n][0], bl[n][1]);
         }
       }
     }
-    // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
-    float fx[NB][2];
+    if (st == steps - 1) {
+      // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
+      float fx[NB][2];
 #pragma unroll
-    for (int n = 0; n < NB; ++n)
+      for (int n = 0; n < NB; ++n)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int bb = n * 8 + 2 * q4 + h;
-        fx[n][h] = (bb < a.batch) ? __ldg(a.xs + (int64_t)bb * a.tiles_per_row + t) : 0.f;
+        for (int h = 0; h < 2; ++h) {
+          const int bb = n * 8 + 2 * q4 + h;
+          fx[n][h] = (bb < a.batch) ? __ldg(a.xs + (int64_t)bb * a.tiles_per_row + t) : 0.f;
+        }
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        float sr[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t r = row0 + 16 * i + 8 * h + g;
+          sr[h] = rowok[i][h] ? __ldg(a.scales + r * a.tiles_per_row + t) : 0.f;
+        }
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          yacc[i][n][0] = fmaf(acc[i][n][0], sr[0] * fx[n][0], yacc[i][n][0]);
+          yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
+          yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
+          yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
+        }
       }
+    }
 #pragma unroll
-    for (int i = 0; i < RG; ++i) {
-      float sr[2];
+    for (int i = 0; i < RG; ++i) { cw[i][0] = ncw[i][0]; cw[i][1] = ncw[i][1]; }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t r = row0 + 16 * i + 8 * h + g;
-        sr[h] = rowok[i][h] ? __ldg(a.scales + r * a.tiles_per_row + t) : 0.f;
-      }
-#pragma unroll
-      for (int n = 0; n < NB; ++n) {
-        yacc[i][n][0] = fmaf(acc[i][n][0], sr[0] * fx[n][0], yacc[i][n][0]);
-        yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
-        yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
-        yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
-      }
+    for (int n = 0; n < NB; ++n) {
+      xhv[n][0] = nxh[n][0]; xhv[n][1] = nxh[n][1];
+      xlv[n][0] = nxl[n][0]; xlv[n][1] = nxl[n][1];
     }
   }
   const bool single = (a.splits == 1);
