@@ -144,6 +144,20 @@ __device__ __forceinline__ void add_to_byte(uint32_t& w0, uint32_t& w1, bool fix
 
 struct BlockCodes8 { uint32_t w0, w1; };
 
+// Keys are non-negative floats when their bit patterns are read as fp32 (bit
+// 31 is clear and the exponent field never reaches 255), so the three-input
+// float min/max of sm_100+ orders them exactly like unsigned integers.
+__device__ __forceinline__ uint32_t key_max3(uint32_t a, uint32_t b, uint32_t c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(__uint_as_float(a)), "f"(__uint_as_float(b)), "f"(__uint_as_float(c)));
+  return __float_as_uint(r);
+}
+__device__ __forceinline__ uint32_t key_min3(uint32_t a, uint32_t b, uint32_t c) {
+  float r;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(__uint_as_float(a)), "f"(__uint_as_float(b)), "f"(__uint_as_float(c)));
+  return __float_as_uint(r);
+}
+
 __device__ __forceinline__ int rint_int(uint32_t tbits) { return (int)(tbits - kRoundMagicBits); }
 
 // E8 = D8 u (D8 + 1/2).  Coset D8: f = rint(y), parity of sum(f), fix the
@@ -154,6 +168,7 @@ __device__ __forceinline__ int rint_int(uint32_t tbits) { return (int)(tbits - k
 //   dA = sum e^2              (+ 1 - 2 max|e| when sum f is odd)
 //   dB = sum e^2 + 2 - sum|e| (+ 2 min|e|     when sum f + #neg is odd)
 // and the D8 candidate is kept when dA <= dB.
+template <bool CHECK>
 __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& range) {
   const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
   float2 t[4], e[4];
@@ -165,23 +180,23 @@ __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& ran
     sq = fma2(e[j], e[j], sq);
   }
   const float dA0 = sq.x + sq.y;
-  uint32_t px = 0, sx = 0, keyA = 0, keyB = 0xFFFFFFFFu;
-  float sabs = 0.f, bmax = 0.f;
+  uint32_t px = 0, sx = 0, ka[8], kb[8];
+  float sabs = 0.f;
   uint32_t tb[8], eb[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float ei = (i & 1) ? e[i >> 1].y : e[i >> 1].x;
-    const float yi = (i & 1) ? y[i >> 1].y : y[i >> 1].x;
     tb[i] = __float_as_uint((i & 1) ? t[i >> 1].y : t[i >> 1].x);
     eb[i] = __float_as_uint(ei);
     px ^= tb[i];
     sx ^= eb[i];
     sabs += fabsf(ei);
-    bmax = fmaxf(bmax, fabsf(yi));
     const uint32_t rot = __funnelshift_l(eb[i], eb[i], 1);
-    keyA = max(keyA, (rot & 0xFFFFFFF1u) | (uint32_t)((7 - i) << 1));
-    keyB = min(keyB, (rot & 0xFFFFFFF1u) | (uint32_t)(i << 1));
+    ka[i] = (rot & 0xFFFFFFF1u) | (uint32_t)((7 - i) << 1);
+    kb[i] = (rot & 0xFFFFFFF1u) | (uint32_t)(i << 1);
   }
+  const uint32_t keyA = max(key_max3(ka[0], ka[1], ka[2]), key_max3(ka[3], ka[4], key_max3(ka[5], ka[6], ka[7])));
+  const uint32_t keyB = min(key_min3(kb[0], kb[1], kb[2]), key_min3(kb[3], kb[4], key_min3(kb[5], kb[6], kb[7])));
   const bool oddA = (px & 1u) != 0;
   const bool oddB = ((px ^ (sx >> 31)) & 1u) != 0;
   const float maxe = __uint_as_float((keyA >> 1) & 0x7FFFFFF8u);
@@ -209,18 +224,24 @@ __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& ran
   const int step = takeB ? (neg ? 2 : -2) : (neg ? -2 : 2);
   const bool fix = takeB ? oddB : oddA;
   add_to_byte(r.w0, r.w1, fix, k, step);
-  if (!(bmax < 62.5f)) {
+  if constexpr (CHECK) {
+    float bmax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int adj = takeB ? (((int32_t)eb[i] >> 31) | 1) : 0;
-      const int ci = 2 * rint_int(tb[i]) + adj + ((fix && i == k) ? step : 0);
-      range |= (ci > 127) || (ci < -127);
+    for (int j = 0; j < 4; ++j) bmax = fmaxf(bmax, fmaxf(fabsf(y[j].x), fabsf(y[j].y)));
+    if (!(bmax < 62.5f)) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int adj = takeB ? (((int32_t)eb[i] >> 31) | 1) : 0;
+        const int ci = 2 * rint_int(tb[i]) + adj + ((fix && i == k) ? step : 0);
+        range |= (ci > 127) || (ci < -127);
+      }
     }
   }
   return r;
 }
 
 // D4 = {x in Z^4 : sum even}: round, fix the worst coordinate when odd.
+template <bool CHECK>
 __device__ __forceinline__ uint32_t decode_d4(const float2 (&y)[2], bool& range) {
   const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
   uint32_t tb[4], px = 0, keyA = 0;
@@ -246,7 +267,7 @@ __device__ __forceinline__ uint32_t decode_d4(const float2 (&y)[2], bool& range)
   const int step = (keyA & 1u) ? -2 : 2;
   const bool fix = (px & 1u) != 0;
   add_to_byte(w, unused, fix, k, step);
-  if (!(bmax < 62.5f)) {
+  if (CHECK && !(bmax < 62.5f)) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int ci = 2 * rint_int(tb[i]) + ((fix && i == k) ? step : 0);
@@ -261,6 +282,7 @@ __device__ __forceinline__ uint32_t decode_d4(const float2 (&y)[2], bool& range)
 // e0^2 + 3 ez^2 for R, (1/2-|e0|)^2 + 3 (1/2-|ez|)^2 for the shifted coset
 // (R kept on equal distance).  Codes (2x, 2y/sqrt3) = (2 f0, 2 fz) or
 // (2 f0 +- 1, 2 fz +- 1), the +-1 toward the coordinate.  Returns 2 bytes.
+template <bool CHECK>
 __device__ __forceinline__ uint32_t decode_a2_pair(float2 y, bool& range) {
   const float z = y.y * 0.57735026918962576f;  // 1/sqrt(3)
   const float2 v = make_float2(y.x, z);
@@ -278,7 +300,7 @@ __device__ __forceinline__ uint32_t decode_a2_pair(float2 y, bool& range) {
   const uint32_t s1 = ((uint32_t)((int32_t)__float_as_uint(e.y) >> 31) | 1u) & bmask;
   const uint32_t c0 = t0 + t0 + s0;
   const uint32_t c1 = t1 + t1 + s1;
-  if (!(fmaxf(fabsf(y.x), fabsf(z)) < 62.5f)) {
+  if (CHECK && !(fmaxf(fabsf(y.x), fabsf(z)) < 62.5f)) {
     const int i0 = 2 * rint_int(t0) + (int)s0, i1 = 2 * rint_int(t1) + (int)s1;
     range |= (i0 > 127) || (i0 < -127) || (i1 > 127) || (i1 < -127);
   }
@@ -286,13 +308,14 @@ __device__ __forceinline__ uint32_t decode_a2_pair(float2 y, bool& range) {
 }
 
 // Z: c = 2 rint(y) for four coordinates.
+template <bool CHECK>
 __device__ __forceinline__ uint32_t decode_z1_quad(float2 a, float2 b, bool& range) {
   const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
   const float2 t0 = add2(a, M2), t1 = add2(b, M2);
   const uint32_t u0 = __float_as_uint(t0.x), u1 = __float_as_uint(t0.y);
   const uint32_t u2 = __float_as_uint(t1.x), u3 = __float_as_uint(t1.y);
   const float m = fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
-  if (!(m < 62.5f)) {
+  if (CHECK && !(m < 62.5f)) {
     const int mx = max(max(abs(rint_int(u0)), abs(rint_int(u1))), max(abs(rint_int(u2)), abs(rint_int(u3))));
     range |= (2 * mx > 127);
   }
@@ -300,14 +323,15 @@ __device__ __forceinline__ uint32_t decode_z1_quad(float2 a, float2 b, bool& ran
 }
 
 // Decode the 64 register-resident coordinates of one lane into 16 code words
-// (word w = columns 4w .. 4w+3).
-template <int LAT>
+// (word w = columns 4w .. 4w+3).  CHECK adds the exact int8 range check; it
+// can be left out when every |y| of the lane is known to be below 62.5.
+template <int LAT, bool CHECK>
 __device__ __forceinline__ void decode_lane(const float2 (&p)[32], uint32_t (&w)[16], bool& range) {
   if constexpr (LAT == LQ_E8) {
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const float2 y[4] = {p[4 * b], p[4 * b + 1], p[4 * b + 2], p[4 * b + 3]};
-      const BlockCodes8 r = decode_e8(y, range);
+      const BlockCodes8 r = decode_e8<CHECK>(y, range);
       w[2 * b] = r.w0;
       w[2 * b + 1] = r.w1;
     }
@@ -315,18 +339,18 @@ __device__ __forceinline__ void decode_lane(const float2 (&p)[32], uint32_t (&w)
 #pragma unroll
     for (int b = 0; b < 16; ++b) {
       const float2 y[2] = {p[2 * b], p[2 * b + 1]};
-      w[b] = decode_d4(y, range);
+      w[b] = decode_d4<CHECK>(y, range);
     }
   } else if constexpr (LAT == LQ_A2) {
 #pragma unroll
     for (int b = 0; b < 16; ++b) {
-      const uint32_t lo = decode_a2_pair(p[2 * b], range);
-      const uint32_t hi = decode_a2_pair(p[2 * b + 1], range);
+      const uint32_t lo = decode_a2_pair<CHECK>(p[2 * b], range);
+      const uint32_t hi = decode_a2_pair<CHECK>(p[2 * b + 1], range);
       w[b] = lo | (hi << 16);
     }
   } else {
 #pragma unroll
-    for (int b = 0; b < 16; ++b) w[b] = decode_z1_quad(p[2 * b], p[2 * b + 1], range);
+    for (int b = 0; b < 16; ++b) w[b] = decode_z1_quad<CHECK>(p[2 * b], p[2 * b + 1], range);
   }
 }
 

@@ -45,6 +45,9 @@ struct RotateArgs {
 
 template <bool BF16>
 __global__ void __launch_bounds__(256, 1) rotate_activation_kernel(RotateArgs a) {
+  // the GEMV that follows may start streaming codes now; it waits for this
+  // grid's results (griddepcontrol.wait) before reading them
+  asm volatile("griddepcontrol.launch_dependents;");
   const int lane = threadIdx.x & 31;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
@@ -155,8 +158,8 @@ struct GemvArgs {
   const __half* xl;
   const float* xs;
   float* y;
-  int splits, tiles_per_split;
-  int64_t tasks;
+  int64_t items;     // row groups x tiles per row
+  int64_t warps;     // warps of the persistent grid
 };
 
 // int8 codes (4 per word) -> two f16x2 words holding the exact values.
@@ -180,86 +183,187 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// One warp: RG groups of 16 rows x the tiles [t0, t1) of one split.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Work: items are (row group of 16 RG rows, tile) pairs in row-group-major
+// order; warp w of the persistent grid takes the contiguous item range
+// [w I / W, (w+1) I / W), so every warp streams the same number of code bytes.
+// A warp flushes its per-row sums whenever its range leaves a row group
+// (atomically when it did not cover the whole row).
+//
 // Fragment mapping (g = lane/4, q4 = lane%4): within a 64-column step the
 // thread loads 16 code bytes of rows g and g+8 at columns 16 q4 .. 16 q4 + 15;
 // MMA k-chunk c uses bytes 4c .. 4c+3, i.e. k-slots (2 q4, 2 q4+1, 2 q4+8,
 // 2 q4+9) hold columns 16 q4 + 4c + (0, 1, 2, 3).  The activation fragment of
 // column n = g uses the same permutation, so the dot products are unchanged.
-template <int NB, int RG>
-__global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
+//
+// Code loads go through a per-thread ring of S stages in shared memory filled
+// with cp.async (each thread reads back only what it copied, so the only wait
+// is cp.async.wait_group on its own copies).  The ring is filled before
+// griddepcontrol.wait: codes do not depend on the activation kernel that
+// precedes this one, so with programmatic dependent launch the code stream
+// starts while that kernel is still running.
+template <int NB, int RG, int S>
+__global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
+  constexpr int kCode = RG * 2;        // 16-byte code slots per thread per stage
+  static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
+  extern __shared__ uint4 gemv_ring[];
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q4 = lane & 3;
-  const int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (task >= a.tasks) return;
-  const int64_t rgrp = task / a.splits;
-  const int ks = (int)(task % a.splits);
-  const int t0 = ks * a.tiles_per_split;
-  const int t1 = min(a.tiles_per_row, t0 + a.tiles_per_split);
-  if (t0 >= t1) return;
-  const int64_t row0 = rgrp * 16 * RG;
+  uint4* ring = gemv_ring + (size_t)warp * S * kCode * 32;
+  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
+  const int64_t i0 = w * a.items / a.warps;
+  const int64_t i1 = (w + 1) * a.items / a.warps;
   const int steps = a.tile >> 6;
+  const int64_t n_it = (i1 - i0) * steps;
 
-  float yacc[RG][NB][4];
+  const bool xok0 = g < a.batch;
+  const bool xok1 = NB > 1 && 8 + g < a.batch;
+  const __half* xh0 = a.xh + (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
+  const __half* xl0 = a.xl + (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
+  const __half* xh1 = a.xh + (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
+  const __half* xl1 = a.xl + (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
+
+  // Position of a step in the warp's range, advanced one step at a time (no
+  // divisions inside the loop).
+  struct Cursor {
+    int64_t grp;
+    int t, st;
+  };
+  auto start_cursor = [&]() {
+    Cursor c;
+    c.grp = i0 / a.tiles_per_row;
+    c.t = (int)(i0 - c.grp * a.tiles_per_row);
+    c.st = 0;
+    return c;
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.st == steps) {
+      c.st = 0;
+      if (++c.t == a.tiles_per_row) { c.t = 0; ++c.grp; }
+    }
+  };
+  auto kof = [&](const Cursor& c) { return (int64_t)c.t * a.tile + c.st * 64; };
+  Cursor ci = start_cursor();   // next step to issue
+  Cursor cx = start_cursor();   // next step whose activations to load
+  Cursor cm = start_cursor();   // step being computed
+  // row pointers of the group the issue cursor is in (recomputed only when
+  // the cursor enters a new row group)
+  const int8_t* irow[RG][2];
+  bool iok[RG][2];
+  int64_t igrp = -1;
+  int istage = 0;                         // ring stage the next issue writes
+  auto issue = [&](int64_t it) {
+    if (it < n_it) {
+      if (ci.grp != igrp) {
+        igrp = ci.grp;
+#pragma unroll
+        for (int i = 0; i < RG; ++i)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t r = igrp * 16 * RG + 16 * i + 8 * h + g;
+            iok[i][h] = r < a.rows;
+            irow[i][h] = a.codes + (iok[i][h] ? r : 0) * a.cols + 16 * q4;
+          }
+      }
+      const int64_t k0 = kof(ci);
+      const uint32_t islot = ring_s + (uint32_t)((istage * kCode * 32 + lane) * 16);
+#pragma unroll
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          cp_async16(islot + (uint32_t)(((2 * i + h) * 32) * 16), irow[i][h] + k0, iok[i][h]);
+      istage = (istage + 1) & (S - 1);
+      advance(ci);
+    }
+    cp_async_commit();
+  };
+  auto load_x = [&](int64_t it, uint4 (&h)[NB][2], uint4 (&l)[NB][2]) {
+    if (it < n_it) {
+      const int64_t k0 = kof(cx);
+      if (xok0) {
+        h[0][0] = __ldg(reinterpret_cast<const uint4*>(xh0 + k0));
+        h[0][1] = __ldg(reinterpret_cast<const uint4*>(xh0 + k0) + 1);
+        l[0][0] = __ldg(reinterpret_cast<const uint4*>(xl0 + k0));
+        l[0][1] = __ldg(reinterpret_cast<const uint4*>(xl0 + k0) + 1);
+      }
+      if constexpr (NB > 1) {
+        if (xok1) {
+          h[1][0] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0));
+          h[1][1] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0) + 1);
+          l[1][0] = __ldg(reinterpret_cast<const uint4*>(xl1 + k0));
+          l[1][1] = __ldg(reinterpret_cast<const uint4*>(xl1 + k0) + 1);
+        }
+      }
+      advance(cx);
+    }
+  };
+
+  // code prefetch first (independent of the preceding kernel), then wait for it
+#pragma unroll
+  for (int it = 0; it < S - 1; ++it) issue(it);
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  float yacc[RG][NB][4], acc[RG][NB][4];
 #pragma unroll
   for (int i = 0; i < RG; ++i)
 #pragma unroll
     for (int n = 0; n < NB; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) yacc[i][n][c] = 0.f;
+  uint4 xhv[NB][2], xlv[NB][2], nxh[NB][2], nxl[NB][2];
+#pragma unroll
+  for (int n = 0; n < NB; ++n) xhv[n][0] = xhv[n][1] = xlv[n][0] = xlv[n][1] = nxh[n][0] = nxh[n][1] =
+      nxl[n][0] = nxl[n][1] = make_uint4(0, 0, 0, 0);
+  load_x(0, xhv, xlv);
+  int64_t cur_grp = -1;
+  int tiles_in_grp = 0;
 
-  const int8_t* rowp[RG][2];
-  bool rowok[RG][2];
-#pragma unroll
-  for (int i = 0; i < RG; ++i)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t r = row0 + 16 * i + 8 * h + g;
-      rowok[i][h] = r < a.rows;
-      rowp[i][h] = a.codes + (rowok[i][h] ? r : 0) * a.cols + 16 * q4;
-    }
-  const __half* xhp[NB];
-  const __half* xlp[NB];
-  bool xok[NB];
-#pragma unroll
-  for (int n = 0; n < NB; ++n) {
-    const int bb = n * 8 + g;
-    xok[n] = bb < a.batch;
-    xhp[n] = a.xh + (int64_t)(xok[n] ? bb : 0) * a.cols + 16 * q4;
-    xlp[n] = a.xl + (int64_t)(xok[n] ? bb : 0) * a.cols + 16 * q4;
-  }
-
-  // Flattened (tile, step) loop with the loads of the next step issued before
-  // the MMAs of the current one (one step of software pipelining).
-  const int n_it = (t1 - t0) * steps;
-  uint4 cw[RG][2], xhv[NB][2], xlv[NB][2];
-  uint4 ncw[RG][2], nxh[NB][2], nxl[NB][2];
-  auto load_step = [&](int it, uint4 (&c)[RG][2], uint4 (&h)[NB][2], uint4 (&l)[NB][2]) {
-    const int t = t0 + it / steps;
-    const int64_t k0 = (int64_t)t * a.tile + (it % steps) * 64;
+  auto flush = [&](int64_t grp, bool whole_row) {
 #pragma unroll
     for (int i = 0; i < RG; ++i)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-        c[i][hh] = rowok[i][hh] ? __ldg(reinterpret_cast<const uint4*>(rowp[i][hh] + k0)) : make_uint4(0, 0, 0, 0);
+      for (int n = 0; n < NB; ++n)
 #pragma unroll
-    for (int n = 0; n < NB; ++n) {
-      if (xok[n]) {
-        const uint4* ph = reinterpret_cast<const uint4*>(xhp[n] + k0);
-        const uint4* pl = reinterpret_cast<const uint4*>(xlp[n] + k0);
-        h[n][0] = __ldg(ph); h[n][1] = __ldg(ph + 1);
-        l[n][0] = __ldg(pl); l[n][1] = __ldg(pl + 1);
-      } else {
-        h[n][0] = h[n][1] = l[n][0] = l[n][1] = make_uint4(0, 0, 0, 0);
-      }
-    }
+        for (int c = 0; c < 4; ++c) {
+          const int64_t r = grp * 16 * RG + 16 * i + 8 * (c >> 1) + g;
+          const int bb = n * 8 + 2 * q4 + (c & 1);
+          if (r < a.rows && bb < a.batch) {
+            float* dst = a.y + (int64_t)bb * a.rows + r;
+            if (whole_row) *dst = yacc[i][n][c]; else atomicAdd(dst, yacc[i][n][c]);
+          }
+          yacc[i][n][c] = 0.f;
+        }
   };
-  load_step(0, cw, xhv, xlv);
-  float acc[RG][NB][4];
-  for (int it = 0; it < n_it; ++it) {
-    const int st = it % steps;
-    const int t = t0 + it / steps;
-    if (it + 1 < n_it) load_step(it + 1, ncw, nxh, nxl);
+
+  for (int64_t it = 0; it < n_it; ++it) {
+    issue(it + S - 1);
+    load_x(it + 1, nxh, nxl);
+    const int64_t grp = cm.grp;
+    const int t = cm.t;
+    const int st = cm.st;
+    advance(cm);
+    if (grp != cur_grp) {
+      if (cur_grp >= 0) flush(cur_grp, tiles_in_grp == a.tiles_per_row);
+      cur_grp = grp;
+      tiles_in_grp = 0;
+    }
+    cp_async_wait<S - 1>();
+    const uint4* slot = ring + (size_t)(it & (S - 1)) * kCode * 32 + lane;
+    uint4 cw[RG][2];
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+      cw[i][0] = slot[(2 * i) * 32];
+      cw[i][1] = slot[(2 * i + 1) * 32];
+    }
     if (st == 0) {
 #pragma unroll
       for (int i = 0; i < RG; ++i)
@@ -309,8 +413,8 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
         float sr[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int64_t r = row0 + 16 * i + 8 * h + g;
-          sr[h] = rowok[i][h] ? __ldg(a.scales + r * a.tiles_per_row + t) : 0.f;
+          const int64_t r = grp * 16 * RG + 16 * i + 8 * h + g;
+          sr[h] = (r < a.rows) ? __ldg(a.scales + r * a.tiles_per_row + t) : 0.f;
         }
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
@@ -320,30 +424,16 @@ __global__ void __launch_bounds__(256) gemv_kernel(GemvArgs a) {
           yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
         }
       }
+      ++tiles_in_grp;
     }
-#pragma unroll
-    for (int i = 0; i < RG; ++i) { cw[i][0] = ncw[i][0]; cw[i][1] = ncw[i][1]; }
 #pragma unroll
     for (int n = 0; n < NB; ++n) {
       xhv[n][0] = nxh[n][0]; xhv[n][1] = nxh[n][1];
       xlv[n][0] = nxl[n][0]; xlv[n][1] = nxl[n][1];
     }
   }
-  const bool single = (a.splits == 1);
-#pragma unroll
-  for (int i = 0; i < RG; ++i)
-#pragma unroll
-    for (int n = 0; n < NB; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int h = c >> 1;
-        const int64_t r = row0 + 16 * i + 8 * h + g;
-        const int bb = n * 8 + 2 * q4 + (c & 1);
-        if (r < a.rows && bb < a.batch) {
-          float* dst = a.y + (int64_t)bb * a.rows + r;
-          if (single) *dst = yacc[i][n][c]; else atomicAdd(dst, yacc[i][n][c]);
-        }
-      }
+  cp_async_wait<0>();
+  if (cur_grp >= 0) flush(cur_grp, tiles_in_grp == a.tiles_per_row);
 }
 
 }  // namespace lq
@@ -370,22 +460,42 @@ GemvWorkspace gemv_workspace_layout(int batch, int64_t cols, int tile) {
 
 template <int NB, int RG>
 lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
+  constexpr int S = 4;                       // ring stages per warp
+  constexpr int kWarps = 4;
+  constexpr size_t smem = (size_t)kWarps * S * (RG * 2) * 32 * 16;
   GemvArgs a = a0;
   static int per_sm = 0;
-  if (per_sm == 0) per_sm = occupancy_per_sm(gemv_kernel<NB, RG>, 256);
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(gemv_kernel<NB, RG, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return LQ_ERR_CUDA;
+    }
+    per_sm = occupancy_per_sm(gemv_kernel<NB, RG, S>, kWarps * 32, smem);
+  }
   const int sms = device_sm_count();
   if (sms <= 0) return LQ_ERR_CUDA;
   const int64_t groups = (a.rows + 16 * RG - 1) / (16 * RG);
-  const int64_t target = (int64_t)sms * per_sm * 8;  // one warp per task, one wave
-  int64_t splits = (target + groups - 1) / groups;
-  if (splits > a.tiles_per_row) splits = a.tiles_per_row;
-  if (splits < 1) splits = 1;
-  a.tiles_per_split = (int)((a.tiles_per_row + splits - 1) / splits);
-  a.splits = (int)((a.tiles_per_row + a.tiles_per_split - 1) / a.tiles_per_split);
-  a.tasks = groups * a.splits;
-  const int64_t grid = (a.tasks + 7) / 8;
-  gemv_kernel<NB, RG><<<(unsigned)grid, 256, 0, st>>>(a);
-  return check_launch();
+  a.items = groups * a.tiles_per_row;
+  int64_t ctas = (int64_t)sms * per_sm;
+  const int64_t need = (a.items + kWarps - 1) / kWarps;   // at least one item per warp
+  if (ctas > need) ctas = need;
+  a.warps = ctas * kWarps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel<NB, RG, S>, a) != cudaSuccess) {
+    cudaGetLastError();
+    return LQ_ERR_CUDA;
+  }
+  return LQ_OK;
 }
 
 }  // namespace
@@ -424,12 +534,11 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   r.xl = reinterpret_cast<__half*>(ws + lay.xl);
   r.xs = reinterpret_cast<float*>(ws + lay.xs);
   r.y = y_dev; r.y_elems = (int64_t)batch * rows; r.status = dev_status_dev;
+  // Few CTAs: one warp per (activation row, 2048-column chunk); they also zero
+  // y.  Keeping this grid small leaves the SMs free for the GEMV launched
+  // right after it (programmatic dependent launch).
   const int64_t units = (int64_t)batch * r.chunks_per_row;
-  const int sms = device_sm_count();
-  if (sms <= 0) return LQ_ERR_CUDA;
   int64_t rgrid = (units + 7) / 8;
-  const int64_t zgrid = (r.y_elems + 255) / 256;
-  if (rgrid < zgrid) rgrid = zgrid < sms ? zgrid : sms;
   if (rgrid < 1) rgrid = 1;
   if (xdtype == LQ_BF16) rotate_activation_kernel<true><<<(unsigned)rgrid, 256, 0, s>>>(r);
   else rotate_activation_kernel<false><<<(unsigned)rgrid, 256, 0, s>>>(r);
@@ -440,7 +549,7 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   g.codes = codes_dev; g.scales = scales_dev; g.rows = rows; g.cols = cols; g.tile = tile;
   g.tiles_per_row = (int)(cols / tile); g.batch = batch;
   g.xh = r.xh; g.xl = r.xl; g.xs = r.xs; g.y = y_dev;
-  g.splits = 1; g.tiles_per_split = g.tiles_per_row; g.tasks = 0;
+  g.items = 0; g.warps = 1;
   if (batch <= 8) return launch_gemv<1, 2>(g, s);
   return launch_gemv<2, 2>(g, s);
 }

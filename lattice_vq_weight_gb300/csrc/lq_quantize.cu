@@ -74,6 +74,38 @@ __device__ __forceinline__ void load_signs(LaneSigns<BF16>& s, const int8_t* sig
   }
 }
 
+// bf16 pair masks of one lane kept in shared memory: uint4 q of lane l at
+// msk[q * 32 + l] holds the masks of column pairs 4q .. 4q+3 (conflict-free).
+__device__ __forceinline__ void store_sign_masks(uint4* msk, int lane, const int8_t* signs_col0) {
+  const uint4* p = reinterpret_cast<const uint4*>(signs_col0);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 v = __ldg(p + q);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      // sign words 2hh, 2hh+1 of this 16-byte run cover column pairs 8q + 4hh .. +3
+      const uint32_t a = w[2 * hh], b = w[2 * hh + 1];
+      msk[(2 * q + hh) * 32 + lane] = make_uint4(__byte_perm(a, 0u, 0x1404) & 0x80008000u,
+                                                 __byte_perm(a, 0u, 0x3424) & 0x80008000u,
+                                                 __byte_perm(b, 0u, 0x1404) & 0x80008000u,
+                                                 __byte_perm(b, 0u, 0x3424) & 0x80008000u);
+    }
+  }
+}
+
+__device__ __forceinline__ void unpack_bf16_smem_signs(const LaneRaw<true>& r, const uint4* msk, int lane,
+                                                       float2 (&p)[32]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 m = msk[i * 32 + lane];
+    const uint32_t w[4] = {r.v[i].x ^ m.x, r.v[i].y ^ m.y, r.v[i].z ^ m.z, r.v[i].w ^ m.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
+  }
+}
+
 // Unpack raw input to fp32 pairs with the signs applied (exact).
 template <bool BF16>
 __device__ __forceinline__ void unpack_signed(const LaneRaw<BF16>& r, const LaneSigns<BF16>& s,
@@ -103,12 +135,20 @@ __device__ __forceinline__ void unpack_signed(const LaneRaw<BF16>& r, const Lane
   }
 }
 
+// ------------------------------------------------------------------ staging
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // ------------------------------------------------------------------ quantize
 struct QuantArgs {
   const void* W;
   int64_t rows, cols, ldw;
-  int tile, lanes_per_tile, tiles_per_row, chunks_per_row;
-  float beta, sqrt_tile;
+  int tile, tile_shift, lanes_per_tile, tiles_per_row, chunks_per_row;
+  float beta, sqrt_tile, inv_tile;
   const int8_t* signs;
   int8_t* codes;
   float* scales;
@@ -116,44 +156,91 @@ struct QuantArgs {
   int64_t units;
 };
 
+constexpr int kQuantThreads = 128;
+
+// Shared memory per warp: two stages of raw input (each lane copies its own
+// 64 columns with cp.async and later reads back only its own copies, so no
+// barrier is needed) and, for bf16, the lane's sign masks.
+template <bool BF16> struct QuantSmem {
+  static constexpr int kRawVec = BF16 ? 8 : 16;             // 16-byte vectors per lane per stage
+  static constexpr int kRawWords = 2 * kRawVec * 32;        // uint4 per warp, both stages
+  static constexpr int kMaskWords = BF16 ? 8 * 32 : 0;      // uint4 per warp
+  static constexpr int kPerWarp = kRawWords + kMaskWords;
+};
+
 template <int LAT, bool BF16>
-__global__ void __launch_bounds__(256, 1) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, 3) quantize_kernel(QuantArgs a) {
+  using SM = QuantSmem<BF16>;
+  extern __shared__ uint4 quant_smem[];
   const int lane = threadIdx.x & 31;
+  uint4* wsm = quant_smem + (threadIdx.x >> 5) * SM::kPerWarp;
+  uint4* raw_sm = wsm;                          // [stage][vec][lane]
+  uint4* msk = wsm + SM::kRawWords;             // bf16 sign masks [q][lane]
+  const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(raw_sm);
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   constexpr int kElemBytes = BF16 ? 2 : 4;
 
-  LaneSigns<BF16> sg;
+  LaneSigns<false> sg;     // fp32 input keeps its 64 sign bits in registers
   int cached_chunk = -1;
   bool range = false, nonfinite = false;
 
-  int64_t u = warp0;
-  LaneRaw<BF16> raw, nxt;
-  auto lane_col = [&](int64_t unit) -> int64_t {
-    return (unit % a.chunks_per_row) * kChunkCols + (int64_t)lane * kLaneElems;
+  // (row, chunk) of the current and next unit, advanced without divisions:
+  // unit u = row * chunks_per_row + chunk, and u grows by nwarps per step.
+  const int64_t d_row = nwarps / a.chunks_per_row;
+  const int d_chunk = (int)(nwarps % a.chunks_per_row);
+  int64_t row = warp0 / a.chunks_per_row;
+  int chunk = (int)(warp0 % a.chunks_per_row);
+  auto next_pos = [&](int64_t& r, int& c) {
+    r += d_row;
+    c += d_chunk;
+    if (c >= a.chunks_per_row) { c -= a.chunks_per_row; ++r; }
   };
-  auto lane_ptr = [&](int64_t unit) -> const char* {
-    const int64_t row = unit / a.chunks_per_row;
-    return reinterpret_cast<const char*>(a.W) + (row * a.ldw + lane_col(unit)) * kElemBytes;
+  auto lane_ptr = [&](int64_t r, int c) -> const char* {
+    return reinterpret_cast<const char*>(a.W) +
+           (r * a.ldw + (int64_t)c * kChunkCols + (int64_t)lane * kLaneElems) * kElemBytes;
   };
-  if (u < a.units && lane_col(u) < a.cols) load_raw<BF16>(raw, lane_ptr(u));
+  // copy the lane's 64 input columns of unit (r, c) into stage st
+  auto stage_in = [&](int64_t r, int c, int st) {
+    if (r < a.rows && (int64_t)c * kChunkCols + (int64_t)lane * kLaneElems < a.cols) {
+      const char* src = lane_ptr(r, c);
+#pragma unroll
+      for (int i = 0; i < SM::kRawVec; ++i)
+        cp_async16(raw_s + (uint32_t)(((st * SM::kRawVec + i) * 32 + lane) * 16), src + 16 * i);
+    }
+    cp_async_commit();
+  };
+  int stage = 0;
+  stage_in(row, chunk, 0);
 
-  for (; u < a.units; u += nwarps) {
-    const int64_t un = u + nwarps;
-    if (un < a.units && lane_col(un) < a.cols) load_raw<BF16>(nxt, lane_ptr(un));
+  for (; row < a.rows; ) {
+    int64_t nrow = row;
+    int nchunk = chunk;
+    next_pos(nrow, nchunk);
+    stage_in(nrow, nchunk, stage ^ 1);
 
-    const int chunk = (int)(u % a.chunks_per_row);
-    const int64_t row = u / a.chunks_per_row;
     const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
     const bool active = col0 < a.cols;
     if (chunk != cached_chunk) {
-      if constexpr (!BF16) { sg.bits[0] = 0; sg.bits[1] = 0; }
-      if (active) load_signs<BF16>(sg, a.signs + col0);
+      if constexpr (BF16) {
+        if (active) store_sign_masks(msk, lane, a.signs + col0);
+      } else {
+        sg.bits[0] = 0;
+        sg.bits[1] = 0;
+        if (active) load_signs<false>(sg, a.signs + col0);
+      }
       cached_chunk = chunk;
     }
+    cp_async_wait1();   // this unit's copies have landed
 
     float2 p[32];
-    unpack_signed<BF16>(raw, sg, p);
+    {
+      LaneRaw<BF16> raw;
+#pragma unroll
+      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[(stage * SM::kRawVec + i) * 32 + lane];
+      if constexpr (BF16) unpack_bf16_smem_signs(raw, msk, lane, p);
+      else unpack_signed<false>(raw, sg, p);
+    }
     fwht64_local(p);
     fwht_cross_lanes(p, a.lanes_per_tile, lane);
 
@@ -163,16 +250,20 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(QuantArgs a) {
     for (int j = 0; j < 32; ++j) acc = fma2(p[j], p[j], acc);
     const float U = tile_lane_sum(acc.x + acc.y, a.lanes_per_tile);
     const bool finite = isfinite(U);
-    float s = a.beta * sqrtf(U) * (1.0f / (float)a.tile);
+    float s = a.beta * sqrtf(U) * a.inv_tile;
     if (!finite) s = 0.f;
     const float k = (s > 0.f) ? 1.0f / (s * a.sqrt_tile) : 0.f;
     const float2 k2 = make_float2(k, k);
 #pragma unroll
     for (int j = 0; j < 32; ++j) p[j] = mul2(p[j], k2);
 
+    // sum of y^2 over this lane bounds every |y| of the lane: below 62.5^2 no
+    // code can leave int8 and the per-block range check is skipped
+    const float lane_y2 = (acc.x + acc.y) * (k * k);
     uint32_t w[16];
     bool r = false;
-    decode_lane<LAT>(p, w, r);
+    if (lane_y2 < 3906.25f) decode_lane<LAT, false>(p, w, r);
+    else decode_lane<LAT, true>(p, w, r);
 
     if (active) {
       range |= r;
@@ -181,10 +272,13 @@ __global__ void __launch_bounds__(256, 1) quantize_kernel(QuantArgs a) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
       if ((lane & (a.lanes_per_tile - 1)) == 0)
-        a.scales[row * a.tiles_per_row + col0 / a.tile] = s;
+        a.scales[row * a.tiles_per_row + (col0 >> a.tile_shift)] = s;
     }
-    raw = nxt;
+    row = nrow;
+    chunk = nchunk;
+    stage ^= 1;
   }
+  cp_async_wait0();
   if (__any_sync(0xffffffffu, range) && lane == 0) raise_flag(a.status, LQ_DEV_RANGE);
   if (__any_sync(0xffffffffu, nonfinite) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
 }
@@ -297,11 +391,19 @@ extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_de
 
 template <int LAT, bool BF16>
 static lq_status launch_quantize(const QuantArgs& a, cudaStream_t st) {
+  constexpr size_t smem = (size_t)(kQuantThreads / 32) * QuantSmem<BF16>::kPerWarp * sizeof(uint4);
   static int per_sm = 0;
-  if (per_sm == 0) per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16>, 256);
-  const int grid = persistent_grid(a.units, 8, a.chunks_per_row, per_sm);
+  if (per_sm == 0) {
+    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return LQ_ERR_CUDA;
+    }
+    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16>, kQuantThreads, smem);
+  }
+  const int grid = persistent_grid(a.units, kQuantThreads / 32, a.chunks_per_row, per_sm);
   if (grid <= 0) return LQ_ERR_CUDA;
-  quantize_kernel<LAT, BF16><<<grid, 256, 0, st>>>(a);
+  quantize_kernel<LAT, BF16><<<grid, kQuantThreads, smem, st>>>(a);
   return check_launch();
 }
 
@@ -330,9 +432,10 @@ extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int
 
   QuantArgs a;
   a.W = W_dev; a.rows = rows; a.cols = cols; a.ldw = ldw;
-  a.tile = tile; a.lanes_per_tile = tile / kLaneElems; a.tiles_per_row = (int)(cols / tile);
+  a.tile = tile; a.tile_shift = __builtin_ctz((unsigned)tile);
+  a.lanes_per_tile = tile / kLaneElems; a.tiles_per_row = (int)(cols / tile);
   a.chunks_per_row = (int)((cols + kChunkCols - 1) / kChunkCols);
-  a.beta = beta; a.sqrt_tile = sqrtf((float)tile);
+  a.beta = beta; a.sqrt_tile = sqrtf((float)tile); a.inv_tile = 1.0f / (float)tile;
   a.signs = signs_dev; a.codes = codes_dev; a.scales = scales_dev; a.status = dev_status_dev;
   a.units = rows * a.chunks_per_row;
   const bool bf = (wdtype == LQ_BF16);

@@ -1,0 +1,77 @@
+"""Small, fixed launch sequences of the liblq kernels for profiler captures.
+
+    python -m lattice_vq_weight_gb300.profile_case quantize   # the 7 Llama-3-8B layer matrices
+    python -m lattice_vq_weight_gb300.profile_case gemv --batch 1
+    python -m lattice_vq_weight_gb300.profile_case gemm --M 256
+
+Each op runs `--reps` passes (default 2) after building inputs on the device;
+the second pass is the one to capture (`ncu -s <launches of one pass>`).
+Inputs: bf16 N(0, 0.02^2) weights of the Llama-3-8B layer shapes (gate-shaped
+only with --gate-only), E8, tile 256, beta 0.25; activations N(0, 1) bf16;
+GEMM on the 8192 x 28672 Llama-3-70B up-like shape with X of M rows.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("op", choices=("quantize", "gemv", "gemm"))
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--M", type=int, default=256)
+    ap.add_argument("--reps", type=int, default=2)
+    ap.add_argument("--gate-only", action="store_true")
+    args = ap.parse_args(argv)
+
+    import torch
+    import lattice_vq_weight_gb300 as L
+    from synthetic import LLAMA3_8B_LAYER
+
+    dev = torch.device("cuda")
+    gen = torch.Generator(device=dev).manual_seed(0)
+    if args.op == "gemm":
+        N, K = 8192, 28672
+        W = (torch.randn((N, K), device=dev, generator=gen) * 0.015).to(torch.bfloat16)
+        codes, scales, signs = L.quantize(W, "e8", 256, 4000, 0.25)
+        del W
+        X = torch.randn((args.M, K), device=dev, generator=gen).to(torch.bfloat16)
+        Y = torch.empty((args.M, N), dtype=torch.float32, device=dev)
+        ws = torch.empty(L.lq_gemm_workspace_size(args.M, N, K), dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            L.lq_gemm("e8", codes, scales, signs, 256, X, Y, ws)
+        torch.cuda.synchronize()
+        print("ok")
+        return
+    shapes = [s for s in LLAMA3_8B_LAYER if (not args.gate_only or s[0] == "gate")]
+    mats = []
+    for _, r, c in shapes:
+        W = (torch.randn((r, c), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        codes = torch.empty((r, c), dtype=torch.int8, device=dev)
+        scales = torch.empty((r, c // 256), dtype=torch.float32, device=dev)
+        signs = torch.empty((c,), dtype=torch.int8, device=dev)
+        L.lq_quantize("e8", W, 256, 1, 0.25, codes, scales, signs)
+        x = torch.randn((args.batch, c), device=dev, generator=gen).to(torch.bfloat16)
+        y = torch.empty((args.batch, r), dtype=torch.float32, device=dev)
+        mats.append((W, codes, scales, signs, x, y))
+    ws = torch.empty(max(L.lq_gemv_workspace_size(args.batch, c, 256) for _, _, c in shapes),
+                     dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    for _ in range(args.reps):
+        for W, codes, scales, signs, x, y in mats:
+            if args.op == "quantize":
+                L.lq_quantize("e8", W, 256, 1, 0.25, codes, scales, signs)
+            else:
+                L.lq_gemv("e8", codes, scales, signs, 256, x, y, ws)
+    torch.cuda.synchronize()
+    print("ok")
+
+
+if __name__ == "__main__":
+    main()
