@@ -14,15 +14,20 @@
 //  2. gemm_kernel: persistent, warp-specialised CTA (one per SM) computing a
 //     128 (weight rows) x 256 (tokens) output tile with
 //       tcgen05.mma.cta_group::1.kind::f16  (A = decoded weights, B = X~, D fp32 in TMEM)
-//     warp 0      TMA producer: int8 code tile [128 x 64] and X~ tile [256 x 64]
+//     warp 0      TMA producer of int8 code tiles [128 x 64] (8-stage ring: the
+//                 codes come from HBM, so this ring is the deep one)
+//     warp 14     TMA producer of X~ tiles [256 x 64] (4-stage ring, mostly L2)
 //     warp 1      allocates TMEM, one lane issues the MMAs
-//     warps 2..5  decoders: codes -> fp16 (c * s[n,t] * f_n / 2) written to
-//                 shared memory in the 128-byte-swizzled K-major layout
-//     warps 6..9  epilogue: tcgen05.ld of the accumulator, Y = D / (f_n g_m)
-//   Shared memory holds 3 stages; TMEM holds two 256-column accumulators so
-//   the epilogue of one tile overlaps the main loop of the next.  Every
-//   mbarrier wait is bounded (about a second of clock cycles); on expiry the
-//   kernel records LQ_DEV_TIMEOUT and winds down.
+//     warps 2..9  decoders (two per SM sub-partition; two 16-code chunks per
+//                 thread per stage): codes -> fp16 (c * s[n,t] * f_n / 2)
+//                 written to a 2-stage ring of A tiles in the 128-byte-swizzled
+//                 K-major layout
+//     warps 10..13 epilogue: tcgen05.ld of the accumulator, Y = D / (f_n g_m)
+//   Each ring has its own full/empty mbarriers, so code loads run far ahead of
+//   the MMAs.  TMEM holds two 256-column accumulators so the epilogue of one
+//   tile overlaps the main loop of the next.  Every mbarrier wait is bounded
+//   (about a second of clock cycles); on expiry the kernel records
+//   LQ_DEV_TIMEOUT and winds down.
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -41,28 +46,37 @@ namespace gemm {
 constexpr int BM = 128;            // weight rows per tile (MMA M)
 constexpr int BN = 256;            // tokens per tile (MMA N)
 constexpr int BK = 64;             // K per pipeline stage
-constexpr int kStages = 3;
+constexpr int kCodeStages = 8;     // int8 code ring (TMA -> decoders)
+constexpr int kXStages = 4;        // X~ ring (TMA -> MMA): covers the L2 latency of a 32 KB tile
+constexpr int kAStages = 2;        // decoded-weight ring (decoders -> MMA)
 constexpr int kCodeBytes = BM * BK;          // int8 codes per stage:   8 KB
 constexpr int kABytes = BM * BK * 2;         // fp16 decoded weights:   16 KB
 constexpr int kXBytes = BN * BK * 2;         // fp16 activations:       32 KB
-constexpr int kThreads = 320;                // 10 warps
-constexpr int kDecodeThreads = 128;
+constexpr int kDecodeWarps = 8;
+constexpr int kDecodeThreads = kDecodeWarps * 32;   // warps 2 .. 2 + kDecodeWarps - 1
+constexpr int kEpiWarp0 = 2 + kDecodeWarps;         // four epilogue warps
+constexpr int kXWarp = kEpiWarp0 + 4;               // X~ producer
+constexpr int kThreads = (kXWarp + 1) * 32;
+constexpr int kDecodePasses = BM * BK / 16 / kDecodeThreads;  // 16-code chunks per thread per stage
+static_assert(kDecodePasses * kDecodeThreads * 16 == BM * BK, "decoders cover the code tile");
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
 constexpr long long kWaitCycles = 2000000000ll;  // about one second
 
-struct Smem;
 struct Smem {
   // stage buffers come first and are 1024-byte aligned (128-byte swizzle atoms)
-  alignas(1024) uint8_t x[kStages][kXBytes];
-  alignas(1024) uint8_t a[kStages][kABytes];
-  alignas(1024) uint8_t codes[kStages][kCodeBytes];
-  alignas(8) uint64_t full[kStages];      // TMA bytes landed (codes + X~)
-  alignas(8) uint64_t decoded[kStages];   // decoders wrote A
-  alignas(8) uint64_t empty[kStages];     // MMAs finished reading the stage
-  alignas(8) uint64_t tmem_full[2];       // accumulator ready for the epilogue
-  alignas(8) uint64_t tmem_empty[2];      // epilogue drained the accumulator
-  alignas(8) uint64_t drain;              // all issued MMAs complete (teardown)
+  alignas(1024) uint8_t x[kXStages][kXBytes];
+  alignas(1024) uint8_t a[kAStages][kABytes];
+  alignas(1024) uint8_t codes[kCodeStages][kCodeBytes];
+  alignas(8) uint64_t full_c[kCodeStages];    // code tile landed
+  alignas(8) uint64_t empty_c[kCodeStages];   // decoders finished reading it
+  alignas(8) uint64_t full_x[kXStages];       // X~ tile landed
+  alignas(8) uint64_t empty_x[kXStages];      // MMAs finished reading it
+  alignas(8) uint64_t full_a[kAStages];       // decoders wrote the A tile
+  alignas(8) uint64_t empty_a[kAStages];      // MMAs finished reading it
+  alignas(8) uint64_t tmem_full[2];           // accumulator ready for the epilogue
+  alignas(8) uint64_t tmem_empty[2];          // epilogue drained the accumulator
+  alignas(8) uint64_t drain;                  // all issued MMAs complete (teardown)
   uint32_t tmem_base;
   int timeout;
 };
@@ -178,10 +192,17 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
   volatile int* timeout = &sm.timeout;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.decoded[s], kDecodeThreads);
-      mbar_init(&sm.empty[s], 1);
+    for (int i = 0; i < kCodeStages; ++i) {
+      mbar_init(&sm.full_c[i], 1);
+      mbar_init(&sm.empty_c[i], kDecodeThreads);
+    }
+    for (int i = 0; i < kXStages; ++i) {
+      mbar_init(&sm.full_x[i], 1);
+      mbar_init(&sm.empty_x[i], 1);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&sm.full_a[i], kDecodeThreads);
+      mbar_init(&sm.empty_a[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tmem_full[i], 1);
@@ -201,34 +222,46 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  // unit u -> (n tile, m tile, K split) and its K-stage range
+  auto unit_range = [&](int64_t u, int& nt, int& mt, int& k0, int& k1) {
+    nt = (int)(u % a.n_tiles);
+    const int64_t rest = u / a.n_tiles;
+    mt = (int)(rest % a.m_tiles);
+    const int sp = (int)(rest / a.m_tiles);
+    k0 = sp * a.stages_per_split;
+    k1 = min(a.k_stages, k0 + a.stages_per_split);
+  };
+
+  if (warp == 0 || warp == kXWarp) {
+    // ------------------------------------------------------------ TMA producers
+    // warp 0 streams code tiles, the last warp streams X~ tiles; each owns one ring.
     if (lane == 0) {
+      const bool codes_side = (warp == 0);
+      const int depth = codes_side ? kCodeStages : kXStages;
+      uint64_t* full = codes_side ? sm.full_c : sm.full_x;
+      uint64_t* empty = codes_side ? sm.empty_c : sm.empty_x;
+      const uint32_t bytes = codes_side ? kCodeBytes : kXBytes;
       int s = 0;
       uint32_t ph = 0;
       int64_t issued = 0;
       for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x) {
-        const int nt = (int)(u % a.n_tiles);
-        const int64_t rest = u / a.n_tiles;
-        const int mt = (int)(rest % a.m_tiles);
-        const int sp = (int)(rest / a.m_tiles);
-        const int k0 = sp * a.stages_per_split;
-        const int k1 = min(a.k_stages, k0 + a.stages_per_split);
+        int nt, mt, k0, k1;
+        unit_range(u, nt, mt, k0, k1);
         for (int ks = k0; ks < k1; ++ks) {
-          if (!mbar_wait(&sm.empty[s], ph ^ 1, timeout)) break;
-          mbar_arrive_expect_tx(&sm.full[s], kCodeBytes + kXBytes);
-          tma_load_2d(sm.codes[s], &map_codes, &sm.full[s], ks * BK, nt * BM);
-          tma_load_2d(sm.x[s], &map_x, &sm.full[s], ks * BK, mt * BN);
+          if (!mbar_wait(&empty[s], ph ^ 1, timeout)) break;
+          mbar_arrive_expect_tx(&full[s], bytes);
+          if (codes_side) tma_load_2d(sm.codes[s], &map_codes, &full[s], ks * BK, nt * BM);
+          else tma_load_2d(sm.x[s], &map_x, &full[s], ks * BK, mt * BN);
           ++issued;
-          if (++s == kStages) { s = 0; ph ^= 1; }
+          if (++s == depth) { s = 0; ph ^= 1; }
         }
       }
       if (*timeout) {
         // let the copies already in flight land before the CTA exits (bounded)
-        for (int i = 0; i < kStages && i < issued; ++i) {
-          if (--s < 0) { s = kStages - 1; ph ^= 1; }
+        for (int i = 0; i < depth && i < issued; ++i) {
+          if (--s < 0) { s = depth - 1; ph ^= 1; }
           const long long t0 = clock64();
-          while (!mbar_try_wait(&sm.full[s], ph) && clock64() - t0 < kWaitCycles) {
+          while (!mbar_try_wait(&full[s], ph) && clock64() - t0 < kWaitCycles) {
           }
         }
       }
@@ -236,14 +269,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
+      int sa = 0, sx = 0;
+      uint32_t pha = 0, phx = 0;
       int it = 0;
       for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x, ++it) {
-        const int64_t rest = u / a.n_tiles;
-        const int sp = (int)(rest / a.m_tiles);
-        const int k0 = sp * a.stages_per_split;
-        const int k1 = min(a.k_stages, k0 + a.stages_per_split);
+        int nt, mt, k0, k1;
+        unit_range(u, nt, mt, k0, k1);
         const int acc = it & 1;
         const uint32_t acc_ph = (uint32_t)((it >> 1) & 1);
         if (!mbar_wait(&sm.tmem_empty[acc], acc_ph ^ 1, timeout)) break;
@@ -251,56 +282,75 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
         bool ok = true;
         for (int ks = k0; ks < k1; ++ks) {
-          if (!mbar_wait(&sm.decoded[s], ph, timeout)) { ok = false; break; }
+          if (!mbar_wait(&sm.full_a[sa], pha, timeout) || !mbar_wait(&sm.full_x[sx], phx, timeout)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sm.a[s]);
-          const uint32_t x_addr = smem_u32(sm.x[s]);
+          const uint32_t a_addr = smem_u32(sm.a[sa]);
+          const uint32_t x_addr = smem_u32(sm.x[sx]);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             mma_f16(d_tmem, sw128_desc(a_addr + kk * 32), sw128_desc(x_addr + kk * 32),
                     (ks > k0 || kk > 0) ? 1u : 0u);
           }
-          mma_commit(&sm.empty[s]);
-          if (++s == kStages) { s = 0; ph ^= 1; }
+          mma_commit(&sm.empty_a[sa]);
+          mma_commit(&sm.empty_x[sx]);
+          if (++sa == kAStages) { sa = 0; pha ^= 1; }
+          if (++sx == kXStages) { sx = 0; phx ^= 1; }
         }
         if (!ok) break;
         mma_commit(&sm.tmem_full[acc]);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ decoders
-    const int d = threadIdx.x - 64;          // 0..127
-    const int rsub = d >> 2;                 // row within a 32-row pass
+    const int d = threadIdx.x - 64;          // 0 .. kDecodeThreads - 1
+    const int rsub = d >> 2;                 // row within a pass
     const int c4 = d & 3;                    // 16-code chunk within the 64-code stage row
-    int s = 0;
-    uint32_t ph = 0;
+    const int stages_per_t = a.tile / BK;
+    int sc = 0, sa = 0;
+    uint32_t phc = 0, pha = 0;
     for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x) {
-      const int nt = (int)(u % a.n_tiles);
-      const int64_t rest = u / a.n_tiles;
-      const int sp = (int)(rest / a.m_tiles);
-      const int k0 = sp * a.stages_per_split;
-      const int k1 = min(a.k_stages, k0 + a.stages_per_split);
-      float fr[4];
+      int nt, mt, k0, k1;
+      unit_range(u, nt, mt, k0, k1);
+      constexpr int P = kDecodePasses;
+      constexpr int kRowsPerPass = kDecodeThreads / 4;
+      float fr[P];
+      const float* srow[P];
 #pragma unroll
-      for (int p = 0; p < 4; ++p) fr[p] = 0.5f * __ldg(a.f + (int64_t)nt * BM + 32 * p + rsub);
-      __half2 sf[4];
-      int cur_t = -1;
+      for (int p = 0; p < P; ++p) {
+        const int64_t row = (int64_t)nt * BM + kRowsPerPass * p + rsub;
+        fr[p] = 0.5f * __ldg(a.f + row);
+        srow[p] = a.scales + row * a.tiles_per_row;
+      }
+      // scales of the current tile and (prefetched) of the next one
+      float s_cur[P], s_nxt[P];
+      int t_cur = k0 / stages_per_t;
+#pragma unroll
+      for (int p = 0; p < P; ++p) s_cur[p] = __ldg(srow[p] + t_cur);
+#pragma unroll
+      for (int p = 0; p < P; ++p) s_nxt[p] = (t_cur + 1 < a.tiles_per_row) ? __ldg(srow[p] + t_cur + 1) : 0.f;
+      __half2 sf[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) sf[p] = __float2half2_rn(s_cur[p] * fr[p]);
       for (int ks = k0; ks < k1; ++ks) {
-        if (!mbar_wait(&sm.full[s], ph, timeout)) break;
-        const int t = (ks * BK) / a.tile;
-        if (t != cur_t) {
+        const int t = ks / stages_per_t;
+        if (t != t_cur) {
+          t_cur = t;
 #pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const int64_t row = (int64_t)nt * BM + 32 * p + rsub;
-            sf[p] = __float2half2_rn(__ldg(a.scales + row * a.tiles_per_row + t) * fr[p]);
+          for (int p = 0; p < P; ++p) {
+            sf[p] = __float2half2_rn(s_nxt[p] * fr[p]);
+            s_nxt[p] = (t + 1 < a.tiles_per_row) ? __ldg(srow[p] + t + 1) : 0.f;
           }
-          cur_t = t;
         }
-        const uint8_t* cbase = sm.codes[s];
-        uint8_t* abase = sm.a[s];
+        if (!mbar_wait(&sm.full_c[sc], phc, timeout)) break;
+        if (!mbar_wait(&sm.empty_a[sa], pha ^ 1, timeout)) break;
+        const uint8_t* cbase = sm.codes[sc];
+        uint8_t* abase = sm.a[sa];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          const int r = 32 * p + rsub;
+        for (int p = 0; p < P; ++p) {
+          const int r = kRowsPerPass * p + rsub;
           const uint4 cw = *reinterpret_cast<const uint4*>(cbase + r * BK + 16 * c4);
           const uint32_t w[4] = {cw.x ^ 0x80808080u, cw.y ^ 0x80808080u, cw.z ^ 0x80808080u, cw.w ^ 0x80808080u};
           uint32_t o[8];
@@ -314,9 +364,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
           *reinterpret_cast<uint4*>(abase + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<uint4*>(abase + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
+        mbar_arrive(&sm.empty_c[sc]);             // code tile consumed
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&sm.decoded[s]);
-        if (++s == kStages) { s = 0; ph ^= 1; }
+        mbar_arrive(&sm.full_a[sa]);              // A tile ready for the tensor cores
+        if (++sc == kCodeStages) { sc = 0; phc ^= 1; }
+        if (++sa == kAStages) { sa = 0; pha ^= 1; }
       }
     }
   } else {
@@ -326,9 +378,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
     int it = 0;
     for (int64_t u = blockIdx.x; u < a.units; u += gridDim.x, ++it) {
       if (__any_sync(0xffffffffu, *timeout != 0)) break;
-      const int nt = (int)(u % a.n_tiles);
-      const int64_t rest = u / a.n_tiles;
-      const int mt = (int)(rest % a.m_tiles);
+      int nt, mt, k0, k1;
+      unit_range(u, nt, mt, k0, k1);
       const int acc = it & 1;
       const uint32_t acc_ph = (uint32_t)((it >> 1) & 1);
       const bool ready = mbar_wait(&sm.tmem_full[acc], acc_ph, timeout);
@@ -392,16 +443,22 @@ struct PrepArgs {
   int32_t* status;
 };
 
-// Blocks [0, M): one token row each.  Blocks [M, M + ceil(N/256)): weight-row
-// factors, one thread per row.
-__global__ void __launch_bounds__(256, 1) gemm_prep_kernel(PrepArgs a) {
-  __shared__ float red[8];
+// Blocks [0, M): one token row each (16 warps: the row's 2048-column chunks
+// are rotated in one round for K up to 32768).  Blocks [M, M + ceil(N/16)):
+// weight-row factors, one warp per row.
+constexpr int kPrepThreads = 512;
+constexpr int kPrepWarps = kPrepThreads / 32;
+
+__global__ void __launch_bounds__(kPrepThreads, 1) gemm_prep_kernel(PrepArgs a) {
+  __shared__ float red[kPrepWarps];
   __shared__ float row_g;
   if (blockIdx.x >= a.M) {
-    const int64_t n = (int64_t)(blockIdx.x - a.M) * 256 + threadIdx.x;
+    const int64_t n = (int64_t)(blockIdx.x - a.M) * kPrepWarps + (threadIdx.x >> 5);
+    const int ln = threadIdx.x & 31;
     if (n >= a.N) return;
     float mx = 0.f;
-    for (int t = 0; t < a.tiles_per_row; ++t) mx = fmaxf(mx, __ldg(a.scales + n * a.tiles_per_row + t));
+    for (int t = ln; t < a.tiles_per_row; t += 32) mx = fmaxf(mx, __ldg(a.scales + n * a.tiles_per_row + t));
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     // |p s| <= 63.5 s; choose f = 2^e with 63.5 * max(s) * f in [2^14, 2^15)
     float fv = 1.f;
     if (mx > 0.f && isfinite(mx)) {
@@ -410,7 +467,7 @@ __global__ void __launch_bounds__(256, 1) gemm_prep_kernel(PrepArgs a) {
       const int ex = max(-126, min(127, 15 - E));
       fv = __uint_as_float((uint32_t)(ex + 127) << 23);
     }
-    a.f[n] = fv;
+    if (ln == 0) a.f[n] = fv;
     return;
   }
   const int64_t m = blockIdx.x;
@@ -418,7 +475,7 @@ __global__ void __launch_bounds__(256, 1) gemm_prep_kernel(PrepArgs a) {
   const __nv_bfloat16* xr = a.X + m * a.K;
   // pass 1: max |x| over the row
   float mx = 0.f;
-  for (int64_t i = (int64_t)threadIdx.x * 8; i < a.K; i += 256 * 8) {
+  for (int64_t i = (int64_t)threadIdx.x * 8; i < a.K; i += kPrepThreads * 8) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(xr + i));
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -430,7 +487,7 @@ __global__ void __launch_bounds__(256, 1) gemm_prep_kernel(PrepArgs a) {
   __syncthreads();
   if (threadIdx.x == 0) {
     float v = 0.f;
-    for (int i = 0; i < 8; ++i) v = fmaxf(v, red[i]);
+    for (int i = 0; i < kPrepWarps; ++i) v = fmaxf(v, red[i]);
     // |x~| <= sqrt(T) max|x| (times sqrt 3 for A2): g = 2^e with that bound in [2^13, 2^14]
     float gv = 1.f;
     if (!isfinite(v)) {
@@ -447,10 +504,10 @@ __global__ void __launch_bounds__(256, 1) gemm_prep_kernel(PrepArgs a) {
   __syncthreads();
   const float g = row_g;
   if (a.zero_y) {
-    for (int64_t i = threadIdx.x; i < a.N; i += 256) a.Y[m * a.N + i] = 0.f;
+    for (int64_t i = threadIdx.x; i < a.N; i += kPrepThreads) a.Y[m * a.N + i] = 0.f;
   }
   // pass 2: rotate 2048-column chunks, one warp per chunk
-  for (int chunk = warp; chunk < a.chunks_per_row; chunk += 8) {
+  for (int chunk = warp; chunk < a.chunks_per_row; chunk += kPrepWarps) {
     const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
     const bool active = col0 < a.K;
     float2 p[32];
@@ -625,8 +682,8 @@ extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* 
   p.a2 = (lattice == LQ_A2);
   p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.f = f; p.Y = Y_dev; p.zero_y = a.splits > 1;
   p.status = dev_status_dev;
-  const int64_t prep_blocks = M + (N + 255) / 256;
-  gemm_prep_kernel<<<(unsigned)prep_blocks, 256, 0, s>>>(p);
+  const int64_t prep_blocks = M + (N + kPrepWarps - 1) / kPrepWarps;
+  gemm_prep_kernel<<<(unsigned)prep_blocks, kPrepThreads, 0, s>>>(p);
   st = check_launch();
   if (st != LQ_OK) return st;
 
