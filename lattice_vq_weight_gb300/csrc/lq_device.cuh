@@ -168,6 +168,13 @@ __device__ __forceinline__ int rint_int(uint32_t tbits) { return (int)(tbits - k
 //   dA = sum e^2              (+ 1 - 2 max|e| when sum f is odd)
 //   dB = sum e^2 + 2 - sum|e| (+ 2 min|e|     when sum f + #neg is odd)
 // and the D8 candidate is kept when dA <= dB.
+// a * b + c on the integer multiply-add path
+__device__ __forceinline__ uint32_t imad(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
 template <bool CHECK>
 __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& range) {
   const float2 M2 = make_float2(kRoundMagic, kRoundMagic);
@@ -180,7 +187,7 @@ __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& ran
     sq = fma2(e[j], e[j], sq);
   }
   const float dA0 = sq.x + sq.y;
-  uint32_t px = 0, sx = 0, ka[8], kb[8];
+  uint32_t px = 0, sx = 0, key[8];
   float sabs = 0.f;
   uint32_t tb[8], eb[8];
 #pragma unroll
@@ -192,11 +199,13 @@ __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& ran
     sx ^= eb[i];
     sabs += fabsf(ei);
     const uint32_t rot = __funnelshift_l(eb[i], eb[i], 1);
-    ka[i] = (rot & 0xFFFFFFF1u) | (uint32_t)((7 - i) << 1);
-    kb[i] = (rot & 0xFFFFFFF1u) | (uint32_t)(i << 1);
+    key[i] = (rot & 0xFFFFFFF1u) | (uint32_t)((7 - i) << 1);
   }
-  const uint32_t keyA = max(key_max3(ka[0], ka[1], ka[2]), key_max3(ka[3], ka[4], key_max3(ka[5], ka[6], ka[7])));
-  const uint32_t keyB = min(key_min3(kb[0], kb[1], kb[2]), key_min3(kb[3], kb[4], key_min3(kb[5], kb[6], kb[7])));
+  // One key per coordinate serves both searches: the largest key is the worst
+  // D8 residual (lowest index on ties); the smallest is the worst D8+1/2
+  // residual (highest index on exact ties -- an equally distant point).
+  const uint32_t keyA = max(key_max3(key[0], key[1], key[2]), key_max3(key[3], key[4], key_max3(key[5], key[6], key[7])));
+  const uint32_t keyB = min(key_min3(key[0], key[1], key[2]), key_min3(key[3], key[4], key_min3(key[5], key[6], key[7])));
   const bool oddA = (px & 1u) != 0;
   const bool oddB = ((px ^ (sx >> 31)) & 1u) != 0;
   const float maxe = __uint_as_float((keyA >> 1) & 0x7FFFFFF8u);
@@ -204,21 +213,19 @@ __device__ __forceinline__ BlockCodes8 decode_e8(const float2 (&y)[4], bool& ran
   const float dA = oddA ? dA0 + fmaf(-2.f, maxe, 1.f) : dA0;
   const float dB = (dA0 + 2.f - sabs) + (oddB ? 2.f * mine : 0.f);
   const bool takeB = dB < dA;
-  // codes: 2 f (low byte of 2 * bits(t)), plus +-1 toward y for the half coset
-  const uint32_t bmask = takeB ? 0xFFFFFFFFu : 0u;
+  // code byte: 2 f for D8; for D8 + 1/2, 2 f + 1 - 2 [e < 0] (the sign of e is
+  // bit 0 of the key) -- built with two multiply-adds
+  const uint32_t bs = takeB ? 1u : 0u;
   uint32_t c[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t adj = ((uint32_t)((int32_t)eb[i] >> 31) | 1u) & bmask;
-    c[i] = tb[i] + tb[i] + adj;
-  }
+  for (int i = 0; i < 8; ++i) c[i] = imad(tb[i], 2u, imad(key[i] & bs, 0xFFFFFFFEu, bs));
   BlockCodes8 r;
   r.w0 = pack4(c[0], c[1], c[2], c[3]);
   r.w1 = pack4(c[4], c[5], c[6], c[7]);
   // parity fix of the chosen coset
-  const uint32_t key = takeB ? keyB : keyA;
-  const int k = takeB ? (int)((keyB >> 1) & 7u) : 7 - (int)((keyA >> 1) & 7u);
-  const bool neg = (key & 1u) != 0;
+  const uint32_t kk = takeB ? keyB : keyA;
+  const int k = 7 - (int)((kk >> 1) & 7u);
+  const bool neg = (kk & 1u) != 0;
   // D8: rounding the other way moves toward y, +1 when e >= 0.
   // D8 + 1/2: e' = e - copysign(1/2, e) has the opposite sign of e.
   const int step = takeB ? (neg ? 2 : -2) : (neg ? -2 : 2);
