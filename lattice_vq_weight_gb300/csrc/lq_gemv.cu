@@ -43,8 +43,14 @@ struct RotateArgs {
   int32_t* status;
 };
 
+// One thread per 16 consecutive columns of one activation row: the tile of T
+// columns spans T/16 consecutive lanes (T <= 512), so the transform is 4
+// register butterfly stages plus log2(T/16) shuffle stages -- a short
+// dependent chain, since this kernel sits in front of every GEMV.
+constexpr int kRotElems = 16;
+
 template <bool BF16>
-__global__ void __launch_bounds__(256, 1) rotate_activation_kernel(RotateArgs a) {
+__global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   // the GEMV that follows may start streaming codes now; it waits for this
   // grid's results (griddepcontrol.wait) before reading them
   asm volatile("griddepcontrol.launch_dependents;");
@@ -53,98 +59,98 @@ __global__ void __launch_bounds__(256, 1) rotate_activation_kernel(RotateArgs a)
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = gtid; i < a.y_elems; i += nthreads) a.y[i] = 0.f;
 
-  const int64_t warp0 = gtid >> 5, nwarps = nthreads >> 5;
-  const int64_t units = (int64_t)a.batch * a.chunks_per_row;
-  bool bad = false;
-  for (int64_t u = warp0; u < units; u += nwarps) {
-    const int64_t b = u / a.chunks_per_row;
-    const int chunk = (int)(u % a.chunks_per_row);
-    const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    const bool active = col0 < a.cols;
-    float2 p[32];
-    if (active) {
-      uint4 sw[4];
-      const uint4* ss = reinterpret_cast<const uint4*>(a.signs + col0);
+  const int64_t per_row = a.cols / kRotElems;
+  const int64_t work = (int64_t)a.batch * per_row;
+  const int lpt = a.tile / kRotElems;                    // lanes per tile
+  // every lane of a warp takes part in the shuffles; lanes past the end work on zeros
+  const bool active = gtid < work;
+  const int64_t b = active ? gtid / per_row : 0;
+  const int64_t col0 = active ? (gtid - b * per_row) * kRotElems : 0;
+  float v[kRotElems];
+  if (active) {
+    const uint4 sw = __ldg(reinterpret_cast<const uint4*>(a.signs + col0));
+    const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
+    if constexpr (BF16) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sw[q] = __ldg(ss + q);
-      if constexpr (BF16) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(src + i);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
-          }
-        }
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 v = __ldg(src + i);
-          p[2 * i] = make_float2(v.x, v.y);
-          p[2 * i + 1] = make_float2(v.z, v.w);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t w[4] = {sw[q].x, sw[q].y, sw[q].z, sw[q].w};
+      for (int i = 0; i < 2; ++i) {
+        const uint4 q = __ldg(src + i);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col = 16 * q + 4 * h + c;
-            const uint32_t sb = ((w[h] >> (8 * c + 7)) & 1u) << 31;
-            float& v = (col & 1) ? p[col >> 1].y : p[col >> 1].x;
-            v = __uint_as_float(__float_as_uint(v) ^ sb);
-          }
+          v[8 * i + 2 * h] = __uint_as_float(w[h] << 16);
+          v[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
         }
       }
     } else {
+      const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) p[j] = make_float2(0.f, 0.f);
+      for (int i = 0; i < 4; ++i) {
+        const float4 q = __ldg(src + i);
+        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+      }
     }
-    fwht64_local(p);
-    fwht_cross_lanes(p, a.lanes_per_tile, lane);
-    const float sc = a.post_scale;
-    const float2 sc2 = make_float2(sc, a.a2 ? sc * 1.7320508075688772f : sc);
-    float m = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      p[j] = mul2(p[j], sc2);
-      m = fmaxf(m, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
+    for (int c = 0; c < kRotElems; ++c) {
+      const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
+      v[c] = __uint_as_float(__float_as_uint(v[c]) ^ sbit);
     }
-    m = tile_lane_max(m, a.lanes_per_tile);
-    float f = 1.f;
-    if (!isfinite(m)) {
-      bad = active;
-    } else if (m > 0.f) {
-      const int E = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 126;  // m in [2^(E-1), 2^E)
-      const int ex = max(-126, min(127, 15 - E));
-      f = __uint_as_float((uint32_t)(ex + 127) << 23);
-    }
-    if (!active) continue;
-    const float2 f2 = make_float2(f, f);
-    uint32_t hw[32], lw[32];
+  } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float2 v = mul2(p[j], f2);
-      const __half2 h = __floats2half2_rn(v.x, v.y);
+    for (int c = 0; c < kRotElems; ++c) v[c] = 0.f;
+  }
+  // unnormalised Walsh-Hadamard over the 16 register columns
+#pragma unroll
+  for (int h = 1; h < kRotElems; h <<= 1)
+#pragma unroll
+    for (int c = 0; c < kRotElems; ++c)
+      if ((c & h) == 0) {
+        const float x0 = v[c], x1 = v[c + h];
+        v[c] = x0 + x1;
+        v[c + h] = x0 - x1;
+      }
+  // remaining stages across the lanes of the tile
+  for (int m = 1; m < lpt; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int c = 0; c < kRotElems; ++c) v[c] = fmaf(v[c], sgn, __shfl_xor_sync(0xffffffffu, v[c], m));
+  }
+  const float sc = a.post_scale;
+  const float sc_odd = a.a2 ? sc * 1.7320508075688772f : sc;
+  float mx = 0.f;
+#pragma unroll
+  for (int c = 0; c < kRotElems; ++c) {
+    v[c] *= (c & 1) ? sc_odd : sc;
+    mx = fmaxf(mx, fabsf(v[c]));
+  }
+  for (int m = 1; m < lpt; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+  float f = 1.f;
+  bool bad = false;
+  if (!isfinite(mx)) {
+    bad = active;
+  } else if (mx > 0.f) {
+    const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 126;  // mx in [2^(E-1), 2^E)
+    const int ex = max(-126, min(127, 15 - E));
+    f = __uint_as_float((uint32_t)(ex + 127) << 23);
+  }
+  if (active) {
+    uint32_t hw[8], lw[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float x0 = v[2 * j] * f, x1 = v[2 * j + 1] * f;
+      const __half2 h = __floats2half2_rn(x0, x1);
       const float2 hf = __half22float2(h);
-      const __half2 l = __floats2half2_rn(v.x - hf.x, v.y - hf.y);
+      const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
       hw[j] = *reinterpret_cast<const uint32_t*>(&h);
       lw[j] = *reinterpret_cast<const uint32_t*>(&l);
     }
     uint4* dh = reinterpret_cast<uint4*>(a.xh + b * a.cols + col0);
     uint4* dl = reinterpret_cast<uint4*>(a.xl + b * a.cols + col0);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      dh[q] = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
-      dl[q] = make_uint4(lw[4 * q], lw[4 * q + 1], lw[4 * q + 2], lw[4 * q + 3]);
-    }
-    if ((lane & (a.lanes_per_tile - 1)) == 0) a.xs[b * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
+    dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+    dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+    if ((lane & (lpt - 1)) == 0) a.xs[b * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
 }
@@ -534,11 +540,13 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   r.xl = reinterpret_cast<__half*>(ws + lay.xl);
   r.xs = reinterpret_cast<float*>(ws + lay.xs);
   r.y = y_dev; r.y_elems = (int64_t)batch * rows; r.status = dev_status_dev;
-  // Few CTAs: one warp per (activation row, 2048-column chunk); they also zero
-  // y.  Keeping this grid small leaves the SMs free for the GEMV launched
-  // right after it (programmatic dependent launch).
-  const int64_t units = (int64_t)batch * r.chunks_per_row;
-  int64_t rgrid = (units + 7) / 8;
+  // One thread per 16 activation columns (a few CTAs), which also zero y;
+  // the small grid leaves the SMs free for the GEMV launched right after it
+  // (programmatic dependent launch).
+  const int64_t rot_threads = (int64_t)batch * (cols / kRotElems);
+  int64_t rgrid = (rot_threads + 255) / 256;
+  const int64_t zgrid = ((int64_t)batch * rows + 256 * 16 - 1) / (256 * 16);
+  if (rgrid < zgrid) rgrid = zgrid;
   if (rgrid < 1) rgrid = 1;
   if (xdtype == LQ_BF16) rotate_activation_kernel<true><<<(unsigned)rgrid, 256, 0, s>>>(r);
   else rotate_activation_kernel<false><<<(unsigned)rgrid, 256, 0, s>>>(r);
