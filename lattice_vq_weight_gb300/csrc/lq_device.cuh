@@ -109,6 +109,49 @@ __device__ __forceinline__ float tile_lane_max(float v, int lanes_per_tile) {
   return v;
 }
 
+// Unnormalised Walsh-Hadamard transform of one tile spread over `lpt`
+// consecutive lanes (lpt a power of two <= 32) holding 16 consecutive columns
+// each: 4 register stages, then log2(lpt) shuffle stages.  Used for
+// activations, where a short dependent chain matters more than lanes.
+__device__ __forceinline__ void fwht16_tile(float (&v)[16], int lpt, int lane) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      if ((c & h) == 0) {
+        const float x0 = v[c], x1 = v[c + h];
+        v[c] = x0 + x1;
+        v[c + h] = x0 - x1;
+      }
+  for (int m = 1; m < lpt; m <<= 1) {
+    const float sgn = (lane & m) ? -1.0f : 1.0f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v[c] = fmaf(v[c], sgn, __shfl_xor_sync(0xffffffffu, v[c], m));
+  }
+}
+
+// 16 bf16 activations (32 bytes) with the column signs applied (exact).
+__device__ __forceinline__ void load16_bf16_signed(const void* src, const int8_t* signs, float (&v)[16]) {
+  const uint4 sw = __ldg(reinterpret_cast<const uint4*>(signs));
+  const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 q = __ldg(p + i);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      v[8 * i + 2 * h] = __uint_as_float(w[h] << 16);
+      v[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
+    v[c] = __uint_as_float(__float_as_uint(v[c]) ^ sbit);
+  }
+}
+
 // ---------------------------------------------------------------- code packing
 // Low bytes of four ints into one word (byte i = low byte of ci).
 __device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {

@@ -443,13 +443,13 @@ struct PrepArgs {
   int32_t* status;
 };
 
-// Blocks [0, M): one token row each (16 warps: the row's 2048-column chunks
-// are rotated in one round for K up to 32768).  Blocks [M, M + ceil(N/16)):
-// weight-row factors, one warp per row.
+// Blocks [0, M): one token row each (max |x| over the row, then the rotation
+// with 16 columns per thread).  Blocks [M, M + ceil(N/16)): weight-row
+// factors, one warp per row.
 constexpr int kPrepThreads = 512;
 constexpr int kPrepWarps = kPrepThreads / 32;
 
-__global__ void __launch_bounds__(kPrepThreads, 1) gemm_prep_kernel(PrepArgs a) {
+__global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
   __shared__ float red[kPrepWarps];
   __shared__ float row_g;
   if (blockIdx.x >= a.M) {
@@ -506,57 +506,35 @@ __global__ void __launch_bounds__(kPrepThreads, 1) gemm_prep_kernel(PrepArgs a) 
   if (a.zero_y) {
     for (int64_t i = threadIdx.x; i < a.N; i += kPrepThreads) a.Y[m * a.N + i] = 0.f;
   }
-  // pass 2: rotate 2048-column chunks, one warp per chunk
-  for (int chunk = warp; chunk < a.chunks_per_row; chunk += kPrepWarps) {
-    const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    const bool active = col0 < a.K;
-    float2 p[32];
+  // pass 2: rotate, 16 consecutive columns per thread (a tile spans T/16 lanes
+  // of one warp; 512 threads cover 8192 columns per round)
+  const int lpt = a.tile / 16;
+  const int64_t groups = a.K / 16;
+  const float sc = a.inv_sqrt_tile * g;
+  const float sc_odd = a.a2 ? sc * 1.7320508075688772f : sc;
+  for (int64_t base = 0; base < groups; base += kPrepThreads) {
+    const int64_t j = base + threadIdx.x;
+    const bool active = j < groups;            // groups is a multiple of lpt: whole tiles
+    const int64_t col0 = (active ? j : 0) * 16;
+    float v[16];
     if (active) {
-      const uint4* src = reinterpret_cast<const uint4*>(xr + col0);
-      const uint4* ss = reinterpret_cast<const uint4*>(a.signs + col0);
-      uint4 sw[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) sw[q] = __ldg(ss + q);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-          p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t w[4] = {sw[q].x, sw[q].y, sw[q].z, sw[q].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int col = 16 * q + 4 * h + c;
-            const uint32_t sbit = ((w[h] >> (8 * c + 7)) & 1u) << 31;
-            float& v = (col & 1) ? p[col >> 1].y : p[col >> 1].x;
-            v = __uint_as_float(__float_as_uint(v) ^ sbit);
-          }
-      }
+      load16_bf16_signed(xr + col0, a.signs + col0, v);
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) p[j] = make_float2(0.f, 0.f);
+      for (int c = 0; c < 16; ++c) v[c] = 0.f;
     }
-    fwht64_local(p);
-    fwht_cross_lanes(p, a.lanes_per_tile, lane);
-    if (!active) continue;
-    const float sc = a.inv_sqrt_tile * g;
-    const float2 sc2 = make_float2(sc, a.a2 ? sc * 1.7320508075688772f : sc);
-    uint32_t hw[32];
+    fwht16_tile(v, lpt, lane);
+    if (active) {
+      uint32_t hw[8];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float2 v = mul2(p[j], sc2);
-      const __half2 h = __floats2half2_rn(v.x, v.y);
-      hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+      for (int q = 0; q < 8; ++q) {
+        const __half2 h = __floats2half2_rn(v[2 * q] * sc, v[2 * q + 1] * sc_odd);
+        hw[q] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.Xt + m * a.K + col0);
+      dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.Xt + m * a.K + col0);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) dst[q] = make_uint4(hw[4 * q], hw[4 * q + 1], hw[4 * q + 2], hw[4 * q + 3]);
   }
 }
 

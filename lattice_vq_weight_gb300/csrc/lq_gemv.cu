@@ -68,53 +68,28 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   const int64_t col0 = active ? (gtid - b * per_row) * kRotElems : 0;
   float v[kRotElems];
   if (active) {
-    const uint4 sw = __ldg(reinterpret_cast<const uint4*>(a.signs + col0));
-    const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
     if constexpr (BF16) {
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const uint4 q = __ldg(src + i);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          v[8 * i + 2 * h] = __uint_as_float(w[h] << 16);
-          v[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
-        }
-      }
+      load16_bf16_signed(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0, a.signs + col0, v);
     } else {
+      const uint4 sw = __ldg(reinterpret_cast<const uint4*>(a.signs + col0));
+      const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
       const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float4 q = __ldg(src + i);
         v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
       }
-    }
 #pragma unroll
-    for (int c = 0; c < kRotElems; ++c) {
-      const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
-      v[c] = __uint_as_float(__float_as_uint(v[c]) ^ sbit);
+      for (int c = 0; c < kRotElems; ++c) {
+        const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
+        v[c] = __uint_as_float(__float_as_uint(v[c]) ^ sbit);
+      }
     }
   } else {
 #pragma unroll
     for (int c = 0; c < kRotElems; ++c) v[c] = 0.f;
   }
-  // unnormalised Walsh-Hadamard over the 16 register columns
-#pragma unroll
-  for (int h = 1; h < kRotElems; h <<= 1)
-#pragma unroll
-    for (int c = 0; c < kRotElems; ++c)
-      if ((c & h) == 0) {
-        const float x0 = v[c], x1 = v[c + h];
-        v[c] = x0 + x1;
-        v[c + h] = x0 - x1;
-      }
-  // remaining stages across the lanes of the tile
-  for (int m = 1; m < lpt; m <<= 1) {
-    const float sgn = (lane & m) ? -1.0f : 1.0f;
-#pragma unroll
-    for (int c = 0; c < kRotElems; ++c) v[c] = fmaf(v[c], sgn, __shfl_xor_sync(0xffffffffu, v[c], m));
-  }
+  fwht16_tile(v, lpt, lane);
   const float sc = a.post_scale;
   const float sc_odd = a.a2 ? sc * 1.7320508075688772f : sc;
   float mx = 0.f;
