@@ -98,7 +98,7 @@ lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_dev, void* st
  *   lattice   LQ_E8 / LQ_D4 / LQ_A2 / LQ_Z1
  *   W_dev     [rows x ldw] elements of type wdtype (LQ_BF16 or LQ_F32);
  *             ldw >= cols and ldw * sizeof(elem) % 16 == 0
- *   tile      128, 256 or 512 (cols % tile == 0)
+ *   tile      128, 256, 512, 1024 or 2048 (cols % tile == 0)
  *   seed      signs are generated from it into signs_dev (int8 [cols], written)
  *   beta      > 0
  *   codes_dev int8 [rows x cols] (written, row stride cols)
@@ -193,7 +193,7 @@ size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * tcgen05 tensor cores accumulate in fp32.
  *   codes_dev int8 [N x K], scales_dev float32 [N x K/tile], signs_dev int8 [K]
  *   X_dev     bf16 [M x K] (raw 16-bit patterns), row stride K
- *   tile      128, 256 or 512;  N % 128 == 0;  K % tile == 0;  M >= 0
+ *   tile      128, 256, 512, 1024 or 2048;  N % 128 == 0;  K % tile == 0;  M >= 0
  *   Y_dev     float32 [M x N] (overwritten)
  *   workspace_dev  lq_gemm_workspace_size(M, N, K) bytes, 256-byte aligned
  *   dev_status_dev  int32 status word or NULL (LQ_DEV_NONFINITE for a

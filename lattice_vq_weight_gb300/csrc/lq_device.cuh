@@ -110,14 +110,16 @@ __device__ __forceinline__ float tile_lane_max(float v, int lanes_per_tile) {
 }
 
 // Unnormalised Walsh-Hadamard transform of one tile spread over `lpt`
-// consecutive lanes (lpt a power of two <= 32) holding 16 consecutive columns
-// each: 4 register stages, then log2(lpt) shuffle stages.  Used for
-// activations, where a short dependent chain matters more than lanes.
-__device__ __forceinline__ void fwht16_tile(float (&v)[16], int lpt, int lane) {
+// consecutive lanes (lpt a power of two <= 32) holding E consecutive columns
+// each: log2(E) register stages, then log2(lpt) shuffle stages.  Used for
+// activations (E = 16 up to 512-column tiles, E = T/32 above), where a short
+// dependent chain matters more than lanes.
+template <int E>
+__device__ __forceinline__ void fwht_tile(float (&v)[E], int lpt, int lane) {
 #pragma unroll
-  for (int h = 1; h < 16; h <<= 1)
+  for (int h = 1; h < E; h <<= 1)
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
+    for (int c = 0; c < E; ++c)
       if ((c & h) == 0) {
         const float x0 = v[c], x1 = v[c + h];
         v[c] = x0 + x1;
@@ -126,17 +128,29 @@ __device__ __forceinline__ void fwht16_tile(float (&v)[16], int lpt, int lane) {
   for (int m = 1; m < lpt; m <<= 1) {
     const float sgn = (lane & m) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) v[c] = fmaf(v[c], sgn, __shfl_xor_sync(0xffffffffu, v[c], m));
+    for (int c = 0; c < E; ++c) v[c] = fmaf(v[c], sgn, __shfl_xor_sync(0xffffffffu, v[c], m));
   }
 }
 
-// 16 bf16 activations (32 bytes) with the column signs applied (exact).
-__device__ __forceinline__ void load16_bf16_signed(const void* src, const int8_t* signs, float (&v)[16]) {
-  const uint4 sw = __ldg(reinterpret_cast<const uint4*>(signs));
-  const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
+// E consecutive bf16 (or fp32) activations with the column signs applied (exact).
+template <int E>
+__device__ __forceinline__ void apply_signs(const int8_t* signs, float (&v)[E]) {
+#pragma unroll
+  for (int q = 0; q < E / 16; ++q) {
+    const uint4 sw = __ldg(reinterpret_cast<const uint4*>(signs) + q);
+    const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
+      v[16 * q + c] = __uint_as_float(__float_as_uint(v[16 * q + c]) ^ sbit);
+    }
+  }
+}
+template <int E>
+__device__ __forceinline__ void load_bf16_signed(const void* src, const int8_t* signs, float (&v)[E]) {
   const uint4* p = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < E / 8; ++i) {
     const uint4 q = __ldg(p + i);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -145,12 +159,21 @@ __device__ __forceinline__ void load16_bf16_signed(const void* src, const int8_t
       v[8 * i + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
     }
   }
-#pragma unroll
-  for (int c = 0; c < 16; ++c) {
-    const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
-    v[c] = __uint_as_float(__float_as_uint(v[c]) ^ sbit);
-  }
+  apply_signs<E>(signs, v);
 }
+template <int E>
+__device__ __forceinline__ void load_f32_signed(const void* src, const int8_t* signs, float (&v)[E]) {
+  const float4* p = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int i = 0; i < E / 4; ++i) {
+    const float4 q = __ldg(p + i);
+    v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
+  }
+  apply_signs<E>(signs, v);
+}
+
+// Columns per thread for the activation transforms: a tile must fit one warp.
+__host__ __device__ constexpr int act_elems_for_tile(int tile) { return tile <= 512 ? 16 : tile / 32; }
 
 // ---------------------------------------------------------------- code packing
 // Low bytes of four ints into one word (byte i = low byte of ci).

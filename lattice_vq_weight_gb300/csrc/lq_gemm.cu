@@ -444,11 +444,12 @@ struct PrepArgs {
 };
 
 // Blocks [0, M): one token row each (max |x| over the row, then the rotation
-// with 16 columns per thread).  Blocks [M, M + ceil(N/16)): weight-row
+// with E columns per thread).  Blocks [M, M + ceil(N/16)): weight-row
 // factors, one warp per row.
 constexpr int kPrepThreads = 512;
 constexpr int kPrepWarps = kPrepThreads / 32;
 
+template <int E>
 __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
   __shared__ float red[kPrepWarps];
   __shared__ float row_g;
@@ -463,8 +464,8 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
     float fv = 1.f;
     if (mx > 0.f && isfinite(mx)) {
       const float top = 63.5f * mx;
-      const int E = (int)((__float_as_uint(top) >> 23) & 0xFFu) - 126;  // top in [2^(E-1), 2^E)
-      const int ex = max(-126, min(127, 15 - E));
+      const int eb = (int)((__float_as_uint(top) >> 23) & 0xFFu) - 126;  // top in [2^(eb-1), 2^eb)
+      const int ex = max(-126, min(127, 15 - eb));
       fv = __uint_as_float((uint32_t)(ex + 127) << 23);
     }
     if (ln == 0) a.f[n] = fv;
@@ -494,8 +495,8 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
       raise_flag(a.status, LQ_DEV_NONFINITE);
     } else if (v > 0.f) {
       const float top = v * (1.0f / a.inv_sqrt_tile) * (a.a2 ? 1.7320508f : 1.f);
-      const int E = (int)((__float_as_uint(top) >> 23) & 0xFFu) - 126;
-      const int ex = max(-126, min(127, 14 - E));
+      const int eb = (int)((__float_as_uint(top) >> 23) & 0xFFu) - 126;
+      const int ex = max(-126, min(127, 14 - eb));
       gv = __uint_as_float((uint32_t)(ex + 127) << 23);
     }
     row_g = gv;
@@ -506,34 +507,36 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
   if (a.zero_y) {
     for (int64_t i = threadIdx.x; i < a.N; i += kPrepThreads) a.Y[m * a.N + i] = 0.f;
   }
-  // pass 2: rotate, 16 consecutive columns per thread (a tile spans T/16 lanes
-  // of one warp; 512 threads cover 8192 columns per round)
-  const int lpt = a.tile / 16;
-  const int64_t groups = a.K / 16;
+  // pass 2: rotate, E consecutive columns per thread (a tile spans T/E lanes of
+  // one warp)
+  const int lpt = a.tile / E;
+  const int64_t groups = a.K / E;
   const float sc = a.inv_sqrt_tile * g;
   const float sc_odd = a.a2 ? sc * 1.7320508075688772f : sc;
   for (int64_t base = 0; base < groups; base += kPrepThreads) {
     const int64_t j = base + threadIdx.x;
     const bool active = j < groups;            // groups is a multiple of lpt: whole tiles
-    const int64_t col0 = (active ? j : 0) * 16;
-    float v[16];
+    const int64_t col0 = (active ? j : 0) * E;
+    float v[E];
     if (active) {
-      load16_bf16_signed(xr + col0, a.signs + col0, v);
+      load_bf16_signed<E>(xr + col0, a.signs + col0, v);
     } else {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) v[c] = 0.f;
+      for (int c = 0; c < E; ++c) v[c] = 0.f;
     }
-    fwht16_tile(v, lpt, lane);
+    fwht_tile<E>(v, lpt, lane);
     if (active) {
-      uint32_t hw[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const __half2 h = __floats2half2_rn(v[2 * q] * sc, v[2 * q + 1] * sc_odd);
-        hw[q] = *reinterpret_cast<const uint32_t*>(&h);
-      }
       uint4* dst = reinterpret_cast<uint4*>(a.Xt + m * a.K + col0);
-      dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+#pragma unroll
+      for (int q = 0; q < E / 8; ++q) {
+        uint32_t hw[4];
+#pragma unroll
+        for (int j2 = 0; j2 < 4; ++j2) {
+          const __half2 h = __floats2half2_rn(v[8 * q + 2 * j2] * sc, v[8 * q + 2 * j2 + 1] * sc_odd);
+          hw[j2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        dst[q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      }
     }
   }
 }
@@ -661,7 +664,10 @@ extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* 
   p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.f = f; p.Y = Y_dev; p.zero_y = a.splits > 1;
   p.status = dev_status_dev;
   const int64_t prep_blocks = M + (N + kPrepWarps - 1) / kPrepWarps;
-  gemm_prep_kernel<<<(unsigned)prep_blocks, kPrepThreads, 0, s>>>(p);
+  const int E = act_elems_for_tile(tile);
+  if (E == 16) gemm_prep_kernel<16><<<(unsigned)prep_blocks, kPrepThreads, 0, s>>>(p);
+  else if (E == 32) gemm_prep_kernel<32><<<(unsigned)prep_blocks, kPrepThreads, 0, s>>>(p);
+  else gemm_prep_kernel<64><<<(unsigned)prep_blocks, kPrepThreads, 0, s>>>(p);
   st = check_launch();
   if (st != LQ_OK) return st;
 

@@ -43,13 +43,11 @@ struct RotateArgs {
   int32_t* status;
 };
 
-// One thread per 16 consecutive columns of one activation row: the tile of T
-// columns spans T/16 consecutive lanes (T <= 512), so the transform is 4
-// register butterfly stages plus log2(T/16) shuffle stages -- a short
-// dependent chain, since this kernel sits in front of every GEMV.
-constexpr int kRotElems = 16;
-
-template <bool BF16>
+// One thread per E consecutive columns of one activation row (E = 16 for
+// tiles up to 512 columns, T/32 above): the tile spans T/E consecutive lanes,
+// so the transform is log2(E) register stages plus log2(T/E) shuffle stages --
+// a short dependent chain, since this kernel sits in front of every GEMV.
+template <bool BF16, int E>
 __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   // the GEMV that follows may start streaming codes now; it waits for this
   // grid's results (griddepcontrol.wait) before reading them
@@ -59,42 +57,27 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = gtid; i < a.y_elems; i += nthreads) a.y[i] = 0.f;
 
-  const int64_t per_row = a.cols / kRotElems;
+  const int64_t per_row = a.cols / E;
   const int64_t work = (int64_t)a.batch * per_row;
-  const int lpt = a.tile / kRotElems;                    // lanes per tile
+  const int lpt = a.tile / E;                            // lanes per tile (<= 32)
   // every lane of a warp takes part in the shuffles; lanes past the end work on zeros
   const bool active = gtid < work;
   const int64_t b = active ? gtid / per_row : 0;
-  const int64_t col0 = active ? (gtid - b * per_row) * kRotElems : 0;
-  float v[kRotElems];
+  const int64_t col0 = active ? (gtid - b * per_row) * E : 0;
+  float v[E];
   if (active) {
-    if constexpr (BF16) {
-      load16_bf16_signed(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0, a.signs + col0, v);
-    } else {
-      const uint4 sw = __ldg(reinterpret_cast<const uint4*>(a.signs + col0));
-      const uint32_t sg[4] = {sw.x, sw.y, sw.z, sw.w};
-      const float4* src = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 q = __ldg(src + i);
-        v[4 * i] = q.x; v[4 * i + 1] = q.y; v[4 * i + 2] = q.z; v[4 * i + 3] = q.w;
-      }
-#pragma unroll
-      for (int c = 0; c < kRotElems; ++c) {
-        const uint32_t sbit = ((sg[c >> 2] >> (8 * (c & 3) + 7)) & 1u) << 31;
-        v[c] = __uint_as_float(__float_as_uint(v[c]) ^ sbit);
-      }
-    }
+    if constexpr (BF16) load_bf16_signed<E>(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0, a.signs + col0, v);
+    else load_f32_signed<E>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0, a.signs + col0, v);
   } else {
 #pragma unroll
-    for (int c = 0; c < kRotElems; ++c) v[c] = 0.f;
+    for (int c = 0; c < E; ++c) v[c] = 0.f;
   }
-  fwht16_tile(v, lpt, lane);
+  fwht_tile<E>(v, lpt, lane);
   const float sc = a.post_scale;
   const float sc_odd = a.a2 ? sc * 1.7320508075688772f : sc;
   float mx = 0.f;
 #pragma unroll
-  for (int c = 0; c < kRotElems; ++c) {
+  for (int c = 0; c < E; ++c) {
     v[c] *= (c & 1) ? sc_odd : sc;
     mx = fmaxf(mx, fabsf(v[c]));
   }
@@ -104,27 +87,28 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   if (!isfinite(mx)) {
     bad = active;
   } else if (mx > 0.f) {
-    const int E = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 126;  // mx in [2^(E-1), 2^E)
-    const int ex = max(-126, min(127, 15 - E));
+    const int Ex = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 126;  // mx in [2^(Ex-1), 2^Ex)
+    const int ex = max(-126, min(127, 15 - Ex));
     f = __uint_as_float((uint32_t)(ex + 127) << 23);
   }
   if (active) {
-    uint32_t hw[8], lw[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float x0 = v[2 * j] * f, x1 = v[2 * j + 1] * f;
-      const __half2 h = __floats2half2_rn(x0, x1);
-      const float2 hf = __half22float2(h);
-      const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
-      hw[j] = *reinterpret_cast<const uint32_t*>(&h);
-      lw[j] = *reinterpret_cast<const uint32_t*>(&l);
-    }
     uint4* dh = reinterpret_cast<uint4*>(a.xh + b * a.cols + col0);
     uint4* dl = reinterpret_cast<uint4*>(a.xl + b * a.cols + col0);
-    dh[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    dh[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
-    dl[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-    dl[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+#pragma unroll
+    for (int q = 0; q < E / 8; ++q) {
+      uint32_t hw[4], lw[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x0 = v[8 * q + 2 * j] * f, x1 = v[8 * q + 2 * j + 1] * f;
+        const __half2 h = __floats2half2_rn(x0, x1);
+        const float2 hf = __half22float2(h);
+        const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+        hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+        lw[j] = *reinterpret_cast<const uint32_t*>(&l);
+      }
+      dh[q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      dl[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
     if ((lane & (lpt - 1)) == 0) a.xs[b * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
@@ -515,16 +499,26 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   r.xl = reinterpret_cast<__half*>(ws + lay.xl);
   r.xs = reinterpret_cast<float*>(ws + lay.xs);
   r.y = y_dev; r.y_elems = (int64_t)batch * rows; r.status = dev_status_dev;
-  // One thread per 16 activation columns (a few CTAs), which also zero y;
-  // the small grid leaves the SMs free for the GEMV launched right after it
+  // One thread per E activation columns (a few CTAs), which also zero y; the
+  // small grid leaves the SMs free for the GEMV launched right after it
   // (programmatic dependent launch).
-  const int64_t rot_threads = (int64_t)batch * (cols / kRotElems);
+  const int E = act_elems_for_tile(tile);
+  const int64_t rot_threads = (int64_t)batch * (cols / E);
   int64_t rgrid = (rot_threads + 255) / 256;
   const int64_t zgrid = ((int64_t)batch * rows + 256 * 16 - 1) / (256 * 16);
   if (rgrid < zgrid) rgrid = zgrid;
   if (rgrid < 1) rgrid = 1;
-  if (xdtype == LQ_BF16) rotate_activation_kernel<true><<<(unsigned)rgrid, 256, 0, s>>>(r);
-  else rotate_activation_kernel<false><<<(unsigned)rgrid, 256, 0, s>>>(r);
+  const bool bf = (xdtype == LQ_BF16);
+  if (E == 16) {
+    if (bf) rotate_activation_kernel<true, 16><<<(unsigned)rgrid, 256, 0, s>>>(r);
+    else rotate_activation_kernel<false, 16><<<(unsigned)rgrid, 256, 0, s>>>(r);
+  } else if (E == 32) {
+    if (bf) rotate_activation_kernel<true, 32><<<(unsigned)rgrid, 256, 0, s>>>(r);
+    else rotate_activation_kernel<false, 32><<<(unsigned)rgrid, 256, 0, s>>>(r);
+  } else {
+    if (bf) rotate_activation_kernel<true, 64><<<(unsigned)rgrid, 256, 0, s>>>(r);
+    else rotate_activation_kernel<false, 64><<<(unsigned)rgrid, 256, 0, s>>>(r);
+  }
   st = check_launch();
   if (st != LQ_OK) return st;
 

@@ -17,7 +17,7 @@ inline bool valid_lattice(int l) { return l == LQ_E8 || l == LQ_D4 || l == LQ_A2
 // Checks shared by quantize, dequantize and gemv: lattice, tile, shape.
 inline lq_status validate_common(int lattice, int64_t rows, int64_t cols, int tile) {
   if (!valid_lattice(lattice)) return LQ_ERR_ARG;
-  if (tile != 128 && tile != 256 && tile != 512) return LQ_ERR_UNSUPPORTED;
+  if (tile != 128 && tile != 256 && tile != 512 && tile != 1024 && tile != 2048) return LQ_ERR_UNSUPPORTED;
   if (rows < 0 || cols <= 0) return LQ_ERR_SHAPE;
   if (cols % tile != 0) return LQ_ERR_SHAPE;
   if (cols > (int64_t(1) << 20)) return LQ_ERR_SHAPE;

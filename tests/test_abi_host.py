@@ -81,6 +81,8 @@ def test_argument_errors_are_synchronous():
         8, good, good, good, 4, cols, tile, good, 1, batch, good, good, nul, s)
     assert g(0) == L.LQ_ERR_SHAPE and g(17) == L.LQ_ERR_SHAPE
     assert g(1, tile=64) == L.LQ_ERR_UNSUPPORTED
+    assert g(1, tile=4096, cols=4096) == L.LQ_ERR_UNSUPPORTED   # tiles stop at 2048
+    assert g(1, tile=2048, cols=3072) == L.LQ_ERR_SHAPE         # cols % tile
     assert lib.lq_dequantize(8, good, good, good, 4, 256, 256, good, 5, s) == L.LQ_ERR_DTYPE
     assert lib.lq_make_signs(0, -1, good, s) == L.LQ_ERR_SHAPE
     assert L.lq_gemv_workspace_size(1, 4096, 256) >= 4096 * 4

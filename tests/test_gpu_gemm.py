@@ -41,11 +41,11 @@ def test_gemm_parity_e8(M, N, K):
     assert rel < 1e-3
 
 
-@pytest.mark.parametrize("lattice", ["d4", "a2", "z1"])
-@pytest.mark.parametrize("tile", [128, 512])
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+@pytest.mark.parametrize("tile", [128, 512, 1024, 2048])
 def test_gemm_parity_lattices_tiles(lattice, tile):
     torch, L = cuda()
-    M, N, K = 70, 128, 1024
+    M, N, K = 70, 128, max(1024, 2 * tile)
     W = gaussian_matrix(N, K, 0.02, 7, dtype="bf16")
     d = O.splitmix64_signs(8, K)
     q = O.quantize(W, lattice, tile, d, 0.25)

@@ -34,11 +34,12 @@ def test_small_fp32_case_gemv():
 
 
 @pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
-@pytest.mark.parametrize("tile", [128, 256, 512])
+@pytest.mark.parametrize("tile", [128, 256, 512, 1024, 2048])
 @pytest.mark.parametrize("batch", [1, 3, 8, 16])
 def test_gemv_parity(lattice, tile, batch):
     torch, L = cuda()
-    rows, cols = 75, 2048 + 2 * tile       # ragged rows and a partial column chunk
+    # ragged rows and (tiles up to 1024) a partial 2048-column chunk
+    rows, cols = 75, (2048 + 2 * tile) if tile <= 512 else 3 * tile
     W = gaussian_matrix(rows, cols, 0.02, 300 + tile, dtype="bf16")
     d = O.splitmix64_signs(11, cols)
     q = O.quantize(W, lattice, tile, d, 0.25)

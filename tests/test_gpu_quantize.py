@@ -35,10 +35,11 @@ def test_signs_match_oracle():
 
 
 @pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
-@pytest.mark.parametrize("tile", [128, 256, 512])
+@pytest.mark.parametrize("tile", [128, 256, 512, 1024, 2048])
 def test_quantize_parity_ragged(lattice, tile):
     torch, L = cuda()
-    rows, cols = 37, 3 * 512 if tile == 512 else 5 * tile   # not a multiple of the 2048-column chunk
+    # not a multiple of the 2048-column chunk (tiles up to 1024)
+    rows, cols = 37, {512: 3 * 512, 1024: 3 * 1024, 2048: 3 * 2048}.get(tile, 5 * tile)
     W = gaussian_matrix(rows, cols, 0.02, 100 + tile, outlier_frac=0.002, dtype="bf16")
     for beta in (0.125, 0.25, 0.5):
         codes, scales, signs, st = run_quantize(torch, L, W, "bf16", lattice, tile, 77, beta)
@@ -126,7 +127,7 @@ def test_empty_rows_is_noop():
 
 
 @pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
-@pytest.mark.parametrize("tile", [128, 256, 512])
+@pytest.mark.parametrize("tile", [128, 256, 512, 1024, 2048])
 def test_dequantize_parity(lattice, tile):
     torch, L = cuda()
     rows, cols = 21, 2 * 2048 + 2 * tile
