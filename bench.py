@@ -20,6 +20,16 @@ roofline = the quantize kernel (largest share of the step) against the measured
 
 --impl reference times the float64 CPU oracle on the same metric over a bounded
 row sample of the same layer (rank 0 only).
+
+Other workloads (--workload), each printed as one JSON line of the same form:
+  stack  32 such layers with 0.1 % x20 outliers (seeds 2000 + 7 layer + index,
+         drawn on the device), all resident in HBM; one step = quantize all 224
+         matrices, then the GEMV at batch 1 and 8 over all of them in layer
+         order, captured as one CUDA graph.
+  sweep  gate- and down-shaped matrices (seeds 3000 / 3001) over every lattice,
+         beta in {0.125, 0.25, 0.5} and tile in {128, 256, 512, 1024, 2048}:
+         relative MSE, normalised second moment, code entropy, quantize GB/s
+         and batch-1 GEMV GB/s per run.
 """
 from __future__ import annotations
 
@@ -183,6 +193,62 @@ def cpu_oracle_sample(frac_rows: float, repeats: int = 1) -> dict:
         times.append(time.perf_counter() - t0)
     _, _, total = step_bytes(shapes, frac_rows)
     return {"seconds": times, "bytes": total}
+
+
+def _oracle_worker(wid, nproc, frac_rows, barrier, q):
+    """One row block of every sampled layer matrix (spawned process, one BLAS thread)."""
+    import numpy as np
+    import oracle as O
+    from synthetic import gaussian_matrix, gaussian_vectors
+    shapes = layer_shapes()
+    work = []
+    for n, r, c, seed in shapes:
+        rr = max(1, int(r * frac_rows))
+        lo, hi = rr * wid // nproc, rr * (wid + 1) // nproc
+        W = gaussian_matrix(rr, c, 0.02, seed, dtype="bf16")[lo:hi].copy()
+        work.append((W, c, seed, {b: gaussian_vectors(b, c, 5000 + b, dtype="bf16") for b in BATCHES}))
+    barrier.wait()
+    t0 = time.perf_counter()
+    for W, c, seed, xs in work:
+        if W.shape[0] == 0:
+            continue
+        d = O.splitmix64_signs(seed, c)
+        qz = O.quantize(W, LATTICE, TILE, d, BETA)
+        for b in BATCHES:
+            O.gemv(qz.codes, qz.scales, d, TILE, LATTICE, xs[b])
+    q.put(time.perf_counter() - t0)
+
+
+def cpu_oracle_all_cores(frac_rows: float, nproc: int) -> dict:
+    """The oracle over row blocks on nproc spawned processes; wall time of the compute."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(nproc + 1)
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker, args=(w, nproc, frac_rows, barrier, q)) for w in range(nproc)]
+    for p in procs:
+        p.start()
+    barrier.wait()
+    t0 = time.perf_counter()
+    per = [q.get() for _ in procs]
+    wall = time.perf_counter() - t0
+    for p in procs:
+        p.join()
+    _, _, total = step_bytes(layer_shapes(), frac_rows)
+    return {"seconds": wall, "bytes": total, "worker_seconds_max": max(per)}
+
+
+def run_cpu_baseline_all_cores(frac_rows: float) -> dict:
+    nproc = os.cpu_count() or 1
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.cpu_oracle_all_cores(%r, %d)))" % (ROOT, frac_rows, nproc))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError("CPU oracle (all cores) failed:\n" + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = nproc
+    return out
 
 
 def run_cpu_baseline(frac_rows: float, repeats: int) -> dict:
@@ -452,8 +518,228 @@ def gpu_arm(args, ws, rank, local):
                            f"b=1,4,16, float64 NumPy, 1 thread, {secs:.1f} s")}
         except Exception as exc:  # reported, not fatal for the GPU number
             line["cpu_baseline"] = {"value": None, "error": str(exc)[-300:]}
+        try:
+            ac = run_cpu_baseline_all_cores(args.cpu_frac)
+            line["cpu_baseline"]["all_cores"] = {
+                "value": round(ac["bytes"] / ac["seconds"] / 1e9, 6), "unit": "GB/s", "cores": ac["cores"],
+                "kind": "oracle", "sample": (f"same sample split into {ac['cores']} row blocks on "
+                                             f"{ac['cores']} spawned processes (1 BLAS thread each), "
+                                             f"{ac['seconds']:.1f} s wall")}
+        except Exception as exc:
+            line["cpu_baseline"]["all_cores"] = {"value": None, "error": str(exc)[-300:]}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def _graph_ms(torch, g, stream, reps):
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def stack_arm(args, ws, rank, local):
+    """32 Llama-3-8B layers resident in HBM: quantize all, then GEMV b = 1 and 8."""
+    import torch
+
+    from lattice_vq_weight_gb300 import build as _build
+    _build.build()
+    import lattice_vq_weight_gb300 as L
+    from synthetic import LLAMA3_8B_LAYER, stack_seed, torch_gaussian_matrix
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    n_layers, batches = 32, (1, 8)
+    mats = []          # (layer, name, rows, cols, seed)
+    for layer in range(n_layers):
+        for i, (n, r, c) in enumerate(LLAMA3_8B_LAYER):
+            mats.append((layer, n, r, c, stack_seed(layer, i)))
+    W = [torch_gaussian_matrix(r, c, 0.02, seed, device=dev, outlier_frac=0.001) for _, _, r, c, seed in mats]
+    codes = [torch.empty((r, c), dtype=torch.int8, device=dev) for _, _, r, c, _ in mats]
+    scales = [torch.empty((r, c // TILE), dtype=torch.float32, device=dev) for _, _, r, c, _ in mats]
+    signs = [torch.empty((c,), dtype=torch.int8, device=dev) for _, _, _, c, _ in mats]
+    cols_set = sorted({c for _, _, _, c, _ in mats})
+    xs = {(b, c): torch.randn((b, c), device=dev, generator=torch.Generator(device=dev).manual_seed(6000 + b)
+                              ).to(torch.bfloat16) for b in batches for c in cols_set}
+    ys = {(b, k): torch.empty((b, r), dtype=torch.float32, device=dev)
+          for b in batches for k, (_, _, r, _, _) in enumerate(mats)}
+    work = torch.empty(max(L.lq_gemv_workspace_size(b, c, TILE) for b in batches for c in cols_set),
+                       dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def quantize_all():
+        for k, (_, _, r, c, seed) in enumerate(mats):
+            L.lq_quantize(LATTICE, W[k], TILE, seed, BETA, codes[k], scales[k], signs[k], status)
+
+    def gemv_all(b):
+        for k, (_, _, r, c, _) in enumerate(mats):
+            L.lq_gemv(LATTICE, codes[k], scales[k], signs[k], TILE, xs[(b, c)], ys[(b, k)], work, status)
+
+    def step():
+        quantize_all()
+        for b in batches:
+            gemv_all(b)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+    graphs = {}
+    for name, fn in (("step", step), ("quantize", quantize_all), ("gemv1", lambda: gemv_all(1)),
+                     ("gemv8", lambda: gemv_all(8))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs[name] = g
+    for _ in range(args.warmup):
+        graphs["step"].replay()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    ms_step = _graph_ms(torch, graphs["step"], stream, args.steps)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    ms_step = max_over_ranks(ws, ms_step, dev)
+    qb = sum(quantize_bytes(r, c) for _, _, r, c, _ in mats)
+    gb = {b: sum(gemv_bytes(r, c, b) for _, _, r, c, _ in mats) for b in batches}
+    total = qb + sum(gb.values())
+    reps = max(3, min(args.steps, 10))
+    ms_q = _graph_ms(torch, graphs["quantize"], stream, reps)
+    ms_g = {b: _graph_ms(torch, graphs[f"gemv{b}"], stream, reps) for b in batches}
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after the timed region")
+    peak, src = hbm_peak("sustained")
+    qgbs = qb / (ms_q * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(total * ws / (ms_step * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16->int8 (fp32 compute)",
+        "data": "synthetic",
+        "config": {"workload": "llama3-8b 32-layer stack e8 tile256 beta0.25 quantize+gemv(b=1,8)",
+                   "matrices": len(mats), "weights_bytes": int(sum(w.numel() * 2 for w in W)),
+                   "codes_bytes": int(sum(cd.numel() for cd in codes)), "outliers": "0.1% x20",
+                   "parallelism": f"replicas{ws}", "l2": "inputs far larger than L2; no flush",
+                   "graph": f"one CUDA graph of {len(mats) * 2 * (1 + len(batches))} launches"},
+        "gpu_launches": len(mats) * 2 * (1 + len(batches)) * args.steps,
+        "parts": {"quantize_gbs": round(qgbs, 1), "quantize_ms": round(ms_q, 3),
+                  **{f"gemv_b{b}_gbs": round(gb[b] / (ms_g[b] * 1e-3) / 1e9, 1) for b in batches},
+                  **{f"gemv_b{b}_ms": round(ms_g[b], 3) for b in batches}},
+        "roofline": {"kernel": "quantize_kernel (224 matrices)", "bound": "hbm", "achieved": round(qgbs, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(qgbs / peak, 4), "peak_source": src,
+                     "traffic": None},
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# covolume and textbook normalised second moment of each lattice at its native scale
+_LATTICE_GEOM = {"e8": (8, 1.0), "d4": (4, 2.0), "a2": (2, 3 ** 0.5 / 2), "z1": (1, 1.0)}
+
+
+def sweep_arm(args, ws, rank, local):
+    """Lattice x beta x tile sweep on gate- and down-shaped bf16 matrices."""
+    import math
+
+    import torch
+
+    from lattice_vq_weight_gb300 import build as _build
+    _build.build()
+    import lattice_vq_weight_gb300 as L
+    from synthetic import LLAMA3_8B_LAYER, torch_gaussian_matrix
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    shapes = {n: (r, c) for n, r, c in LLAMA3_8B_LAYER if n in ("gate", "down")}
+    seeds = {"gate": 3000, "down": 3001}
+    runs = []
+    reps = max(3, min(args.steps, 10))
+    for name, (r, c) in shapes.items():
+        W = torch_gaussian_matrix(r, c, 0.02, seeds[name], device=dev)
+        Wf = W.double()
+        w2 = float((Wf * Wf).sum())
+        x = torch.randn((1, c), device=dev, generator=torch.Generator(device=dev).manual_seed(6100)).to(torch.bfloat16)
+        for lat in ("e8", "d4", "a2", "z1"):
+            n, vol = _LATTICE_GEOM[lat]
+            for beta in (0.125, 0.25, 0.5):
+                for tile in (128, 256, 512, 1024, 2048):
+                    codes = torch.empty((r, c), dtype=torch.int8, device=dev)
+                    sc = torch.empty((r, c // tile), dtype=torch.float32, device=dev)
+                    sg = torch.empty((c,), dtype=torch.int8, device=dev)
+                    y = torch.empty((1, r), dtype=torch.float32, device=dev)
+                    wk = torch.empty(L.lq_gemv_workspace_size(1, c, tile), dtype=torch.uint8, device=dev)
+                    st = torch.zeros(1, dtype=torch.int32, device=dev)
+                    with torch.cuda.stream(stream):
+                        L.lq_quantize(lat, W, tile, seeds[name], beta, codes, sc, sg, st)
+                        L.lq_gemv(lat, codes, sc, sg, tile, x, y, wk, st)
+                    torch.cuda.synchronize(dev)
+                    gq = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gq, stream=stream):
+                        for _ in range(4):
+                            L.lq_quantize(lat, W, tile, seeds[name], beta, codes, sc, sg, st)
+                    gg = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gg, stream=stream):
+                        for _ in range(4):
+                            L.lq_gemv(lat, codes, sc, sg, tile, x, y, wk, st)
+                    gq.replay(); gg.replay()
+                    torch.cuda.synchronize(dev)
+                    ms_q = _graph_ms(torch, gq, stream, reps) / 4
+                    ms_g = _graph_ms(torch, gg, stream, reps) / 4
+                    What = L.dequantize(codes, sc, sg, lattice=lat, tile=tile, dtype=torch.float32)
+                    err = (What.double() - Wf)
+                    # per-dimension distortion in lattice units: the rotation is orthonormal,
+                    # so |w - w^|^2 over a tile equals |w~ - s p|^2 = s^2 |y - p|^2
+                    tile_err = (err * err).view(r, c // tile, tile).sum(-1)
+                    s2 = sc.double() ** 2
+                    nz = s2 > 0
+                    d_per_dim = float((tile_err[nz] / s2[nz]).sum()) / (int(nz.sum()) * tile)
+                    G = d_per_dim / vol ** (2.0 / n)
+                    hist = torch.bincount((codes.view(-1).to(torch.int32) + 128), minlength=256).double()
+                    pr = hist[hist > 0] / hist.sum()
+                    ent = float(-(pr * pr.log2()).sum())
+                    runs.append({"shape": name, "lattice": lat, "beta": beta, "tile": tile,
+                                 "rel_mse": float((err * err).sum()) / w2, "G": round(G, 6),
+                                 "code_entropy_bits": round(ent, 4), "status": int(st.item()),
+                                 "quantize_gbs": round(quantize_bytes_t(r, c, tile) / (ms_q * 1e-3) / 1e9, 1),
+                                 "gemv_b1_gbs": round(gemv_bytes_t(r, c, 1, tile) / (ms_g * 1e-3) / 1e9, 1)})
+                    del codes, sc, sg, y, wk, What, err, gq, gg
+        del W, Wf
+    e8 = [x for x in runs if x["lattice"] == "e8" and x["tile"] == TILE and x["beta"] == BETA]
+    best_q = max(x["quantize_gbs"] for x in runs)
+    line = {
+        "metric": METRIC, "value": round(statistics.mean(x["quantize_gbs"] for x in e8), 1), "unit": "GB/s",
+        "n_gpus": ws, "steps": reps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16->int8 (fp32 compute)", "data": "synthetic",
+        "config": {"workload": "lattice sweep: gate 14336x4096 and down 4096x14336 bf16, "
+                               "{e8,d4,a2,z1} x beta {0.125,0.25,0.5} x tile {128..2048}",
+                   "value_is": "mean quantize GB/s of the e8 tile-256 beta-0.25 runs",
+                   "best_quantize_gbs": best_q},
+        "textbook_G": {"e8": 929 / 12960, "d4": 0.076603, "a2": 5 / (36 * math.sqrt(3)), "z1": 1 / 12},
+        "runs": runs,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def quantize_bytes_t(rows, cols, tile, in_bytes=2):
+    return rows * cols * (in_bytes + 1 + 4.0 / tile) + cols
+
+
+def gemv_bytes_t(rows, cols, b, tile, x_bytes=2):
+    return rows * cols * (1 + 4.0 / tile) + cols + b * cols * x_bytes + b * rows * 4
 
 
 def gemm_part(L, torch, dev, stream, reps):
@@ -512,8 +798,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("lq", "reference"), default="lq")
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-frac", type=float, default=0.25)
+    ap.add_argument("--cpu-frac", type=float, default=0.75)
     ap.add_argument("--reference-frac", type=float, default=1.0 / 64)
+    ap.add_argument("--workload", choices=("layer", "stack", "sweep"), default="layer")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -521,6 +808,10 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             reference_arm(args, ws, rank)
+        elif args.workload == "stack":
+            stack_arm(args, ws, rank, local)
+        elif args.workload == "sweep":
+            sweep_arm(args, ws, rank, local)
         else:
             gpu_arm(args, ws, rank, local)
     finally:

@@ -6,8 +6,8 @@
 // decoders.
 //
 // Work decomposition: a warp unit is one 2048-column chunk of one row; lane l
-// owns columns [64 l, 64 l + 64) of the chunk (see lq_device.cuh).  Units are
-// visited by a persistent grid of 8-warp CTAs, and each warp loads the raw
+// loads columns [64 l, 64 l + 64) of the chunk (see lq_device.cuh).  Units are
+// visited by a persistent grid of 4-warp CTAs, and each warp loads the raw
 // data of its next unit before working on the current one.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -159,17 +159,83 @@ struct QuantArgs {
 constexpr int kQuantThreads = 128;
 
 // Shared memory per warp: two stages of raw input (each lane copies its own
-// 64 columns with cp.async and later reads back only its own copies, so no
-// barrier is needed) and, for bf16, the lane's sign masks.
+// 64 columns with cp.async and later reads back only its own copies) and, for
+// bf16, the lane's sign masks.  Once a stage has been read into registers it
+// doubles as the buffer of the butterfly exchange below, so a stage holds at
+// least the exchange's 284 16-byte slots.
 template <bool BF16> struct QuantSmem {
   static constexpr int kRawVec = BF16 ? 8 : 16;             // 16-byte vectors per lane per stage
-  static constexpr int kRawWords = 2 * kRawVec * 32;        // uint4 per warp, both stages
+  static constexpr int kStageVec = BF16 ? 288 : 512;        // uint4 per warp per stage
+  static constexpr int kRawWords = 2 * kStageVec;           // uint4 per warp, both stages
   static constexpr int kMaskWords = BF16 ? 8 * 32 : 0;      // uint4 per warp
   static constexpr int kPerWarp = kRawWords + kMaskWords;
 };
 
-template <int LAT, bool BF16>
-__global__ void __launch_bounds__(kQuantThreads, 3) quantize_kernel(QuantArgs a) {
+// Butterfly stages of tile bits 6 .. 6+MP-1 without shuffles.  After the six
+// register stages, lane bits 0 .. MP-1 of a lane hold tile bits 6 .. and its
+// register index bits 3 .. 3+MP-1 hold tile bits 3 ..; one pass through shared
+// memory swaps the two, so those stages run in registers as well and every
+// 8-coordinate block (tile bits 0 .. 2) stays in one lane.  The pass goes in
+// two halves (register bit 2) of 32 values per lane.  Slot of the value with
+// lane group G, spectator register bits ux, lane bits a and register bits c:
+//   (G >> (3 - MP)) * kBlk + ux * kUxSpan + (G & (X - 1)) * Q + a + 9 c,
+// additive in a and c, so every access is a per-lane base plus a constant,
+// and conflict-free for 16-byte accesses both when a varies (writes) and when
+// c varies (reads): the slots of the 8 lanes of a phase differ modulo 8.
+template <int MP> struct Xchg {
+  static constexpr int Q = 1 << MP;          // lanes whose bits are swapped
+  static constexpr int X = 8 >> MP;          // spectator register values per half
+  static constexpr int kUxSpan = 9 * Q - 1;
+  static constexpr int kBlk = X * kUxSpan;
+  static constexpr int kSlots = 4 * kBlk;
+};
+static_assert(Xchg<2>::kSlots <= 288 && Xchg<3>::kSlots <= 288, "exchange slots");
+
+template <int MP>
+__device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf, int lane) {
+  using XC = Xchg<MP>;
+  const int q = lane & (XC::Q - 1), G = lane >> MP;
+  const uint32_t g = (uint32_t)((G >> (3 - MP)) * XC::kBlk + (G & (XC::X - 1)) * XC::Q);
+  const uint32_t wb = buf + (g + (uint32_t)q) * 16u;
+  const uint32_t rb = buf + (g + 9u * (uint32_t)q) * 16u;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t off = (uint32_t)(((u >> MP) * XC::kUxSpan + 9 * (u & (XC::Q - 1))) * 16);
+      const float2 v0 = p[4 * u + 2 * h], v1 = p[4 * u + 2 * h + 1];
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(wb + off), "f"(v0.x), "f"(v0.y),
+                   "f"(v1.x), "f"(v1.y) : "memory");
+    }
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t off = (uint32_t)(((u >> MP) * XC::kUxSpan + (u & (XC::Q - 1))) * 16);
+      float2 v0, v1;
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v0.x), "=f"(v0.y), "=f"(v1.x), "=f"(v1.y)
+                   : "r"(rb + off) : "memory");
+      p[4 * u + 2 * h] = v0;
+      p[4 * u + 2 * h + 1] = v1;
+    }
+  }
+  __syncwarp();
+  // the swapped tile bits now sit in register index bits 3 .. 3+MP-1 (float2 bits 2 ..)
+#pragma unroll
+  for (int hp = 4; hp < (4 << MP); hp <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if ((j & hp) == 0) {
+        const float2 x0 = p[j], x1 = p[j + hp];
+        p[j] = add2(x0, x1);
+        p[j + hp] = sub2(x0, x1);
+      }
+    }
+  }
+}
+
+template <int LAT, bool BF16, int MP>
+__global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a) {
   using SM = QuantSmem<BF16>;
   extern __shared__ uint4 quant_smem[];
   const int lane = threadIdx.x & 31;
@@ -206,7 +272,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3) quantize_kernel(QuantArgs a)
       const char* src = lane_ptr(r, c);
 #pragma unroll
       for (int i = 0; i < SM::kRawVec; ++i)
-        cp_async16(raw_s + (uint32_t)(((st * SM::kRawVec + i) * 32 + lane) * 16), src + 16 * i);
+        cp_async16(raw_s + (uint32_t)((st * SM::kStageVec + i * 32 + lane) * 16), src + 16 * i);
     }
     cp_async_commit();
   };
@@ -237,12 +303,25 @@ __global__ void __launch_bounds__(kQuantThreads, 3) quantize_kernel(QuantArgs a)
     {
       LaneRaw<BF16> raw;
 #pragma unroll
-      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[(stage * SM::kRawVec + i) * 32 + lane];
+      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[stage * SM::kStageVec + i * 32 + lane];
       if constexpr (BF16) unpack_bf16_smem_signs(raw, msk, lane, p);
       else unpack_signed<false>(raw, sg, p);
     }
     fwht64_local(p);
-    fwht_cross_lanes(p, a.lanes_per_tile, lane);
+    if constexpr (MP > 0) exchange_tile_bits<MP>(p, raw_s + (uint32_t)(stage * SM::kStageVec * 16), lane);
+    // lane bits not exchanged (MP = 0: all of them; tiles of 1024 and 2048
+    // columns: tile bits 9 .. on lane bits 3 ..) cross lanes with shuffles
+    for (int m = (MP == 0 ? 1 : 8); m < a.lanes_per_tile; m <<= 1) {
+      const float sgn = (lane & m) ? -1.0f : 1.0f;
+      const float2 sg2 = make_float2(sgn, sgn);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float2 o;
+        o.x = __shfl_xor_sync(0xffffffffu, p[j].x, m);
+        o.y = __shfl_xor_sync(0xffffffffu, p[j].y, m);
+        p[j] = fma2(p[j], sg2, o);
+      }
+    }
 
     // U = sum u^2 over the tile; s = beta sqrt(U) / T; y = u / (s sqrt(T))
     float2 acc = make_float2(0.f, 0.f);
@@ -257,20 +336,33 @@ __global__ void __launch_bounds__(kQuantThreads, 3) quantize_kernel(QuantArgs a)
 #pragma unroll
     for (int j = 0; j < 32; ++j) p[j] = mul2(p[j], k2);
 
-    // sum of y^2 over this lane bounds every |y| of the lane: below 62.5^2 no
-    // code can leave int8 and the per-block range check is skipped
+    // every |y| of the lane below 62.5 keeps every code inside int8, and the
+    // per-block range check is left out; the lane's sum of y^2 decides that
+    // for free in most cases, the lane maximum otherwise
     const float lane_y2 = (acc.x + acc.y) * (k * k);
+    bool small = lane_y2 < 3906.25f;
+    if (!small) {
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) m = fmaxf(m, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
+      small = m < 62.5f;
+    }
     uint32_t w[16];
     bool r = false;
-    if (lane_y2 < 3906.25f) decode_lane<LAT, false>(p, w, r);
+    if (small) decode_lane<LAT, false>(p, w, r);
     else decode_lane<LAT, true>(p, w, r);
 
     if (active) {
       range |= r;
       nonfinite |= !finite;
-      uint4* dst = reinterpret_cast<uint4*>(a.codes + row * a.cols + col0);
+      // register block u holds tile columns 8 q + 8 Q ux + 64 a (q = lane bits,
+      // ux = u >> MP, a = u & (Q - 1)) of the tile group G = lane >> MP
+      constexpr int Q = 1 << MP;
+      int8_t* dst = a.codes + row * a.cols + (int64_t)chunk * kChunkCols + (lane >> MP) * (64 * Q) +
+                    8 * (lane & (Q - 1));
 #pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint2*>(dst + (u >> MP) * (8 * Q) + 64 * (u & (Q - 1))) = make_uint2(w[2 * u], w[2 * u + 1]);
       if ((lane & (a.lanes_per_tile - 1)) == 0)
         a.scales[row * a.tiles_per_row + (col0 >> a.tile_shift)] = s;
     }
@@ -389,22 +481,31 @@ extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_de
   return check_launch();
 }
 
-template <int LAT, bool BF16>
-static lq_status launch_quantize(const QuantArgs& a, cudaStream_t st) {
+template <int LAT, bool BF16, int MP>
+static lq_status launch_quantize_mp(const QuantArgs& a, cudaStream_t st) {
   constexpr size_t smem = (size_t)(kQuantThreads / 32) * QuantSmem<BF16>::kPerWarp * sizeof(uint4);
   static int per_sm = 0;
   if (per_sm == 0) {
-    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess) {
+    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
     }
-    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16>, kQuantThreads, smem);
+    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP>, kQuantThreads, smem);
   }
   const int grid = persistent_grid(a.units, kQuantThreads / 32, a.chunks_per_row, per_sm);
   if (grid <= 0) return LQ_ERR_CUDA;
-  quantize_kernel<LAT, BF16><<<grid, kQuantThreads, smem, st>>>(a);
+  quantize_kernel<LAT, BF16, MP><<<grid, kQuantThreads, smem, st>>>(a);
   return check_launch();
+}
+
+// MP = tile bits exchanged through shared memory: log2(tile / 64), at most 3.
+// A 128-column tile has a single cross-lane stage, cheaper as a shuffle (MP = 0).
+template <int LAT, bool BF16>
+static lq_status launch_quantize(const QuantArgs& a, cudaStream_t st) {
+  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0>(a, st);
+  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2>(a, st);
+  return launch_quantize_mp<LAT, BF16, 3>(a, st);
 }
 
 extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,

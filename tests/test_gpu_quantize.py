@@ -3,7 +3,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from synthetic import gaussian_matrix, small_fp32_case
+from synthetic import gaussian_matrix, gaussian_vectors, small_fp32_case
 from tests._parity import compare_codes, normwise_rel
 from tests.gpu_util import cuda, to_dev, to_dev_bf16
 
@@ -157,3 +157,30 @@ def test_full_size_gate_matrix_sampled():
     np.testing.assert_allclose(scales[rows], q.scales, rtol=1e-6)
     compare_codes(codes[rows], q, "e8")
     assert np.all(O.code_membership_ok("e8", codes.reshape(-1, 8).astype(np.int64)))
+
+
+def test_stack_recipe_down_matrix_with_outliers_sampled():
+    """down_proj 4096 x 14336 drawn on the device as in the 32-layer stack workload
+    (N(0, 0.02^2), 0.1 % x20 outliers, bf16), E8, tile 256, beta 0.25, one launch;
+    oracle on 64 sampled rows of the same bf16 values, then the batch-8 GEMV of the
+    stack workload on the same rows."""
+    torch, L = cuda()
+    from synthetic import stack_seed, torch_gaussian_matrix
+    seed = stack_seed(31, 6)
+    Wd = torch_gaussian_matrix(4096, 14336, 0.02, seed, device="cuda", outlier_frac=0.001)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    codes, scales, signs = L.quantize(Wd, lattice="e8", tile=256, seed=seed, beta=0.25, dev_status=st)
+    x = gaussian_vectors(8, 14336, 6008, dtype="bf16")
+    y = L.gemv(codes, scales, signs, to_dev_bf16(torch, x), lattice="e8", tile=256, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rng = np.random.default_rng(1)
+    rows = np.sort(np.concatenate([[0, 4095], rng.choice(4096, 62, replace=False)]))
+    W = Wd[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    assert np.abs(W).max() > 0.2          # the sample holds outliers
+    d = O.splitmix64_signs(seed, 14336)
+    q = O.quantize(W, "e8", 256, d, 0.25)
+    np.testing.assert_allclose(scales.cpu().numpy()[rows], q.scales, rtol=1e-6)
+    compare_codes(codes.cpu().numpy()[rows], q, "e8")
+    ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
+    assert normwise_rel(y.cpu().numpy()[:, rows], ref) < 2e-3
