@@ -5,7 +5,9 @@ One step = the whole path over one Llama-3-8B decoder layer (q, k, v, o,
 gate, up, down; bf16 N(0, 0.02^2) weights, seeds 1000..1006):
   quantize every matrix to E8 codes (tile 256, beta 0.25; signs, RHT, scale,
   nearest point, int8 codes + fp32 scales), then the decode GEMV y = W^ x from
-  the codes at batch 1, 4 and 16 (x ~ N(0, 1) bf16) over every matrix.
+  the codes at batch 1, 4 and 16 (x ~ N(0, 1) bf16) over every matrix, one
+  call per group of matrices that share an activation (q+k+v, o, gate+up,
+  down).
 The step is captured once as a CUDA graph and replayed; the timed region is
 exactly K replays between barriers and device synchronisations.
 
@@ -61,18 +63,35 @@ def quantize_bytes(rows, cols, in_bytes=2):
     return rows * cols * (in_bytes + 1 + 4.0 / TILE) + cols
 
 
+# Matrices of a layer that share one activation; each group is one GEMV call
+# (q, k and v read the attention input, gate and up the MLP input).
+LAYER_GROUPS = (("q", "k", "v"), ("o",), ("gate", "up"), ("down",))
+
+
 def gemv_bytes(rows, cols, b, x_bytes=2):
     return rows * cols * (1 + 4.0 / TILE) + cols + b * cols * x_bytes + b * rows * 4
+
+
+def group_gemv_bytes(rows_list, cols, b, x_bytes=2):
+    """One call over matrices sharing x: codes, scales, signs and y of each, x once."""
+    return sum(r * cols * (1 + 4.0 / TILE) + cols + b * r * 4 for r in rows_list) + b * cols * x_bytes
+
+
+def layer_groups(shapes):
+    """Index lists of `shapes` per activation group."""
+    pos = {n: i for i, (n, _, _, _) in enumerate(shapes)}
+    return [[pos[n] for n in grp] for grp in LAYER_GROUPS]
 
 
 def step_bytes(shapes, frac_rows=1.0):
     q = g = 0.0
     per_b = {}
-    for _, r, c, _ in shapes:
-        rr = max(1, int(r * frac_rows))
+    rows = [max(1, int(r * frac_rows)) for _, r, _, _ in shapes]
+    for (_, r, c, _), rr in zip(shapes, rows):
         q += quantize_bytes(rr, c)
     for b in BATCHES:
-        per_b[b] = sum(gemv_bytes(max(1, int(r * frac_rows)), c, b) for _, r, c, _ in shapes)
+        per_b[b] = sum(group_gemv_bytes([rows[i] for i in grp], shapes[grp[0]][2], b)
+                       for grp in layer_groups(shapes))
         g += per_b[b]
     return q, per_b, q + g
 
@@ -355,7 +374,9 @@ def gpu_arm(args, ws, rank, local):
     signs = [torch.empty((c,), dtype=torch.int8, device=dev) for _, _, c, _ in shapes]
     ys = {(b, i): torch.empty((b, r), dtype=torch.float32, device=dev)
           for b in BATCHES for i, (_, r, _, _) in enumerate(shapes)}
-    ws_bytes = max(L.lq_gemv_workspace_size(b, c, TILE) for b in BATCHES for _, _, c, _ in shapes)
+    groups = layer_groups(shapes)
+    ws_bytes = max(L.lq_gemv_grouped_workspace_size(len(grp), b, shapes[grp[0]][2], TILE)
+                   for b in BATCHES for grp in groups)
     work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -365,15 +386,21 @@ def gpu_arm(args, ws, rank, local):
             L.lq_quantize(LATTICE, dev_w[i], TILE, seed, BETA, codes[i], scales[i], signs[i], status)
 
     def gemv_all(b):
-        for i, (n, r, c, seed) in enumerate(shapes):
-            L.lq_gemv(LATTICE, codes[i], scales[i], signs[i], TILE, dev_x[(b, c)], ys[(b, i)], work, status)
+        for grp in groups:
+            x = dev_x[(b, shapes[grp[0]][2])]
+            if len(grp) == 1:
+                i = grp[0]
+                L.lq_gemv(LATTICE, codes[i], scales[i], signs[i], TILE, x, ys[(b, i)], work, status)
+            else:
+                L.lq_gemv_grouped(LATTICE, [codes[i] for i in grp], [scales[i] for i in grp],
+                                  [signs[i] for i in grp], TILE, x, [ys[(b, i)] for i in grp], work, status)
 
     def step():
         quantize_all()
         for b in BATCHES:
             gemv_all(b)
 
-    launches_per_step = 2 * len(shapes) + 2 * len(shapes) * len(BATCHES)
+    launches_per_step = 2 * len(shapes) + 2 * len(groups) * len(BATCHES)
 
     with torch.cuda.stream(stream):
         for _ in range(max(1, args.warmup)):
@@ -494,7 +521,8 @@ def gpu_arm(args, ws, rank, local):
                    "matrices": [f"{n} {r}x{c}" for n, r, c, _ in shapes], "lattice": LATTICE, "tile": TILE,
                    "beta": BETA, "batches": list(BATCHES), "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (436 MB bf16 weights, 218 MB codes per step); no flush",
-                   "graph": "step captured as one CUDA graph"},
+                   "graph": "step captured as one CUDA graph",
+                   "gemv_groups": "q+k+v, o, gate+up, down (one call each, activation shared in a group)"},
         "gpu_launches": launches_per_step * args.steps,
         "parts": parts,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
@@ -568,8 +596,11 @@ def stack_arm(args, ws, rank, local):
                               ).to(torch.bfloat16) for b in batches for c in cols_set}
     ys = {(b, k): torch.empty((b, r), dtype=torch.float32, device=dev)
           for b in batches for k, (_, _, r, _, _) in enumerate(mats)}
-    work = torch.empty(max(L.lq_gemv_workspace_size(b, c, TILE) for b in batches for c in cols_set),
-                       dtype=torch.uint8, device=dev)
+    # activation groups of every layer (matrix indices into mats), in layer order
+    shapes7 = [(n, r, c, 0) for n, r, c in LLAMA3_8B_LAYER]
+    groups = [[7 * layer + i for i in grp] for layer in range(n_layers) for grp in layer_groups(shapes7)]
+    work = torch.empty(max(L.lq_gemv_grouped_workspace_size(len(grp), b, mats[grp[0]][3], TILE)
+                           for b in batches for grp in groups), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -578,8 +609,14 @@ def stack_arm(args, ws, rank, local):
             L.lq_quantize(LATTICE, W[k], TILE, seed, BETA, codes[k], scales[k], signs[k], status)
 
     def gemv_all(b):
-        for k, (_, _, r, c, _) in enumerate(mats):
-            L.lq_gemv(LATTICE, codes[k], scales[k], signs[k], TILE, xs[(b, c)], ys[(b, k)], work, status)
+        for grp in groups:
+            x = xs[(b, mats[grp[0]][3])]
+            if len(grp) == 1:
+                k = grp[0]
+                L.lq_gemv(LATTICE, codes[k], scales[k], signs[k], TILE, x, ys[(b, k)], work, status)
+            else:
+                L.lq_gemv_grouped(LATTICE, [codes[k] for k in grp], [scales[k] for k in grp],
+                                  [signs[k] for k in grp], TILE, x, [ys[(b, k)] for k in grp], work, status)
 
     def step():
         quantize_all()
@@ -613,7 +650,8 @@ def stack_arm(args, ws, rank, local):
     clk = clocks.stop()
     ms_step = max_over_ranks(ws, ms_step, dev)
     qb = sum(quantize_bytes(r, c) for _, _, r, c, _ in mats)
-    gb = {b: sum(gemv_bytes(r, c, b) for _, _, r, c, _ in mats) for b in batches}
+    gb = {b: sum(group_gemv_bytes([mats[k][2] for k in grp], mats[grp[0]][3], b) for grp in groups)
+          for b in batches}
     total = qb + sum(gb.values())
     reps = max(3, min(args.steps, 10))
     ms_q = _graph_ms(torch, graphs["quantize"], stream, reps)
@@ -631,8 +669,9 @@ def stack_arm(args, ws, rank, local):
                    "matrices": len(mats), "weights_bytes": int(sum(w.numel() * 2 for w in W)),
                    "codes_bytes": int(sum(cd.numel() for cd in codes)), "outliers": "0.1% x20",
                    "parallelism": f"replicas{ws}", "l2": "inputs far larger than L2; no flush",
-                   "graph": f"one CUDA graph of {len(mats) * 2 * (1 + len(batches))} launches"},
-        "gpu_launches": len(mats) * 2 * (1 + len(batches)) * args.steps,
+                   "graph": f"one CUDA graph of {2 * len(mats) + 2 * len(groups) * len(batches)} launches",
+                   "gemv_groups": "q+k+v, o, gate+up, down per layer (one call each)"},
+        "gpu_launches": (2 * len(mats) + 2 * len(groups) * len(batches)) * args.steps,
         "parts": {"quantize_gbs": round(qgbs, 1), "quantize_ms": round(ms_q, 3),
                   **{f"gemv_b{b}_gbs": round(gb[b] / (ms_g[b] * 1e-3) / 1e9, 1) for b in batches},
                   **{f"gemv_b{b}_ms": round(ms_g[b], 3) for b in batches}},

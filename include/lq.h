@@ -125,7 +125,8 @@ lq_status lq_dequantize(int lattice, const int8_t* codes_dev, const float* scale
 /*
  * Workspace bytes lq_gemv needs for `batch` activation rows of length `cols`
  * with tile `tile` (the rotated activation split into two fp16 halves plus one
- * float per (row, tile)).
+ * float per (row, tile)).  lq_gemv_grouped_workspace_size(n, ...) is the same
+ * for n matrices (one rotated activation per matrix).
  */
 size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile);
 
@@ -147,6 +148,32 @@ lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,
                   const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
                   const void* x_dev, int xdtype, int batch, float* y_dev,
                   void* workspace_dev, int32_t* dev_status_dev, void* stream);
+
+/*
+ * lq_gemv over a group of n matrices that share one activation x (for example
+ * the q, k and v projections of a transformer layer, or its gate and up
+ * projections), in one launch pair instead of n.  The method's pages describe
+ * the product per linear layer; grouping only merges launches: every result
+ * equals the lq_gemv of that matrix.
+ *   n          1 .. LQ_GEMV_MAX_GROUP
+ *   codes_dev, scales_dev, signs_dev, y_dev
+ *              HOST arrays of n DEVICE pointers, one entry per matrix, each as
+ *              in lq_gemv (matrix m has rows[m] rows, cols columns, its own
+ *              signs and scales, and writes y_dev[m], float32 [batch x rows[m]])
+ *   rows       HOST array of n row counts (0 allowed: that matrix is skipped)
+ *   cols, tile, x_dev, xdtype, batch   shared by the group, as in lq_gemv
+ *   workspace_dev  lq_gemv_grouped_workspace_size(n, batch, cols, tile) bytes,
+ *             16-byte aligned
+ * The host arrays are read during the call only.  Errors as in lq_gemv;
+ * LQ_ERR_ARG when n is out of range.
+ */
+#define LQ_GEMV_MAX_GROUP 8
+size_t lq_gemv_grouped_workspace_size(int n, int batch, int64_t cols, int tile);
+lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* codes_dev,
+                          const float* const* scales_dev, const int8_t* const* signs_dev,
+                          const int64_t* rows, int64_t cols, int tile, const void* x_dev,
+                          int xdtype, int batch, float* const* y_dev, void* workspace_dev,
+                          int32_t* dev_status_dev, void* stream);
 
 /*
  * lq_gemv without a caller-provided workspace (the method's pages have no

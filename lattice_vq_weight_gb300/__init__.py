@@ -33,6 +33,8 @@ SIGNATURES = {
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
     "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "lq_gemv_noalloc": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P]),
+    "lq_gemv_grouped_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I64, _I32]),
+    "lq_gemv_grouped": (_I32, [_I32, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
 }
@@ -163,6 +165,32 @@ def lq_gemv_noalloc(lattice, codes, scales, signs, tile: int, x, y, dev_status=N
     _check("lq_gemv_noalloc", _get_lib().lq_gemv_noalloc(
         _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), rows, cols, int(tile),
         _ptr(x), _dtype_id(x), batch, _ptr(y), _ptr(dev_status), _stream(stream)))
+
+
+# Largest group lq_gemv_grouped takes (LQ_GEMV_MAX_GROUP in lq.h)
+LQ_GEMV_MAX_GROUP = 8
+
+
+def lq_gemv_grouped_workspace_size(n: int, batch: int, cols: int, tile: int) -> int:
+    return int(_get_lib().lq_gemv_grouped_workspace_size(int(n), int(batch), int(cols), int(tile)))
+
+
+def _ptr_array(tensors):
+    arr = (ctypes.c_void_p * len(tensors))(*[None if t is None else t.data_ptr() for t in tensors])
+    return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+
+def lq_gemv_grouped(lattice, codes, scales, signs, tile: int, x, ys, workspace, dev_status=None,
+                    stream=None) -> None:
+    """lq_gemv for n matrices sharing x: lists codes[m], scales[m], signs[m], ys[m]."""
+    n = len(codes)
+    cols = codes[0].shape[1]
+    rows = (ctypes.c_int64 * n)(*[int(c.shape[0]) for c in codes])
+    keep = [_ptr_array(codes), _ptr_array(scales), _ptr_array(signs), _ptr_array(ys)]
+    _check("lq_gemv_grouped", _get_lib().lq_gemv_grouped(
+        _lattice_id(lattice), n, keep[0][1], keep[1][1], keep[2][1], ctypes.cast(rows, ctypes.c_void_p),
+        cols, int(tile), _ptr(x), _dtype_id(x), x.shape[0], keep[3][1], _ptr(workspace), _ptr(dev_status),
+        _stream(stream)))
 
 
 def lq_gemm_workspace_size(M: int, N: int, K: int) -> int:

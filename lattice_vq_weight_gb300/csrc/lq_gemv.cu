@@ -15,8 +15,11 @@
 //     turn them into exact fp16 values (magic-number conversion: the fp16 with
 //     bits 0x6400 | u is 1024 + u), and run m16n8k16 fp16 MMAs with fp32
 //     accumulation against hi and lo.  One accumulator per tile is scaled by
-//     s[r, t] * 2^-e[b, t] and summed; warps that split a row's tiles combine
-//     with fp32 atomics.
+//     s[r, t] * 2^-e[b, t] and summed; warps that split a row combine with
+//     fp32 atomics.
+// Both kernels take a group of up to kGemvMaxMats matrices that share the
+// activation x (for example the q, k and v projections of a layer), each with
+// its own signs, scales and output: one launch pair serves the whole group.
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -28,18 +31,21 @@
 
 namespace lq {
 
+constexpr int kGemvMaxMats = LQ_GEMV_MAX_GROUP;
+
 struct RotateArgs {
   const void* x;
-  const int8_t* signs;
+  const int8_t* signs[kGemvMaxMats];
+  float* y[kGemvMaxMats];
+  int64_t y_elems[kGemvMaxMats];
+  int n_mats;
   int64_t cols;
-  int batch, tile, lanes_per_tile, tiles_per_row, chunks_per_row;
+  int batch, tile, tiles_per_row;
   float post_scale;    // 1 / (2 sqrt(T))
   int a2;              // multiply odd coordinates by sqrt(3)
-  __half* xh;
+  __half* xh;          // [n_mats x batch x cols]
   __half* xl;
-  float* xs;           // [batch x tiles] = 2^-e
-  float* y;
-  int64_t y_elems;
+  float* xs;           // [n_mats x batch x tiles] = 2^-e
   int32_t* status;
 };
 
@@ -55,19 +61,25 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t gtid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = gtid; i < a.y_elems; i += nthreads) a.y[i] = 0.f;
+  for (int m = 0; m < a.n_mats; ++m)
+    for (int64_t i = gtid; i < a.y_elems[m]; i += nthreads) a.y[m][i] = 0.f;
 
+  // thread -> (matrix, activation row, E-column group); rows of x~ are
+  // stored matrix-major: x~ row mb = m * batch + b
   const int64_t per_row = a.cols / E;
-  const int64_t work = (int64_t)a.batch * per_row;
+  const int64_t work = (int64_t)a.n_mats * a.batch * per_row;
   const int lpt = a.tile / E;                            // lanes per tile (<= 32)
   // every lane of a warp takes part in the shuffles; lanes past the end work on zeros
   const bool active = gtid < work;
-  const int64_t b = active ? gtid / per_row : 0;
-  const int64_t col0 = active ? (gtid - b * per_row) * E : 0;
+  const int64_t mb = active ? gtid / per_row : 0;
+  const int64_t col0 = active ? (gtid - mb * per_row) * E : 0;
+  const int m = (int)(mb / a.batch);
+  const int64_t b = mb - (int64_t)m * a.batch;
   float v[E];
   if (active) {
-    if constexpr (BF16) load_bf16_signed<E>(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0, a.signs + col0, v);
-    else load_f32_signed<E>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0, a.signs + col0, v);
+    const int8_t* sg = a.signs[m] + col0;
+    if constexpr (BF16) load_bf16_signed<E>(reinterpret_cast<const __nv_bfloat16*>(a.x) + b * a.cols + col0, sg, v);
+    else load_f32_signed<E>(reinterpret_cast<const float*>(a.x) + b * a.cols + col0, sg, v);
   } else {
 #pragma unroll
     for (int c = 0; c < E; ++c) v[c] = 0.f;
@@ -92,8 +104,8 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
     f = __uint_as_float((uint32_t)(ex + 127) << 23);
   }
   if (active) {
-    uint4* dh = reinterpret_cast<uint4*>(a.xh + b * a.cols + col0);
-    uint4* dl = reinterpret_cast<uint4*>(a.xl + b * a.cols + col0);
+    uint4* dh = reinterpret_cast<uint4*>(a.xh + mb * a.cols + col0);
+    uint4* dl = reinterpret_cast<uint4*>(a.xl + mb * a.cols + col0);
 #pragma unroll
     for (int q = 0; q < E / 8; ++q) {
       uint32_t hw[4], lw[4];
@@ -109,22 +121,30 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
       dh[q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
       dl[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
-    if ((lane & (lpt - 1)) == 0) a.xs[b * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
+    if ((lane & (lpt - 1)) == 0) a.xs[mb * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
 }
 
-struct GemvArgs {
+struct GemvMat {
   const int8_t* codes;
   const float* scales;
-  int64_t rows, cols;
-  int tile, tiles_per_row, batch;
-  const __half* xh;
-  const __half* xl;
-  const float* xs;
   float* y;
-  int64_t items;     // row groups x tiles per row
-  int64_t warps;     // warps of the persistent grid
+  int64_t rows;
+  int64_t groups;        // row groups of 16 RG rows
+  int64_t step_begin;    // first step of this matrix in the group's step order
+};
+
+struct GemvArgs {
+  GemvMat mat[kGemvMaxMats];
+  int n_mats;
+  int64_t cols;
+  int tile, tiles_per_row, batch;
+  const __half* xh;      // [n_mats x batch x cols]
+  const __half* xl;
+  const float* xs;       // [n_mats x batch x tiles]
+  int64_t steps;         // total steps (row group, 64-column slice) of all matrices
+  int64_t warps;         // warps of the persistent grid
 };
 
 // int8 codes (4 per word) -> two f16x2 words holding the exact values.
@@ -156,17 +176,20 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-// Work: items are (row group of 16 RG rows, tile) pairs in row-group-major
-// order; warp w of the persistent grid takes the contiguous item range
-// [w I / W, (w+1) I / W), so every warp streams the same number of code bytes.
-// A warp flushes its per-row sums whenever its range leaves a row group
-// (atomically when it did not cover the whole row).
+// Work: a step is one 64-column slice of one group of 16 RG rows; the steps of
+// all matrices are ordered matrix, row group, column.  Warp w of the
+// persistent grid takes the contiguous step range [w S / W, (w+1) S / W), so
+// every warp streams the same number of code bytes whatever the tile size or
+// the matrices' shapes.  The per-tile scale is applied when a tile ends or
+// the range ends (the tile sum splits linearly), and a warp flushes its
+// per-row sums whenever its range leaves a row group -- with plain stores
+// when it covered the whole row, else with fp32 atomics.
 //
-// Fragment mapping (g = lane/4, q4 = lane%4): within a 64-column step the
-// thread loads 16 code bytes of rows g and g+8 at columns 16 q4 .. 16 q4 + 15;
-// MMA k-chunk c uses bytes 4c .. 4c+3, i.e. k-slots (2 q4, 2 q4+1, 2 q4+8,
-// 2 q4+9) hold columns 16 q4 + 4c + (0, 1, 2, 3).  The activation fragment of
-// column n = g uses the same permutation, so the dot products are unchanged.
+// Fragment mapping (g = lane/4, q4 = lane%4): within a step the thread loads
+// 16 code bytes of rows g and g+8 at columns 16 q4 .. 16 q4 + 15; MMA k-chunk
+// c uses bytes 4c .. 4c+3, i.e. k-slots (2 q4, 2 q4+1, 2 q4+8, 2 q4+9) hold
+// columns 16 q4 + 4c + (0, 1, 2, 3).  The activation fragment of column n = g
+// uses the same permutation, so the dot products are unchanged.
 //
 // Code loads go through a per-thread ring of S stages in shared memory filled
 // with cp.async (each thread reads back only what it copied, so the only wait
@@ -175,7 +198,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // precedes this one, so with programmatic dependent launch the code stream
 // starts while that kernel is still running.
 template <int NB, int RG, int S>
-__global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
+__global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) {
   constexpr int kCode = RG * 2;        // 16-byte code slots per thread per stage
   static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
   extern __shared__ uint4 gemv_ring[];
@@ -185,58 +208,66 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
   uint4* ring = gemv_ring + (size_t)warp * S * kCode * 32;
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-  const int64_t i0 = w * a.items / a.warps;
-  const int64_t i1 = (w + 1) * a.items / a.warps;
-  const int steps = a.tile >> 6;
-  const int64_t n_it = (i1 - i0) * steps;
+  const int64_t i0 = w * a.steps / a.warps;
+  const int64_t i1 = (w + 1) * a.steps / a.warps;
+  const int steps = a.tile >> 6;                 // steps per tile (power of two)
+  const int64_t n_it = i1 - i0;
+  const int per_grp = a.tiles_per_row * steps;          // steps per row group
 
   const bool xok0 = g < a.batch;
   const bool xok1 = NB > 1 && 8 + g < a.batch;
-  const __half* xh0 = a.xh + (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
-  const __half* xl0 = a.xl + (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
-  const __half* xh1 = a.xh + (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
-  const __half* xl1 = a.xl + (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
+  const int64_t xoff0 = (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
+  const int64_t xoff1 = (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
+  const int64_t xmat = (int64_t)a.batch * a.cols;      // x~ elements per matrix
 
-  // Position of a step in the warp's range, advanced one step at a time (no
-  // divisions inside the loop).
+  // Position of a step, advanced one step at a time (divisions only at start).
   struct Cursor {
-    int64_t grp;
-    int t, st;
+    int m, grp, t, st;
   };
   auto start_cursor = [&]() {
     Cursor c;
-    c.grp = i0 / a.tiles_per_row;
-    c.t = (int)(i0 - c.grp * a.tiles_per_row);
-    c.st = 0;
+    c.m = 0;
+    while (c.m + 1 < a.n_mats && i0 >= a.mat[c.m + 1].step_begin) ++c.m;
+    const int64_t local = i0 - a.mat[c.m].step_begin;
+    c.grp = (int)(local / per_grp);
+    const int rem = (int)(local - (int64_t)c.grp * per_grp);
+    c.t = rem / steps;
+    c.st = rem - c.t * steps;
     return c;
   };
   auto advance = [&](Cursor& c) {
     if (++c.st == steps) {
       c.st = 0;
-      if (++c.t == a.tiles_per_row) { c.t = 0; ++c.grp; }
+      if (++c.t == a.tiles_per_row) {
+        c.t = 0;
+        if (++c.grp == a.mat[c.m].groups) { c.grp = 0; ++c.m; }
+      }
     }
   };
   auto kof = [&](const Cursor& c) { return (int64_t)c.t * a.tile + c.st * 64; };
   Cursor ci = start_cursor();   // next step to issue
-  Cursor cx = start_cursor();   // next step whose activations to load
-  Cursor cm = start_cursor();   // step being computed
-  // row pointers of the group the issue cursor is in (recomputed only when
-  // the cursor enters a new row group)
+  Cursor cx = ci;               // next step whose activations to load
+  Cursor cm = ci;               // step being computed
+  // row pointers of the row group the issue cursor is in (recomputed only
+  // when the cursor enters a new row group)
   const int8_t* irow[RG][2];
   bool iok[RG][2];
-  int64_t igrp = -1;
+  int igrp = -1, im = -1;
   int istage = 0;                         // ring stage the next issue writes
   auto issue = [&](int64_t it) {
     if (it < n_it) {
-      if (ci.grp != igrp) {
+      if (ci.grp != igrp || ci.m != im) {
         igrp = ci.grp;
+        im = ci.m;
+        const int8_t* codes = a.mat[im].codes;
+        const int64_t rows = a.mat[im].rows;
 #pragma unroll
         for (int i = 0; i < RG; ++i)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int64_t r = igrp * 16 * RG + 16 * i + 8 * h + g;
-            iok[i][h] = r < a.rows;
-            irow[i][h] = a.codes + (iok[i][h] ? r : 0) * a.cols + 16 * q4;
+            const int64_t r = (int64_t)igrp * 16 * RG + 16 * i + 8 * h + g;
+            iok[i][h] = r < rows;
+            irow[i][h] = codes + (iok[i][h] ? r : 0) * a.cols + 16 * q4;
           }
       }
       const int64_t k0 = kof(ci);
@@ -253,19 +284,19 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
   };
   auto load_x = [&](int64_t it, uint4 (&h)[NB][2], uint4 (&l)[NB][2]) {
     if (it < n_it) {
-      const int64_t k0 = kof(cx);
+      const int64_t k0 = kof(cx) + (int64_t)cx.m * xmat;
       if (xok0) {
-        h[0][0] = __ldg(reinterpret_cast<const uint4*>(xh0 + k0));
-        h[0][1] = __ldg(reinterpret_cast<const uint4*>(xh0 + k0) + 1);
-        l[0][0] = __ldg(reinterpret_cast<const uint4*>(xl0 + k0));
-        l[0][1] = __ldg(reinterpret_cast<const uint4*>(xl0 + k0) + 1);
+        h[0][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0));
+        h[0][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0) + 1);
+        l[0][0] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff0 + k0));
+        l[0][1] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff0 + k0) + 1);
       }
       if constexpr (NB > 1) {
         if (xok1) {
-          h[1][0] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0));
-          h[1][1] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0) + 1);
-          l[1][0] = __ldg(reinterpret_cast<const uint4*>(xl1 + k0));
-          l[1][1] = __ldg(reinterpret_cast<const uint4*>(xl1 + k0) + 1);
+          h[1][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0));
+          h[1][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0) + 1);
+          l[1][0] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff1 + k0));
+          l[1][1] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff1 + k0) + 1);
         }
       }
       advance(cx);
@@ -283,26 +314,28 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
 #pragma unroll
     for (int n = 0; n < NB; ++n)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) yacc[i][n][c] = 0.f;
+      for (int c = 0; c < 4; ++c) yacc[i][n][c] = acc[i][n][c] = 0.f;
   uint4 xhv[NB][2], xlv[NB][2], nxh[NB][2], nxl[NB][2];
 #pragma unroll
   for (int n = 0; n < NB; ++n) xhv[n][0] = xhv[n][1] = xlv[n][0] = xlv[n][1] = nxh[n][0] = nxh[n][1] =
       nxl[n][0] = nxl[n][1] = make_uint4(0, 0, 0, 0);
   load_x(0, xhv, xlv);
-  int64_t cur_grp = -1;
-  int tiles_in_grp = 0;
+  int cur_grp = -1, cur_m = -1, steps_in_grp = 0;
 
-  auto flush = [&](int64_t grp, bool whole_row) {
+  auto flush = [&]() {
+    const bool whole_row = steps_in_grp == per_grp;
+    float* y = a.mat[cur_m].y;
+    const int64_t rows = a.mat[cur_m].rows;
 #pragma unroll
     for (int i = 0; i < RG; ++i)
 #pragma unroll
       for (int n = 0; n < NB; ++n)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int64_t r = grp * 16 * RG + 16 * i + 8 * (c >> 1) + g;
+          const int64_t r = (int64_t)cur_grp * 16 * RG + 16 * i + 8 * (c >> 1) + g;
           const int bb = n * 8 + 2 * q4 + (c & 1);
-          if (r < a.rows && bb < a.batch) {
-            float* dst = a.y + (int64_t)bb * a.rows + r;
+          if (r < rows && bb < a.batch) {
+            float* dst = y + (int64_t)bb * rows + r;
             if (whole_row) *dst = yacc[i][n][c]; else atomicAdd(dst, yacc[i][n][c]);
           }
           yacc[i][n][c] = 0.f;
@@ -312,15 +345,18 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
   for (int64_t it = 0; it < n_it; ++it) {
     issue(it + S - 1);
     load_x(it + 1, nxh, nxl);
-    const int64_t grp = cm.grp;
+    const int grp = cm.grp;
+    const int m = cm.m;
     const int t = cm.t;
     const int st = cm.st;
     advance(cm);
-    if (grp != cur_grp) {
-      if (cur_grp >= 0) flush(cur_grp, tiles_in_grp == a.tiles_per_row);
+    if (grp != cur_grp || m != cur_m) {
+      if (cur_grp >= 0) flush();
       cur_grp = grp;
-      tiles_in_grp = 0;
+      cur_m = m;
+      steps_in_grp = 0;
     }
+    ++steps_in_grp;
     cp_async_wait<S - 1>();
     const uint4* slot = ring + (size_t)(it & (S - 1)) * kCode * 32 + lane;
     uint4 cw[RG][2];
@@ -328,14 +364,6 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
     for (int i = 0; i < RG; ++i) {
       cw[i][0] = slot[(2 * i) * 32];
       cw[i][1] = slot[(2 * i + 1) * 32];
-    }
-    if (st == 0) {
-#pragma unroll
-      for (int i = 0; i < RG; ++i)
-#pragma unroll
-        for (int n = 0; n < NB; ++n)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -363,23 +391,26 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
         }
       }
     }
-    if (st == steps - 1) {
+    if (st == steps - 1 || it == n_it - 1) {
       // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
+      const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
+      const float* scales = a.mat[m].scales + t;
+      const int64_t rows = a.mat[m].rows;
       float fx[NB][2];
 #pragma unroll
       for (int n = 0; n < NB; ++n)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int bb = n * 8 + 2 * q4 + h;
-          fx[n][h] = (bb < a.batch) ? __ldg(a.xs + (int64_t)bb * a.tiles_per_row + t) : 0.f;
+          fx[n][h] = (bb < a.batch) ? __ldg(xs + (int64_t)bb * a.tiles_per_row) : 0.f;
         }
 #pragma unroll
       for (int i = 0; i < RG; ++i) {
         float sr[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int64_t r = grp * 16 * RG + 16 * i + 8 * h + g;
-          sr[h] = (r < a.rows) ? __ldg(a.scales + r * a.tiles_per_row + t) : 0.f;
+          const int64_t r = (int64_t)grp * 16 * RG + 16 * i + 8 * h + g;
+          sr[h] = (r < rows) ? __ldg(scales + r * a.tiles_per_row) : 0.f;
         }
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
@@ -387,9 +418,10 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
           yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
           yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
           yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
         }
       }
-      ++tiles_in_grp;
     }
 #pragma unroll
     for (int n = 0; n < NB; ++n) {
@@ -398,7 +430,7 @@ __global__ void __launch_bounds__(128) gemv_kernel(GemvArgs a) {
     }
   }
   cp_async_wait<0>();
-  if (cur_grp >= 0) flush(cur_grp, tiles_in_grp == a.tiles_per_row);
+  if (cur_grp >= 0) flush();
 }
 
 }  // namespace lq
@@ -413,15 +445,20 @@ struct GemvWorkspace {
   size_t xh, xl, xs, total;
 };
 
-GemvWorkspace gemv_workspace_layout(int batch, int64_t cols, int tile) {
+GemvWorkspace gemv_workspace_layout(int n_mats, int batch, int64_t cols, int tile) {
   GemvWorkspace w;
-  const size_t half_bytes = align256((size_t)batch * (size_t)cols * 2);
+  const size_t rows = (size_t)n_mats * (size_t)batch;
+  const size_t half_bytes = align256(rows * (size_t)cols * 2);
   w.xh = 0;
   w.xl = half_bytes;
   w.xs = 2 * half_bytes;
-  w.total = w.xs + align256((size_t)batch * (size_t)(cols / tile) * 4);
+  w.total = w.xs + align256(rows * (size_t)(cols / tile) * 4);
   return w;
 }
+
+// Minimum steps per warp: below it the ring fill and flush of a warp cost more
+// than its share of the stream.
+constexpr int64_t kMinStepsPerWarp = 4;
 
 template <int NB, int RG>
 lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
@@ -440,11 +477,18 @@ lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
   }
   const int sms = device_sm_count();
   if (sms <= 0) return LQ_ERR_CUDA;
-  const int64_t groups = (a.rows + 16 * RG - 1) / (16 * RG);
-  a.items = groups * a.tiles_per_row;
+  const int64_t steps_per_grp = (int64_t)a.tiles_per_row * (a.tile >> 6);
+  int64_t total = 0;
+  for (int m = 0; m < a.n_mats; ++m) {
+    a.mat[m].groups = (a.mat[m].rows + 16 * RG - 1) / (16 * RG);
+    a.mat[m].step_begin = total;
+    total += a.mat[m].groups * steps_per_grp;
+  }
+  a.steps = total;
   int64_t ctas = (int64_t)sms * per_sm;
-  const int64_t need = (a.items + kWarps - 1) / kWarps;   // at least one item per warp
+  const int64_t need = (total + kWarps * kMinStepsPerWarp - 1) / (kWarps * kMinStepsPerWarp);
   if (ctas > need) ctas = need;
+  if (ctas < 1) ctas = 1;
   a.warps = ctas * kWarps;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
@@ -463,49 +507,66 @@ lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
   return LQ_OK;
 }
 
-}  // namespace
-
-extern "C" size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile) {
-  if (batch <= 0 || cols <= 0 || tile <= 0) return 0;
-  return gemv_workspace_layout(batch, cols, tile).total;
-}
-
-extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,
-                             const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
-                             const void* x_dev, int xdtype, int batch, float* y_dev,
-                             void* workspace_dev, int32_t* dev_status_dev, void* stream) {
-  lq_status st = validate_common(lattice, rows, cols, tile);
+// Validation and both launches for a group of n matrices sharing x.
+lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const float* const* scales_dev,
+                     const int8_t* const* signs_dev, const int64_t* rows, int64_t cols, int tile,
+                     const void* x_dev, int xdtype, int batch, float* const* y_dev, void* workspace_dev,
+                     int32_t* dev_status_dev, cudaStream_t s) {
+  if (n < 1 || n > kGemvMaxMats) return LQ_ERR_ARG;
+  if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || rows == nullptr ||
+      y_dev == nullptr)
+    return LQ_ERR_ARG;
+  lq_status st = validate_common(lattice, 0, cols, tile);
   if (st != LQ_OK) return st;
   if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
   if (batch < 1 || batch > 16) return LQ_ERR_SHAPE;
-  if (rows == 0) return LQ_OK;
-  if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || x_dev == nullptr ||
-      y_dev == nullptr || workspace_dev == nullptr)
+  int64_t total_rows = 0;
+  for (int m = 0; m < n; ++m) {
+    st = validate_common(lattice, rows[m], cols, tile);
+    if (st != LQ_OK) return st;
+    total_rows += rows[m];
+  }
+  if (total_rows == 0) return LQ_OK;
+  if (x_dev == nullptr || workspace_dev == nullptr) return LQ_ERR_ARG;
+  if (!aligned16(x_dev) || !aligned16(workspace_dev) || (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
     return LQ_ERR_ARG;
-  if (!aligned16(codes_dev) || !aligned16(signs_dev) || !aligned16(x_dev) || !aligned16(workspace_dev) ||
-      !aligned4(scales_dev) || !aligned4(y_dev) || (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
-    return LQ_ERR_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  const GemvWorkspace lay = gemv_workspace_layout(batch, cols, tile);
+  for (int m = 0; m < n; ++m) {
+    if (signs_dev[m] == nullptr || !aligned16(signs_dev[m])) return LQ_ERR_ARG;
+    if (rows[m] == 0) continue;
+    if (codes_dev[m] == nullptr || scales_dev[m] == nullptr || y_dev[m] == nullptr) return LQ_ERR_ARG;
+    if (!aligned16(codes_dev[m]) || !aligned4(scales_dev[m]) || !aligned4(y_dev[m])) return LQ_ERR_ARG;
+  }
+  const GemvWorkspace lay = gemv_workspace_layout(n, batch, cols, tile);
   char* ws = reinterpret_cast<char*>(workspace_dev);
+  // matrices without rows take no part (the kernels see only the others)
+  int idx[kGemvMaxMats];
+  int ne = 0;
+  for (int m = 0; m < n; ++m)
+    if (rows[m] > 0) idx[ne++] = m;
 
-  RotateArgs r;
-  r.x = x_dev; r.signs = signs_dev; r.cols = cols; r.batch = batch; r.tile = tile;
-  r.lanes_per_tile = tile / kLaneElems; r.tiles_per_row = (int)(cols / tile);
-  r.chunks_per_row = (int)((cols + kChunkCols - 1) / kChunkCols);
+  RotateArgs r = {};
+  r.x = x_dev; r.n_mats = ne; r.cols = cols; r.batch = batch; r.tile = tile;
+  r.tiles_per_row = (int)(cols / tile);
   r.post_scale = (float)(0.5 / sqrt((double)tile));
   r.a2 = (lattice == LQ_A2);
   r.xh = reinterpret_cast<__half*>(ws + lay.xh);
   r.xl = reinterpret_cast<__half*>(ws + lay.xl);
   r.xs = reinterpret_cast<float*>(ws + lay.xs);
-  r.y = y_dev; r.y_elems = (int64_t)batch * rows; r.status = dev_status_dev;
-  // One thread per E activation columns (a few CTAs), which also zero y; the
-  // small grid leaves the SMs free for the GEMV launched right after it
-  // (programmatic dependent launch).
+  r.status = dev_status_dev;
+  int64_t max_y = 0;
+  for (int j = 0; j < ne; ++j) {
+    r.signs[j] = signs_dev[idx[j]];
+    r.y[j] = y_dev[idx[j]];
+    r.y_elems[j] = (int64_t)batch * rows[idx[j]];
+    if (r.y_elems[j] > max_y) max_y = r.y_elems[j];
+  }
+  // One thread per E activation columns of every (matrix, row) (a few CTAs),
+  // which also zero y; the small grid leaves the SMs free for the GEMV
+  // launched right after it (programmatic dependent launch).
   const int E = act_elems_for_tile(tile);
-  const int64_t rot_threads = (int64_t)batch * (cols / E);
+  const int64_t rot_threads = (int64_t)ne * batch * (cols / E);
   int64_t rgrid = (rot_threads + 255) / 256;
-  const int64_t zgrid = ((int64_t)batch * rows + 256 * 16 - 1) / (256 * 16);
+  const int64_t zgrid = (max_y + 256 * 16 - 1) / (256 * 16);
   if (rgrid < zgrid) rgrid = zgrid;
   if (rgrid < 1) rgrid = 1;
   const bool bf = (xdtype == LQ_BF16);
@@ -522,13 +583,55 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   st = check_launch();
   if (st != LQ_OK) return st;
 
-  GemvArgs g;
-  g.codes = codes_dev; g.scales = scales_dev; g.rows = rows; g.cols = cols; g.tile = tile;
-  g.tiles_per_row = (int)(cols / tile); g.batch = batch;
-  g.xh = r.xh; g.xl = r.xl; g.xs = r.xs; g.y = y_dev;
-  g.items = 0; g.warps = 1;
+  GemvArgs g = {};
+  for (int j = 0; j < ne; ++j) {
+    g.mat[j].codes = codes_dev[idx[j]];
+    g.mat[j].scales = scales_dev[idx[j]];
+    g.mat[j].y = y_dev[idx[j]];
+    g.mat[j].rows = rows[idx[j]];
+  }
+  g.n_mats = ne;
+  g.cols = cols; g.tile = tile; g.tiles_per_row = (int)(cols / tile); g.batch = batch;
+  g.xh = r.xh; g.xl = r.xl; g.xs = r.xs;
   if (batch <= 8) return launch_gemv<1, 2>(g, s);
   return launch_gemv<2, 2>(g, s);
+}
+
+}  // namespace
+
+extern "C" size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile) {
+  if (batch <= 0 || cols <= 0 || tile <= 0) return 0;
+  return gemv_workspace_layout(1, batch, cols, tile).total;
+}
+
+extern "C" size_t lq_gemv_grouped_workspace_size(int n, int batch, int64_t cols, int tile) {
+  if (n <= 0 || batch <= 0 || cols <= 0 || tile <= 0) return 0;
+  return gemv_workspace_layout(n, batch, cols, tile).total;
+}
+
+extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                             const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                             const void* x_dev, int xdtype, int batch, float* y_dev,
+                             void* workspace_dev, int32_t* dev_status_dev, void* stream) {
+  lq_status st = validate_common(lattice, rows, cols, tile);
+  if (st != LQ_OK) return st;
+  if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
+  if (batch < 1 || batch > 16) return LQ_ERR_SHAPE;
+  if (rows == 0) return LQ_OK;
+  if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || x_dev == nullptr ||
+      y_dev == nullptr || workspace_dev == nullptr)
+    return LQ_ERR_ARG;
+  return gemv_group(lattice, 1, &codes_dev, &scales_dev, &signs_dev, &rows, cols, tile, x_dev, xdtype, batch,
+                    &y_dev, workspace_dev, dev_status_dev, (cudaStream_t)stream);
+}
+
+extern "C" lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* codes_dev,
+                                     const float* const* scales_dev, const int8_t* const* signs_dev,
+                                     const int64_t* rows, int64_t cols, int tile, const void* x_dev, int xdtype,
+                                     int batch, float* const* y_dev, void* workspace_dev,
+                                     int32_t* dev_status_dev, void* stream) {
+  return gemv_group(lattice, n, codes_dev, scales_dev, signs_dev, rows, cols, tile, x_dev, xdtype, batch, y_dev,
+                    workspace_dev, dev_status_dev, (cudaStream_t)stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -85,5 +85,10 @@ def test_argument_errors_are_synchronous():
     assert g(1, tile=2048, cols=3072) == L.LQ_ERR_SHAPE         # cols % tile
     assert lib.lq_dequantize(8, good, good, good, 4, 256, 256, good, 5, s) == L.LQ_ERR_DTYPE
     assert lib.lq_make_signs(0, -1, good, s) == L.LQ_ERR_SHAPE
+    arr = (ctypes.c_void_p * 9)(*([0x10000] * 9))
+    rows = (ctypes.c_int64 * 9)(*([4] * 9))
+    gg = lambda n: lib.lq_gemv_grouped(8, n, arr, arr, arr, rows, 256, 256, good, 1, 1, arr, good, nul, s)
+    assert gg(0) == L.LQ_ERR_ARG and gg(9) == L.LQ_ERR_ARG      # group size 1 .. 8
+    assert L.lq_gemv_grouped_workspace_size(3, 2, 4096, 256) >= 3 * 2 * 4096 * 4   # hi + lo fp16 per matrix
     assert L.lq_gemv_workspace_size(1, 4096, 256) >= 4096 * 4
     assert L.lq_gemv_workspace_size(0, 4096, 256) == 0

@@ -101,3 +101,53 @@ def test_full_size_down_matrix_sampled_rows(batch):
     torch.cuda.synchronize()
     ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
     assert normwise_rel(y.cpu().numpy()[:, rows], ref) < TOL
+
+
+@pytest.mark.parametrize("tile", [128, 256, 2048])
+@pytest.mark.parametrize("batch", [1, 5, 16])
+def test_grouped_gemv_parity(tile, batch):
+    """Three matrices of different heights (one without rows) sharing x, each with
+    its own signs and scales, in one grouped call: each y against the oracle."""
+    torch, L = cuda()
+    cols = 2 * tile if tile >= 1024 else 2048 + tile
+    heights = [75, 0, 130, 33]
+    mats, refs = [], []
+    x = gaussian_vectors(batch, cols, 900 + batch, dtype="bf16")
+    for k, rows in enumerate(heights):
+        W = gaussian_matrix(max(rows, 1), cols, 0.02, 910 + k, dtype="bf16")[:rows]
+        d = O.splitmix64_signs(920 + k, cols)
+        q = O.quantize(W, "e8", tile, d, 0.25)
+        mats.append((to_dev(torch, q.codes.reshape(rows, cols)), to_dev(torch, q.scales.reshape(rows, cols // tile)),
+                     to_dev(torch, d)))
+        refs.append(O.gemv(q.codes, q.scales, d, tile, "e8", x) if rows else None)
+    ys = [torch.full((batch, rows), float("nan"), dtype=torch.float32, device="cuda") for rows in heights]
+    ws = torch.empty(L.lq_gemv_grouped_workspace_size(len(mats), batch, cols, tile), dtype=torch.uint8,
+                     device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.lq_gemv_grouped("e8", [m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], tile,
+                      to_dev_bf16(torch, x), ys, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for y, ref in zip(ys, refs):
+        if ref is not None:
+            assert normwise_rel(y.cpu().numpy(), ref) < TOL
+
+
+def test_grouped_gemv_matches_single_calls():
+    """Grouping merges launches only: q/k/v-shaped matrices (4096, 1024, 1024 rows x
+    4096) give the results of three lq_gemv calls (to fp32 summation order)."""
+    torch, L = cuda()
+    from synthetic import torch_gaussian_matrix
+    cols, tile = 4096, 256
+    mats = []
+    for k, rows in enumerate((4096, 1024, 1024)):
+        W = torch_gaussian_matrix(rows, cols, 0.02, 930 + k, device="cuda")
+        mats.append(L.quantize(W, lattice="e8", tile=tile, seed=930 + k, beta=0.25))
+    x = torch.randn((4, cols), device="cuda").to(torch.bfloat16)
+    singles = [L.gemv(c, s, g, x, lattice="e8", tile=tile) for c, s, g in mats]
+    ys = [torch.empty((4, c.shape[0]), dtype=torch.float32, device="cuda") for c, _, _ in mats]
+    ws = torch.empty(L.lq_gemv_grouped_workspace_size(3, 4, cols, tile), dtype=torch.uint8, device="cuda")
+    L.lq_gemv_grouped("e8", [m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], tile, x, ys, ws)
+    torch.cuda.synchronize()
+    for y, y1 in zip(ys, singles):
+        assert normwise_rel(y.cpu().numpy(), y1.cpu().numpy()) < 1e-6
