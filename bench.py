@@ -14,7 +14,8 @@ exactly K replays between barriers and device synchronisations.
 value  = algorithmic bytes of the step / step time (GB/s, whole job over all ranks)
 e2e    = the same bytes / time of a step that also copies the layer's weights
          and activations from pinned host memory and reads codes, scales and
-         y back to the host
+         y back to the host (copies in, kernels and copies out pipelined on
+         three streams, row piece by row piece, one CUDA graph per step)
 parts  = quantize GB/s, GEMV GB/s per batch, and (when available) the prefill
          GEMM TFLOP/s on the Llama-3-70B MLP shapes
 roofline = the quantize kernel (largest share of the step) against the measured
@@ -471,25 +472,75 @@ def gpu_arm(args, ws, rank, local):
     h2d = sum(w.numel() * 2 for w in host_w) + sum(x.numel() * 2 for x in host_x.values())
     d2h = sum(c.numel() for c in codes) + sum(s.numel() * 4 for s in scales) + sum(v.numel() * 4 for v in ys.values())
 
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            for i in range(len(shapes)):
-                dev_w[i].copy_(host_w[i], non_blocking=True)
+    # One step end to end, pipelined over three streams and captured as one graph:
+    # s_in copies x and the weights in (row piece by row piece), `stream`
+    # quantizes each piece as soon as it has landed and then runs the GEMVs,
+    # s_out copies each piece's codes and scales out as soon as they are
+    # written, then y.  The host link (about 0.2 TB/s each way here) bounds it.
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+
+    # row pieces of about 16 MB of bf16 weights, so that copies in, quantize and
+    # copies out overlap with a short head and tail
+    def pieces(r, c):
+        step = max(1, (8 << 20) // c)
+        return [(r0, min(r, r0 + step)) for r0 in range(0, r, step)]
+
+    def e2e_body():
+        start = torch.cuda.Event()
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        work_items = []          # (matrix, r0, r1, event after its copy in)
+        with torch.cuda.stream(s_in):
             for k in host_x:
                 dev_x[k].copy_(host_x[k], non_blocking=True)
-            g_step.replay()
-            for i in range(len(shapes)):
-                h_codes[i].copy_(codes[i], non_blocking=True)
-                h_scales[i].copy_(scales[i], non_blocking=True)
-            for k in ys:
-                h_ys[k].copy_(ys[k], non_blocking=True)
+            for i, (n, r, c, seed) in enumerate(shapes):
+                for r0, r1 in pieces(r, c):
+                    dev_w[i][r0:r1].copy_(host_w[i][r0:r1], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s_in)
+                    work_items.append((i, r0, r1, ev))
+        done_q = []
+        with torch.cuda.stream(stream):
+            for i, r0, r1, ev_in in work_items:
+                stream.wait_event(ev_in)
+                seed = shapes[i][3]
+                L.lq_quantize(LATTICE, dev_w[i][r0:r1], TILE, seed, BETA, codes[i][r0:r1], scales[i][r0:r1],
+                              signs[i], status)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+                done_q.append((i, r0, r1, ev))
+        with torch.cuda.stream(s_out):
+            for i, r0, r1, ev in done_q:
+                s_out.wait_event(ev)
+                h_codes[i][r0:r1].copy_(codes[i][r0:r1], non_blocking=True)
+                h_scales[i][r0:r1].copy_(scales[i][r0:r1], non_blocking=True)
+        for b in BATCHES:
+            with torch.cuda.stream(stream):
+                gemv_all(b)
+                ev = torch.cuda.Event()
+                ev.record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev)
+                for i in range(len(shapes)):
+                    h_ys[(b, i)].copy_(ys[(b, i)], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        stream.wait_event(done)
 
-    e2e_step()
+    with torch.cuda.stream(stream):
+        e2e_body()
+    torch.cuda.synchronize(dev)
+    g_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_e2e, stream=stream):
+        e2e_body()
+    g_e2e.replay()
     torch.cuda.synchronize(dev)
     barrier(ws)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        e2e_step()
+        g_e2e.replay()
     torch.cuda.synchronize(dev)
     barrier(ws)
     e2e_ms = max_over_ranks(ws, (time.perf_counter() - t0) * 1e3 / args.steps, dev)
