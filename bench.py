@@ -16,8 +16,9 @@ e2e    = the same bytes / time of a step that also copies the layer's weights
          and activations from pinned host memory and reads codes, scales and
          y back to the host (copies in, kernels and copies out pipelined on
          three streams, row piece by row piece, one CUDA graph per step)
-parts  = quantize GB/s, GEMV GB/s per batch, and (when available) the prefill
-         GEMM TFLOP/s on the Llama-3-70B MLP shapes
+parts  = quantize GB/s, GEMV GB/s per batch, the Rice format of the same codes
+         (bits per weight, encode GB/s, GEMV-from-stream GB/s per batch) and
+         the prefill GEMM TFLOP/s on the Llama-3-70B MLP shapes
 roofline = the quantize kernel (largest share of the step) against the measured
          HBM copy bandwidth
 
@@ -548,6 +549,9 @@ def gpu_arm(args, ws, rank, local):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed region")
 
+    # ---- Rice format of the same codes: encode, and the GEMV from the stream
+    rice = rice_part(L, torch, dev, stream, shapes, codes, scales, signs, dev_x, reps=max(3, min(args.steps, 10)))
+
     # ---- prefill GEMM (Llama-3-70B MLP shapes), when the library provides it
     gemm = None
     if not args.no_gemm:
@@ -584,6 +588,7 @@ def gpu_arm(args, ws, rank, local):
                      "traffic": traffic},
         "clocks": clk,
     }
+    line["parts"].update(rice)
     if gemm is not None:
         line["parts"].update(gemm)
 
@@ -830,6 +835,67 @@ def quantize_bytes_t(rows, cols, tile, in_bytes=2):
 
 def gemv_bytes_t(rows, cols, b, tile, x_bytes=2):
     return rows * cols * (1 + 4.0 / tile) + cols + b * cols * x_bytes + b * rows * 4
+
+
+def rice_part(L, torch, dev, stream, shapes, codes, scales, signs, dev_x, reps):
+    """Rice stream of the layer's codes: bits per weight, encode GB/s (codes in,
+    stream + offsets out) and GEMV-from-stream GB/s per batch (stream, offsets,
+    scales, signs, x in; y out)."""
+    enc = []
+    for i, (n, r, c, seed) in enumerate(shapes):
+        nbytes = L.lq_rice_stream_bound(LATTICE, r, c, TILE)
+        enc.append((torch.empty(nbytes // 4, dtype=torch.int32, device=dev),
+                    torch.empty((r, c // TILE), dtype=torch.int32, device=dev),
+                    torch.empty(1, dtype=torch.int64, device=dev),
+                    torch.empty(L.lq_rice_workspace_size(r, c, TILE), dtype=torch.uint8, device=dev)))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def encode_all():
+        for i in range(len(shapes)):
+            words, offs, tot, ws = enc[i]
+            L.lq_rice_encode(LATTICE, codes[i], TILE, words, offs, tot, ws, status)
+
+    with torch.cuda.stream(stream):
+        encode_all()
+    torch.cuda.synchronize(dev)
+    bits = [int(e[2].item()) for e in enc]
+    ys = {(b, i): torch.empty((b, r), dtype=torch.float32, device=dev)
+          for b in BATCHES for i, (_, r, _, _) in enumerate(shapes)}
+    work = torch.empty(max(L.lq_gemv_workspace_size(b, c, TILE) for b in BATCHES for _, _, c, _ in shapes),
+                       dtype=torch.uint8, device=dev)
+
+    def gemv_all(b):
+        for i, (n, r, c, seed) in enumerate(shapes):
+            words, offs, _, _ = enc[i]
+            L.lq_gemv_rice(LATTICE, words, offs, scales[i], signs[i], TILE, dev_x[(b, c)], ys[(b, i)], work, status)
+
+    def graph_of(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    out = {}
+    weights = sum(r * c for _, r, c, _ in shapes)
+    stream_bytes = sum(bits) / 8.0
+    offs_bytes = sum(4 * r * (c // TILE) for _, r, c, _ in shapes)
+    g_enc = graph_of(encode_all)
+    ms = _graph_ms(torch, g_enc, stream, reps)
+    out["rice_bits_per_weight"] = round(sum(bits) / weights, 4)
+    out["rice_encode_gbs"] = round((weights + stream_bytes + offs_bytes) / (ms * 1e-3) / 1e9, 1)
+    for b in BATCHES:
+        g = graph_of(lambda b=b: gemv_all(b))
+        ms = _graph_ms(torch, g, stream, reps)
+        nbytes = stream_bytes + sum(4 * r * (c // TILE) * 2 + c + b * c * 2 + b * r * 4 for _, r, c, _ in shapes)
+        out[f"rice_gemv_b{b}_gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+        out[f"rice_gemv_b{b}_ms"] = round(ms, 4)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the Rice part")
+    return out
 
 
 def gemm_part(L, torch, dev, stream, reps):

@@ -60,7 +60,8 @@ typedef enum {
 enum {
     LQ_DEV_NONFINITE = 1,   /* a tile held NaN or Inf: that tile's codes are unspecified */
     LQ_DEV_RANGE = 2,       /* some |code| > 127 (or an fp16 activation overflowed) */
-    LQ_DEV_TIMEOUT = 4      /* a bounded wait on an mbarrier expired; outputs unspecified */
+    LQ_DEV_TIMEOUT = 4,     /* a bounded wait on an mbarrier expired; outputs unspecified */
+    LQ_DEV_FORMAT = 8       /* codes given to the Rice encoder lack the lattice's pinned bits */
 };
 
 typedef enum { LQ_Z1 = 1, LQ_A2 = 2, LQ_D4 = 4, LQ_E8 = 8 } lq_lattice;
@@ -232,6 +233,72 @@ lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
                   const int8_t* signs_dev, int64_t N, int64_t K, int tile,
                   const uint16_t* X_dev, int64_t M, float* Y_dev,
                   void* workspace_dev, int32_t* dev_status_dev, void* stream);
+
+/*
+ * ------------------------------------------------------------------------
+ * Rice format of the codes (HyperQuant page, "Key algorithmic ingredients":
+ * lossless bit-stripping, then Rice entropy codes; mma="bf16" paragraph: the
+ * weight kept as a ~4 bps bitstream that the GEMV decodes directly).  The
+ * pages fix no layout; this library's format is:
+ *  - per block of n codes: E8 and A2 store the block's common parity as one raw
+ *    bit, then the halved codes u_i = floor(c_i / 2); D4 and Z1 codes are even
+ *    and store u_i = c_i / 2.  E8 and D4: the u_i sum to an even number, so
+ *    the last one is stored as floor(u_{n-1} / 2).
+ *  - symbols are zigzag-mapped (z = 2u, or -2u - 1 for u < 0) and Rice coded
+ *    with parameter K: floor(z / 2^K) one-bits, a zero-bit, the K low bits of z
+ *    (least significant first).
+ *  - one segment per (row, tile): K (0..7, the shortest segment, smallest K on
+ *    ties) in 3 bits, then the blocks in column order.  Segments follow each
+ *    other in row-major (row, tile) order without padding; stream bit b is bit
+ *    (b mod 32) of 32-bit word b / 32.  tile_offsets[row * tiles + tile] is the
+ *    segment's first bit.
+ * Limits: rows * cols <= 2^28 (offsets are 32-bit bit counts).
+ * ------------------------------------------------------------------------
+ */
+
+/* Bytes a stream may need for these codes (worst case plus 16 bytes of
+ * padding); 0 for invalid shapes. */
+size_t lq_rice_stream_bound(int lattice, int64_t rows, int64_t cols, int tile);
+
+/* Workspace bytes of lq_rice_encode (segment lengths, K values, scan sums). */
+size_t lq_rice_workspace_size(int64_t rows, int64_t cols, int tile);
+
+/*
+ * Encode int8 codes [rows x cols] (as written by lq_quantize) into the Rice
+ * format.
+ *   stream_dev        uint32 words, stream_bytes >= lq_rice_stream_bound(...);
+ *                     zeroed, then written; 16-byte aligned
+ *   tile_offsets_dev  uint32 [rows x cols/tile] (written)
+ *   total_bits_dev    one uint64 (written): the stream's length in bits
+ *   workspace_dev     lq_rice_workspace_size(...) bytes, 256-byte aligned
+ *   dev_status_dev    LQ_DEV_FORMAT when a block lacks the pinned bits (its
+ *                     segment then does not decode to the same codes)
+ * Six kernels run on `stream` (lengths, three scan passes, bits).
+ */
+lq_status lq_rice_encode(int lattice, const int8_t* codes_dev, int64_t rows, int64_t cols, int tile,
+                         uint32_t* stream_dev, size_t stream_bytes, uint32_t* tile_offsets_dev,
+                         uint64_t* total_bits_dev, void* workspace_dev, int32_t* dev_status_dev,
+                         void* stream);
+
+/*
+ * Decode a Rice stream back into int8 codes [rows x cols] (written).  Reads
+ * never go past stream_bytes (bits beyond it read as zero).
+ */
+lq_status lq_rice_decode(int lattice, const uint32_t* stream_dev, size_t stream_bytes,
+                         const uint32_t* tile_offsets_dev, int64_t rows, int64_t cols, int tile,
+                         int8_t* codes_dev, void* stream);
+
+/*
+ * lq_gemv computed from the Rice stream instead of int8 codes: the codes are
+ * decoded inside the product (never written to memory).  Arguments as in
+ * lq_gemv, with (stream_dev, stream_bytes, tile_offsets_dev) in place of
+ * codes_dev; workspace_dev has lq_gemv_workspace_size(batch, cols, tile) bytes.
+ */
+lq_status lq_gemv_rice(int lattice, const uint32_t* stream_dev, size_t stream_bytes,
+                       const uint32_t* tile_offsets_dev, const float* scales_dev,
+                       const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                       const void* x_dev, int xdtype, int batch, float* y_dev, void* workspace_dev,
+                       int32_t* dev_status_dev, void* stream);
 
 #ifdef __cplusplus
 }

@@ -15,7 +15,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "liblq.so")
 
 LQ_OK, LQ_ERR_ARG, LQ_ERR_SHAPE, LQ_ERR_DTYPE, LQ_ERR_CUDA, LQ_ERR_UNSUPPORTED = range(6)
-LQ_DEV_NONFINITE, LQ_DEV_RANGE, LQ_DEV_TIMEOUT = 1, 2, 4
+LQ_DEV_NONFINITE, LQ_DEV_RANGE, LQ_DEV_TIMEOUT, LQ_DEV_FORMAT = 1, 2, 4, 8
 LQ_Z1, LQ_A2, LQ_D4, LQ_E8 = 1, 2, 4, 8
 LQ_F32, LQ_BF16 = 0, 1
 LATTICE_IDS = {"z1": LQ_Z1, "a2": LQ_A2, "d4": LQ_D4, "e8": LQ_E8}
@@ -37,6 +37,12 @@ SIGNATURES = {
     "lq_gemv_grouped": (_I32, [_I32, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
     "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
+    "lq_rice_stream_bound": (ctypes.c_size_t, [_I32, _I64, _I64, _I32]),
+    "lq_rice_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I32]),
+    "lq_rice_encode": (_I32, [_I32, _P, _I64, _I64, _I32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P]),
+    "lq_rice_decode": (_I32, [_I32, _P, ctypes.c_size_t, _P, _I64, _I64, _I32, _P, _P]),
+    "lq_gemv_rice": (_I32, [_I32, _P, ctypes.c_size_t, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P,
+                            _P, _P]),
 }
 
 
@@ -205,6 +211,43 @@ def lq_gemm(lattice, codes, scales, signs, tile: int, X, Y, workspace, dev_statu
     _check("lq_gemm", _get_lib().lq_gemm(
         _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), N, K, int(tile), _ptr(X), M,
         _ptr(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def lq_rice_stream_bound(lattice, rows: int, cols: int, tile: int) -> int:
+    return int(_get_lib().lq_rice_stream_bound(_lattice_id(lattice), int(rows), int(cols), int(tile)))
+
+
+def lq_rice_workspace_size(rows: int, cols: int, tile: int) -> int:
+    return int(_get_lib().lq_rice_workspace_size(int(rows), int(cols), int(tile)))
+
+
+def lq_rice_encode(lattice, codes, tile: int, stream_words, tile_offsets, total_bits, workspace,
+                   dev_status=None, stream=None) -> None:
+    """codes int8 [rows x cols] -> Rice stream (uint32 words, as int32 tensor), offsets, total bits."""
+    rows, cols = codes.shape
+    _check("lq_rice_encode", _get_lib().lq_rice_encode(
+        _lattice_id(lattice), _ptr(codes), rows, cols, int(tile), _ptr(stream_words),
+        stream_words.numel() * stream_words.element_size(), _ptr(tile_offsets), _ptr(total_bits),
+        _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def lq_rice_decode(lattice, stream_words, tile_offsets, tile: int, codes, stream=None) -> None:
+    rows, cols = codes.shape
+    _check("lq_rice_decode", _get_lib().lq_rice_decode(
+        _lattice_id(lattice), _ptr(stream_words), stream_words.numel() * stream_words.element_size(),
+        _ptr(tile_offsets), rows, cols, int(tile), _ptr(codes), _stream(stream)))
+
+
+def lq_gemv_rice(lattice, stream_words, tile_offsets, scales, signs, tile: int, x, y, workspace,
+                 dev_status=None, stream=None) -> None:
+    """lq_gemv from the Rice stream; y float32 [batch x rows]."""
+    rows = tile_offsets.shape[0]
+    cols = signs.numel()
+    batch = x.shape[0]
+    _check("lq_gemv_rice", _get_lib().lq_gemv_rice(
+        _lattice_id(lattice), _ptr(stream_words), stream_words.numel() * stream_words.element_size(),
+        _ptr(tile_offsets), _ptr(scales), _ptr(signs), rows, cols, int(tile), _ptr(x), _dtype_id(x), batch,
+        _ptr(y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
 
 
 # ------------------------------------------------------------------ allocating helpers

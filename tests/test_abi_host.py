@@ -91,4 +91,11 @@ def test_argument_errors_are_synchronous():
     assert gg(0) == L.LQ_ERR_ARG and gg(9) == L.LQ_ERR_ARG      # group size 1 .. 8
     assert L.lq_gemv_grouped_workspace_size(3, 2, 4096, 256) >= 3 * 2 * 4096 * 4   # hi + lo fp16 per matrix
     assert L.lq_gemv_workspace_size(1, 4096, 256) >= 4096 * 4
+    # Rice format: worst case 8 bits per symbol + parity bits + 3 bits per segment, 16 bytes of padding
+    assert L.lq_rice_stream_bound("e8", 2, 256, 256) == ((2 * 3 + 2 * 256 * 8 + 2 * 32 + 31) // 32) * 4 + 16
+    assert L.lq_rice_stream_bound("e8", 1 << 15, 1 << 14, 256) == 0          # more than 2^28 weights
+    enc = lambda rows, cols, tile, nbytes: lib.lq_rice_encode(8, good, rows, cols, tile, good, nbytes, good,
+                                                             P(0x10008), good, nul, s)
+    assert enc(2, 256, 256, 16) == L.LQ_ERR_SHAPE                  # stream smaller than the bound
+    assert enc(2, 256, 100, 1 << 20) == L.LQ_ERR_UNSUPPORTED
     assert L.lq_gemv_workspace_size(0, 4096, 256) == 0
