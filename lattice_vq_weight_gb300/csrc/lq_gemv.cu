@@ -105,9 +105,12 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
   const int64_t xoff1 = (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
   const int64_t xmat = (int64_t)a.batch * a.cols;      // x~ elements per matrix
 
-  // Position of a step, advanced one step at a time (divisions only at start).
+  // Position of a step: matrix, row group and step s within the group (the
+  // group's steps run along k: s covers columns 64 s .. 64 s + 63), advanced
+  // one step at a time (divisions only at start).
+  const int steps_log2 = __ffs(steps) - 1;
   struct Cursor {
-    int m, grp, t, st;
+    int m, grp, s;
   };
   auto start_cursor = [&]() {
     Cursor c;
@@ -115,21 +118,16 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     while (c.m + 1 < a.n_mats && i0 >= a.mat[c.m + 1].step_begin) ++c.m;
     const int64_t local = i0 - a.mat[c.m].step_begin;
     c.grp = (int)(local / per_grp);
-    const int rem = (int)(local - (int64_t)c.grp * per_grp);
-    c.t = rem / steps;
-    c.st = rem - c.t * steps;
+    c.s = (int)(local - (int64_t)c.grp * per_grp);
     return c;
   };
   auto advance = [&](Cursor& c) {
-    if (++c.st == steps) {
-      c.st = 0;
-      if (++c.t == a.tiles_per_row) {
-        c.t = 0;
-        if (++c.grp == a.mat[c.m].groups) { c.grp = 0; ++c.m; }
-      }
+    if (++c.s == per_grp) {
+      c.s = 0;
+      if (++c.grp == a.mat[c.m].groups) { c.grp = 0; ++c.m; }
     }
   };
-  auto kof = [&](const Cursor& c) { return (int64_t)c.t * a.tile + c.st * 64; };
+  auto kof = [&](const Cursor& c) { return (int64_t)c.s * 64; };
   Cursor ci = start_cursor();   // next step to issue
   Cursor cx = ci;               // next step whose activations to load
   Cursor cm = ci;               // step being computed
@@ -232,8 +230,8 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     load_x(it + 1, nxh, nxl);
     const int grp = cm.grp;
     const int m = cm.m;
-    const int t = cm.t;
-    const int st = cm.st;
+    const int t = cm.s >> steps_log2;
+    const bool tile_end = (cm.s & (steps - 1)) == steps - 1;
     advance(cm);
     if (grp != cur_grp || m != cur_m) {
       if (cur_grp >= 0) flush();
@@ -276,7 +274,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
         }
       }
     }
-    if (st == steps - 1 || it == n_it - 1) {
+    if (tile_end || it == n_it - 1) {
       // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
       const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
       const float* scales = a.mat[m].scales + t;
