@@ -18,7 +18,9 @@ calls, not the procedure; the readings taken here (also in the design notes):
   ch. 2 and 21), so beta = sqrt(10^(-SNR/10) / (G V^(2/n))).
 * Scale for a target rate: bisection on log2(beta) over [-8, 4], 24 halvings;
   the rate decreases as beta grows; the answer is the upper end of the final
-  bracket (rate <= target), reported with its rate and SNR.
+  bracket (rate <= target), reported with its rate and SNR.  A probe whose
+  codes leave int8 counts as above the target (the scale is too fine for the
+  code range).
 """
 from __future__ import annotations
 
@@ -56,8 +58,11 @@ def rate_and_snr(W: np.ndarray, lattice: str, T: int, signs: np.ndarray, beta: f
     return total / float(W.size), snr_db(W, W_hat)
 
 
-def rate_bits(W: np.ndarray, lattice: str, T: int, signs: np.ndarray, beta: float) -> int:
+def rate_bits(W: np.ndarray, lattice: str, T: int, signs: np.ndarray, beta: float):
+    """Bits of the Rice stream at beta, or None when a code leaves int8."""
     q = LO.quantize(W, lattice, T, signs, beta)
+    if q.range_error:
+        return None
     return R.encode(q.codes, lattice, T)[2]
 
 
@@ -69,7 +74,8 @@ def calibrate_bps(W: np.ndarray, lattice: str, T: int, signs: np.ndarray, target
     target_bits = target_bps * W.size
     for _ in range(BISECT_STEPS):
         mid = 0.5 * (lo + hi)
-        if rate_bits(W, lattice, T, signs, float(np.float32(2.0 ** mid))) > target_bits:
+        bits = rate_bits(W, lattice, T, signs, float(np.float32(2.0 ** mid)))
+        if bits is None or bits > target_bits:
             lo = mid
         else:
             hi = mid
