@@ -33,7 +33,8 @@ Other workloads (--workload), each printed as one JSON line of the same form:
   sweep  gate- and down-shaped matrices (seeds 3000 / 3001) over every lattice,
          beta in {0.125, 0.25, 0.5} and tile in {128, 256, 512, 1024, 2048}:
          relative MSE, normalised second moment, code entropy, quantize GB/s
-         and batch-1 GEMV GB/s per run.
+         and batch-1 GEMV GB/s per run; then the scale that meets 3, 4 and 5
+         bits per weight of the Rice stream for every lattice, with its SNR.
 """
 from __future__ import annotations
 
@@ -812,6 +813,18 @@ def sweep_arm(args, ws, rank, local):
                                  "gemv_b1_gbs": round(gemv_bytes_t(r, c, 1, tile) / (ms_g * 1e-3) / 1e9, 1)})
                     del codes, sc, sg, y, wk, What, err, gq, gg
         del W, Wf
+    # rate -> scale calibration (bisection of beta for a target Rice rate) per lattice
+    calib = []
+    Wc = torch_gaussian_matrix(1024, 4096, 1.0, 3002, device=dev)
+    for lat in ("e8", "d4", "a2", "z1"):
+        wsc = torch.empty(L.lq_calibrate_workspace_size(lat, 1024, 4096, TILE), dtype=torch.uint8, device=dev)
+        for target in (3.0, 4.0, 5.0):
+            t0 = time.perf_counter()
+            beta, bps, snr = L.lq_calibrate_bps(lat, TILE, target, Wc, 0, wsc)
+            calib.append({"lattice": lat, "target_bps": target, "beta": round(beta, 6), "bps": round(bps, 4),
+                          "snr_db": round(snr, 3), "closed_form_beta_at_snr": round(L.lq_beta_for_snr(lat, snr), 6),
+                          "ms": round((time.perf_counter() - t0) * 1e3, 2)})
+        del wsc
     e8 = [x for x in runs if x["lattice"] == "e8" and x["tile"] == TILE and x["beta"] == BETA]
     best_q = max(x["quantize_gbs"] for x in runs)
     line = {
@@ -824,6 +837,8 @@ def sweep_arm(args, ws, rank, local):
                    "best_quantize_gbs": best_q},
         "textbook_G": {"e8": 929 / 12960, "d4": 0.076603, "a2": 5 / (36 * math.sqrt(3)), "z1": 1 / 12},
         "runs": runs,
+        "calibration": {"sample": "1024 x 4096 N(0, 1) fp32 (seed 3002), tile 256; 25 quantize + Rice encode "
+                                  "probes per target", "results": calib},
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -300,6 +300,44 @@ lq_status lq_gemv_rice(int lattice, const uint32_t* stream_dev, size_t stream_by
                        const void* x_dev, int xdtype, int batch, float* y_dev, void* workspace_dev,
                        int32_t* dev_status_dev, void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * Rate / SNR calibration (HyperQuant page, usage section and "bps" table: a
+ * calibration sweep maps a target rate in bits per scalar to an SNR, and the
+ * lattice scale follows from a target SNR).  SNR = 10 log10(sum w^2 /
+ * sum (w - w^)^2) in dB.
+ * ------------------------------------------------------------------------
+ */
+
+/* beta giving `snr_db` in the high-resolution regime: sqrt(10^(-snr/10) /
+ * (G V^(2/n))), G the lattice's normalised second moment (Conway & Sloane
+ * table 2.3), V its cell volume at the quantizer's scale.  Host only; 0 for an
+ * invalid lattice. */
+double lq_beta_for_snr(int lattice, double snr_db);
+
+/* sums_dev[0] = sum w^2, sums_dev[1] = sum (w - w^)^2 (double; zeroed first)
+ * over W [rows x ldw] (bf16 or fp32) and W^ float32 [rows x cols]. */
+lq_status lq_error_sums(const void* W_dev, int wdtype, int64_t rows, int64_t cols, int64_t ldw,
+                        const float* What_dev, double* sums_dev, void* stream);
+
+/* Workspace bytes of lq_calibrate_bps (codes, scales, signs, Rice stream and
+ * its workspace, a float32 reconstruction); 0 for unsupported shapes. */
+size_t lq_calibrate_workspace_size(int lattice, int64_t rows, int64_t cols, int tile);
+
+/*
+ * The scale beta at which the Rice rate of the sample W (bits per weight of
+ * the bit-stripped stream) is at most `target_bps`: bisection on log2(beta)
+ * over [-8, 4], 24 halvings, keeping the upper end; each probe quantizes
+ * (signs from `seed`) and encodes on the GPU, and a probe whose codes leave
+ * int8 counts as above the target.  SYNCHRONOUS: returns after the
+ * stream has drained.  result (host, 3 doubles) = {beta, bits per weight,
+ * SNR in dB} at that beta.  LQ_ERR_UNSUPPORTED when the final scale leaves
+ * int8 (targets above about 6 bps) or the sample is not finite.
+ */
+lq_status lq_calibrate_bps(int lattice, int tile, double target_bps, const void* W_dev, int wdtype,
+                           int64_t rows, int64_t cols, int64_t ldw, uint64_t seed, void* workspace_dev,
+                           size_t workspace_bytes, double* result, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,6 +43,11 @@ SIGNATURES = {
     "lq_rice_decode": (_I32, [_I32, _P, ctypes.c_size_t, _P, _I64, _I64, _I32, _P, _P]),
     "lq_gemv_rice": (_I32, [_I32, _P, ctypes.c_size_t, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P,
                             _P, _P]),
+    "lq_beta_for_snr": (ctypes.c_double, [_I32, ctypes.c_double]),
+    "lq_error_sums": (_I32, [_P, _I32, _I64, _I64, _I64, _P, _P, _P]),
+    "lq_calibrate_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I64, _I32]),
+    "lq_calibrate_bps": (_I32, [_I32, _I32, ctypes.c_double, _P, _I32, _I64, _I64, _I64, _U64, _P, ctypes.c_size_t,
+                                _P, _P]),
 }
 
 
@@ -248,6 +253,31 @@ def lq_gemv_rice(lattice, stream_words, tile_offsets, scales, signs, tile: int, 
         _lattice_id(lattice), _ptr(stream_words), stream_words.numel() * stream_words.element_size(),
         _ptr(tile_offsets), _ptr(scales), _ptr(signs), rows, cols, int(tile), _ptr(x), _dtype_id(x), batch,
         _ptr(y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def lq_beta_for_snr(lattice, snr_db: float) -> float:
+    return float(_get_lib().lq_beta_for_snr(_lattice_id(lattice), float(snr_db)))
+
+
+def lq_error_sums(W, W_hat, sums, stream=None) -> None:
+    """sums (float64 device tensor of 2) = (sum w^2, sum (w - w^)^2)."""
+    rows, cols = W.shape
+    _check("lq_error_sums", _get_lib().lq_error_sums(
+        _ptr(W), _dtype_id(W), rows, cols, W.stride(0), _ptr(W_hat), _ptr(sums), _stream(stream)))
+
+
+def lq_calibrate_workspace_size(lattice, rows: int, cols: int, tile: int) -> int:
+    return int(_get_lib().lq_calibrate_workspace_size(_lattice_id(lattice), int(rows), int(cols), int(tile)))
+
+
+def lq_calibrate_bps(lattice, tile: int, target_bps: float, W, seed: int, workspace, stream=None):
+    """(beta, bits per weight, SNR dB) of the scale that meets target_bps on the sample W (synchronous)."""
+    rows, cols = W.shape
+    out = (ctypes.c_double * 3)()
+    _check("lq_calibrate_bps", _get_lib().lq_calibrate_bps(
+        _lattice_id(lattice), int(tile), float(target_bps), _ptr(W), _dtype_id(W), rows, cols, W.stride(0),
+        int(seed), _ptr(workspace), workspace.numel(), ctypes.cast(out, ctypes.c_void_p), _stream(stream)))
+    return float(out[0]), float(out[1]), float(out[2])
 
 
 # ------------------------------------------------------------------ allocating helpers

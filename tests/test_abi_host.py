@@ -98,4 +98,10 @@ def test_argument_errors_are_synchronous():
                                                              P(0x10008), good, nul, s)
     assert enc(2, 256, 256, 16) == L.LQ_ERR_SHAPE                  # stream smaller than the bound
     assert enc(2, 256, 100, 1 << 20) == L.LQ_ERR_UNSUPPORTED
+    # closed-form scale for a target SNR: the library's host function against the oracle
+    import oracle.calibration_oracle as C
+    for lat in ("e8", "d4", "a2", "z1"):
+        for snr in (10.0, 20.0, 30.0):
+            assert abs(L.lq_beta_for_snr(lat, snr) / C.beta_for_snr(lat, snr) - 1) < 1e-6
+    assert L.lq_beta_for_snr(3, 20.0) == 0.0
     assert L.lq_gemv_workspace_size(0, 4096, 256) == 0
