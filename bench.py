@@ -927,6 +927,7 @@ def gemm_part(L, torch, dev, stream, reps):
                             ).to(torch.bfloat16)
             Y = torch.empty((M, N), dtype=torch.float32, device=dev)
             wsz = torch.empty(L.lq_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+            torch.cuda.synchronize(dev)      # inputs were written on the default stream
             try:
                 with torch.cuda.stream(stream):
                     L.lq_gemm("e8", codes, scales, signs, TILE, X, Y, wsz)

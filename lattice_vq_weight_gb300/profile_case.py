@@ -2,13 +2,16 @@
 
     python -m lattice_vq_weight_gb300.profile_case quantize   # the 7 Llama-3-8B layer matrices
     python -m lattice_vq_weight_gb300.profile_case gemv --batch 1
+    python -m lattice_vq_weight_gb300.profile_case gemv --batch 1 --gate-up   # one grouped call
     python -m lattice_vq_weight_gb300.profile_case gemm --M 256
 
 Each op runs `--reps` passes (default 2) after building inputs on the device;
 the second pass is the one to capture (`ncu -s <launches of one pass>`).
 Inputs: bf16 N(0, 0.02^2) weights of the Llama-3-8B layer shapes (gate-shaped
 only with --gate-only), E8, tile 256, beta 0.25; activations N(0, 1) bf16;
-GEMM on the 8192 x 28672 Llama-3-70B up-like shape with X of M rows.
+GEMM on the 8192 x 28672 Llama-3-70B up-like shape with X of M rows.  With
+--gate-up the GEMV is one grouped call over the gate and up matrices (as in
+the benchmark's layer step).
 """
 from __future__ import annotations
 
@@ -28,6 +31,7 @@ def main(argv=None):
     ap.add_argument("--M", type=int, default=256)
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--gate-only", action="store_true")
+    ap.add_argument("--gate-up", action="store_true")
     args = ap.parse_args(argv)
 
     import torch
@@ -49,7 +53,8 @@ def main(argv=None):
         torch.cuda.synchronize()
         print("ok")
         return
-    shapes = [s for s in LLAMA3_8B_LAYER if (not args.gate_only or s[0] == "gate")]
+    keep = ("gate",) if args.gate_only else ("gate", "up") if args.gate_up else None
+    shapes = [s for s in LLAMA3_8B_LAYER if keep is None or s[0] in keep]
     mats = []
     for _, r, c in shapes:
         W = (torch.randn((r, c), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
@@ -63,7 +68,14 @@ def main(argv=None):
     ws = torch.empty(max(L.lq_gemv_workspace_size(args.batch, c, 256) for _, _, c in shapes),
                      dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
+    if args.gate_up:
+        ws = torch.empty(L.lq_gemv_grouped_workspace_size(2, args.batch, 4096, 256), dtype=torch.uint8,
+                         device=dev)
     for _ in range(args.reps):
+        if args.op == "gemv" and args.gate_up:
+            L.lq_gemv_grouped("e8", [m[1] for m in mats], [m[2] for m in mats], [m[3] for m in mats], 256,
+                              mats[0][4], [m[5] for m in mats], ws)
+            continue
         for W, codes, scales, signs, x, y in mats:
             if args.op == "quantize":
                 L.lq_quantize("e8", W, 256, 1, 0.25, codes, scales, signs)
