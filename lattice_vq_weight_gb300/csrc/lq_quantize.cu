@@ -21,6 +21,9 @@ namespace lq {
 // SplitMix64 (Steele, Lea & Flood 2014): output k mixes seed + (k+1) * golden
 // gamma through two xor-shift-multiply rounds; the sign is the top bit.
 __global__ void make_signs_kernel(uint64_t seed, int64_t n, int8_t* signs) {
+  // the quantize kernel launched next may start now: it prefetches its input
+  // and waits for these signs (griddepcontrol.wait) before reading them
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   uint64_t z = seed + (uint64_t)(i + 1) * 0x9E3779B97F4A7C15ull;
@@ -278,6 +281,8 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a)
   };
   int stage = 0;
   stage_in(row, chunk, 0);
+  // the signs come from the kernel launched just before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   for (; row < a.rows; ) {
     int64_t nrow = row;
@@ -495,8 +500,22 @@ static lq_status launch_quantize_mp(const QuantArgs& a, cudaStream_t st) {
   }
   const int grid = persistent_grid(a.units, kQuantThreads / 32, a.chunks_per_row, per_sm);
   if (grid <= 0) return LQ_ERR_CUDA;
-  quantize_kernel<LAT, BF16, MP><<<grid, kQuantThreads, smem, st>>>(a);
-  return check_launch();
+  // programmatic dependent launch after the signs kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kQuantThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP>, a) != cudaSuccess) {
+    cudaGetLastError();
+    return LQ_ERR_CUDA;
+  }
+  return LQ_OK;
 }
 
 // MP = tile bits exchanged through shared memory: log2(tile / 64), at most 3.
