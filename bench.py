@@ -30,6 +30,10 @@ Other workloads (--workload), each printed as one JSON line of the same form:
          drawn on the device), all resident in HBM; one step = quantize all 224
          matrices, then the GEMV at batch 1 and 8 over all of them in layer
          order, captured as one CUDA graph.
+  kv     one decode step of attention over a Llama-3-8B KV cache (32 layers,
+         8 kv heads, 32 query heads, head_dim 128) quantized to E8 codes
+         (tile = head_dim, beta 0.25), at 4 K, 32 K and 128 K cached tokens,
+         computed from the codes; GB/s of cache bytes (codes + scales) read.
   sweep  gate- and down-shaped matrices (seeds 3000 / 3001) over every lattice,
          beta in {0.125, 0.25, 0.5} and tile in {128, 256, 512, 1024, 2048}:
          relative MSE, normalised second moment, code entropy, quantize GB/s
@@ -844,6 +848,75 @@ def sweep_arm(args, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def kv_arm(args, ws, rank, local):
+    """Decode attention over a quantized 32-layer Llama-3-8B KV cache."""
+    import torch
+
+    from lattice_vq_weight_gb300 import build as _build
+    _build.build()
+    import lattice_vq_weight_gb300 as L
+    from synthetic import torch_gaussian_matrix
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    layers, kvh, qh, d = 32, 8, 32, 128
+    results = {}
+    reps = max(3, min(args.steps, 10))
+    for tokens in (4096, 32768, 131072):
+        caches = []
+        for layer in range(layers):
+            pair = []
+            for which in range(2):
+                X = torch_gaussian_matrix(tokens, kvh * d, 1.0, 7000 + 2 * layer + which, device=dev)
+                pair.append(L.quantize(X, lattice="e8", tile=d, seed=7100 + 2 * layer + which, beta=BETA))
+                del X
+            caches.append(pair)
+        q = [torch.randn((qh, d), device=dev, generator=torch.Generator(device=dev).manual_seed(7200 + i)
+                         ).to(torch.bfloat16) for i in range(layers)]
+        out = [torch.empty((qh, d), dtype=torch.float32, device=dev) for _ in range(layers)]
+        wsz = torch.empty(L.lq_attention_workspace_size(tokens, kvh, qh, d), dtype=torch.uint8, device=dev)
+
+        def step():
+            for i, ((kc, ks, kd), (vc, vs, vd)) in enumerate(caches):
+                L.lq_attention_decode("e8", kc, ks, kd, vc, vs, vd, q[i], out[i], wsz)
+
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ms = _graph_ms(torch, g, stream, reps)
+        cache_bytes = layers * 2 * tokens * kvh * (d + 4)
+        results[f"ctx{tokens}"] = {"ms_per_step": round(ms, 4), "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
+                                   "cache_bytes": cache_bytes,
+                                   "compression_vs_bf16": round(2.0 * d / (d + 4), 3)}
+        del caches, q, out, wsz, g
+        torch.cuda.empty_cache()
+    peak, src = hbm_peak("burst")
+    best = max(r["cache_gbs"] for r in results.values())
+    line = {
+        "metric": METRIC, "value": results["ctx32768"]["cache_gbs"], "unit": "GB/s",
+        "n_gpus": ws, "steps": reps, "warmup": args.warmup, "ms_per_step": results["ctx32768"]["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 codes (fp32 compute)",
+        "data": "synthetic",
+        "config": {"workload": "llama3-8b decode attention over an E8-quantized KV cache (32 layers, 8 kv heads, "
+                               "32 q heads, head_dim 128), one graph of 64 launches per step",
+                   "value_is": "cache GB/s at 32 768 tokens", "beta": BETA, "tile": 128},
+        "gpu_launches": layers * 2 * reps,
+        "contexts": results,
+        "roofline": {"kernel": "attn_partial_kernel + attn_combine_kernel", "bound": "hbm", "achieved": best,
+                     "peak": peak, "unit": "GB/s", "frac": round(best / peak, 4), "peak_source": src,
+                     "traffic": None},
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def quantize_bytes_t(rows, cols, tile, in_bytes=2):
     return rows * cols * (in_bytes + 1 + 4.0 / tile) + cols
 
@@ -972,7 +1045,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-frac", type=float, default=0.75)
     ap.add_argument("--reference-frac", type=float, default=1.0 / 64)
-    ap.add_argument("--workload", choices=("layer", "stack", "sweep"), default="layer")
+    ap.add_argument("--workload", choices=("layer", "stack", "sweep", "kv"), default="layer")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
@@ -984,6 +1057,8 @@ def main(argv=None):
             stack_arm(args, ws, rank, local)
         elif args.workload == "sweep":
             sweep_arm(args, ws, rank, local)
+        elif args.workload == "kv":
+            kv_arm(args, ws, rank, local)
         else:
             gpu_arm(args, ws, rank, local)
     finally:

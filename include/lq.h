@@ -338,6 +338,39 @@ lq_status lq_calibrate_bps(int lattice, int tile, double target_bps, const void*
                            int64_t rows, int64_t cols, int64_t ldw, uint64_t seed, void* workspace_dev,
                            size_t workspace_bytes, double* result, void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * KV cache (HyperQuant page, KV-cache section: lattice codes plus one norm per
+ * vector after a random sign rotation; attention on the quantized cache).  A
+ * K or V cache [tokens x kv_heads * head_dim] is quantized with lq_quantize,
+ * tile = head_dim: every (token, head) vector is one tile, its scale the
+ * vector's norm / sqrt(head_dim) * beta.
+ * ------------------------------------------------------------------------
+ */
+
+/* Workspace bytes of lq_attention_decode; 0 for unsupported shapes. */
+size_t lq_attention_workspace_size(int64_t tokens, int kv_heads, int q_heads, int head_dim);
+
+/*
+ * One decode step of attention over quantized K and V caches, computed from
+ * the codes (no dequantized cache in memory):
+ *     out[h] = softmax(K^_g q[h] / sqrt(head_dim)) V^_g,  g = h / (q_heads / kv_heads)
+ *   k_codes_dev, v_codes_dev   int8 [tokens x kv_heads * head_dim]
+ *   k_scales_dev, v_scales_dev float32 [tokens x kv_heads]
+ *   k_signs_dev, v_signs_dev   int8 [kv_heads * head_dim]
+ *   q_dev      [q_heads x head_dim] of type qdtype (LQ_BF16 or LQ_F32)
+ *   out_dev    float32 [q_heads x head_dim] (written)
+ *   head_dim   128;  q_heads / kv_heads in {1, 2, 4, 8};  tokens >= 1
+ *   workspace_dev  lq_attention_workspace_size(...) bytes (workspace_bytes)
+ * Two kernels run on `stream` (per-range partial softmax sums, then the merge
+ * and the inverse rotation).
+ */
+lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev, const float* k_scales_dev,
+                              const int8_t* k_signs_dev, const int8_t* v_codes_dev,
+                              const float* v_scales_dev, const int8_t* v_signs_dev, int64_t tokens,
+                              int kv_heads, int q_heads, int head_dim, const void* q_dev, int qdtype,
+                              float* out_dev, void* workspace_dev, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -48,6 +48,9 @@ SIGNATURES = {
     "lq_calibrate_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I64, _I32]),
     "lq_calibrate_bps": (_I32, [_I32, _I32, ctypes.c_double, _P, _I32, _I64, _I64, _I64, _U64, _P, ctypes.c_size_t,
                                 _P, _P]),
+    "lq_attention_workspace_size": (ctypes.c_size_t, [_I64, _I32, _I32, _I32]),
+    "lq_attention_decode": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _I32, _P, _P,
+                                   ctypes.c_size_t, _P]),
 }
 
 
@@ -278,6 +281,22 @@ def lq_calibrate_bps(lattice, tile: int, target_bps: float, W, seed: int, worksp
         _lattice_id(lattice), int(tile), float(target_bps), _ptr(W), _dtype_id(W), rows, cols, W.stride(0),
         int(seed), _ptr(workspace), workspace.numel(), ctypes.cast(out, ctypes.c_void_p), _stream(stream)))
     return float(out[0]), float(out[1]), float(out[2])
+
+
+def lq_attention_workspace_size(tokens: int, kv_heads: int, q_heads: int, head_dim: int) -> int:
+    return int(_get_lib().lq_attention_workspace_size(int(tokens), int(kv_heads), int(q_heads), int(head_dim)))
+
+
+def lq_attention_decode(lattice, k_codes, k_scales, k_signs, v_codes, v_scales, v_signs, q, out, workspace,
+                        stream=None) -> None:
+    """out [q_heads x d] = softmax(K^ q / sqrt d) V^ from quantized caches [tokens x kv_heads*d]."""
+    tokens = k_codes.shape[0]
+    kv_heads = k_scales.shape[1]
+    q_heads, head_dim = q.shape
+    _check("lq_attention_decode", _get_lib().lq_attention_decode(
+        _lattice_id(lattice), _ptr(k_codes), _ptr(k_scales), _ptr(k_signs), _ptr(v_codes), _ptr(v_scales),
+        _ptr(v_signs), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 # ------------------------------------------------------------------ allocating helpers

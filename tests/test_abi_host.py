@@ -104,4 +104,11 @@ def test_argument_errors_are_synchronous():
         for snr in (10.0, 20.0, 30.0):
             assert abs(L.lq_beta_for_snr(lat, snr) / C.beta_for_snr(lat, snr) - 1) < 1e-6
     assert L.lq_beta_for_snr(3, 20.0) == 0.0
+    # attention: head_dim 128 only, group sizes 1/2/4/8
+    att = lambda kvh, qh, d, ws_bytes=1 << 30: lib.lq_attention_decode(
+        8, good, good, good, good, good, good, 100, kvh, qh, d, good, 1, good, good, ws_bytes, s)
+    assert att(2, 8, 64) == L.LQ_ERR_UNSUPPORTED
+    assert att(4, 6, 128) == L.LQ_ERR_SHAPE and att(2, 6, 128) == L.LQ_ERR_UNSUPPORTED
+    assert att(2, 8, 128, 16) == L.LQ_ERR_SHAPE                      # workspace too small
+    assert L.lq_attention_workspace_size(100, 2, 8, 64) == 0
     assert L.lq_gemv_workspace_size(0, 4096, 256) == 0
