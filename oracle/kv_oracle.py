@@ -18,6 +18,13 @@ readings taken (also listed in the design notes):
 * Decode attention of query head h (kv head h // group, group = q_heads /
   kv_heads): o_h = softmax(K^_h q_h / sqrt(head_dim)) V^_h over all tokens,
   with K^, V^ the dequantized caches -- the textbook definition, float64.
+* The "qjl" rotation (Haar-uniform, "strictly unbiased inner products on
+  average"): a Haar orthogonal matrix Q [d x d] drawn as the Q factor of a
+  Gaussian matrix with the signs of R's diagonal folded in (Mezzadri, "How to
+  generate random matrices from the classical compact groups", Notices AMS
+  2007), applied to every head vector (x -> Q x) before the quantizer's own
+  sign rotation; queries are rotated by the same Q and the attention output is
+  rotated back by Q^T (inner products are unchanged by an orthogonal Q).
 """
 from __future__ import annotations
 
@@ -54,3 +61,20 @@ def attention_from_codes(q, k_codes, k_scales, k_signs, v_codes, v_scales, v_sig
     K_hat = LO.dequantize(k_codes, k_scales, k_signs, head_dim, lattice)
     V_hat = LO.dequantize(v_codes, v_scales, v_signs, head_dim, lattice)
     return attention_decode(q, K_hat, V_hat, kv_heads, head_dim)
+
+
+def haar_rotation(d: int, seed: int) -> np.ndarray:
+    """Haar-distributed orthogonal d x d matrix from a seeded Gaussian matrix."""
+    rng = np.random.default_rng(seed)
+    A = rng.standard_normal((d, d))
+    Q, R = np.linalg.qr(A)
+    return Q * np.sign(np.diag(R))[None, :]
+
+
+def rotate_blocks(X: np.ndarray, Q: np.ndarray, transpose: bool = False) -> np.ndarray:
+    """Every d-column block x of every row of X -> Q x (Q^T x with transpose)."""
+    X = np.asarray(X, dtype=np.float64)
+    d = Q.shape[0]
+    M = Q.T if transpose else Q
+    rows, cols = X.shape
+    return (X.reshape(rows, cols // d, d) @ M.T).reshape(rows, cols)

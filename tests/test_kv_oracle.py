@@ -63,3 +63,27 @@ def test_quantized_attention_tracks_exact_attention():
     ref = KV.attention_decode(q, X, Y, 2, 128)
     rel = np.linalg.norm(o - ref) / np.linalg.norm(ref)
     assert rel < 0.06, rel
+
+
+def test_haar_rotation_is_orthogonal_and_haar_like():
+    Q = KV.haar_rotation(128, 3)
+    np.testing.assert_allclose(Q.T @ Q, np.eye(128), atol=1e-12)
+    assert abs(abs(np.linalg.det(Q)) - 1) < 1e-9
+    # Haar: every entry has mean 0 and variance 1/d (checked over many draws)
+    Qs = np.stack([KV.haar_rotation(16, s) for s in range(400)])
+    assert abs(Qs.mean()) < 0.01 and abs((Qs ** 2).mean() - 1 / 16) < 0.002
+    # the sign fix matters: diag(R) > 0 convention gives E[Q_00] = 0, not a biased sign
+    assert abs(Qs[:, 0, 0].mean()) < 0.05
+
+
+def test_rotated_attention_is_unchanged_without_quantization():
+    """Rotating K, V and q by the same orthogonal Q and the output back by Q^T leaves
+    exact attention unchanged (scores are inner products)."""
+    rng = np.random.default_rng(4)
+    K = rng.standard_normal((40, 256))
+    V = rng.standard_normal((40, 256))
+    q = rng.standard_normal((4, 128))
+    Q = KV.haar_rotation(128, 9)
+    o = KV.attention_decode(q, K, V, 2, 128)
+    o_rot = KV.attention_decode(KV.rotate_blocks(q, Q), KV.rotate_blocks(K, Q), KV.rotate_blocks(V, Q), 2, 128)
+    np.testing.assert_allclose(KV.rotate_blocks(o_rot, Q, transpose=True), o, rtol=1e-10, atol=1e-12)
