@@ -371,6 +371,19 @@ lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev, const floa
                               int kv_heads, int q_heads, int head_dim, const void* q_dev, int qdtype,
                               float* out_dev, void* workspace_dev, size_t workspace_bytes, void* stream);
 
+/*
+ * The "qjl" rotation of the KV cache (HyperQuant page, KV-cache section:
+ * Haar-uniform rotation for unbiased inner products): y = M x for every
+ * head_dim-column block x of every row of X, M = R (transpose = 0) or R^T
+ * (transpose = 1).  R_dev: float32 [head_dim x head_dim] row-major, an
+ * orthogonal matrix drawn by the caller; X [rows x ldx] bf16 or fp32; Y float32
+ * [rows x ldy] (written).  Rotate K/V rows and queries by R before quantizing /
+ * attending, and the attention output back by R^T.  head_dim 128.
+ */
+lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, const void* X_dev,
+                           int xdtype, int64_t rows, int64_t cols, int64_t ldx, float* Y_dev,
+                           int64_t ldy, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

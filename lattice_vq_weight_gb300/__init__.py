@@ -51,6 +51,7 @@ SIGNATURES = {
     "lq_attention_workspace_size": (ctypes.c_size_t, [_I64, _I32, _I32, _I32]),
     "lq_attention_decode": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _P, _I32, _P, _P,
                                    ctypes.c_size_t, _P]),
+    "lq_rotate_blocks": (_I32, [_P, _I32, _I32, _P, _I32, _I64, _I64, _I64, _P, _I64, _P]),
 }
 
 
@@ -297,6 +298,14 @@ def lq_attention_decode(lattice, k_codes, k_scales, k_signs, v_codes, v_scales, 
         _lattice_id(lattice), _ptr(k_codes), _ptr(k_scales), _ptr(k_signs), _ptr(v_codes), _ptr(v_scales),
         _ptr(v_signs), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lq_rotate_blocks(R, X, Y, transpose: bool = False, stream=None) -> None:
+    """Y (float32) = every 128-column block of X rotated by R (or R^T)."""
+    rows, cols = X.shape
+    _check("lq_rotate_blocks", _get_lib().lq_rotate_blocks(
+        _ptr(R), int(bool(transpose)), R.shape[0], _ptr(X), _dtype_id(X), rows, cols, X.stride(0), _ptr(Y),
+        Y.stride(0), _stream(stream)))
 
 
 # ------------------------------------------------------------------ allocating helpers

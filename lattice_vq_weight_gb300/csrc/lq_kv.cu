@@ -242,6 +242,56 @@ __global__ void __launch_bounds__(D) attn_combine_kernel(AttnArgs a, int G) {
   a.out[(int64_t)qh * D + i] = r[i] * (float)a.vsg[kvh * D + i];
 }
 
+// Dense rotation of every D-column block: y = M x with M = R or R^T (R [D x D]
+// row-major, fp32).  M^T is staged in shared memory (64 KB) so that lane j
+// reads M[j][i] conflict-free; each warp rotates one block at a time, lane j
+// computing outputs j, j + 32, j + 64, j + 96.
+struct RotArgs {
+  const float* R;
+  int transpose;
+  const void* X;
+  int xbf16;
+  int64_t rows, blocks_per_row, ldx, ldy;
+  float* Y;
+};
+
+__global__ void __launch_bounds__(256) rotate_blocks_kernel(RotArgs a) {
+  extern __shared__ float rot_smem[];
+  float* mt = rot_smem;                 // mt[i * D + j] = M[j][i]
+  float* xs = rot_smem + D * D;         // one D-vector per warp
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < D * D; e += blockDim.x) {
+    const int i = e / D, j = e % D;
+    mt[e] = a.transpose ? a.R[i * D + j] : a.R[j * D + i];   // M[j][i]
+  }
+  __syncthreads();
+  float* xw = xs + warp * D;
+  const int64_t nvec = a.rows * a.blocks_per_row;
+  for (int64_t v = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; v < nvec;
+       v += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+    const int64_t r = v / a.blocks_per_row, b = v - r * a.blocks_per_row;
+    const int64_t xo = r * a.ldx + b * D;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = lane + 32 * k;
+      xw[i] = a.xbf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.X)[xo + i])
+                      : reinterpret_cast<const float*>(a.X)[xo + i];
+    }
+    __syncwarp();
+    float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) {
+      const float xi = xw[i];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) y[k] = fmaf(mt[i * D + lane + 32 * k], xi, y[k]);
+    }
+    float* yo = a.Y + r * a.ldy + b * D;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) yo[lane + 32 * k] = y[k];
+    __syncwarp();
+  }
+}
+
 }  // namespace kv
 }  // namespace lq
 
@@ -310,5 +360,36 @@ extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev,
   lq_status st = check_launch();
   if (st != LQ_OK) return st;
   attn_combine_kernel<<<(unsigned)q_heads, D, 0, s>>>(a, group);
+  return check_launch();
+}
+
+extern "C" lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, const void* X_dev,
+                                      int xdtype, int64_t rows, int64_t cols, int64_t ldx, float* Y_dev,
+                                      int64_t ldy, void* stream) {
+  if (head_dim != D) return LQ_ERR_UNSUPPORTED;
+  if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
+  if (rows < 0 || cols <= 0 || cols % D != 0 || ldx < cols || ldy < cols) return LQ_ERR_SHAPE;
+  if (rows == 0) return LQ_OK;
+  if (R_dev == nullptr || X_dev == nullptr || Y_dev == nullptr) return LQ_ERR_ARG;
+  if (!aligned4(R_dev) || !aligned4(Y_dev) || !aligned4(X_dev)) return LQ_ERR_ARG;
+  RotArgs a;
+  a.R = R_dev; a.transpose = transpose != 0; a.X = X_dev; a.xbf16 = (xdtype == LQ_BF16);
+  a.rows = rows; a.blocks_per_row = cols / D; a.ldx = ldx; a.ldy = ldy; a.Y = Y_dev;
+  const size_t smem = (size_t)(D * D + 8 * D) * sizeof(float);
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(rotate_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return LQ_ERR_CUDA;
+    }
+    attr = true;
+  }
+  const int sms = device_sm_count();
+  if (sms <= 0) return LQ_ERR_CUDA;
+  const int64_t nvec = rows * (cols / D);
+  int64_t grid = (nvec + 7) / 8;
+  if (grid > (int64_t)sms * 3) grid = (int64_t)sms * 3;
+  rotate_blocks_kernel<<<(unsigned)grid, 256, smem, (cudaStream_t)stream>>>(a);
   return check_launch();
 }

@@ -74,3 +74,48 @@ def test_llama3_8b_cache_32k_tokens():
     ref = KV.attention_from_codes(q.float().cpu().numpy(), kc.cpu().numpy(), ks.cpu().numpy(), kd.cpu().numpy(),
                                   vc.cpu().numpy(), vs.cpu().numpy(), vd.cpu().numpy(), kvh, 128, "e8")
     assert normwise_rel(out.cpu().numpy(), ref) < TOL
+
+
+@pytest.mark.parametrize("xdtype", ["bf16", "fp32"])
+def test_rotate_blocks_matches_oracle(xdtype):
+    torch, L = cuda()
+    X = gaussian_matrix(333, 384, 1.0, 61, dtype="bf16")
+    Q = KV.haar_rotation(128, 62)
+    Xd = to_dev_bf16(torch, X) if xdtype == "bf16" else to_dev(torch, X.astype(np.float32))
+    Rd = to_dev(torch, Q.astype(np.float32))
+    for transpose in (False, True):
+        Y = torch.empty((333, 384), dtype=torch.float32, device="cuda")
+        L.lq_rotate_blocks(Rd, Xd, Y, transpose=transpose)
+        torch.cuda.synchronize()
+        ref = KV.rotate_blocks(X, Q.astype(np.float32).astype(np.float64), transpose=transpose)
+        assert normwise_rel(Y.cpu().numpy(), ref) < 1e-6
+
+
+def test_qjl_rotated_cache_attention():
+    """K, V and q rotated by a Haar matrix before quantization, the output rotated back:
+    matches the oracle applied to the same rotated inputs."""
+    torch, L = cuda()
+    tokens, kvh, qh = 900, 2, 8
+    X = gaussian_matrix(tokens, kvh * 128, 1.0, 63, dtype="bf16")
+    Y = gaussian_matrix(tokens, kvh * 128, 1.0, 64, dtype="bf16")
+    q = gaussian_matrix(qh, 128, 1.0, 65, dtype="bf16")
+    Q = KV.haar_rotation(128, 66)
+    Rd = to_dev(torch, Q.astype(np.float32))
+    rot = lambda A: (lambda out: (L.lq_rotate_blocks(Rd, A, out), out)[1])(
+        torch.empty(A.shape, dtype=torch.float32, device="cuda"))
+    Kr, Vr, qr = rot(to_dev_bf16(torch, X)), rot(to_dev_bf16(torch, Y)), rot(to_dev_bf16(torch, q))
+    kc, ks, kd = L.quantize(Kr, lattice="e8", tile=128, seed=67, beta=0.25)
+    vc, vs, vd = L.quantize(Vr, lattice="e8", tile=128, seed=68, beta=0.25)
+    out_r = torch.empty((qh, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(L.lq_attention_workspace_size(tokens, kvh, qh, 128), dtype=torch.uint8, device="cuda")
+    L.lq_attention_decode("e8", kc, ks, kd, vc, vs, vd, qr, out_r, ws)
+    out = torch.empty_like(out_r)
+    L.lq_rotate_blocks(Rd, out_r, out, transpose=True)
+    torch.cuda.synchronize()
+    # oracle on the same rotated fp32 inputs
+    kq = KV.kv_quantize(Kr.cpu().numpy(), "e8", 128, kd.cpu().numpy(), 0.25)
+    vq = KV.kv_quantize(Vr.cpu().numpy(), "e8", 128, vd.cpu().numpy(), 0.25)
+    o_r = KV.attention_from_codes(qr.cpu().numpy(), kq.codes, kq.scales, kd.cpu().numpy(), vq.codes, vq.scales,
+                                  vd.cpu().numpy(), kvh, 128, "e8")
+    ref = KV.rotate_blocks(o_r, Q.astype(np.float32).astype(np.float64), transpose=True)
+    assert normwise_rel(out.cpu().numpy(), ref) < TOL
