@@ -604,7 +604,7 @@ int choose_splits(int64_t tiles, int k_stages, int sms) {
     if (k_stages / s < 8) break;
     const int64_t units = tiles * s;
     const double waves = (double)units / sms;
-    const double eff = waves / (double)((units + sms - 1) / sms) - 0.03 * (s - 1);
+    const double eff = waves / (double)((units + sms - 1) / sms) - 0.01 * (s - 1);
     if (eff > best_eff + 1e-9) { best_eff = eff; best = s; }
   }
   return best;
