@@ -354,3 +354,33 @@ def gemm(codes, scales, signs, X, lattice: str = "e8", tile: int = 256, workspac
         workspace = torch.empty(lq_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=codes.device)
     lq_gemm(lattice, codes, scales, signs, tile, X, Y, workspace, dev_status, stream)
     return Y
+
+
+# ------------------------------------------------------------------ checkpoint
+CHECKPOINT_FORMAT = "lq-codes-v1"
+
+
+def save_quantized(path, codes, scales, signs, lattice: str, tile: int, seed: int, beta: float) -> None:
+    """Write codes, scales and signs with the header needed to use them again
+    (lattice, tile, seed, beta, shape) in one torch.save file."""
+    import torch
+    torch.save({"format": CHECKPOINT_FORMAT, "lattice": str(lattice), "tile": int(tile), "seed": int(seed),
+                "beta": float(beta), "shape": list(codes.shape), "codes": codes.detach().cpu(),
+                "scales": scales.detach().cpu(), "signs": signs.detach().cpu()}, path)
+
+
+def load_quantized(path, device=None) -> dict:
+    """Read a file written by :func:`save_quantized`; tensors moved to `device` when given."""
+    import torch
+    d = torch.load(path, map_location="cpu", weights_only=True)
+    if d.get("format") != CHECKPOINT_FORMAT:
+        raise ValueError(f"{path}: not a {CHECKPOINT_FORMAT} file")
+    rows, cols = d["shape"]
+    if tuple(d["codes"].shape) != (rows, cols) or tuple(d["scales"].shape) != (rows, cols // d["tile"]) \
+            or tuple(d["signs"].shape) != (cols,):
+        raise ValueError(f"{path}: tensor shapes do not match the header")
+    if device is not None:
+        for k in ("codes", "scales", "signs"):
+            d[k] = d[k].to(device)
+    return d
+

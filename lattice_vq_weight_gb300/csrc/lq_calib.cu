@@ -107,6 +107,7 @@ extern "C" double lq_beta_for_snr(int lattice, double snr_db) {
 
 extern "C" lq_status lq_error_sums(const void* W_dev, int wdtype, int64_t rows, int64_t cols, int64_t ldw,
                                    const float* What_dev, double* sums_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_error_sums");
   if (wdtype != LQ_BF16 && wdtype != LQ_F32) return LQ_ERR_DTYPE;
   if (rows < 0 || cols <= 0 || ldw < cols) return LQ_ERR_SHAPE;
   if (sums_dev == nullptr || (reinterpret_cast<uintptr_t>(sums_dev) & 7u) != 0) return LQ_ERR_ARG;
@@ -137,6 +138,7 @@ extern "C" size_t lq_calibrate_workspace_size(int lattice, int64_t rows, int64_t
 extern "C" lq_status lq_calibrate_bps(int lattice, int tile, double target_bps, const void* W_dev, int wdtype,
                                       int64_t rows, int64_t cols, int64_t ldw, uint64_t seed, void* workspace_dev,
                                       size_t workspace_bytes, double* result, void* stream) {
+  LQ_NVTX_RANGE("lq_calibrate_bps");
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (rows <= 0) return LQ_ERR_SHAPE;

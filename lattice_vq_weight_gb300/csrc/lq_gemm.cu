@@ -621,6 +621,7 @@ extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* 
                              const int8_t* signs_dev, int64_t N, int64_t K, int tile,
                              const uint16_t* X_dev, int64_t M, float* Y_dev, void* workspace_dev,
                              int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemm");
   lq_status st = validate_common(lattice, N, K, tile);
   if (st != LQ_OK) return st;
   if (M < 0) return LQ_ERR_SHAPE;

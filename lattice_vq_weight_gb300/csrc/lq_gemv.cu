@@ -476,6 +476,7 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
                              const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
                              const void* x_dev, int xdtype, int batch, float* y_dev,
                              void* workspace_dev, int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemv");
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
@@ -493,6 +494,7 @@ extern "C" lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* co
                                      const int64_t* rows, int64_t cols, int tile, const void* x_dev, int xdtype,
                                      int batch, float* const* y_dev, void* workspace_dev,
                                      int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemv_grouped");
   return gemv_group(lattice, n, codes_dev, scales_dev, signs_dev, rows, cols, tile, x_dev, xdtype, batch, y_dev,
                     workspace_dev, dev_status_dev, (cudaStream_t)stream);
 }
@@ -539,6 +541,7 @@ extern "C" lq_status lq_gemv_noalloc(int lattice, const int8_t* codes_dev, const
                                      const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
                                      const void* x_dev, int xdtype, int batch, float* y_dev,
                                      int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemv_noalloc");
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (batch < 1 || batch > 16) return LQ_ERR_SHAPE;

@@ -325,6 +325,7 @@ extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev,
                                          int kv_heads, int q_heads, int head_dim, const void* q_dev, int qdtype,
                                          float* out_dev, void* workspace_dev, size_t workspace_bytes,
                                          void* stream) {
+  LQ_NVTX_RANGE("lq_attention_decode");
   if (!valid_lattice(lattice)) return LQ_ERR_ARG;
   if (head_dim != D) return LQ_ERR_UNSUPPORTED;
   if (qdtype != LQ_BF16 && qdtype != LQ_F32) return LQ_ERR_DTYPE;
@@ -366,6 +367,7 @@ extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev,
 extern "C" lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, const void* X_dev,
                                       int xdtype, int64_t rows, int64_t cols, int64_t ldx, float* Y_dev,
                                       int64_t ldy, void* stream) {
+  LQ_NVTX_RANGE("lq_rotate_blocks");
   if (head_dim != D) return LQ_ERR_UNSUPPORTED;
   if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
   if (rows < 0 || cols <= 0 || cols % D != 0 || ldx < cols || ldy < cols) return LQ_ERR_SHAPE;

@@ -477,6 +477,7 @@ using namespace lq;
 
 // ------------------------------------------------------------------ host side
 extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_make_signs");
   if (cols < 0) return LQ_ERR_SHAPE;
   if (cols == 0) return LQ_OK;
   if (signs_dev == nullptr) return LQ_ERR_ARG;
@@ -531,6 +532,7 @@ extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int
                                  int64_t ldw, int tile, uint64_t seed, float beta, int8_t* codes_dev,
                                  float* scales_dev, int8_t* signs_dev, int32_t* dev_status_dev,
                                  void* stream) {
+  LQ_NVTX_RANGE("lq_quantize");
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (wdtype != LQ_BF16 && wdtype != LQ_F32) return LQ_ERR_DTYPE;
@@ -580,6 +582,7 @@ static lq_status launch_dequant(const DequantArgs& a, cudaStream_t st) {
 extern "C" lq_status lq_dequantize(int lattice, const int8_t* codes_dev, const float* scales_dev,
                                    const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
                                    void* What_dev, int out_dtype, void* stream) {
+  LQ_NVTX_RANGE("lq_dequantize");
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (out_dtype != LQ_BF16 && out_dtype != LQ_F32) return LQ_ERR_DTYPE;

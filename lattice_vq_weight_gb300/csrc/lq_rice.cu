@@ -679,6 +679,7 @@ extern "C" lq_status lq_rice_encode(int lattice, const int8_t* codes_dev, int64_
                                     uint32_t* stream_dev, size_t stream_bytes, uint32_t* tile_offsets_dev,
                                     uint64_t* total_bits_dev, void* workspace_dev, int32_t* dev_status_dev,
                                     void* stream) {
+  LQ_NVTX_RANGE("lq_rice_encode");
   lq_status st = check_shape(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (stream_dev == nullptr || tile_offsets_dev == nullptr || total_bits_dev == nullptr) return LQ_ERR_ARG;
@@ -722,6 +723,7 @@ extern "C" lq_status lq_rice_encode(int lattice, const int8_t* codes_dev, int64_
 extern "C" lq_status lq_rice_decode(int lattice, const uint32_t* stream_dev, size_t stream_bytes,
                                     const uint32_t* tile_offsets_dev, int64_t rows, int64_t cols, int tile,
                                     int8_t* codes_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_rice_decode");
   lq_status st = check_shape(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (rows == 0) return LQ_OK;
@@ -739,6 +741,7 @@ extern "C" lq_status lq_gemv_rice(int lattice, const uint32_t* stream_dev, size_
                                   const int8_t* signs_dev, int64_t rows, int64_t cols, int tile, const void* x_dev,
                                   int xdtype, int batch, float* y_dev, void* workspace_dev,
                                   int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemv_rice");
   lq_status st = check_shape(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
