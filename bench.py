@@ -905,9 +905,9 @@ def kv_arm(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8 codes (fp32 compute)",
         "data": "synthetic",
         "config": {"workload": "llama3-8b decode attention over an E8-quantized KV cache (32 layers, 8 kv heads, "
-                               "32 q heads, head_dim 128), one graph of 64 launches per step",
+                               "32 q heads, head_dim 128), one graph of 96 launches per step",
                    "value_is": "cache GB/s at 32 768 tokens", "beta": BETA, "tile": 128},
-        "gpu_launches": layers * 2 * reps,
+        "gpu_launches": layers * 3 * reps,
         "contexts": results,
         "roofline": {"kernel": "attn_partial_kernel + attn_combine_kernel", "bound": "hbm", "achieved": best,
                      "peak": peak, "unit": "GB/s", "frac": round(best / peak, 4), "peak_source": src,

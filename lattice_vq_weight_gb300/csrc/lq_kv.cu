@@ -11,11 +11,11 @@
 //     sum_j p_j v^_j = D H (sum_j p_j s_j c~_j) / (2 sqrt d)
 //                                      (accumulate codes in the rotated domain,
 //                                       rotate back once per head)
-// Kernel 1 (one CTA per kv head and token range, four warps): each warp takes
-// 32 tokens at a time -- lane = token for the scores (128 codes against the
-// group's rotated queries), an online softmax, then lane = 4 dimensions for
-// the value sum over those 32 tokens.  Kernel 2 merges the ranges and rotates
-// the result back.
+// Kernel 1 rotates the queries.  Kernel 2 (one CTA per kv head and token
+// range, four warps): each warp takes 32 tokens at a time -- lane = token for
+// the scores (128 codes against the group's rotated queries), an online
+// softmax, then lane = 4 dimensions for the value sum over those 32 tokens.
+// Kernel 3 merges the ranges and rotates the result back.
 #include <cmath>
 
 #include <cuda_runtime.h>
@@ -44,6 +44,7 @@ struct AttnArgs {
   int kv_heads, group, splits;
   int a2;
   float* part;        // [kv_heads x splits x group x (2 + D)]: m, l, acc[D]
+  float* qrot;        // [q_heads x D]: rotated, scaled queries
   float* out;         // [q_heads x D]
 };
 
@@ -64,8 +65,21 @@ __device__ __forceinline__ void block_fwht(float* v) {
   __syncthreads();
 }
 
+// One block per query head: x~ = H D q / sqrt(d), times 1/2 (codes are
+// doubled), sqrt 3 on A2 odd coordinates and the softmax scale 1/sqrt(d).
+__global__ void __launch_bounds__(D) rotate_query_kernel(AttnArgs a) {
+  __shared__ float v[D];
+  const int qh = blockIdx.x, kvh = qh / a.group, i = threadIdx.x;
+  const int64_t qi = (int64_t)qh * D + i;
+  const float x = a.qbf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qi])
+                          : reinterpret_cast<const float*>(a.q)[qi];
+  v[i] = x * (float)a.ksg[kvh * D + i];
+  block_fwht(v);
+  a.qrot[qi] = v[i] * (0.5f / (float)D) * ((a.a2 && (i & 1)) ? 1.7320508075688772f : 1.f);
+}
+
 template <int G>
-__global__ void __launch_bounds__(kThreads) attn_partial_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(AttnArgs a) {
   __shared__ __align__(16) float qr[G][D];         // rotated, scaled queries
   __shared__ float wm[kWarps][G], wl[kWarps][G];
   __shared__ __align__(16) float wacc[kWarps][G][D];
@@ -74,20 +88,10 @@ __global__ void __launch_bounds__(kThreads) attn_partial_kernel(AttnArgs a) {
   const int64_t ld = (int64_t)a.kv_heads * D;
   const int64_t j0 = split * a.tokens / a.splits, j1 = (split + 1) * a.tokens / a.splits;
 
-  // rotate the group's queries: x~ = H D q / sqrt(d), times 1/2 (codes are
-  // doubled), sqrt 3 on A2 odd coordinates and the softmax scale 1/sqrt(d)
-  for (int g = 0; g < G; ++g) {
-    const int qh = kvh * a.group + g;
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
-      const int64_t qi = (int64_t)qh * D + i;
-      const float x = a.qbf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.q)[qi])
-                              : reinterpret_cast<const float*>(a.q)[qi];
-      qr[g][i] = x * (float)a.ksg[kvh * D + i];
-    }
-    block_fwht(qr[g]);
-    for (int i = threadIdx.x; i < D; i += blockDim.x)
-      qr[g][i] *= (0.5f / (float)D) * ((a.a2 && (i & 1)) ? 1.7320508075688772f : 1.f);
-  }
+  // the group's rotated queries
+  for (int e = threadIdx.x; e < G * D / 4; e += blockDim.x)
+    reinterpret_cast<float4*>(&qr[0][0])[e] =
+        reinterpret_cast<const float4*>(a.qrot + (int64_t)kvh * a.group * D)[e];
   __syncthreads();
 
   float m[G], l[G], acc[G][4];
@@ -300,6 +304,13 @@ using namespace lq::kv;
 
 namespace {
 
+// floats of the per-range partial results, rounded up to 64 (the rotated
+// queries that follow them are read as float4)
+size_t part_floats(int kv_heads, int splits, int group) {
+  const size_t n = (size_t)kv_heads * splits * group * (2 + D);
+  return (n + 63) & ~(size_t)63;
+}
+
 int attn_splits(int64_t tokens, int kv_heads) {
   const int sms = device_sm_count();
   // about four CTAs per SM and at least 128 tokens (one chunk per warp) per range
@@ -316,7 +327,7 @@ int attn_splits(int64_t tokens, int kv_heads) {
 extern "C" size_t lq_attention_workspace_size(int64_t tokens, int kv_heads, int q_heads, int head_dim) {
   if (tokens <= 0 || kv_heads <= 0 || q_heads <= 0 || head_dim != D || q_heads % kv_heads != 0) return 0;
   const int splits = attn_splits(tokens, kv_heads);
-  return (size_t)kv_heads * splits * (q_heads / kv_heads) * (2 + D) * sizeof(float);
+  return (part_floats(kv_heads, splits, q_heads / kv_heads) + (size_t)q_heads * D) * sizeof(float);
 }
 
 extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev, const float* k_scales_dev,
@@ -349,8 +360,11 @@ extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev,
   a.splits = attn_splits(tokens, kv_heads);
   a.a2 = (lattice == LQ_A2);
   a.part = reinterpret_cast<float*>(workspace_dev);
+  a.qrot = a.part + part_floats(kv_heads, a.splits, group);
   a.out = out_dev;
   cudaStream_t s = (cudaStream_t)stream;
+  if (!aligned16(workspace_dev)) return LQ_ERR_ARG;
+  rotate_query_kernel<<<(unsigned)q_heads, D, 0, s>>>(a);
   const unsigned grid = (unsigned)(kv_heads * a.splits);
   switch (group) {
     case 1: attn_partial_kernel<1><<<grid, kThreads, 0, s>>>(a); break;

@@ -4,6 +4,7 @@
     python -m lattice_vq_weight_gb300.profile_case gemv --batch 1
     python -m lattice_vq_weight_gb300.profile_case gemv --batch 1 --gate-up   # one grouped call
     python -m lattice_vq_weight_gb300.profile_case gemm --M 256
+    python -m lattice_vq_weight_gb300.profile_case kv --tokens 32768
 
 Each op runs `--reps` passes (default 2) after building inputs on the device;
 the second pass is the one to capture (`ncu -s <launches of one pass>`).
@@ -11,7 +12,9 @@ Inputs: bf16 N(0, 0.02^2) weights of the Llama-3-8B layer shapes (gate-shaped
 only with --gate-only), E8, tile 256, beta 0.25; activations N(0, 1) bf16;
 GEMM on the 8192 x 28672 Llama-3-70B up-like shape with X of M rows.  With
 --gate-up the GEMV is one grouped call over the gate and up matrices (as in
-the benchmark's layer step).
+the benchmark's layer step).  kv: one layer of a Llama-3-8B KV cache (8 kv
+heads, 32 query heads, head_dim 128, N(0, 1) K and V, E8, beta 0.25) and the
+decode attention over --tokens cached tokens.
 """
 from __future__ import annotations
 
@@ -26,7 +29,8 @@ if ROOT not in sys.path:
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=("quantize", "gemv", "gemm"))
+    ap.add_argument("op", choices=("quantize", "gemv", "gemm", "kv"))
+    ap.add_argument("--tokens", type=int, default=32768)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--M", type=int, default=256)
     ap.add_argument("--reps", type=int, default=2)
@@ -40,6 +44,20 @@ def main(argv=None):
 
     dev = torch.device("cuda")
     gen = torch.Generator(device=dev).manual_seed(0)
+    if args.op == "kv":
+        from synthetic import torch_gaussian_matrix
+        K = torch_gaussian_matrix(args.tokens, 8 * 128, 1.0, 7000, device=dev)
+        V = torch_gaussian_matrix(args.tokens, 8 * 128, 1.0, 7001, device=dev)
+        kc, ks, kd = L.quantize(K, "e8", 128, 7100, 0.25)
+        vc, vs, vd = L.quantize(V, "e8", 128, 7101, 0.25)
+        q = torch.randn((32, 128), device=dev, generator=gen).to(torch.bfloat16)
+        out = torch.empty((32, 128), dtype=torch.float32, device=dev)
+        ws = torch.empty(L.lq_attention_workspace_size(args.tokens, 8, 32, 128), dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            L.lq_attention_decode("e8", kc, ks, kd, vc, vs, vd, q, out, ws)
+        torch.cuda.synchronize()
+        print("ok")
+        return
     if args.op == "gemm":
         N, K = 8192, 28672
         W = (torch.randn((N, K), device=dev, generator=gen) * 0.015).to(torch.bfloat16)
