@@ -125,8 +125,8 @@ lq_status lq_dequantize(int lattice, const int8_t* codes_dev, const float* scale
 
 /*
  * Workspace bytes lq_gemv needs for `batch` activation rows of length `cols`
- * with tile `tile` (the rotated activation split into two fp16 halves plus one
- * float per (row, tile)).  lq_gemv_grouped_workspace_size(n, ...) is the same
+ * with tile `tile` (the rotated activation in fp16 plus one float per
+ * (row, tile)).  lq_gemv_grouped_workspace_size(n, ...) is the same
  * for n matrices (one rotated activation per matrix).
  */
 size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile);

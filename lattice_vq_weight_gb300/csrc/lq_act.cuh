@@ -1,7 +1,7 @@
 // Activation side of the products computed from the codes, shared by the
-// int8-code GEMV and the Rice-stream GEMV: the per-tile rotation of x into two
-// fp16 halves (plus a power of two per (row, tile)), the conversion of int8
-// codes to exact fp16 values and the m16n8k16 tensor-core step.  Internal.
+// int8-code GEMV and the Rice-stream GEMV: the per-tile rotation of x into fp16
+// (times a power of two per (row, tile)), the conversion of int8 codes to exact
+// fp16 values and the m16n8k16 tensor-core step.  Internal.
 #pragma once
 
 #include <cstdint>
@@ -26,8 +26,7 @@ struct RotateArgs {
   int batch, tile, tiles_per_row;
   float post_scale;    // 1 / (2 sqrt(T))
   int a2;              // multiply odd coordinates by sqrt(3)
-  __half* xh;          // [n_mats x batch x cols]
-  __half* xl;
+  __half* xh;          // [n_mats x batch x cols]: x~ times 2^e[row, tile], fp16
   float* xs;           // [n_mats x batch x tiles] = 2^-e
   int32_t* status;
 };
@@ -88,21 +87,15 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   }
   if (active) {
     uint4* dh = reinterpret_cast<uint4*>(a.xh + mb * a.cols + col0);
-    uint4* dl = reinterpret_cast<uint4*>(a.xl + mb * a.cols + col0);
 #pragma unroll
     for (int q = 0; q < E / 8; ++q) {
-      uint32_t hw[4], lw[4];
+      uint32_t hw[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float x0 = v[8 * q + 2 * j] * f, x1 = v[8 * q + 2 * j + 1] * f;
-        const __half2 h = __floats2half2_rn(x0, x1);
-        const float2 hf = __half22float2(h);
-        const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+        const __half2 h = __floats2half2_rn(v[8 * q + 2 * j] * f, v[8 * q + 2 * j + 1] * f);
         hw[j] = *reinterpret_cast<const uint32_t*>(&h);
-        lw[j] = *reinterpret_cast<const uint32_t*>(&l);
       }
       dh[q] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      dl[q] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     }
     if ((lane & (lpt - 1)) == 0) a.xs[mb * a.tiles_per_row + col0 / a.tile] = 1.0f / f;
   }

