@@ -389,8 +389,9 @@ def gpu_arm(args, ws, rank, local):
     stream = torch.cuda.Stream(device=dev)
 
     def quantize_all():
-        for i, (n, r, c, seed) in enumerate(shapes):
-            L.lq_quantize(LATTICE, dev_w[i], TILE, seed, BETA, codes[i], scales[i], signs[i], status)
+        # the layer's seven matrices in one grouped call (one launch pair)
+        L.lq_quantize_grouped(LATTICE, dev_w, TILE, [seed for _, _, _, seed in shapes], BETA, codes, scales,
+                              signs, status)
 
     def gemv_all(b):
         for grp in groups:
@@ -407,7 +408,7 @@ def gpu_arm(args, ws, rank, local):
         for b in BATCHES:
             gemv_all(b)
 
-    launches_per_step = 2 * len(shapes) + 2 * len(groups) * len(BATCHES)
+    launches_per_step = 2 + 2 * len(groups) * len(BATCHES)
 
     with torch.cuda.stream(stream):
         for _ in range(max(1, args.warmup)):
@@ -582,6 +583,7 @@ def gpu_arm(args, ws, rank, local):
                    "beta": BETA, "batches": list(BATCHES), "parallelism": f"replicas{ws}",
                    "l2": "inputs larger than L2 (436 MB bf16 weights, 218 MB codes per step); no flush",
                    "graph": "step captured as one CUDA graph",
+                   "quantize": "the seven matrices in one grouped call (one launch pair)",
                    "gemv_groups": "q+k+v, o, gate+up, down (one call each, activation shared in a group)"},
         "gpu_launches": launches_per_step * args.steps,
         "parts": parts,
@@ -666,8 +668,10 @@ def stack_arm(args, ws, rank, local):
     stream = torch.cuda.Stream(device=dev)
 
     def quantize_all():
-        for k, (_, _, r, c, seed) in enumerate(mats):
-            L.lq_quantize(LATTICE, W[k], TILE, seed, BETA, codes[k], scales[k], signs[k], status)
+        # one grouped call (one launch pair) per layer
+        for k0 in range(0, len(mats), 7):
+            L.lq_quantize_grouped(LATTICE, W[k0:k0 + 7], TILE, [m[4] for m in mats[k0:k0 + 7]], BETA,
+                                  codes[k0:k0 + 7], scales[k0:k0 + 7], signs[k0:k0 + 7], status)
 
     def gemv_all(b):
         for grp in groups:
@@ -730,9 +734,10 @@ def stack_arm(args, ws, rank, local):
                    "matrices": len(mats), "weights_bytes": int(sum(w.numel() * 2 for w in W)),
                    "codes_bytes": int(sum(cd.numel() for cd in codes)), "outliers": "0.1% x20",
                    "parallelism": f"replicas{ws}", "l2": "inputs far larger than L2; no flush",
-                   "graph": f"one CUDA graph of {2 * len(mats) + 2 * len(groups) * len(batches)} launches",
+                   "graph": f"one CUDA graph of {2 * n_layers + 2 * len(groups) * len(batches)} launches",
+                   "quantize": "one grouped call (one launch pair) per layer",
                    "gemv_groups": "q+k+v, o, gate+up, down per layer (one call each)"},
-        "gpu_launches": (2 * len(mats) + 2 * len(groups) * len(batches)) * args.steps,
+        "gpu_launches": (2 * n_layers + 2 * len(groups) * len(batches)) * args.steps,
         "parts": {"quantize_gbs": round(qgbs, 1), "quantize_ms": round(ms_q, 3),
                   **{f"gemv_b{b}_gbs": round(gb[b] / (ms_g[b] * 1e-3) / 1e9, 1) for b in batches},
                   **{f"gemv_b{b}_ms": round(ms_g[b], 3) for b in batches}},

@@ -113,6 +113,32 @@ lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, 
                       int32_t* dev_status_dev, void* stream);
 
 /*
+ * lq_quantize over a group of n matrices (for example the seven linear layers
+ * of a transformer block) in one launch pair instead of n.  The pages quantize
+ * every linear layer of a model independently; grouping only merges launches:
+ * every matrix's signs, codes and scales equal those of lq_quantize with its
+ * own arguments.
+ *   n          1 .. LQ_QUANTIZE_MAX_GROUP
+ *   W_dev, codes_dev, scales_dev, signs_dev
+ *              HOST arrays of n DEVICE pointers, one entry per matrix, each as
+ *              in lq_quantize
+ *   rows, cols, ldw, seeds
+ *              HOST arrays of n values, each as in lq_quantize (rows 0
+ *              allowed: that matrix only gets its signs)
+ *   lattice, wdtype, tile, beta   shared by the group, as in lq_quantize
+ *   dev_status_dev  one int32 status word for the whole group, or NULL
+ * The host arrays are read during the call only.  Errors as in lq_quantize
+ * (the first failing matrix decides, before any launch); LQ_ERR_ARG when n is
+ * out of range.  Limit: at most 2^40 warp units of 2048 columns in all.
+ */
+#define LQ_QUANTIZE_MAX_GROUP 8
+lq_status lq_quantize_grouped(int lattice, int n, const void* const* W_dev, int wdtype,
+                              const int64_t* rows, const int64_t* cols, const int64_t* ldw, int tile,
+                              const uint64_t* seeds, float beta, int8_t* const* codes_dev,
+                              float* const* scales_dev, int8_t* const* signs_dev,
+                              int32_t* dev_status_dev, void* stream);
+
+/*
  * Reconstruct W^ = D H (s * p) / sqrt(tile) per tile, the inverse of the
  * rotation applied to the scaled lattice points (HyperQuant page, mma="int8"
  * paragraph: the codes are decoded, never stored as a weight).

@@ -29,6 +29,7 @@ SIGNATURES = {
     "lq_pick_tile": (_I32, [_I64, _I32]),
     "lq_make_signs": (_I32, [_U64, _I64, _P, _P]),
     "lq_quantize": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _F32, _P, _P, _P, _P, _P]),
+    "lq_quantize_grouped": (_I32, [_I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _F32, _P, _P, _P, _P, _P]),
     "lq_dequantize": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _P]),
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
     "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
@@ -116,6 +117,11 @@ def _lattice_id(lattice) -> int:
     return LATTICE_IDS[lattice] if isinstance(lattice, str) else int(lattice)
 
 
+def _row_stride(W) -> int:
+    """Row stride in elements; an empty matrix (whose stride torch may report as 0) passes its width."""
+    return int(W.stride(0)) if W.shape[0] > 0 else int(W.shape[1])
+
+
 def _dtype_id(t) -> int:
     import torch
     if t.dtype == torch.bfloat16:
@@ -144,7 +150,7 @@ def lq_quantize(lattice, W, tile: int, seed: int, beta: float, codes, scales, si
     rows, cols = W.shape
     assert W.stride(1) == 1
     _check("lq_quantize", _get_lib().lq_quantize(
-        _lattice_id(lattice), _ptr(W), _dtype_id(W), rows, cols, W.stride(0), int(tile), int(seed),
+        _lattice_id(lattice), _ptr(W), _dtype_id(W), rows, cols, _row_stride(W), int(tile), int(seed),
         float(beta), _ptr(codes), _ptr(scales), _ptr(signs), _ptr(dev_status), _stream(stream)))
 
 
@@ -180,6 +186,30 @@ def lq_gemv_noalloc(lattice, codes, scales, signs, tile: int, x, y, dev_status=N
     _check("lq_gemv_noalloc", _get_lib().lq_gemv_noalloc(
         _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), rows, cols, int(tile),
         _ptr(x), _dtype_id(x), batch, _ptr(y), _ptr(dev_status), _stream(stream)))
+
+
+# Largest group lq_quantize_grouped takes (LQ_QUANTIZE_MAX_GROUP in lq.h)
+LQ_QUANTIZE_MAX_GROUP = 8
+
+
+def lq_quantize_grouped(lattice, Ws, tile: int, seeds, beta: float, codes, scales, signs, dev_status=None,
+                        stream=None) -> None:
+    """lq_quantize for n matrices in one launch pair: lists Ws[m], seeds[m], codes[m], scales[m], signs[m].
+
+    Every W has the same dtype; rows, cols and the row stride are taken per matrix."""
+    n = len(Ws)
+    if any(W.dtype != Ws[0].dtype for W in Ws):
+        raise TypeError("lq_quantize_grouped: every matrix of a group has the same dtype")
+    rows = (ctypes.c_int64 * n)(*[int(W.shape[0]) for W in Ws])
+    cols = (ctypes.c_int64 * n)(*[int(W.shape[1]) for W in Ws])
+    ldw = (ctypes.c_int64 * n)(*[_row_stride(W) for W in Ws])
+    sd = (ctypes.c_uint64 * n)(*[int(x) & 0xFFFFFFFFFFFFFFFF for x in seeds])
+    keep = [_ptr_array(Ws), _ptr_array(codes), _ptr_array(scales), _ptr_array(signs)]
+    _check("lq_quantize_grouped", _get_lib().lq_quantize_grouped(
+        _lattice_id(lattice), n, keep[0][1], _dtype_id(Ws[0]), ctypes.cast(rows, ctypes.c_void_p),
+        ctypes.cast(cols, ctypes.c_void_p), ctypes.cast(ldw, ctypes.c_void_p), int(tile),
+        ctypes.cast(sd, ctypes.c_void_p), float(beta), keep[1][1], keep[2][1], keep[3][1], _ptr(dev_status),
+        _stream(stream)))
 
 
 # Largest group lq_gemv_grouped takes (LQ_GEMV_MAX_GROUP in lq.h)
@@ -267,7 +297,7 @@ def lq_error_sums(W, W_hat, sums, stream=None) -> None:
     """sums (float64 device tensor of 2) = (sum w^2, sum (w - w^)^2)."""
     rows, cols = W.shape
     _check("lq_error_sums", _get_lib().lq_error_sums(
-        _ptr(W), _dtype_id(W), rows, cols, W.stride(0), _ptr(W_hat), _ptr(sums), _stream(stream)))
+        _ptr(W), _dtype_id(W), rows, cols, _row_stride(W), _ptr(W_hat), _ptr(sums), _stream(stream)))
 
 
 def lq_calibrate_workspace_size(lattice, rows: int, cols: int, tile: int) -> int:
@@ -279,7 +309,7 @@ def lq_calibrate_bps(lattice, tile: int, target_bps: float, W, seed: int, worksp
     rows, cols = W.shape
     out = (ctypes.c_double * 3)()
     _check("lq_calibrate_bps", _get_lib().lq_calibrate_bps(
-        _lattice_id(lattice), int(tile), float(target_bps), _ptr(W), _dtype_id(W), rows, cols, W.stride(0),
+        _lattice_id(lattice), int(tile), float(target_bps), _ptr(W), _dtype_id(W), rows, cols, _row_stride(W),
         int(seed), _ptr(workspace), workspace.numel(), ctypes.cast(out, ctypes.c_void_p), _stream(stream)))
     return float(out[0]), float(out[1]), float(out[2])
 

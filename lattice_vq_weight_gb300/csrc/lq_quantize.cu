@@ -17,20 +17,30 @@
 
 namespace lq {
 
+constexpr int kQuantMaxMats = LQ_QUANTIZE_MAX_GROUP;
+
+struct SignsArgs {
+  uint64_t seed[kQuantMaxMats];
+  int64_t n[kQuantMaxMats];
+  int8_t* out[kQuantMaxMats];
+};
+
 // ------------------------------------------------------------------ signs
 // SplitMix64 (Steele, Lea & Flood 2014): output k mixes seed + (k+1) * golden
 // gamma through two xor-shift-multiply rounds; the sign is the top bit.
-__global__ void make_signs_kernel(uint64_t seed, int64_t n, int8_t* signs) {
+// blockIdx.y selects the matrix of a group (each with its own seed).
+__global__ void make_signs_kernel(SignsArgs a) {
   // the quantize kernel launched next may start now: it prefetches its input
   // and waits for these signs (griddepcontrol.wait) before reading them
   asm volatile("griddepcontrol.launch_dependents;");
+  const int m = blockIdx.y;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  uint64_t z = seed + (uint64_t)(i + 1) * 0x9E3779B97F4A7C15ull;
+  if (i >= a.n[m]) return;
+  uint64_t z = a.seed[m] + (uint64_t)(i + 1) * 0x9E3779B97F4A7C15ull;
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
   z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
   z ^= z >> 31;
-  signs[i] = (z >> 63) ? (int8_t)-1 : (int8_t)1;
+  a.out[m][i] = (z >> 63) ? (int8_t)-1 : (int8_t)1;
 }
 
 // ------------------------------------------------------------------ loading
@@ -147,16 +157,33 @@ __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_g
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------------ quantize
-struct QuantArgs {
+// One matrix of a quantize launch.  Its warp units (row, 2048-column chunk)
+// are numbered row * chunks_per_row + chunk and taken four at a time by the
+// four warps of a CTA: CTA unit k of the matrix (global CTA unit cta_begin + k)
+// holds warp units 4k .. 4k + 3, those past the matrix's end doing nothing.
+// The grid strides over CTA units, so every warp of a CTA is always in the
+// same matrix.  A warp unit's row is local / chunks_per_row, computed as the
+// high half of local * cpr_recip with cpr_recip = ceil(2^64 / chunks_per_row)
+// (exact for every local below 2^64 / chunks_per_row; 0 marks one chunk per
+// row), so the kernel divides nothing.
+struct QuantMat {
   const void* W;
-  int64_t rows, cols, ldw;
-  int tile, tile_shift, lanes_per_tile, tiles_per_row, chunks_per_row;
-  float beta, sqrt_tile, inv_tile;
-  const int8_t* signs;
   int8_t* codes;
   float* scales;
+  const int8_t* signs;
+  int64_t rows, cols, ldw;
+  int64_t cta_begin;
+  uint64_t cpr_recip;
+  int tiles_per_row, chunks_per_row;
+};
+
+struct QuantArgs {
+  QuantMat mat[kQuantMaxMats];
+  int n_mats;
+  int tile, tile_shift, lanes_per_tile;
+  float beta, sqrt_tile, inv_tile;
   int32_t* status;
-  int64_t units;
+  int64_t cta_units;  // CTA units of all matrices
 };
 
 constexpr int kQuantThreads = 128;
@@ -237,7 +264,12 @@ __device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf
   }
 }
 
-template <int LAT, bool BF16, int MP>
+// GROUPED = false: one matrix (a.mat[0]); a warp takes warp units w, w + W,
+// w + 2W, ... (W = warps of the grid), advanced without divisions.
+// GROUPED = true: the CTA-unit walk over several matrices described above.
+// Both walks feed the same per-unit body; they are separate instantiations
+// because the single-matrix walk keeps fewer values live across the decode.
+template <int LAT, bool BF16, int MP, bool GROUPED>
 __global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a) {
   using SM = QuantSmem<BF16>;
   extern __shared__ uint4 quant_smem[];
@@ -246,61 +278,38 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a)
   uint4* raw_sm = wsm;                          // [stage][vec][lane]
   uint4* msk = wsm + SM::kRawWords;             // bf16 sign masks [q][lane]
   const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(raw_sm);
-  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   constexpr int kElemBytes = BF16 ? 2 : 4;
 
   LaneSigns<false> sg;     // fp32 input keeps its 64 sign bits in registers
-  int cached_chunk = -1;
+  int cached_chunk = -1, cached_m = -1;
   bool range = false, nonfinite = false;
 
-  // (row, chunk) of the current and next unit, advanced without divisions:
-  // unit u = row * chunks_per_row + chunk, and u grows by nwarps per step.
-  const int64_t d_row = nwarps / a.chunks_per_row;
-  const int d_chunk = (int)(nwarps % a.chunks_per_row);
-  int64_t row = warp0 / a.chunks_per_row;
-  int chunk = (int)(warp0 % a.chunks_per_row);
-  auto next_pos = [&](int64_t& r, int& c) {
-    r += d_row;
-    c += d_chunk;
-    if (c >= a.chunks_per_row) { c -= a.chunks_per_row; ++r; }
-  };
-  auto lane_ptr = [&](int64_t r, int c) -> const char* {
-    return reinterpret_cast<const char*>(a.W) +
-           (r * a.ldw + (int64_t)c * kChunkCols + (int64_t)lane * kLaneElems) * kElemBytes;
-  };
-  // copy the lane's 64 input columns of unit (r, c) into stage st
-  auto stage_in = [&](int64_t r, int c, int st) {
-    if (r < a.rows && (int64_t)c * kChunkCols + (int64_t)lane * kLaneElems < a.cols) {
-      const char* src = lane_ptr(r, c);
+  // copy the lane's 64 input columns of unit (row, chunk) of M into stage st
+  auto stage_in = [&](bool valid, const QuantMat& M, int64_t row, int chunk, int st) {
+    const int64_t c = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
+    if (valid && row < M.rows && c < M.cols) {
+      const char* src = reinterpret_cast<const char*>(M.W) + (row * M.ldw + c) * kElemBytes;
 #pragma unroll
       for (int i = 0; i < SM::kRawVec; ++i)
         cp_async16(raw_s + (uint32_t)((st * SM::kStageVec + i * 32 + lane) * 16), src + 16 * i);
     }
     cp_async_commit();
   };
-  int stage = 0;
-  stage_in(row, chunk, 0);
-  // the signs come from the kernel launched just before this one
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  for (; row < a.rows; ) {
-    int64_t nrow = row;
-    int nchunk = chunk;
-    next_pos(nrow, nchunk);
-    stage_in(nrow, nchunk, stage ^ 1);
-
+  // quantize unit (row, chunk) of matrix m, whose input is in stage st
+  auto process = [&](const QuantMat& M, int m, int64_t row, int chunk, int st) {
     const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    const bool active = col0 < a.cols;
-    if (chunk != cached_chunk) {
+    const bool active = col0 < M.cols;
+    if (chunk != cached_chunk || m != cached_m) {
       if constexpr (BF16) {
-        if (active) store_sign_masks(msk, lane, a.signs + col0);
+        if (active) store_sign_masks(msk, lane, M.signs + col0);
       } else {
         sg.bits[0] = 0;
         sg.bits[1] = 0;
-        if (active) load_signs<false>(sg, a.signs + col0);
+        if (active) load_signs<false>(sg, M.signs + col0);
       }
       cached_chunk = chunk;
+      cached_m = m;
     }
     cp_async_wait1();   // this unit's copies have landed
 
@@ -308,22 +317,22 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a)
     {
       LaneRaw<BF16> raw;
 #pragma unroll
-      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[stage * SM::kStageVec + i * 32 + lane];
+      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[st * SM::kStageVec + i * 32 + lane];
       if constexpr (BF16) unpack_bf16_smem_signs(raw, msk, lane, p);
       else unpack_signed<false>(raw, sg, p);
     }
     fwht64_local(p);
-    if constexpr (MP > 0) exchange_tile_bits<MP>(p, raw_s + (uint32_t)(stage * SM::kStageVec * 16), lane);
+    if constexpr (MP > 0) exchange_tile_bits<MP>(p, raw_s + (uint32_t)(st * SM::kStageVec * 16), lane);
     // lane bits not exchanged (MP = 0: all of them; tiles of 1024 and 2048
     // columns: tile bits 9 .. on lane bits 3 ..) cross lanes with shuffles
-    for (int m = (MP == 0 ? 1 : 8); m < a.lanes_per_tile; m <<= 1) {
-      const float sgn = (lane & m) ? -1.0f : 1.0f;
+    for (int mm = (MP == 0 ? 1 : 8); mm < a.lanes_per_tile; mm <<= 1) {
+      const float sgn = (lane & mm) ? -1.0f : 1.0f;
       const float2 sg2 = make_float2(sgn, sgn);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float2 o;
-        o.x = __shfl_xor_sync(0xffffffffu, p[j].x, m);
-        o.y = __shfl_xor_sync(0xffffffffu, p[j].y, m);
+        o.x = __shfl_xor_sync(0xffffffffu, p[j].x, mm);
+        o.y = __shfl_xor_sync(0xffffffffu, p[j].y, mm);
         p[j] = fma2(p[j], sg2, o);
       }
     }
@@ -347,10 +356,10 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a)
     const float lane_y2 = (acc.x + acc.y) * (k * k);
     bool small = lane_y2 < 3906.25f;
     if (!small) {
-      float m = 0.f;
+      float mx = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) m = fmaxf(m, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
-      small = m < 62.5f;
+      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
+      small = mx < 62.5f;
     }
     uint32_t w[16];
     bool r = false;
@@ -363,17 +372,72 @@ __global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a)
       // register block u holds tile columns 8 q + 8 Q ux + 64 a (q = lane bits,
       // ux = u >> MP, a = u & (Q - 1)) of the tile group G = lane >> MP
       constexpr int Q = 1 << MP;
-      int8_t* dst = a.codes + row * a.cols + (int64_t)chunk * kChunkCols + (lane >> MP) * (64 * Q) +
+      int8_t* dst = M.codes + row * M.cols + (int64_t)chunk * kChunkCols + (lane >> MP) * (64 * Q) +
                     8 * (lane & (Q - 1));
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         *reinterpret_cast<uint2*>(dst + (u >> MP) * (8 * Q) + 64 * (u & (Q - 1))) = make_uint2(w[2 * u], w[2 * u + 1]);
       if ((lane & (a.lanes_per_tile - 1)) == 0)
-        a.scales[row * a.tiles_per_row + (col0 >> a.tile_shift)] = s;
+        M.scales[row * M.tiles_per_row + (col0 >> a.tile_shift)] = s;
     }
-    row = nrow;
-    chunk = nchunk;
-    stage ^= 1;
+  };
+
+  int stage = 0;
+  if constexpr (!GROUPED) {
+    const QuantMat& M = a.mat[0];
+    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    // unit u = row * chunks_per_row + chunk grows by nwarps per step
+    const int64_t d_row = nwarps / M.chunks_per_row;
+    const int d_chunk = (int)(nwarps % M.chunks_per_row);
+    int64_t row = warp0 / M.chunks_per_row;
+    int chunk = (int)(warp0 % M.chunks_per_row);
+    stage_in(true, M, row, chunk, 0);
+    // the signs come from the kernel launched just before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    while (row < M.rows) {
+      int64_t nrow = row + d_row;
+      int nchunk = chunk + d_chunk;
+      if (nchunk >= M.chunks_per_row) { nchunk -= M.chunks_per_row; ++nrow; }
+      stage_in(true, M, nrow, nchunk, stage ^ 1);
+      process(M, 0, row, chunk, stage);
+      row = nrow;
+      chunk = nchunk;
+      stage ^= 1;
+    }
+  } else {
+    // (matrix, row, chunk) of a CTA unit's warp unit for this warp
+    struct Pos {
+      int m, chunk;
+      int64_t row;
+    };
+    const int wic = threadIdx.x >> 5;   // warp in the CTA
+    auto locate = [&](int64_t cu, Pos& p) {
+      while (p.m + 1 < a.n_mats && cu >= a.mat[p.m + 1].cta_begin) ++p.m;
+      const QuantMat& M = a.mat[p.m];
+      const uint64_t local = (uint64_t)(cu - M.cta_begin) * (kQuantThreads / 32) + (uint64_t)wic;
+      const uint64_t r = M.cpr_recip ? __umul64hi(local, M.cpr_recip) : local;
+      p.row = (int64_t)r;
+      p.chunk = (int)(local - r * (uint64_t)M.chunks_per_row);
+    };
+    int64_t cu = blockIdx.x;
+    Pos cur;
+    cur.m = 0;
+    cur.row = 0;
+    cur.chunk = 0;
+    if (cu < a.cta_units) locate(cu, cur);
+    stage_in(cu < a.cta_units, a.mat[cur.m], cur.row, cur.chunk, 0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (; cu < a.cta_units; cu += gridDim.x) {
+      const int64_t cn = cu + gridDim.x;
+      Pos nxt = cur;
+      if (cn < a.cta_units) locate(cn, nxt);
+      stage_in(cn < a.cta_units, a.mat[nxt.m], nxt.row, nxt.chunk, stage ^ 1);
+      const QuantMat& M = a.mat[cur.m];
+      if (cur.row < M.rows) process(M, cur.m, cur.row, cur.chunk, stage);   // else past the matrix's end
+      cur = nxt;
+      stage ^= 1;
+    }
   }
   cp_async_wait0();
   if (__any_sync(0xffffffffu, range) && lane == 0) raise_flag(a.status, LQ_DEV_RANGE);
@@ -476,30 +540,60 @@ __global__ void __launch_bounds__(256, 1) dequantize_kernel(DequantArgs a) {
 using namespace lq;
 
 // ------------------------------------------------------------------ host side
+namespace {
+
+lq_status launch_signs(const SignsArgs& a, int n_mats, int64_t max_cols, cudaStream_t s) {
+  if (max_cols <= 0) return LQ_OK;
+  const int threads = 256;
+  const int64_t blocks = (max_cols + threads - 1) / threads;
+  make_signs_kernel<<<dim3((unsigned)blocks, (unsigned)n_mats), threads, 0, s>>>(a);
+  return check_launch();
+}
+
+int64_t gcd64(int64_t x, int64_t y) {
+  while (y) {
+    const int64_t t = x % y;
+    x = y;
+    y = t;
+  }
+  return x;
+}
+
+}  // namespace
+
 extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_dev, void* stream) {
   LQ_NVTX_RANGE("lq_make_signs");
   if (cols < 0) return LQ_ERR_SHAPE;
   if (cols == 0) return LQ_OK;
   if (signs_dev == nullptr) return LQ_ERR_ARG;
-  const int threads = 256;
-  const int64_t blocks = (cols + threads - 1) / threads;
-  make_signs_kernel<<<(unsigned)blocks, threads, 0, (cudaStream_t)stream>>>(seed, cols, signs_dev);
-  return check_launch();
+  SignsArgs a = {};
+  a.seed[0] = seed;
+  a.n[0] = cols;
+  a.out[0] = signs_dev;
+  return launch_signs(a, 1, cols, (cudaStream_t)stream);
 }
 
-template <int LAT, bool BF16, int MP>
-static lq_status launch_quantize_mp(const QuantArgs& a, cudaStream_t st) {
+template <int LAT, bool BF16, int MP, bool GROUPED>
+static lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
   constexpr size_t smem = (size_t)(kQuantThreads / 32) * QuantSmem<BF16>::kPerWarp * sizeof(uint4);
   static int per_sm = 0;
   if (per_sm == 0) {
-    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
     }
-    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP>, kQuantThreads, smem);
+    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP, GROUPED>, kQuantThreads, smem);
   }
-  const int grid = persistent_grid(a.units, kQuantThreads / 32, a.chunks_per_row, per_sm);
+  // a warp count that is a multiple of every matrix's chunks per row keeps
+  // each warp on one chunk (one set of signs) within a matrix
+  int64_t modulus = 1;
+  for (int m = 0; m < a.n_mats; ++m) {
+    const int64_t c = a.mat[m].chunks_per_row;
+    modulus = modulus / gcd64(modulus, c) * c;
+    if (modulus > 64) { modulus = 1; break; }
+  }
+  const int grid = persistent_grid(a.cta_units * (kQuantThreads / 32), kQuantThreads / 32, (int)modulus, per_sm);
   if (grid <= 0) return LQ_ERR_CUDA;
   // programmatic dependent launch after the signs kernel
   cudaLaunchConfig_t cfg = {};
@@ -512,7 +606,7 @@ static lq_status launch_quantize_mp(const QuantArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP>, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP, GROUPED>, a) != cudaSuccess) {
     cudaGetLastError();
     return LQ_ERR_CUDA;
   }
@@ -522,17 +616,23 @@ static lq_status launch_quantize_mp(const QuantArgs& a, cudaStream_t st) {
 // MP = tile bits exchanged through shared memory: log2(tile / 64), at most 3.
 // A 128-column tile has a single cross-lane stage, cheaper as a shuffle (MP = 0).
 template <int LAT, bool BF16>
-static lq_status launch_quantize(const QuantArgs& a, cudaStream_t st) {
-  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0>(a, st);
-  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2>(a, st);
-  return launch_quantize_mp<LAT, BF16, 3>(a, st);
+static lq_status launch_quantize(QuantArgs& a, cudaStream_t st) {
+  if (a.n_mats == 1) {
+    if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, false>(a, st);
+    if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, false>(a, st);
+    return launch_quantize_mp<LAT, BF16, 3, false>(a, st);
+  }
+  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, true>(a, st);
+  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, true>(a, st);
+  return launch_quantize_mp<LAT, BF16, 3, true>(a, st);
 }
 
-extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
-                                 int64_t ldw, int tile, uint64_t seed, float beta, int8_t* codes_dev,
-                                 float* scales_dev, int8_t* signs_dev, int32_t* dev_status_dev,
-                                 void* stream) {
-  LQ_NVTX_RANGE("lq_quantize");
+namespace {
+
+// Checks of one matrix's arguments, in the order lq_quantize reports them.
+lq_status validate_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols, int64_t ldw,
+                            int tile, float beta, const int8_t* codes_dev, const float* scales_dev,
+                            const int8_t* signs_dev, const int32_t* dev_status_dev) {
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (wdtype != LQ_BF16 && wdtype != LQ_F32) return LQ_ERR_DTYPE;
@@ -547,19 +647,41 @@ extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int
         (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
       return LQ_ERR_ARG;
   }
-  cudaStream_t s = (cudaStream_t)stream;
-  st = lq_make_signs(seed, cols, signs_dev, stream);
-  if (st != LQ_OK) return st;
-  if (rows == 0) return LQ_OK;
+  return LQ_OK;
+}
 
-  QuantArgs a;
-  a.W = W_dev; a.rows = rows; a.cols = cols; a.ldw = ldw;
+lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, const int64_t* rows,
+                         const int64_t* cols, const int64_t* ldw, int tile, const uint64_t* seeds, float beta,
+                         int8_t* const* codes, float* const* scales, int8_t* const* signs, int32_t* dev_status,
+                         cudaStream_t s) {
+  SignsArgs sa = {};
+  QuantArgs a = {};
+  int64_t max_cols = 0, units = 0;
+  int k = 0;
+  for (int m = 0; m < n; ++m) {
+    sa.seed[m] = seeds[m];
+    sa.n[m] = cols[m];
+    sa.out[m] = signs[m];
+    if (cols[m] > max_cols) max_cols = cols[m];
+    if (rows[m] == 0) continue;   // signs only
+    QuantMat& M = a.mat[k++];
+    M.W = W[m]; M.codes = codes[m]; M.scales = scales[m]; M.signs = signs[m];
+    M.rows = rows[m]; M.cols = cols[m]; M.ldw = ldw[m];
+    M.tiles_per_row = (int)(cols[m] / tile);
+    M.chunks_per_row = (int)((cols[m] + kChunkCols - 1) / kChunkCols);
+    M.cta_begin = units;
+    M.cpr_recip = M.chunks_per_row == 1 ? 0 : ~0ull / (uint64_t)M.chunks_per_row + 1;
+    units += (rows[m] * M.chunks_per_row + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+  }
+  if (units >= ((int64_t)1 << 40)) return LQ_ERR_SHAPE;
+  lq_status st = launch_signs(sa, n, max_cols, s);
+  if (st != LQ_OK || k == 0) return st;
+  a.n_mats = k;
   a.tile = tile; a.tile_shift = __builtin_ctz((unsigned)tile);
-  a.lanes_per_tile = tile / kLaneElems; a.tiles_per_row = (int)(cols / tile);
-  a.chunks_per_row = (int)((cols + kChunkCols - 1) / kChunkCols);
+  a.lanes_per_tile = tile / kLaneElems;
   a.beta = beta; a.sqrt_tile = sqrtf((float)tile); a.inv_tile = 1.0f / (float)tile;
-  a.signs = signs_dev; a.codes = codes_dev; a.scales = scales_dev; a.status = dev_status_dev;
-  a.units = rows * a.chunks_per_row;
+  a.status = dev_status;
+  a.cta_units = units;
   const bool bf = (wdtype == LQ_BF16);
   switch (lattice) {
     case LQ_E8: return bf ? launch_quantize<LQ_E8, true>(a, s) : launch_quantize<LQ_E8, false>(a, s);
@@ -567,6 +689,39 @@ extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int
     case LQ_A2: return bf ? launch_quantize<LQ_A2, true>(a, s) : launch_quantize<LQ_A2, false>(a, s);
     default:    return bf ? launch_quantize<LQ_Z1, true>(a, s) : launch_quantize<LQ_Z1, false>(a, s);
   }
+}
+
+}  // namespace
+
+extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
+                                 int64_t ldw, int tile, uint64_t seed, float beta, int8_t* codes_dev,
+                                 float* scales_dev, int8_t* signs_dev, int32_t* dev_status_dev,
+                                 void* stream) {
+  LQ_NVTX_RANGE("lq_quantize");
+  const lq_status st = validate_quantize(lattice, W_dev, wdtype, rows, cols, ldw, tile, beta, codes_dev,
+                                         scales_dev, signs_dev, dev_status_dev);
+  if (st != LQ_OK) return st;
+  return quantize_group(lattice, 1, &W_dev, wdtype, &rows, &cols, &ldw, tile, &seed, beta, &codes_dev,
+                        &scales_dev, &signs_dev, dev_status_dev, (cudaStream_t)stream);
+}
+
+extern "C" lq_status lq_quantize_grouped(int lattice, int n, const void* const* W_dev, int wdtype,
+                                         const int64_t* rows, const int64_t* cols, const int64_t* ldw, int tile,
+                                         const uint64_t* seeds, float beta, int8_t* const* codes_dev,
+                                         float* const* scales_dev, int8_t* const* signs_dev,
+                                         int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_quantize_grouped");
+  if (n < 1 || n > kQuantMaxMats) return LQ_ERR_ARG;
+  if (W_dev == nullptr || rows == nullptr || cols == nullptr || ldw == nullptr || seeds == nullptr ||
+      codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr)
+    return LQ_ERR_ARG;
+  for (int m = 0; m < n; ++m) {
+    const lq_status st = validate_quantize(lattice, W_dev[m], wdtype, rows[m], cols[m], ldw[m], tile, beta,
+                                           codes_dev[m], scales_dev[m], signs_dev[m], dev_status_dev);
+    if (st != LQ_OK) return st;
+  }
+  return quantize_group(lattice, n, W_dev, wdtype, rows, cols, ldw, tile, seeds, beta, codes_dev, scales_dev,
+                        signs_dev, dev_status_dev, (cudaStream_t)stream);
 }
 
 template <int LAT, bool OB>

@@ -89,8 +89,25 @@ def test_argument_errors_are_synchronous():
     rows = (ctypes.c_int64 * 9)(*([4] * 9))
     gg = lambda n: lib.lq_gemv_grouped(8, n, arr, arr, arr, rows, 256, 256, good, 1, 1, arr, good, nul, s)
     assert gg(0) == L.LQ_ERR_ARG and gg(9) == L.LQ_ERR_ARG      # group size 1 .. 8
-    assert L.lq_gemv_grouped_workspace_size(3, 2, 4096, 256) >= 3 * 2 * 4096 * 4   # hi + lo fp16 per matrix
-    assert L.lq_gemv_workspace_size(1, 4096, 256) >= 4096 * 4
+    # one fp16 plane per matrix and batch row, plus one float per (batch row, tile)
+    assert L.lq_gemv_grouped_workspace_size(3, 2, 4096, 256) >= 3 * 2 * (4096 * 2 + 16 * 4)
+    assert L.lq_gemv_workspace_size(1, 4096, 256) >= 4096 * 2 + 16 * 4
+    # grouped quantize: group size, then the per-matrix checks of lq_quantize
+    I64 = ctypes.c_int64 * 9
+    ones = (ctypes.c_uint64 * 9)(*([1] * 9))
+    qg = lambda n, rows, cols, ldw, tile=256, beta=0.25, Ws=arr: lib.lq_quantize_grouped(
+        8, n, Ws, 1, I64(*rows), I64(*cols), I64(*ldw), tile, ones, beta, arr, arr, arr, nul, s)
+    r9, c9 = [4] * 9, [256] * 9
+    assert qg(0, r9, c9, c9) == L.LQ_ERR_ARG and qg(9, r9, c9, c9) == L.LQ_ERR_ARG
+    assert qg(2, r9, [256, 384] + c9[2:], [256, 384] + c9[2:]) == L.LQ_ERR_SHAPE        # cols % tile
+    assert qg(2, r9, c9, [256, 128] + c9[2:]) == L.LQ_ERR_SHAPE                         # ldw < cols
+    assert qg(2, [4, -1] + r9[2:], c9, c9) == L.LQ_ERR_SHAPE
+    assert qg(2, r9, c9, c9, tile=100) == L.LQ_ERR_UNSUPPORTED
+    assert qg(2, r9, c9, c9, beta=0.0) == L.LQ_ERR_ARG
+    bad = (ctypes.c_void_p * 9)(*([0x10000, 0x10004] + [0x10000] * 7))
+    assert qg(2, r9, c9, c9, Ws=bad) == L.LQ_ERR_ARG                                    # W alignment
+    assert lib.lq_quantize_grouped(8, 2, nul, 1, I64(*r9), I64(*c9), I64(*c9), 256, ones, 0.25, arr, arr, arr,
+                                   nul, s) == L.LQ_ERR_ARG
     # Rice format: worst case 8 bits per symbol + parity bits + 3 bits per segment, 16 bytes of padding
     assert L.lq_rice_stream_bound("e8", 2, 256, 256) == ((2 * 3 + 2 * 256 * 8 + 2 * 32 + 31) // 32) * 4 + 16
     assert L.lq_rice_stream_bound("e8", 1 << 15, 1 << 14, 256) == 0          # more than 2^28 weights

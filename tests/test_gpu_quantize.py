@@ -184,3 +184,72 @@ def test_stack_recipe_down_matrix_with_outliers_sampled():
     compare_codes(codes.cpu().numpy()[rows], q, "e8")
     ref = O.gemv(q.codes, q.scales, d, 256, "e8", x)
     assert normwise_rel(y.cpu().numpy()[:, rows], ref) < 2e-3
+
+
+def _grouped(torch, L, Ws, tile, seeds, beta, lattice):
+    codes = [torch.empty(W.shape, dtype=torch.int8, device="cuda") for W in Ws]
+    scales = [torch.empty((W.shape[0], W.shape[1] // tile), dtype=torch.float32, device="cuda") for W in Ws]
+    signs = [torch.empty(W.shape[1], dtype=torch.int8, device="cuda") for W in Ws]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.lq_quantize_grouped(lattice, Ws, tile, seeds, beta, codes, scales, signs, dev_status=st)
+    torch.cuda.synchronize()
+    return codes, scales, signs, int(st.item())
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_quantize_grouped_parity(lattice, dtype):
+    """One grouped launch over matrices of different shapes (a ragged last chunk,
+    several chunks per row, an empty matrix, a padded row stride): every matrix
+    equals the oracle with its own seed, and the single-matrix call bit for bit."""
+    torch, L = cuda()
+    tile = 256
+    shapes = [(37, 768), (0, 512), (64, 2304), (5, 256), (130, 4352), (19, 4096)]
+    seeds = [11, 12, 2**63 + 5, 14, 15, 16]
+    Ws, Wn = [], []
+    for i, (r, c) in enumerate(shapes):
+        W = gaussian_matrix(r, c, 0.02, 200 + i, outlier_frac=0.002, dtype="bf16")
+        pad = 8 if i == 2 else 0
+        full = np.zeros((r, c + pad), dtype=np.float32)
+        full[:, :c] = W
+        Wd = to_dev_bf16(torch, full) if dtype == "bf16" else to_dev(torch, full)
+        Ws.append(Wd[:, :c])
+        Wn.append(W)
+    codes, scales, signs, st = _grouped(torch, L, Ws, tile, seeds, 0.25, lattice)
+    any_range = False
+    for m, W in enumerate(Wn):
+        d = O.splitmix64_signs(seeds[m], W.shape[1])
+        np.testing.assert_array_equal(signs[m].cpu().numpy(), d)
+        if W.shape[0] == 0:
+            continue
+        q = O.quantize(W, lattice, tile, d, 0.25)
+        any_range |= q.range_error
+        np.testing.assert_allclose(scales[m].cpu().numpy(), q.scales, rtol=1e-6, atol=0)
+        compare_codes(codes[m].cpu().numpy(), q, lattice)
+        c1, s1, g1 = L.quantize(Ws[m], lattice=lattice, tile=tile, seed=seeds[m], beta=0.25)
+        torch.cuda.synchronize()
+        assert torch.equal(c1, codes[m]) and torch.equal(s1, scales[m]) and torch.equal(g1, signs[m])
+    assert st == (2 if any_range else 0)
+
+
+def test_quantize_grouped_layer_matches_single_calls():
+    """The seven Llama-3-8B layer matrices (bf16, seeds 1000 + index) in one grouped
+    launch equal seven single-matrix launches bit for bit; oracle on sampled rows
+    of the down projection (the group's only 7-chunk rows)."""
+    torch, L = cuda()
+    from synthetic import LLAMA3_8B_LAYER, torch_gaussian_matrix
+    Ws = [torch_gaussian_matrix(r, c, 0.02, 1000 + i, device="cuda") for i, (_, r, c) in enumerate(LLAMA3_8B_LAYER)]
+    seeds = [1000 + i for i in range(len(Ws))]
+    codes, scales, signs, st = _grouped(torch, L, Ws, 256, seeds, 0.25, "e8")
+    assert st == 0
+    for m, W in enumerate(Ws):
+        c1, s1, g1 = L.quantize(W, lattice="e8", tile=256, seed=seeds[m], beta=0.25)
+        torch.cuda.synchronize()
+        assert torch.equal(c1, codes[m]) and torch.equal(s1, scales[m]) and torch.equal(g1, signs[m])
+        del c1, s1, g1
+    rng = np.random.default_rng(2)
+    rows = np.sort(np.concatenate([[0, 4095], rng.choice(4096, 30, replace=False)]))
+    Wd = Ws[6][torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    q = O.quantize(Wd, "e8", 256, O.splitmix64_signs(seeds[6], 14336), 0.25)
+    np.testing.assert_allclose(scales[6].cpu().numpy()[rows], q.scales, rtol=1e-6)
+    compare_codes(codes[6].cpu().numpy()[rows], q, "e8")
