@@ -42,3 +42,4 @@ from .lattice_oracle import (  # noqa: F401
     code_entropy_bits,
     QuantResult,
 )
+from . import scale_formats  # noqa: F401,E402
