@@ -410,6 +410,62 @@ lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, cons
                            int xdtype, int64_t rows, int64_t cols, int64_t ldx, float* Y_dev,
                            int64_t ldy, void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * Scale formats.  Every call above stores and reads one float32 scale per
+ * (row, tile).  The _ex calls below take the format as an argument:
+ *   LQ_SCALE_TILE_F32  float32 [rows x cols/tile]: the format of the calls above.
+ *   LQ_SCALE_ROW_BF16  bfloat16 [rows] (raw 16-bit patterns): one scale per row,
+ *                      s_r = beta * RMS of the whole row (HyperQuant page,
+ *                      mma="int8" paragraph: row-normalised weights stored
+ *                      with a bf16 per-row scale).
+ *   LQ_SCALE_TILE_F16  float16 [rows x cols/tile] (raw 16-bit patterns): the
+ *                      per-tile scale in half precision (the page's KV cache:
+ *                      int8 codes with fp16 norms).
+ * With a 16-bit format the stored value is the scale rounded to nearest-even,
+ * and the codes are the nearest lattice points of the rotated tile divided by
+ * that stored value, so that reconstruction and products use exactly what is
+ * stored.  An fp16 scale that overflows raises LQ_DEV_RANGE (codes of that tile
+ * unspecified); a row holding a non-finite value gets scale 0 and
+ * LQ_DEV_NONFINITE.
+ * ------------------------------------------------------------------------
+ */
+#define LQ_SCALE_TILE_F32 0
+#define LQ_SCALE_ROW_BF16 1
+#define LQ_SCALE_TILE_F16 2
+
+/* lq_quantize writing scales_dev in scale_format.  LQ_SCALE_ROW_BF16 reads W
+ * twice (a row-norm pass, then the quantize pass), in row blocks small enough
+ * for the second read to come from L2. */
+lq_status lq_quantize_ex(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
+                         int64_t ldw, int tile, uint64_t seed, float beta, int scale_format,
+                         int8_t* codes_dev, void* scales_dev, int8_t* signs_dev,
+                         int32_t* dev_status_dev, void* stream);
+
+/* lq_dequantize reading scales_dev in scale_format. */
+lq_status lq_dequantize_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
+                           const int8_t* signs_dev, int64_t rows, int64_t cols, int tile, void* What_dev,
+                           int out_dtype, void* stream);
+
+/* lq_gemv reading scales_dev in scale_format (same workspace). */
+lq_status lq_gemv_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
+                     const int8_t* signs_dev, int64_t rows, int64_t cols, int tile, const void* x_dev,
+                     int xdtype, int batch, float* y_dev, void* workspace_dev, int32_t* dev_status_dev,
+                     void* stream);
+
+/* lq_gemm reading scales_dev in scale_format (same workspace). */
+lq_status lq_gemm_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
+                     const int8_t* signs_dev, int64_t N, int64_t K, int tile, const uint16_t* X_dev, int64_t M,
+                     float* Y_dev, void* workspace_dev, int32_t* dev_status_dev, void* stream);
+
+/* lq_attention_decode with both caches' scales in scale_format
+ * (LQ_SCALE_TILE_F32 or LQ_SCALE_TILE_F16, [tokens x kv_heads]). */
+lq_status lq_attention_decode_ex(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
+                                 const int8_t* k_signs_dev, const int8_t* v_codes_dev, const void* v_scales_dev,
+                                 const int8_t* v_signs_dev, int scale_format, int64_t tokens, int kv_heads,
+                                 int q_heads, int head_dim, const void* q_dev, int qdtype, float* out_dev,
+                                 void* workspace_dev, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -31,6 +31,12 @@ SIGNATURES = {
     "lq_quantize": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _F32, _P, _P, _P, _P, _P]),
     "lq_quantize_grouped": (_I32, [_I32, _I32, _P, _I32, _P, _P, _P, _I32, _P, _F32, _P, _P, _P, _P, _P]),
     "lq_dequantize": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _P]),
+    "lq_quantize_ex": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _F32, _I32, _P, _P, _P, _P, _P]),
+    "lq_dequantize_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I32, _P]),
+    "lq_gemv_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
+    "lq_gemm_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
+    "lq_attention_decode_ex": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P,
+                                      _P, ctypes.c_size_t, _P]),
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
     "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "lq_gemv_noalloc": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P]),
@@ -328,6 +334,82 @@ def lq_attention_decode(lattice, k_codes, k_scales, k_signs, v_codes, v_scales, 
         _lattice_id(lattice), _ptr(k_codes), _ptr(k_scales), _ptr(k_signs), _ptr(v_codes), _ptr(v_scales),
         _ptr(v_signs), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# Scale formats (LQ_SCALE_* in lq.h)
+LQ_SCALE_TILE_F32, LQ_SCALE_ROW_BF16, LQ_SCALE_TILE_F16 = 0, 1, 2
+_SCALE_FORMATS = {"tile_f32": 0, "row_bf16": 1, "tile_f16": 2}
+
+
+def _scale_format_id(fmt) -> int:
+    return int(_SCALE_FORMATS.get(fmt, fmt))
+
+
+def scales_tensor(rows: int, cols: int, tile: int, scale_format, device):
+    """Empty scale tensor of the shape and dtype `scale_format` stores."""
+    import torch
+    f = _scale_format_id(scale_format)
+    if f == LQ_SCALE_ROW_BF16:
+        return torch.empty((rows,), dtype=torch.bfloat16, device=device)
+    dt = torch.float16 if f == LQ_SCALE_TILE_F16 else torch.float32
+    return torch.empty((rows, cols // tile), dtype=dt, device=device)
+
+
+def lq_quantize_ex(lattice, W, tile: int, seed: int, beta: float, scale_format, codes, scales, signs,
+                   dev_status=None, stream=None) -> None:
+    """lq_quantize storing the scales in `scale_format` ("tile_f32", "row_bf16", "tile_f16")."""
+    rows, cols = W.shape
+    _check("lq_quantize_ex", _get_lib().lq_quantize_ex(
+        _lattice_id(lattice), _ptr(W), _dtype_id(W), rows, cols, _row_stride(W), int(tile),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, float(beta), _scale_format_id(scale_format), _ptr(codes), _ptr(scales),
+        _ptr(signs), _ptr(dev_status), _stream(stream)))
+
+
+def quantize_ex(W, lattice: str = "e8", tile: int = 256, seed: int = 0, beta: float = 0.25,
+                scale_format="row_bf16", dev_status=None, stream=None):
+    """Allocate outputs and call :func:`lq_quantize_ex`; returns (codes, scales, signs)."""
+    import torch
+    rows, cols = W.shape
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=W.device)
+    scales = scales_tensor(rows, cols, tile, scale_format, W.device)
+    signs = torch.empty((cols,), dtype=torch.int8, device=W.device)
+    lq_quantize_ex(lattice, W, tile, seed, beta, scale_format, codes, scales, signs, dev_status, stream)
+    return codes, scales, signs
+
+
+def lq_dequantize_ex(lattice, codes, scales, scale_format, signs, tile: int, W_hat, stream=None) -> None:
+    rows, cols = codes.shape
+    _check("lq_dequantize_ex", _get_lib().lq_dequantize_ex(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _scale_format_id(scale_format), _ptr(signs), rows, cols,
+        int(tile), _ptr(W_hat), _dtype_id(W_hat), _stream(stream)))
+
+
+def lq_gemv_ex(lattice, codes, scales, scale_format, signs, tile: int, x, y, workspace, dev_status=None,
+               stream=None) -> None:
+    rows, cols = codes.shape
+    _check("lq_gemv_ex", _get_lib().lq_gemv_ex(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _scale_format_id(scale_format), _ptr(signs), rows, cols,
+        int(tile), _ptr(x), _dtype_id(x), x.shape[0], _ptr(y), _ptr(workspace), _ptr(dev_status),
+        _stream(stream)))
+
+
+def lq_gemm_ex(lattice, codes, scales, scale_format, signs, tile: int, X, Y, workspace, dev_status=None,
+               stream=None) -> None:
+    N, K = codes.shape
+    _check("lq_gemm_ex", _get_lib().lq_gemm_ex(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _scale_format_id(scale_format), _ptr(signs), N, K,
+        int(tile), _ptr(X), X.shape[0], _ptr(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def lq_attention_decode_ex(lattice, k_codes, k_scales, k_signs, v_codes, v_scales, v_signs, scale_format, q, out,
+                           workspace, stream=None) -> None:
+    tokens = k_codes.shape[0]
+    kv_heads = k_scales.shape[1]
+    q_heads, head_dim = q.shape
+    _check("lq_attention_decode_ex", _get_lib().lq_attention_decode_ex(
+        _lattice_id(lattice), _ptr(k_codes), _ptr(k_scales), _ptr(k_signs), _ptr(v_codes), _ptr(v_scales),
+        _ptr(v_signs), _scale_format_id(scale_format), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q),
+        _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lq_rotate_blocks(R, X, Y, transpose: bool = False, stream=None) -> None:

@@ -175,6 +175,29 @@ __device__ __forceinline__ void load_f32_signed(const void* src, const int8_t* s
 // Columns per thread for the activation transforms: a tile must fit one warp.
 __host__ __device__ constexpr int act_elems_for_tile(int tile) { return tile <= 512 ? 16 : tile / 32; }
 
+// ---------------------------------------------------------------- scales
+// Stored scale of (row, tile t) in one of the LQ_SCALE_* formats (lq.h):
+// float32 [rows x tiles], bfloat16 [rows] or float16 [rows x tiles].
+__device__ __forceinline__ float load_scale(const void* base, int fmt, int64_t row, int64_t t,
+                                            int64_t tiles_per_row) {
+  if (fmt == LQ_SCALE_ROW_BF16)
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(base) + row) << 16);
+  if (fmt == LQ_SCALE_TILE_F16)
+    return __half2float(__ldg(reinterpret_cast<const __half*>(base) + row * tiles_per_row + t));
+  return __ldg(reinterpret_cast<const float*>(base) + row * tiles_per_row + t);
+}
+
+// The same with the format fixed at compile time (for hot loops).
+template <int SF>
+__device__ __forceinline__ float load_scale_t(const void* base, int64_t row, int64_t t, int64_t tiles_per_row) {
+  if constexpr (SF == LQ_SCALE_ROW_BF16)
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(base) + row) << 16);
+  else if constexpr (SF == LQ_SCALE_TILE_F16)
+    return __half2float(__ldg(reinterpret_cast<const __half*>(base) + row * tiles_per_row + t));
+  else
+    return __ldg(reinterpret_cast<const float*>(base) + row * tiles_per_row + t);
+}
+
 // ---------------------------------------------------------------- code packing
 // Low bytes of four ints into one word (byte i = low byte of ci).
 __device__ __forceinline__ uint32_t pack4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3) {

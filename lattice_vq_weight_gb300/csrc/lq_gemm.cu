@@ -86,7 +86,7 @@ struct Args {
   int tile, tiles_per_row;
   int n_tiles, m_tiles, splits, stages_per_split, k_stages;
   int64_t units;
-  const float* scales;    // [N x K/T]
+  const void* scales;     // [N x K/T] or [N], in gemm_kernel's format SF
   const float* f;         // [N]   row factors 2^e
   const float* inv_g;     // [M]   1 / g_m
   float* Y;               // [M x N]
@@ -183,6 +183,19 @@ __device__ __forceinline__ uint32_t code_pair_f16(uint32_t u, uint32_t sel, __ha
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// Storage type of one scale in format SF and its value.
+template <int SF> struct ScaleType { using T = float; };
+template <> struct ScaleType<LQ_SCALE_ROW_BF16> { using T = unsigned short; };
+template <> struct ScaleType<LQ_SCALE_TILE_F16> { using T = __half; };
+template <int SF>
+__device__ __forceinline__ float scale_value(const typename ScaleType<SF>::T* p) {
+  if constexpr (SF == LQ_SCALE_ROW_BF16) return __uint_as_float((uint32_t)__ldg(p) << 16);
+  else if constexpr (SF == LQ_SCALE_TILE_F16) return __half2float(__ldg(p));
+  else return __ldg(p);
+}
+
+// SF: the scale format (LQ_SCALE_*), fixed at compile time for the decode loop.
+template <int SF>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x, Args a) {
   extern __shared__ uint8_t smem_raw[];
@@ -316,21 +329,25 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
       unit_range(u, nt, mt, k0, k1);
       constexpr int P = kDecodePasses;
       constexpr int kRowsPerPass = kDecodeThreads / 4;
+      // per pass: the row's first tile scale (the row's scale for the per-row format)
+      using ST = typename ScaleType<SF>::T;
+      constexpr int kTileStep = (SF == LQ_SCALE_ROW_BF16) ? 0 : 1;
       float fr[P];
-      const float* srow[P];
+      const ST* srow[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) {
         const int64_t row = (int64_t)nt * BM + kRowsPerPass * p + rsub;
         fr[p] = 0.5f * __ldg(a.f + row);
-        srow[p] = a.scales + row * a.tiles_per_row;
+        srow[p] = reinterpret_cast<const ST*>(a.scales) + row * (kTileStep ? a.tiles_per_row : 1);
       }
       // scales of the current tile and (prefetched) of the next one
       float s_cur[P], s_nxt[P];
       int t_cur = k0 / stages_per_t;
 #pragma unroll
-      for (int p = 0; p < P; ++p) s_cur[p] = __ldg(srow[p] + t_cur);
+      for (int p = 0; p < P; ++p) s_cur[p] = scale_value<SF>(srow[p] + kTileStep * t_cur);
 #pragma unroll
-      for (int p = 0; p < P; ++p) s_nxt[p] = (t_cur + 1 < a.tiles_per_row) ? __ldg(srow[p] + t_cur + 1) : 0.f;
+      for (int p = 0; p < P; ++p)
+        s_nxt[p] = (t_cur + 1 < a.tiles_per_row) ? scale_value<SF>(srow[p] + kTileStep * (t_cur + 1)) : 0.f;
       __half2 sf[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) sf[p] = __float2half2_rn(s_cur[p] * fr[p]);
@@ -341,7 +358,7 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
 #pragma unroll
           for (int p = 0; p < P; ++p) {
             sf[p] = __float2half2_rn(s_nxt[p] * fr[p]);
-            s_nxt[p] = (t + 1 < a.tiles_per_row) ? __ldg(srow[p] + t + 1) : 0.f;
+            s_nxt[p] = (t + 1 < a.tiles_per_row) ? scale_value<SF>(srow[p] + kTileStep * (t + 1)) : 0.f;
           }
         }
         if (!mbar_wait(&sm.full_c[sc], phc, timeout)) break;
@@ -436,7 +453,8 @@ struct PrepArgs {
   int a2;
   __half* Xt;                // [M x K]
   float* inv_g;              // [M]
-  const float* scales;       // [N x K/T]
+  const void* scales;        // [N x K/T] or [N], format sfmt
+  int sfmt;
   float* f;                  // [N]
   float* Y;                  // zeroed when zero_y
   int zero_y;
@@ -458,7 +476,12 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
     const int ln = threadIdx.x & 31;
     if (n >= a.N) return;
     float mx = 0.f;
-    for (int t = ln; t < a.tiles_per_row; t += 32) mx = fmaxf(mx, __ldg(a.scales + n * a.tiles_per_row + t));
+    if (a.sfmt == LQ_SCALE_TILE_F32) {
+      const float* sc = reinterpret_cast<const float*>(a.scales) + n * a.tiles_per_row;
+      for (int t = ln; t < a.tiles_per_row; t += 32) mx = fmaxf(mx, __ldg(sc + t));
+    } else {
+      for (int t = ln; t < a.tiles_per_row; t += 32) mx = fmaxf(mx, load_scale(a.scales, a.sfmt, n, t, a.tiles_per_row));
+    }
     for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     // |p s| <= 63.5 s; choose f = 2^e with 63.5 * max(s) * f in [2^14, 2^15)
     float fv = 1.f;
@@ -617,11 +640,13 @@ extern "C" size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
   return gemm_layout(M, N, K).total;
 }
 
-extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
-                             const int8_t* signs_dev, int64_t N, int64_t K, int tile,
-                             const uint16_t* X_dev, int64_t M, float* Y_dev, void* workspace_dev,
-                             int32_t* dev_status_dev, void* stream) {
-  LQ_NVTX_RANGE("lq_gemm");
+namespace {
+
+lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev, int sfmt, const int8_t* signs_dev,
+                   int64_t N, int64_t K, int tile, const uint16_t* X_dev, int64_t M, float* Y_dev,
+                   void* workspace_dev, int32_t* dev_status_dev, void* stream) {
+  if (sfmt != LQ_SCALE_TILE_F32 && sfmt != LQ_SCALE_ROW_BF16 && sfmt != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
+  const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
   lq_status st = validate_common(lattice, N, K, tile);
   if (st != LQ_OK) return st;
   if (M < 0) return LQ_ERR_SHAPE;
@@ -632,7 +657,8 @@ extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* 
       Y_dev == nullptr || workspace_dev == nullptr)
     return LQ_ERR_ARG;
   if (!aligned16(codes_dev) || !aligned16(signs_dev) || !aligned16(X_dev) || !aligned16(Y_dev) ||
-      (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0 || !aligned4(scales_dev) ||
+      (reinterpret_cast<uintptr_t>(workspace_dev) & 255u) != 0 ||
+      (reinterpret_cast<uintptr_t>(scales_dev) & salign) != 0 ||
       (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
     return LQ_ERR_ARG;
   cudaStream_t s = (cudaStream_t)stream;
@@ -662,7 +688,7 @@ extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* 
   p.chunks_per_row = (int)((K + kChunkCols - 1) / kChunkCols);
   p.inv_sqrt_tile = (float)(1.0 / sqrt((double)tile));
   p.a2 = (lattice == LQ_A2);
-  p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.f = f; p.Y = Y_dev; p.zero_y = a.splits > 1;
+  p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.sfmt = sfmt; p.f = f; p.Y = Y_dev; p.zero_y = a.splits > 1;
   p.status = dev_status_dev;
   const int64_t prep_blocks = M + (N + kPrepWarps - 1) / kPrepWarps;
   const int E = act_elems_for_tile(tile);
@@ -684,13 +710,43 @@ extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* 
   static_assert(sizeof(Smem) + 1024 <= 227 * 1024, "shared memory budget");
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(gemm_kernel<LQ_SCALE_TILE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_kernel<LQ_SCALE_ROW_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_kernel<LQ_SCALE_TILE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
     }
     attr_set = true;
   }
   const int64_t grid = a.units < sms ? a.units : sms;
-  gemm_kernel<<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
+  if (sfmt == LQ_SCALE_ROW_BF16)
+    gemm_kernel<LQ_SCALE_ROW_BF16><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
+  else if (sfmt == LQ_SCALE_TILE_F16)
+    gemm_kernel<LQ_SCALE_TILE_F16><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
+  else
+    gemm_kernel<LQ_SCALE_TILE_F32><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
   return check_launch();
+}
+
+}  // namespace
+
+extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                             const int8_t* signs_dev, int64_t N, int64_t K, int tile,
+                             const uint16_t* X_dev, int64_t M, float* Y_dev, void* workspace_dev,
+                             int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemm");
+  return gemm_fmt(lattice, codes_dev, scales_dev, LQ_SCALE_TILE_F32, signs_dev, N, K, tile, X_dev, M, Y_dev,
+                  workspace_dev, dev_status_dev, stream);
+}
+
+extern "C" lq_status lq_gemm_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
+                                const int8_t* signs_dev, int64_t N, int64_t K, int tile, const uint16_t* X_dev,
+                                int64_t M, float* Y_dev, void* workspace_dev, int32_t* dev_status_dev,
+                                void* stream) {
+  LQ_NVTX_RANGE("lq_gemm_ex");
+  return gemm_fmt(lattice, codes_dev, scales_dev, scale_format, signs_dev, N, K, tile, X_dev, M, Y_dev,
+                  workspace_dev, dev_status_dev, stream);
 }

@@ -35,7 +35,7 @@ namespace lq {
 
 struct GemvMat {
   const int8_t* codes;
-  const float* scales;
+  const void* scales;    // in the launch's scale format (gemv_kernel's SF)
   float* y;
   int64_t rows;
   int64_t groups;        // row groups of 16 RG rows
@@ -82,7 +82,7 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // griddepcontrol.wait: codes do not depend on the activation kernel that
 // precedes this one, so with programmatic dependent launch the code stream
 // starts while that kernel is still running.
-template <int NB, int RG, int S>
+template <int NB, int RG, int S, int SF>
 __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) {
   constexpr int kCode = RG * 2;        // 16-byte code slots per thread per stage
   static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     if (tile_end || it == n_it - 1) {
       // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
       const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
-      const float* scales = a.mat[m].scales + t;
+      const void* scales = a.mat[m].scales;
       const int64_t rows = a.mat[m].rows;
       float fx[NB][2];
 #pragma unroll
@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int64_t r = (int64_t)grp * 16 * RG + 16 * i + 8 * h + g;
-          sr[h] = (r < rows) ? __ldg(scales + r * a.tiles_per_row) : 0.f;
+          sr[h] = (r < rows) ? load_scale_t<SF>(scales, r, t, a.tiles_per_row) : 0.f;
         }
 #pragma unroll
         for (int n = 0; n < NB; ++n) {
@@ -331,7 +331,7 @@ GemvWorkspace gemv_workspace_layout(int n_mats, int batch, int64_t cols, int til
 // than its share of the stream.
 constexpr int64_t kMinStepsPerWarp = 4;
 
-template <int NB, int RG>
+template <int NB, int RG, int SF>
 lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
   constexpr int S = 4;                       // ring stages per warp
   constexpr int kWarps = 4;
@@ -339,12 +339,12 @@ lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
   GemvArgs a = a0;
   static int per_sm = 0;
   if (per_sm == 0) {
-    if (cudaFuncSetAttribute(gemv_kernel<NB, RG, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+    if (cudaFuncSetAttribute(gemv_kernel<NB, RG, S, SF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
     }
-    per_sm = occupancy_per_sm(gemv_kernel<NB, RG, S>, kWarps * 32, smem);
+    per_sm = occupancy_per_sm(gemv_kernel<NB, RG, S, SF>, kWarps * 32, smem);
   }
   const int sms = device_sm_count();
   if (sms <= 0) return LQ_ERR_CUDA;
@@ -371,7 +371,7 @@ lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, gemv_kernel<NB, RG, S>, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, gemv_kernel<NB, RG, S, SF>, a) != cudaSuccess) {
     cudaGetLastError();
     return LQ_ERR_CUDA;
   }
@@ -379,11 +379,13 @@ lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
 }
 
 // Validation and both launches for a group of n matrices sharing x.
-lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const float* const* scales_dev,
+lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const void* const* scales_dev,
                      const int8_t* const* signs_dev, const int64_t* rows, int64_t cols, int tile,
                      const void* x_dev, int xdtype, int batch, float* const* y_dev, void* workspace_dev,
-                     int32_t* dev_status_dev, cudaStream_t s) {
+                     int32_t* dev_status_dev, cudaStream_t s, int sfmt = LQ_SCALE_TILE_F32) {
   if (n < 1 || n > kGemvMaxMats) return LQ_ERR_ARG;
+  if (sfmt != LQ_SCALE_TILE_F32 && sfmt != LQ_SCALE_ROW_BF16 && sfmt != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
+  const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
   if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || rows == nullptr ||
       y_dev == nullptr)
     return LQ_ERR_ARG;
@@ -405,7 +407,9 @@ lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const f
     if (signs_dev[m] == nullptr || !aligned16(signs_dev[m])) return LQ_ERR_ARG;
     if (rows[m] == 0) continue;
     if (codes_dev[m] == nullptr || scales_dev[m] == nullptr || y_dev[m] == nullptr) return LQ_ERR_ARG;
-    if (!aligned16(codes_dev[m]) || !aligned4(scales_dev[m]) || !aligned4(y_dev[m])) return LQ_ERR_ARG;
+    if (!aligned16(codes_dev[m]) || (reinterpret_cast<uintptr_t>(scales_dev[m]) & salign) != 0 ||
+        !aligned4(y_dev[m]))
+      return LQ_ERR_ARG;
   }
   const GemvWorkspace lay = gemv_workspace_layout(n, batch, cols, tile);
   char* ws = reinterpret_cast<char*>(workspace_dev);
@@ -443,8 +447,11 @@ lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const f
   g.n_mats = ne;
   g.cols = cols; g.tile = tile; g.tiles_per_row = (int)(cols / tile); g.batch = batch;
   g.xh = r.xh; g.xs = r.xs;
-  if (batch <= 8) return launch_gemv<1, 2>(g, s);
-  return launch_gemv<2, 2>(g, s);
+  if (sfmt == LQ_SCALE_ROW_BF16)
+    return batch <= 8 ? launch_gemv<1, 2, LQ_SCALE_ROW_BF16>(g, s) : launch_gemv<2, 2, LQ_SCALE_ROW_BF16>(g, s);
+  if (sfmt == LQ_SCALE_TILE_F16)
+    return batch <= 8 ? launch_gemv<1, 2, LQ_SCALE_TILE_F16>(g, s) : launch_gemv<2, 2, LQ_SCALE_TILE_F16>(g, s);
+  return batch <= 8 ? launch_gemv<1, 2, LQ_SCALE_TILE_F32>(g, s) : launch_gemv<2, 2, LQ_SCALE_TILE_F32>(g, s);
 }
 
 }  // namespace
@@ -472,8 +479,26 @@ extern "C" lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* 
   if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || x_dev == nullptr ||
       y_dev == nullptr || workspace_dev == nullptr)
     return LQ_ERR_ARG;
-  return gemv_group(lattice, 1, &codes_dev, &scales_dev, &signs_dev, &rows, cols, tile, x_dev, xdtype, batch,
+  const void* sc = scales_dev;
+  return gemv_group(lattice, 1, &codes_dev, &sc, &signs_dev, &rows, cols, tile, x_dev, xdtype, batch,
                     &y_dev, workspace_dev, dev_status_dev, (cudaStream_t)stream);
+}
+
+extern "C" lq_status lq_gemv_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
+                                const int8_t* signs_dev, int64_t rows, int64_t cols, int tile, const void* x_dev,
+                                int xdtype, int batch, float* y_dev, void* workspace_dev,
+                                int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemv_ex");
+  lq_status st = validate_common(lattice, rows, cols, tile);
+  if (st != LQ_OK) return st;
+  if (xdtype != LQ_BF16 && xdtype != LQ_F32) return LQ_ERR_DTYPE;
+  if (batch < 1 || batch > 16) return LQ_ERR_SHAPE;
+  if (rows == 0) return LQ_OK;
+  if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || x_dev == nullptr ||
+      y_dev == nullptr || workspace_dev == nullptr)
+    return LQ_ERR_ARG;
+  return gemv_group(lattice, 1, &codes_dev, &scales_dev, &signs_dev, &rows, cols, tile, x_dev, xdtype, batch,
+                    &y_dev, workspace_dev, dev_status_dev, (cudaStream_t)stream, scale_format);
 }
 
 extern "C" lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* codes_dev,
@@ -482,7 +507,10 @@ extern "C" lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* co
                                      int batch, float* const* y_dev, void* workspace_dev,
                                      int32_t* dev_status_dev, void* stream) {
   LQ_NVTX_RANGE("lq_gemv_grouped");
-  return gemv_group(lattice, n, codes_dev, scales_dev, signs_dev, rows, cols, tile, x_dev, xdtype, batch, y_dev,
+  if (n < 1 || n > kGemvMaxMats || scales_dev == nullptr) return LQ_ERR_ARG;
+  const void* sc[kGemvMaxMats];
+  for (int m = 0; m < n; ++m) sc[m] = scales_dev[m];
+  return gemv_group(lattice, n, codes_dev, sc, signs_dev, rows, cols, tile, x_dev, xdtype, batch, y_dev,
                     workspace_dev, dev_status_dev, (cudaStream_t)stream);
 }
 

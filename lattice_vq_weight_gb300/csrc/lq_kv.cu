@@ -33,11 +33,12 @@ constexpr int kThreads = kWarps * 32;
 
 struct AttnArgs {
   const int8_t* kc;
-  const float* ks;
+  const void* ks;        // [tokens x kv_heads], format sfmt (LQ_SCALE_TILE_F32 / _F16)
   const int8_t* ksg;
   const int8_t* vc;
-  const float* vs;
+  const void* vs;
   const int8_t* vsg;
+  int sfmt;
   const void* q;
   int qbf16;
   int64_t tokens;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(D) rotate_query_kernel(AttnArgs a) {
   a.qrot[qi] = v[i] * (0.5f / (float)D) * ((a.a2 && (i & 1)) ? 1.7320508075688772f : 1.f);
 }
 
-template <int G>
+template <int G, bool F16S>
 __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(AttnArgs a) {
   __shared__ __align__(16) float qr[G][D];         // rotated, scaled queries
   __shared__ float wm[kWarps][G], wl[kWarps][G];
@@ -116,8 +117,13 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(
       const uint4* kp = reinterpret_cast<const uint4*>(a.kc + j * ld + (int64_t)kvh * D);
 #pragma unroll
       for (int q = 0; q < D / 16; ++q) kw[q] = __ldg(kp + q);
-      s_k = __ldg(a.ks + j * a.kv_heads + kvh);
-      s_v = __ldg(a.vs + j * a.kv_heads + kvh);
+      if constexpr (F16S) {
+        s_k = __half2float(__ldg(reinterpret_cast<const __half*>(a.ks) + j * a.kv_heads + kvh));
+        s_v = __half2float(__ldg(reinterpret_cast<const __half*>(a.vs) + j * a.kv_heads + kvh));
+      } else {
+        s_k = __ldg(reinterpret_cast<const float*>(a.ks) + j * a.kv_heads + kvh);
+        s_v = __ldg(reinterpret_cast<const float*>(a.vs) + j * a.kv_heads + kvh);
+      }
     } else {
 #pragma unroll
       for (int q = 0; q < D / 16; ++q) kw[q] = make_uint4(0, 0, 0, 0);
@@ -330,14 +336,16 @@ extern "C" size_t lq_attention_workspace_size(int64_t tokens, int kv_heads, int 
   return (part_floats(kv_heads, splits, q_heads / kv_heads) + (size_t)q_heads * D) * sizeof(float);
 }
 
-extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev, const float* k_scales_dev,
-                                         const int8_t* k_signs_dev, const int8_t* v_codes_dev,
-                                         const float* v_scales_dev, const int8_t* v_signs_dev, int64_t tokens,
-                                         int kv_heads, int q_heads, int head_dim, const void* q_dev, int qdtype,
-                                         float* out_dev, void* workspace_dev, size_t workspace_bytes,
-                                         void* stream) {
-  LQ_NVTX_RANGE("lq_attention_decode");
+namespace {
+
+lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
+                        const int8_t* k_signs_dev, const int8_t* v_codes_dev, const void* v_scales_dev,
+                        const int8_t* v_signs_dev, int sfmt, int64_t tokens, int kv_heads, int q_heads, int head_dim,
+                        const void* q_dev, int qdtype, float* out_dev, void* workspace_dev, size_t workspace_bytes,
+                        void* stream) {
   if (!valid_lattice(lattice)) return LQ_ERR_ARG;
+  if (sfmt != LQ_SCALE_TILE_F32 && sfmt != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
+  const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
   if (head_dim != D) return LQ_ERR_UNSUPPORTED;
   if (qdtype != LQ_BF16 && qdtype != LQ_F32) return LQ_ERR_DTYPE;
   if (tokens <= 0 || kv_heads <= 0 || q_heads <= 0 || q_heads % kv_heads != 0) return LQ_ERR_SHAPE;
@@ -348,13 +356,15 @@ extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev,
       v_scales_dev == nullptr || v_signs_dev == nullptr || q_dev == nullptr || out_dev == nullptr ||
       workspace_dev == nullptr)
     return LQ_ERR_ARG;
-  if (!aligned16(k_codes_dev) || !aligned16(v_codes_dev) || !aligned4(k_scales_dev) || !aligned4(v_scales_dev) ||
+  if (!aligned16(k_codes_dev) || !aligned16(v_codes_dev) || (reinterpret_cast<uintptr_t>(k_scales_dev) & salign) ||
+      (reinterpret_cast<uintptr_t>(v_scales_dev) & salign) ||
       !aligned4(out_dev) || !aligned4(workspace_dev))
     return LQ_ERR_ARG;
   if (workspace_bytes < lq_attention_workspace_size(tokens, kv_heads, q_heads, head_dim)) return LQ_ERR_SHAPE;
   AttnArgs a;
   a.kc = k_codes_dev; a.ks = k_scales_dev; a.ksg = k_signs_dev;
   a.vc = v_codes_dev; a.vs = v_scales_dev; a.vsg = v_signs_dev;
+  a.sfmt = sfmt;
   a.q = q_dev; a.qbf16 = (qdtype == LQ_BF16);
   a.tokens = tokens; a.kv_heads = kv_heads; a.group = group;
   a.splits = attn_splits(tokens, kv_heads);
@@ -366,16 +376,47 @@ extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev,
   if (!aligned16(workspace_dev)) return LQ_ERR_ARG;
   rotate_query_kernel<<<(unsigned)q_heads, D, 0, s>>>(a);
   const unsigned grid = (unsigned)(kv_heads * a.splits);
+  const bool h = (sfmt == LQ_SCALE_TILE_F16);
   switch (group) {
-    case 1: attn_partial_kernel<1><<<grid, kThreads, 0, s>>>(a); break;
-    case 2: attn_partial_kernel<2><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: attn_partial_kernel<4><<<grid, kThreads, 0, s>>>(a); break;
-    default: attn_partial_kernel<8><<<grid, kThreads, 0, s>>>(a); break;
+    case 1: h ? attn_partial_kernel<1, true><<<grid, kThreads, 0, s>>>(a)
+              : attn_partial_kernel<1, false><<<grid, kThreads, 0, s>>>(a); break;
+    case 2: h ? attn_partial_kernel<2, true><<<grid, kThreads, 0, s>>>(a)
+              : attn_partial_kernel<2, false><<<grid, kThreads, 0, s>>>(a); break;
+    case 4: h ? attn_partial_kernel<4, true><<<grid, kThreads, 0, s>>>(a)
+              : attn_partial_kernel<4, false><<<grid, kThreads, 0, s>>>(a); break;
+    default: h ? attn_partial_kernel<8, true><<<grid, kThreads, 0, s>>>(a)
+               : attn_partial_kernel<8, false><<<grid, kThreads, 0, s>>>(a); break;
   }
   lq_status st = check_launch();
   if (st != LQ_OK) return st;
   attn_combine_kernel<<<(unsigned)q_heads, D, 0, s>>>(a, group);
   return check_launch();
+}
+
+}  // namespace
+
+extern "C" lq_status lq_attention_decode(int lattice, const int8_t* k_codes_dev, const float* k_scales_dev,
+                                         const int8_t* k_signs_dev, const int8_t* v_codes_dev,
+                                         const float* v_scales_dev, const int8_t* v_signs_dev, int64_t tokens,
+                                         int kv_heads, int q_heads, int head_dim, const void* q_dev, int qdtype,
+                                         float* out_dev, void* workspace_dev, size_t workspace_bytes,
+                                         void* stream) {
+  LQ_NVTX_RANGE("lq_attention_decode");
+  return attention_fmt(lattice, k_codes_dev, k_scales_dev, k_signs_dev, v_codes_dev, v_scales_dev, v_signs_dev,
+                       LQ_SCALE_TILE_F32, tokens, kv_heads, q_heads, head_dim, q_dev, qdtype, out_dev,
+                       workspace_dev, workspace_bytes, stream);
+}
+
+extern "C" lq_status lq_attention_decode_ex(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
+                                            const int8_t* k_signs_dev, const int8_t* v_codes_dev,
+                                            const void* v_scales_dev, const int8_t* v_signs_dev, int scale_format,
+                                            int64_t tokens, int kv_heads, int q_heads, int head_dim,
+                                            const void* q_dev, int qdtype, float* out_dev, void* workspace_dev,
+                                            size_t workspace_bytes, void* stream) {
+  LQ_NVTX_RANGE("lq_attention_decode_ex");
+  return attention_fmt(lattice, k_codes_dev, k_scales_dev, k_signs_dev, v_codes_dev, v_scales_dev, v_signs_dev,
+                       scale_format, tokens, kv_heads, q_heads, head_dim, q_dev, qdtype, out_dev, workspace_dev,
+                       workspace_bytes, stream);
 }
 
 extern "C" lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, const void* X_dev,

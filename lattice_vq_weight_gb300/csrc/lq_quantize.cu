@@ -1,4 +1,5 @@
-// Quantize (tile RHT + lattice nearest point), dequantize and sign generation.
+// Quantize entry points (tile RHT + lattice nearest point), dequantize and
+// sign generation; the quantize kernel itself is in lq_quantize_kernel.cuh.
 //
 // HyperQuant page, "Key algorithmic ingredients": per-tile randomized Hadamard
 // transform, then optimal low-dimensional lattice VQ (E8, D4, A2, Z1).
@@ -9,15 +10,9 @@
 // loads columns [64 l, 64 l + 64) of the chunk (see lq_device.cuh).  Units are
 // visited by a persistent grid of 4-warp CTAs, and each warp loads the raw
 // data of its next unit before working on the current one.
-#include <cuda_runtime.h>
-#include <cuda_bf16.h>
-
-#include "lq_device.cuh"
-#include "lq_host.h"
+#include "lq_quantize_kernel.cuh"
 
 namespace lq {
-
-constexpr int kQuantMaxMats = LQ_QUANTIZE_MAX_GROUP;
 
 struct SignsArgs {
   uint64_t seed[kQuantMaxMats];
@@ -43,411 +38,66 @@ __global__ void make_signs_kernel(SignsArgs a) {
   a.out[m][i] = (z >> 63) ? (int8_t)-1 : (int8_t)1;
 }
 
-// ------------------------------------------------------------------ loading
-// Raw storage of one lane's 64 input columns.
-template <bool BF16> struct LaneRaw;
-template <> struct LaneRaw<true> { uint4 v[8]; };    // 64 bf16
-template <> struct LaneRaw<false> { uint4 v[16]; };  // 64 fp32
+// ------------------------------------------------------------------ row scales
+// Per-row bf16 scale s_r = beta * RMS of the row (the tile Hadamards are
+// orthonormal, so the RMS of the raw row is that of the rotated one), rounded
+// to nearest-even.  One warp per row; 16-byte loads; per-lane partial sums of
+// eight squares, then the warp sum.
+struct RowScaleArgs {
+  const void* W;
+  int64_t rows, cols, ldw;
+  float beta;
+  uint16_t* out;
+  int32_t* status;
+};
+
+constexpr int kRowScaleWarps = 8;
 
 template <bool BF16>
-__device__ __forceinline__ void load_raw(LaneRaw<BF16>& r, const void* base) {
-  const uint4* p = reinterpret_cast<const uint4*>(base);
-#pragma unroll
-  for (int i = 0; i < (BF16 ? 8 : 16); ++i) r.v[i] = __ldg(p + i);
-}
-
-// Sign masks of the lane's 64 columns.  bf16: one word per column pair with
-// bits 15 and 31 set where the sign is -1.  fp32: the 64 sign bits in 2 words.
-template <bool BF16> struct LaneSigns;
-template <> struct LaneSigns<true> { uint32_t m[32]; };
-template <> struct LaneSigns<false> { uint32_t bits[2]; };
-
-template <bool BF16>
-__device__ __forceinline__ void load_signs(LaneSigns<BF16>& s, const int8_t* signs_col0) {
-  const uint4* p = reinterpret_cast<const uint4*>(signs_col0);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = __ldg(p + q);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__global__ void __launch_bounds__(kRowScaleWarps * 32) row_scale_kernel(RowScaleArgs a) {
+  // the quantize kernel launched next may stage its input meanwhile
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int64_t row = (int64_t)blockIdx.x * kRowScaleWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  constexpr int kPer = BF16 ? 8 : 4;   // elements per 16-byte vector
+  const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(a.W) +
+                                                    row * a.ldw * (BF16 ? 2 : 4));
+  const int64_t nvec = a.cols / kPer;
+  float acc = 0.f;
+  for (int64_t v = lane; v < nvec; v += 32) {
+    const uint4 q = __ldg(src + v);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    float part = 0.f;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      // word w[h] holds the signs of columns 16q + 4h .. 16q + 4h + 3
       if constexpr (BF16) {
-        s.m[8 * q + 2 * h] = __byte_perm(w[h], 0u, 0x1404) & 0x80008000u;
-        s.m[8 * q + 2 * h + 1] = __byte_perm(w[h], 0u, 0x3424) & 0x80008000u;
+        const float lo = __uint_as_float(w[h] << 16), hi = __uint_as_float(w[h] & 0xFFFF0000u);
+        part = fmaf(lo, lo, fmaf(hi, hi, part));
       } else {
-        // bit 7 of each byte -> one bit per column
-        uint32_t b = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) b |= ((w[h] >> (8 * c + 7)) & 1u) << c;
-        const int col = 16 * q + 4 * h;
-        s.bits[col >> 5] |= b << (col & 31);
+        const float x = __uint_as_float(w[h]);
+        part = fmaf(x, x, part);
       }
     }
+    acc += part;
   }
-}
-
-// bf16 pair masks of one lane kept in shared memory: uint4 q of lane l at
-// msk[q * 32 + l] holds the masks of column pairs 4q .. 4q+3 (conflict-free).
-__device__ __forceinline__ void store_sign_masks(uint4* msk, int lane, const int8_t* signs_col0) {
-  const uint4* p = reinterpret_cast<const uint4*>(signs_col0);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = __ldg(p + q);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      // sign words 2hh, 2hh+1 of this 16-byte run cover column pairs 8q + 4hh .. +3
-      const uint32_t a = w[2 * hh], b = w[2 * hh + 1];
-      msk[(2 * q + hh) * 32 + lane] = make_uint4(__byte_perm(a, 0u, 0x1404) & 0x80008000u,
-                                                 __byte_perm(a, 0u, 0x3424) & 0x80008000u,
-                                                 __byte_perm(b, 0u, 0x1404) & 0x80008000u,
-                                                 __byte_perm(b, 0u, 0x3424) & 0x80008000u);
+  for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    float sc = a.beta * sqrtf(acc / (float)a.cols);
+    if (!isfinite(sc)) {
+      sc = 0.f;
+      raise_flag(a.status, LQ_DEV_NONFINITE);
     }
+    const __nv_bfloat16 b = __float2bfloat16_rn(sc);
+    a.out[row] = *reinterpret_cast<const uint16_t*>(&b);
   }
-}
-
-__device__ __forceinline__ void unpack_bf16_smem_signs(const LaneRaw<true>& r, const uint4* msk, int lane,
-                                                       float2 (&p)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 m = msk[i * 32 + lane];
-    const uint32_t w[4] = {r.v[i].x ^ m.x, r.v[i].y ^ m.y, r.v[i].z ^ m.z, r.v[i].w ^ m.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-      p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
-  }
-}
-
-// Unpack raw input to fp32 pairs with the signs applied (exact).
-template <bool BF16>
-__device__ __forceinline__ void unpack_signed(const LaneRaw<BF16>& r, const LaneSigns<BF16>& s,
-                                              float2 (&p)[32]) {
-  if constexpr (BF16) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint32_t x = w[h] ^ s.m[4 * i + h];
-        p[4 * i + h] = make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int col = 4 * i + h;
-        const uint32_t sb = ((s.bits[col >> 5] >> (col & 31)) & 1u) << 31;
-        const float v = __uint_as_float(w[h] ^ sb);
-        if (h & 1) p[col >> 1].y = v; else p[col >> 1].x = v;
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------ staging
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// ------------------------------------------------------------------ quantize
-// One matrix of a quantize launch.  Its warp units (row, 2048-column chunk)
-// are numbered row * chunks_per_row + chunk and taken four at a time by the
-// four warps of a CTA: CTA unit k of the matrix (global CTA unit cta_begin + k)
-// holds warp units 4k .. 4k + 3, those past the matrix's end doing nothing.
-// The grid strides over CTA units, so every warp of a CTA is always in the
-// same matrix.  A warp unit's row is local / chunks_per_row, computed as the
-// high half of local * cpr_recip with cpr_recip = ceil(2^64 / chunks_per_row)
-// (exact for every local below 2^64 / chunks_per_row; 0 marks one chunk per
-// row), so the kernel divides nothing.
-struct QuantMat {
-  const void* W;
-  int8_t* codes;
-  float* scales;
-  const int8_t* signs;
-  int64_t rows, cols, ldw;
-  int64_t cta_begin;
-  uint64_t cpr_recip;
-  int tiles_per_row, chunks_per_row;
-};
-
-struct QuantArgs {
-  QuantMat mat[kQuantMaxMats];
-  int n_mats;
-  int tile, tile_shift, lanes_per_tile;
-  float beta, sqrt_tile, inv_tile;
-  int32_t* status;
-  int64_t cta_units;  // CTA units of all matrices
-};
-
-constexpr int kQuantThreads = 128;
-
-// Shared memory per warp: two stages of raw input (each lane copies its own
-// 64 columns with cp.async and later reads back only its own copies) and, for
-// bf16, the lane's sign masks.  Once a stage has been read into registers it
-// doubles as the buffer of the butterfly exchange below, so a stage holds at
-// least the exchange's 284 16-byte slots.
-template <bool BF16> struct QuantSmem {
-  static constexpr int kRawVec = BF16 ? 8 : 16;             // 16-byte vectors per lane per stage
-  static constexpr int kStageVec = BF16 ? 288 : 512;        // uint4 per warp per stage
-  static constexpr int kRawWords = 2 * kStageVec;           // uint4 per warp, both stages
-  static constexpr int kMaskWords = BF16 ? 8 * 32 : 0;      // uint4 per warp
-  static constexpr int kPerWarp = kRawWords + kMaskWords;
-};
-
-// Butterfly stages of tile bits 6 .. 6+MP-1 without shuffles.  After the six
-// register stages, lane bits 0 .. MP-1 of a lane hold tile bits 6 .. and its
-// register index bits 3 .. 3+MP-1 hold tile bits 3 ..; one pass through shared
-// memory swaps the two, so those stages run in registers as well and every
-// 8-coordinate block (tile bits 0 .. 2) stays in one lane.  The pass goes in
-// two halves (register bit 2) of 32 values per lane.  Slot of the value with
-// lane group G, spectator register bits ux, lane bits a and register bits c:
-//   (G >> (3 - MP)) * kBlk + ux * kUxSpan + (G & (X - 1)) * Q + a + 9 c,
-// additive in a and c, so every access is a per-lane base plus a constant,
-// and conflict-free for 16-byte accesses both when a varies (writes) and when
-// c varies (reads): the slots of the 8 lanes of a phase differ modulo 8.
-template <int MP> struct Xchg {
-  static constexpr int Q = 1 << MP;          // lanes whose bits are swapped
-  static constexpr int X = 8 >> MP;          // spectator register values per half
-  static constexpr int kUxSpan = 9 * Q - 1;
-  static constexpr int kBlk = X * kUxSpan;
-  static constexpr int kSlots = 4 * kBlk;
-};
-static_assert(Xchg<2>::kSlots <= 288 && Xchg<3>::kSlots <= 288, "exchange slots");
-
-template <int MP>
-__device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf, int lane) {
-  using XC = Xchg<MP>;
-  const int q = lane & (XC::Q - 1), G = lane >> MP;
-  const uint32_t g = (uint32_t)((G >> (3 - MP)) * XC::kBlk + (G & (XC::X - 1)) * XC::Q);
-  const uint32_t wb = buf + (g + (uint32_t)q) * 16u;
-  const uint32_t rb = buf + (g + 9u * (uint32_t)q) * 16u;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t off = (uint32_t)(((u >> MP) * XC::kUxSpan + 9 * (u & (XC::Q - 1))) * 16);
-      const float2 v0 = p[4 * u + 2 * h], v1 = p[4 * u + 2 * h + 1];
-      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(wb + off), "f"(v0.x), "f"(v0.y),
-                   "f"(v1.x), "f"(v1.y) : "memory");
-    }
-    __syncwarp();
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t off = (uint32_t)(((u >> MP) * XC::kUxSpan + (u & (XC::Q - 1))) * 16);
-      float2 v0, v1;
-      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v0.x), "=f"(v0.y), "=f"(v1.x), "=f"(v1.y)
-                   : "r"(rb + off) : "memory");
-      p[4 * u + 2 * h] = v0;
-      p[4 * u + 2 * h + 1] = v1;
-    }
-  }
-  __syncwarp();
-  // the swapped tile bits now sit in register index bits 3 .. 3+MP-1 (float2 bits 2 ..)
-#pragma unroll
-  for (int hp = 4; hp < (4 << MP); hp <<= 1) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if ((j & hp) == 0) {
-        const float2 x0 = p[j], x1 = p[j + hp];
-        p[j] = add2(x0, x1);
-        p[j + hp] = sub2(x0, x1);
-      }
-    }
-  }
-}
-
-// GROUPED = false: one matrix (a.mat[0]); a warp takes warp units w, w + W,
-// w + 2W, ... (W = warps of the grid), advanced without divisions.
-// GROUPED = true: the CTA-unit walk over several matrices described above.
-// Both walks feed the same per-unit body; they are separate instantiations
-// because the single-matrix walk keeps fewer values live across the decode.
-template <int LAT, bool BF16, int MP, bool GROUPED>
-__global__ void __launch_bounds__(kQuantThreads, 4) quantize_kernel(QuantArgs a) {
-  using SM = QuantSmem<BF16>;
-  extern __shared__ uint4 quant_smem[];
-  const int lane = threadIdx.x & 31;
-  uint4* wsm = quant_smem + (threadIdx.x >> 5) * SM::kPerWarp;
-  uint4* raw_sm = wsm;                          // [stage][vec][lane]
-  uint4* msk = wsm + SM::kRawWords;             // bf16 sign masks [q][lane]
-  const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(raw_sm);
-  constexpr int kElemBytes = BF16 ? 2 : 4;
-
-  LaneSigns<false> sg;     // fp32 input keeps its 64 sign bits in registers
-  int cached_chunk = -1, cached_m = -1;
-  bool range = false, nonfinite = false;
-
-  // copy the lane's 64 input columns of unit (row, chunk) of M into stage st
-  auto stage_in = [&](bool valid, const QuantMat& M, int64_t row, int chunk, int st) {
-    const int64_t c = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    if (valid && row < M.rows && c < M.cols) {
-      const char* src = reinterpret_cast<const char*>(M.W) + (row * M.ldw + c) * kElemBytes;
-#pragma unroll
-      for (int i = 0; i < SM::kRawVec; ++i)
-        cp_async16(raw_s + (uint32_t)((st * SM::kStageVec + i * 32 + lane) * 16), src + 16 * i);
-    }
-    cp_async_commit();
-  };
-
-  // quantize unit (row, chunk) of matrix m, whose input is in stage st
-  auto process = [&](const QuantMat& M, int m, int64_t row, int chunk, int st) {
-    const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    const bool active = col0 < M.cols;
-    if (chunk != cached_chunk || m != cached_m) {
-      if constexpr (BF16) {
-        if (active) store_sign_masks(msk, lane, M.signs + col0);
-      } else {
-        sg.bits[0] = 0;
-        sg.bits[1] = 0;
-        if (active) load_signs<false>(sg, M.signs + col0);
-      }
-      cached_chunk = chunk;
-      cached_m = m;
-    }
-    cp_async_wait1();   // this unit's copies have landed
-
-    float2 p[32];
-    {
-      LaneRaw<BF16> raw;
-#pragma unroll
-      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[st * SM::kStageVec + i * 32 + lane];
-      if constexpr (BF16) unpack_bf16_smem_signs(raw, msk, lane, p);
-      else unpack_signed<false>(raw, sg, p);
-    }
-    fwht64_local(p);
-    if constexpr (MP > 0) exchange_tile_bits<MP>(p, raw_s + (uint32_t)(st * SM::kStageVec * 16), lane);
-    // lane bits not exchanged (MP = 0: all of them; tiles of 1024 and 2048
-    // columns: tile bits 9 .. on lane bits 3 ..) cross lanes with shuffles
-    for (int mm = (MP == 0 ? 1 : 8); mm < a.lanes_per_tile; mm <<= 1) {
-      const float sgn = (lane & mm) ? -1.0f : 1.0f;
-      const float2 sg2 = make_float2(sgn, sgn);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float2 o;
-        o.x = __shfl_xor_sync(0xffffffffu, p[j].x, mm);
-        o.y = __shfl_xor_sync(0xffffffffu, p[j].y, mm);
-        p[j] = fma2(p[j], sg2, o);
-      }
-    }
-
-    // U = sum u^2 over the tile; s = beta sqrt(U) / T; y = u / (s sqrt(T))
-    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc = fma2(p[j], p[j], acc);
-    const float U = tile_lane_sum(acc.x + acc.y, a.lanes_per_tile);
-    const bool finite = isfinite(U);
-    float s = a.beta * sqrtf(U) * a.inv_tile;
-    if (!finite) s = 0.f;
-    const float k = (s > 0.f) ? 1.0f / (s * a.sqrt_tile) : 0.f;
-    const float2 k2 = make_float2(k, k);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) p[j] = mul2(p[j], k2);
-
-    // every |y| of the lane below 62.5 keeps every code inside int8, and the
-    // per-block range check is left out; the lane's sum of y^2 decides that
-    // for free in most cases, the lane maximum otherwise
-    const float lane_y2 = (acc.x + acc.y) * (k * k);
-    bool small = lane_y2 < 3906.25f;
-    if (!small) {
-      float mx = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
-      small = mx < 62.5f;
-    }
-    uint32_t w[16];
-    bool r = false;
-    if (small) decode_lane<LAT, false>(p, w, r);
-    else decode_lane<LAT, true>(p, w, r);
-
-    if (active) {
-      range |= r;
-      nonfinite |= !finite;
-      // register block u holds tile columns 8 q + 8 Q ux + 64 a (q = lane bits,
-      // ux = u >> MP, a = u & (Q - 1)) of the tile group G = lane >> MP
-      constexpr int Q = 1 << MP;
-      int8_t* dst = M.codes + row * M.cols + (int64_t)chunk * kChunkCols + (lane >> MP) * (64 * Q) +
-                    8 * (lane & (Q - 1));
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint2*>(dst + (u >> MP) * (8 * Q) + 64 * (u & (Q - 1))) = make_uint2(w[2 * u], w[2 * u + 1]);
-      if ((lane & (a.lanes_per_tile - 1)) == 0)
-        M.scales[row * M.tiles_per_row + (col0 >> a.tile_shift)] = s;
-    }
-  };
-
-  int stage = 0;
-  if constexpr (!GROUPED) {
-    const QuantMat& M = a.mat[0];
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    // unit u = row * chunks_per_row + chunk grows by nwarps per step
-    const int64_t d_row = nwarps / M.chunks_per_row;
-    const int d_chunk = (int)(nwarps % M.chunks_per_row);
-    int64_t row = warp0 / M.chunks_per_row;
-    int chunk = (int)(warp0 % M.chunks_per_row);
-    stage_in(true, M, row, chunk, 0);
-    // the signs come from the kernel launched just before this one
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    while (row < M.rows) {
-      int64_t nrow = row + d_row;
-      int nchunk = chunk + d_chunk;
-      if (nchunk >= M.chunks_per_row) { nchunk -= M.chunks_per_row; ++nrow; }
-      stage_in(true, M, nrow, nchunk, stage ^ 1);
-      process(M, 0, row, chunk, stage);
-      row = nrow;
-      chunk = nchunk;
-      stage ^= 1;
-    }
-  } else {
-    // (matrix, row, chunk) of a CTA unit's warp unit for this warp
-    struct Pos {
-      int m, chunk;
-      int64_t row;
-    };
-    const int wic = threadIdx.x >> 5;   // warp in the CTA
-    auto locate = [&](int64_t cu, Pos& p) {
-      while (p.m + 1 < a.n_mats && cu >= a.mat[p.m + 1].cta_begin) ++p.m;
-      const QuantMat& M = a.mat[p.m];
-      const uint64_t local = (uint64_t)(cu - M.cta_begin) * (kQuantThreads / 32) + (uint64_t)wic;
-      const uint64_t r = M.cpr_recip ? __umul64hi(local, M.cpr_recip) : local;
-      p.row = (int64_t)r;
-      p.chunk = (int)(local - r * (uint64_t)M.chunks_per_row);
-    };
-    int64_t cu = blockIdx.x;
-    Pos cur;
-    cur.m = 0;
-    cur.row = 0;
-    cur.chunk = 0;
-    if (cu < a.cta_units) locate(cu, cur);
-    stage_in(cu < a.cta_units, a.mat[cur.m], cur.row, cur.chunk, 0);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (; cu < a.cta_units; cu += gridDim.x) {
-      const int64_t cn = cu + gridDim.x;
-      Pos nxt = cur;
-      if (cn < a.cta_units) locate(cn, nxt);
-      stage_in(cn < a.cta_units, a.mat[nxt.m], nxt.row, nxt.chunk, stage ^ 1);
-      const QuantMat& M = a.mat[cur.m];
-      if (cur.row < M.rows) process(M, cur.m, cur.row, cur.chunk, stage);   // else past the matrix's end
-      cur = nxt;
-      stage ^= 1;
-    }
-  }
-  cp_async_wait0();
-  if (__any_sync(0xffffffffu, range) && lane == 0) raise_flag(a.status, LQ_DEV_RANGE);
-  if (__any_sync(0xffffffffu, nonfinite) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
 }
 
 // ------------------------------------------------------------------ dequantize
 struct DequantArgs {
   const int8_t* codes;
-  const float* scales;
+  const void* scales;     // in format sfmt (LQ_SCALE_*)
+  int sfmt;
   const int8_t* signs;
   int64_t rows, cols;
   int tile, lanes_per_tile, tiles_per_row, chunks_per_row;
@@ -494,7 +144,7 @@ __global__ void __launch_bounds__(256, 1) dequantize_kernel(DequantArgs a) {
     fwht64_local(p);
     fwht_cross_lanes(p, a.lanes_per_tile, lane);
     if (!active) continue;
-    const float f = a.scales[row * a.tiles_per_row + col0 / a.tile] * a.inv_2sqrt_tile;
+    const float f = load_scale(a.scales, a.sfmt, row, col0 / a.tile, a.tiles_per_row) * a.inv_2sqrt_tile;
     const float2 f2 = make_float2(f, f);
     float2 o[32];
 #pragma unroll
@@ -550,14 +200,6 @@ lq_status launch_signs(const SignsArgs& a, int n_mats, int64_t max_cols, cudaStr
   return check_launch();
 }
 
-int64_t gcd64(int64_t x, int64_t y) {
-  while (y) {
-    const int64_t t = x % y;
-    x = y;
-    y = t;
-  }
-  return x;
-}
 
 }  // namespace
 
@@ -573,69 +215,27 @@ extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_de
   return launch_signs(a, 1, cols, (cudaStream_t)stream);
 }
 
-template <int LAT, bool BF16, int MP, bool GROUPED>
-static lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
-  constexpr size_t smem = (size_t)(kQuantThreads / 32) * QuantSmem<BF16>::kPerWarp * sizeof(uint4);
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP, GROUPED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess) {
-      cudaGetLastError();
-      return LQ_ERR_CUDA;
-    }
-    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP, GROUPED>, kQuantThreads, smem);
-  }
-  // a warp count that is a multiple of every matrix's chunks per row keeps
-  // each warp on one chunk (one set of signs) within a matrix
-  int64_t modulus = 1;
-  for (int m = 0; m < a.n_mats; ++m) {
-    const int64_t c = a.mat[m].chunks_per_row;
-    modulus = modulus / gcd64(modulus, c) * c;
-    if (modulus > 64) { modulus = 1; break; }
-  }
-  const int grid = persistent_grid(a.cta_units * (kQuantThreads / 32), kQuantThreads / 32, (int)modulus, per_sm);
-  if (grid <= 0) return LQ_ERR_CUDA;
-  // programmatic dependent launch after the signs kernel
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kQuantThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP, GROUPED>, a) != cudaSuccess) {
-    cudaGetLastError();
-    return LQ_ERR_CUDA;
-  }
-  return LQ_OK;
-}
-
-// MP = tile bits exchanged through shared memory: log2(tile / 64), at most 3.
-// A 128-column tile has a single cross-lane stage, cheaper as a shuffle (MP = 0).
 template <int LAT, bool BF16>
-static lq_status launch_quantize(QuantArgs& a, cudaStream_t st) {
-  if (a.n_mats == 1) {
-    if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, false>(a, st);
-    if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, false>(a, st);
-    return launch_quantize_mp<LAT, BF16, 3, false>(a, st);
-  }
-  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, true>(a, st);
-  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, true>(a, st);
-  return launch_quantize_mp<LAT, BF16, 3, true>(a, st);
+static lq_status launch_quantize(QuantArgs& a, int sf, cudaStream_t st) {
+  if (a.n_mats > 1) return launch_quantize_walk<LAT, BF16, true, LQ_SCALE_TILE_F32>(a, st);
+  if (sf != LQ_SCALE_TILE_F32) return launch_quantize_scaled16(a, LAT, BF16, sf, st);
+  return launch_quantize_walk<LAT, BF16, false, LQ_SCALE_TILE_F32>(a, st);
 }
 
 namespace {
 
+bool valid_scale_format(int f) {
+  return f == LQ_SCALE_TILE_F32 || f == LQ_SCALE_ROW_BF16 || f == LQ_SCALE_TILE_F16;
+}
+
 // Checks of one matrix's arguments, in the order lq_quantize reports them.
 lq_status validate_quantize(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols, int64_t ldw,
-                            int tile, float beta, const int8_t* codes_dev, const float* scales_dev,
-                            const int8_t* signs_dev, const int32_t* dev_status_dev) {
+                            int tile, float beta, const int8_t* codes_dev, const void* scales_dev,
+                            const int8_t* signs_dev, const int32_t* dev_status_dev, int sf = LQ_SCALE_TILE_F32) {
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (wdtype != LQ_BF16 && wdtype != LQ_F32) return LQ_ERR_DTYPE;
+  if (!valid_scale_format(sf)) return LQ_ERR_ARG;
   if (!(beta > 0.f) || !(beta < 1e30f)) return LQ_ERR_ARG;
   if (ldw < cols) return LQ_ERR_SHAPE;
   const int esize = (wdtype == LQ_BF16) ? 2 : 4;
@@ -643,17 +243,20 @@ lq_status validate_quantize(int lattice, const void* W_dev, int wdtype, int64_t 
   if (signs_dev == nullptr || !aligned16(signs_dev)) return LQ_ERR_ARG;
   if (rows > 0) {
     if (W_dev == nullptr || codes_dev == nullptr || scales_dev == nullptr) return LQ_ERR_ARG;
-    if (!aligned16(W_dev) || !aligned16(codes_dev) || !aligned4(scales_dev) ||
+    const uintptr_t salign = (sf == LQ_SCALE_TILE_F32) ? 3u : 1u;
+    if (!aligned16(W_dev) || !aligned16(codes_dev) || (reinterpret_cast<uintptr_t>(scales_dev) & salign) != 0 ||
         (dev_status_dev != nullptr && !aligned4(dev_status_dev)))
       return LQ_ERR_ARG;
   }
   return LQ_OK;
 }
 
+// The quantize launch over n matrices (rows 0: skipped), after the signs
+// launch when make_signs_too is set.
 lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, const int64_t* rows,
                          const int64_t* cols, const int64_t* ldw, int tile, const uint64_t* seeds, float beta,
-                         int8_t* const* codes, float* const* scales, int8_t* const* signs, int32_t* dev_status,
-                         cudaStream_t s) {
+                         int8_t* const* codes, void* const* scales, int8_t* const* signs, int32_t* dev_status,
+                         int sf, bool make_signs_too, cudaStream_t s) {
   SignsArgs sa = {};
   QuantArgs a = {};
   int64_t max_cols = 0, units = 0;
@@ -665,7 +268,7 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
     if (cols[m] > max_cols) max_cols = cols[m];
     if (rows[m] == 0) continue;   // signs only
     QuantMat& M = a.mat[k++];
-    M.W = W[m]; M.codes = codes[m]; M.scales = scales[m]; M.signs = signs[m];
+    M.W = W[m]; M.codes = codes[m]; M.scales = reinterpret_cast<float*>(scales[m]); M.signs = signs[m];
     M.rows = rows[m]; M.cols = cols[m]; M.ldw = ldw[m];
     M.tiles_per_row = (int)(cols[m] / tile);
     M.chunks_per_row = (int)((cols[m] + kChunkCols - 1) / kChunkCols);
@@ -674,8 +277,11 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
     units += (rows[m] * M.chunks_per_row + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
   }
   if (units >= ((int64_t)1 << 40)) return LQ_ERR_SHAPE;
-  lq_status st = launch_signs(sa, n, max_cols, s);
-  if (st != LQ_OK || k == 0) return st;
+  if (make_signs_too) {
+    const lq_status st = launch_signs(sa, n, max_cols, s);
+    if (st != LQ_OK) return st;
+  }
+  if (k == 0) return LQ_OK;
   a.n_mats = k;
   a.tile = tile; a.tile_shift = __builtin_ctz((unsigned)tile);
   a.lanes_per_tile = tile / kLaneElems;
@@ -684,12 +290,17 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
   a.cta_units = units;
   const bool bf = (wdtype == LQ_BF16);
   switch (lattice) {
-    case LQ_E8: return bf ? launch_quantize<LQ_E8, true>(a, s) : launch_quantize<LQ_E8, false>(a, s);
-    case LQ_D4: return bf ? launch_quantize<LQ_D4, true>(a, s) : launch_quantize<LQ_D4, false>(a, s);
-    case LQ_A2: return bf ? launch_quantize<LQ_A2, true>(a, s) : launch_quantize<LQ_A2, false>(a, s);
-    default:    return bf ? launch_quantize<LQ_Z1, true>(a, s) : launch_quantize<LQ_Z1, false>(a, s);
+    case LQ_E8: return bf ? launch_quantize<LQ_E8, true>(a, sf, s) : launch_quantize<LQ_E8, false>(a, sf, s);
+    case LQ_D4: return bf ? launch_quantize<LQ_D4, true>(a, sf, s) : launch_quantize<LQ_D4, false>(a, sf, s);
+    case LQ_A2: return bf ? launch_quantize<LQ_A2, true>(a, sf, s) : launch_quantize<LQ_A2, false>(a, sf, s);
+    default:    return bf ? launch_quantize<LQ_Z1, true>(a, sf, s) : launch_quantize<LQ_Z1, false>(a, sf, s);
   }
 }
+
+// Rows per block of the per-row-scale quantize: the row-norm pass reads a
+// block and the quantize pass reads it again, from L2 while the block stays
+// well below its 129 MB.
+constexpr int64_t kRowScaleBlockBytes = (int64_t)40 << 20;
 
 }  // namespace
 
@@ -701,8 +312,48 @@ extern "C" lq_status lq_quantize(int lattice, const void* W_dev, int wdtype, int
   const lq_status st = validate_quantize(lattice, W_dev, wdtype, rows, cols, ldw, tile, beta, codes_dev,
                                          scales_dev, signs_dev, dev_status_dev);
   if (st != LQ_OK) return st;
-  return quantize_group(lattice, 1, &W_dev, wdtype, &rows, &cols, &ldw, tile, &seed, beta, &codes_dev,
-                        &scales_dev, &signs_dev, dev_status_dev, (cudaStream_t)stream);
+  void* sc = scales_dev;
+  return quantize_group(lattice, 1, &W_dev, wdtype, &rows, &cols, &ldw, tile, &seed, beta, &codes_dev, &sc,
+                        &signs_dev, dev_status_dev, LQ_SCALE_TILE_F32, true, (cudaStream_t)stream);
+}
+
+extern "C" lq_status lq_quantize_ex(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
+                                    int64_t ldw, int tile, uint64_t seed, float beta, int scale_format,
+                                    int8_t* codes_dev, void* scales_dev, int8_t* signs_dev,
+                                    int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_quantize_ex");
+  lq_status st = validate_quantize(lattice, W_dev, wdtype, rows, cols, ldw, tile, beta, codes_dev, scales_dev,
+                                   signs_dev, dev_status_dev, scale_format);
+  if (st != LQ_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (scale_format != LQ_SCALE_ROW_BF16 || rows == 0)
+    return quantize_group(lattice, 1, &W_dev, wdtype, &rows, &cols, &ldw, tile, &seed, beta, &codes_dev,
+                          &scales_dev, &signs_dev, dev_status_dev, scale_format, true, s);
+  st = lq_make_signs(seed, cols, signs_dev, stream);
+  if (st != LQ_OK) return st;
+  const int esize = (wdtype == LQ_BF16) ? 2 : 4;
+  int64_t block = kRowScaleBlockBytes / (ldw * esize);
+  if (block < 1) block = 1;
+  for (int64_t r0 = 0; r0 < rows; r0 += block) {
+    const int64_t nr = (rows - r0 < block) ? rows - r0 : block;
+    RowScaleArgs ra;
+    ra.W = reinterpret_cast<const char*>(W_dev) + r0 * ldw * esize;
+    ra.rows = nr; ra.cols = cols; ra.ldw = ldw; ra.beta = beta;
+    ra.out = reinterpret_cast<uint16_t*>(scales_dev) + r0;
+    ra.status = dev_status_dev;
+    const unsigned grid = (unsigned)((nr + kRowScaleWarps - 1) / kRowScaleWarps);
+    if (wdtype == LQ_BF16) row_scale_kernel<true><<<grid, kRowScaleWarps * 32, 0, s>>>(ra);
+    else row_scale_kernel<false><<<grid, kRowScaleWarps * 32, 0, s>>>(ra);
+    st = check_launch();
+    if (st != LQ_OK) return st;
+    const void* Wb = ra.W;
+    int8_t* cb = codes_dev + r0 * cols;
+    void* sb = ra.out;
+    st = quantize_group(lattice, 1, &Wb, wdtype, &nr, &cols, &ldw, tile, &seed, beta, &cb, &sb, &signs_dev,
+                        dev_status_dev, LQ_SCALE_ROW_BF16, false, s);
+    if (st != LQ_OK) return st;
+  }
+  return LQ_OK;
 }
 
 extern "C" lq_status lq_quantize_grouped(int lattice, int n, const void* const* W_dev, int wdtype,
@@ -720,8 +371,10 @@ extern "C" lq_status lq_quantize_grouped(int lattice, int n, const void* const* 
                                            codes_dev[m], scales_dev[m], signs_dev[m], dev_status_dev);
     if (st != LQ_OK) return st;
   }
-  return quantize_group(lattice, n, W_dev, wdtype, rows, cols, ldw, tile, seeds, beta, codes_dev, scales_dev,
-                        signs_dev, dev_status_dev, (cudaStream_t)stream);
+  void* sc[kQuantMaxMats];
+  for (int m = 0; m < n; ++m) sc[m] = scales_dev[m];
+  return quantize_group(lattice, n, W_dev, wdtype, rows, cols, ldw, tile, seeds, beta, codes_dev, sc, signs_dev,
+                        dev_status_dev, LQ_SCALE_TILE_F32, true, (cudaStream_t)stream);
 }
 
 template <int LAT, bool OB>
@@ -734,31 +387,52 @@ static lq_status launch_dequant(const DequantArgs& a, cudaStream_t st) {
   return check_launch();
 }
 
-extern "C" lq_status lq_dequantize(int lattice, const int8_t* codes_dev, const float* scales_dev,
-                                   const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
-                                   void* What_dev, int out_dtype, void* stream) {
-  LQ_NVTX_RANGE("lq_dequantize");
+namespace {
+
+lq_status dequantize_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev, int sfmt,
+                         const int8_t* signs_dev, int64_t rows, int64_t cols, int tile, void* What_dev,
+                         int out_dtype, cudaStream_t s) {
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (out_dtype != LQ_BF16 && out_dtype != LQ_F32) return LQ_ERR_DTYPE;
+  if (!valid_scale_format(sfmt)) return LQ_ERR_ARG;
   if (rows == 0) return LQ_OK;
   if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || What_dev == nullptr)
     return LQ_ERR_ARG;
-  if (!aligned16(codes_dev) || !aligned16(signs_dev) || !aligned16(What_dev) || !aligned4(scales_dev))
+  const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
+  if (!aligned16(codes_dev) || !aligned16(signs_dev) || !aligned16(What_dev) ||
+      (reinterpret_cast<uintptr_t>(scales_dev) & salign) != 0)
     return LQ_ERR_ARG;
   DequantArgs a;
-  a.codes = codes_dev; a.scales = scales_dev; a.signs = signs_dev; a.rows = rows; a.cols = cols;
+  a.codes = codes_dev; a.scales = scales_dev; a.sfmt = sfmt; a.signs = signs_dev; a.rows = rows; a.cols = cols;
   a.tile = tile; a.lanes_per_tile = tile / kLaneElems; a.tiles_per_row = (int)(cols / tile);
   a.chunks_per_row = (int)((cols + kChunkCols - 1) / kChunkCols);
   a.inv_2sqrt_tile = (float)(0.5 / sqrt((double)tile));
   a.out = What_dev;
   a.units = rows * a.chunks_per_row;
   const bool ob = (out_dtype == LQ_BF16);
-  cudaStream_t s = (cudaStream_t)stream;
   switch (lattice) {
     case LQ_E8: return ob ? launch_dequant<LQ_E8, true>(a, s) : launch_dequant<LQ_E8, false>(a, s);
     case LQ_D4: return ob ? launch_dequant<LQ_D4, true>(a, s) : launch_dequant<LQ_D4, false>(a, s);
     case LQ_A2: return ob ? launch_dequant<LQ_A2, true>(a, s) : launch_dequant<LQ_A2, false>(a, s);
     default:    return ob ? launch_dequant<LQ_Z1, true>(a, s) : launch_dequant<LQ_Z1, false>(a, s);
   }
+}
+
+}  // namespace
+
+extern "C" lq_status lq_dequantize(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                                   const int8_t* signs_dev, int64_t rows, int64_t cols, int tile,
+                                   void* What_dev, int out_dtype, void* stream) {
+  LQ_NVTX_RANGE("lq_dequantize");
+  return dequantize_fmt(lattice, codes_dev, scales_dev, LQ_SCALE_TILE_F32, signs_dev, rows, cols, tile, What_dev,
+                        out_dtype, (cudaStream_t)stream);
+}
+
+extern "C" lq_status lq_dequantize_ex(int lattice, const int8_t* codes_dev, const void* scales_dev,
+                                      int scale_format, const int8_t* signs_dev, int64_t rows, int64_t cols,
+                                      int tile, void* What_dev, int out_dtype, void* stream) {
+  LQ_NVTX_RANGE("lq_dequantize_ex");
+  return dequantize_fmt(lattice, codes_dev, scales_dev, scale_format, signs_dev, rows, cols, tile, What_dev,
+                        out_dtype, (cudaStream_t)stream);
 }

@@ -108,6 +108,20 @@ def test_argument_errors_are_synchronous():
     assert qg(2, r9, c9, c9, Ws=bad) == L.LQ_ERR_ARG                                    # W alignment
     assert lib.lq_quantize_grouped(8, 2, nul, 1, I64(*r9), I64(*c9), I64(*c9), 256, ones, 0.25, arr, arr, arr,
                                    nul, s) == L.LQ_ERR_ARG
+    # scale formats: unknown format -> LQ_ERR_ARG; 16-bit scales need 2-byte, float32 4-byte alignment
+    two = P(0x10002)
+    qx = lambda fmt, scales: lib.lq_quantize_ex(8, good, 1, 4, 256, 256, 256, 0, 0.25, fmt, good, scales, good,
+                                                nul, s)
+    assert qx(3, good) == L.LQ_ERR_ARG and qx(-1, good) == L.LQ_ERR_ARG
+    assert qx(L.LQ_SCALE_TILE_F32, two) == L.LQ_ERR_ARG
+    assert lib.lq_dequantize_ex(8, good, good, 9, good, 4, 256, 256, good, 0, s) == L.LQ_ERR_ARG
+    assert lib.lq_dequantize_ex(8, good, P(0x10001), L.LQ_SCALE_TILE_F16, good, 4, 256, 256, good, 0,
+                                s) == L.LQ_ERR_ARG
+    assert lib.lq_gemv_ex(8, good, good, 5, good, 4, 256, 256, good, 1, 1, good, good, nul, s) == L.LQ_ERR_ARG
+    assert lib.lq_gemm_ex(8, good, good, 7, good, 128, 256, 256, good, 4, good, good, nul, s) == L.LQ_ERR_ARG
+    # the KV attention takes float32 or fp16 tile scales only
+    assert lib.lq_attention_decode_ex(8, good, good, good, good, good, good, L.LQ_SCALE_ROW_BF16, 16, 1, 1, 128,
+                                      good, 1, good, good, ctypes.c_size_t(1 << 20), s) == L.LQ_ERR_ARG
     # Rice format: worst case 8 bits per symbol + parity bits + 3 bits per segment, 16 bytes of padding
     assert L.lq_rice_stream_bound("e8", 2, 256, 256) == ((2 * 3 + 2 * 256 * 8 + 2 * 32 + 31) // 32) * 4 + 16
     assert L.lq_rice_stream_bound("e8", 1 << 15, 1 << 14, 256) == 0          # more than 2^28 weights
