@@ -558,6 +558,9 @@ def gpu_arm(args, ws, rank, local):
     # ---- Rice format of the same codes: encode, and the GEMV from the stream
     rice = rice_part(L, torch, dev, stream, shapes, codes, scales, signs, dev_x, reps=max(3, min(args.steps, 10)))
 
+    # ---- per-row bf16 scale format (the int8 layout): quantize and GEMV of the same layer
+    rowfmt = rowscale_part(L, torch, dev, stream, shapes, dev_w, dev_x, reps=max(3, min(args.steps, 10)))
+
     # ---- prefill GEMM (Llama-3-70B MLP shapes), when the library provides it
     gemm = None
     if not args.no_gemm:
@@ -596,6 +599,7 @@ def gpu_arm(args, ws, rank, local):
         "clocks": clk,
     }
     line["parts"].update(rice)
+    line["parts"].update(rowfmt)
     if gemm is not None:
         line["parts"].update(gemm)
 
@@ -868,13 +872,15 @@ def kv_arm(args, ws, rank, local):
     layers, kvh, qh, d = 32, 8, 32, 128
     results = {}
     reps = max(3, min(args.steps, 10))
-    for tokens in (4096, 32768, 131072):
+    # float32 norms at every context; fp16 norms (the pages' cache layout) at 32 K
+    for tokens, fmt in ((4096, "tile_f32"), (32768, "tile_f32"), (32768, "tile_f16"), (131072, "tile_f32")):
         caches = []
         for layer in range(layers):
             pair = []
             for which in range(2):
                 X = torch_gaussian_matrix(tokens, kvh * d, 1.0, 7000 + 2 * layer + which, device=dev)
-                pair.append(L.quantize(X, lattice="e8", tile=d, seed=7100 + 2 * layer + which, beta=BETA))
+                pair.append(L.quantize_ex(X, lattice="e8", tile=d, seed=7100 + 2 * layer + which, beta=BETA,
+                                          scale_format=fmt))
                 del X
             caches.append(pair)
         q = [torch.randn((qh, d), device=dev, generator=torch.Generator(device=dev).manual_seed(7200 + i)
@@ -884,7 +890,7 @@ def kv_arm(args, ws, rank, local):
 
         def step():
             for i, ((kc, ks, kd), (vc, vs, vd)) in enumerate(caches):
-                L.lq_attention_decode("e8", kc, ks, kd, vc, vs, vd, q[i], out[i], wsz)
+                L.lq_attention_decode_ex("e8", kc, ks, kd, vc, vs, vd, fmt, q[i], out[i], wsz)
 
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
@@ -896,10 +902,11 @@ def kv_arm(args, ws, rank, local):
         g.replay()
         torch.cuda.synchronize(dev)
         ms = _graph_ms(torch, g, stream, reps)
-        cache_bytes = layers * 2 * tokens * kvh * (d + 4)
-        results[f"ctx{tokens}"] = {"ms_per_step": round(ms, 4), "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
-                                   "cache_bytes": cache_bytes,
-                                   "compression_vs_bf16": round(2.0 * d / (d + 4), 3)}
+        sbytes = 2 if fmt == "tile_f16" else 4
+        cache_bytes = layers * 2 * tokens * kvh * (d + sbytes)
+        key = f"ctx{tokens}" + ("_fp16_norms" if fmt == "tile_f16" else "")
+        results[key] = {"ms_per_step": round(ms, 4), "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
+                        "cache_bytes": cache_bytes, "compression_vs_bf16": round(2.0 * d / (d + sbytes), 3)}
         del caches, q, out, wsz, g
         torch.cuda.empty_cache()
     peak, src = hbm_peak("burst")
@@ -911,7 +918,7 @@ def kv_arm(args, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": "llama3-8b decode attention over an E8-quantized KV cache (32 layers, 8 kv heads, "
                                "32 q heads, head_dim 128), one graph of 96 launches per step",
-                   "value_is": "cache GB/s at 32 768 tokens", "beta": BETA, "tile": 128},
+                   "value_is": "cache GB/s at 32 768 tokens (float32 norms)", "beta": BETA, "tile": 128},
         "gpu_launches": layers * 3 * reps,
         "contexts": results,
         "roofline": {"kernel": "attn_partial_kernel + attn_combine_kernel", "bound": "hbm", "achieved": best,
@@ -988,6 +995,51 @@ def rice_part(L, torch, dev, stream, shapes, codes, scales, signs, dev_x, reps):
     torch.cuda.synchronize(dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the Rice part")
+    return out
+
+
+def rowscale_part(L, torch, dev, stream, shapes, dev_w, dev_x, reps):
+    """The layer with one bf16 scale per row (lq_quantize_ex / lq_gemv_ex): quantize
+    GB/s (W in, codes + row scales out; W is read twice, the second time in L2-sized
+    row blocks) and GEMV GB/s per batch (codes, row scales, signs, x in; y out)."""
+    fmt = "row_bf16"
+    codes = [torch.empty((r, c), dtype=torch.int8, device=dev) for _, r, c, _ in shapes]
+    scales = [L.scales_tensor(r, c, TILE, fmt, dev) for _, r, c, _ in shapes]
+    signs = [torch.empty((c,), dtype=torch.int8, device=dev) for _, _, c, _ in shapes]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ys = {(b, i): torch.empty((b, r), dtype=torch.float32, device=dev)
+          for b in BATCHES for i, (_, r, _, _) in enumerate(shapes)}
+    work = torch.empty(max(L.lq_gemv_workspace_size(b, c, TILE) for b in BATCHES for _, _, c, _ in shapes),
+                       dtype=torch.uint8, device=dev)
+
+    def quant_all():
+        for i, (n, r, c, seed) in enumerate(shapes):
+            L.lq_quantize_ex(LATTICE, dev_w[i], TILE, seed, BETA, fmt, codes[i], scales[i], signs[i], status)
+
+    def gemv_all(b):
+        for i, (n, r, c, seed) in enumerate(shapes):
+            L.lq_gemv_ex(LATTICE, codes[i], scales[i], fmt, signs[i], TILE, dev_x[(b, c)], ys[(b, i)], work, status)
+
+    def graph_of(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        return g
+
+    out = {}
+    ms = _graph_ms(torch, graph_of(quant_all), stream, reps)
+    qbytes = sum(r * c * 3 + 2 * r + c for _, r, c, _ in shapes)
+    out["rowbf16_quantize_gbs"] = round(qbytes / (ms * 1e-3) / 1e9, 1)
+    for b in BATCHES:
+        ms = _graph_ms(torch, graph_of(lambda b=b: gemv_all(b)), stream, reps)
+        nbytes = sum(r * c + 2 * r + c + b * c * 2 + b * r * 4 for _, r, c, _ in shapes)
+        out[f"rowbf16_gemv_b{b}_gbs"] = round(nbytes / (ms * 1e-3) / 1e9, 1)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the row-scale part")
     return out
 
 
