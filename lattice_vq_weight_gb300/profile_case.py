@@ -1,6 +1,7 @@
 """Small, fixed launch sequences of the liblq kernels for profiler captures.
 
     python -m lattice_vq_weight_gb300.profile_case quantize   # the 7 Llama-3-8B layer matrices
+    python -m lattice_vq_weight_gb300.profile_case quantize --grouped   # the same in one grouped call
     python -m lattice_vq_weight_gb300.profile_case gemv --batch 1
     python -m lattice_vq_weight_gb300.profile_case gemv --batch 1 --gate-up   # one grouped call
     python -m lattice_vq_weight_gb300.profile_case gemm --M 256
@@ -11,6 +12,7 @@ the second pass is the one to capture (`ncu -s <launches of one pass>`).
 Inputs: bf16 N(0, 0.02^2) weights of the Llama-3-8B layer shapes (gate-shaped
 only with --gate-only), E8, tile 256, beta 0.25; activations N(0, 1) bf16;
 GEMM on the 8192 x 28672 Llama-3-70B up-like shape with X of M rows.  With
+--grouped the quantize is one lq_quantize_grouped call over the matrices.  With
 --gate-up the GEMV is one grouped call over the gate and up matrices (as in
 the benchmark's layer step).  kv: one layer of a Llama-3-8B KV cache (8 kv
 heads, 32 query heads, head_dim 128, N(0, 1) K and V, E8, beta 0.25) and the
@@ -36,6 +38,7 @@ def main(argv=None):
     ap.add_argument("--reps", type=int, default=2)
     ap.add_argument("--gate-only", action="store_true")
     ap.add_argument("--gate-up", action="store_true")
+    ap.add_argument("--grouped", action="store_true")
     args = ap.parse_args(argv)
 
     import torch
@@ -90,6 +93,10 @@ def main(argv=None):
         ws = torch.empty(L.lq_gemv_grouped_workspace_size(2, args.batch, 4096, 256), dtype=torch.uint8,
                          device=dev)
     for _ in range(args.reps):
+        if args.op == "quantize" and args.grouped:
+            L.lq_quantize_grouped("e8", [m[0] for m in mats], 256, [1] * len(mats), 0.25, [m[1] for m in mats],
+                                  [m[2] for m in mats], [m[3] for m in mats])
+            continue
         if args.op == "gemv" and args.gate_up:
             L.lq_gemv_grouped("e8", [m[1] for m in mats], [m[2] for m in mats], [m[3] for m in mats], 256,
                               mats[0][4], [m[5] for m in mats], ws)
