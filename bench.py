@@ -873,14 +873,21 @@ def kv_arm(args, ws, rank, local):
     results = {}
     reps = max(3, min(args.steps, 10))
     # float32 norms at every context; fp16 norms (the pages' cache layout) at 32 K
-    for tokens, fmt in ((4096, "tile_f32"), (32768, "tile_f32"), (32768, "tile_f16"), (131072, "tile_f32")):
+    # and the subtractive dither (fp16 norms, dither regenerated on chip) at 32 K
+    for tokens, fmt, dith in ((4096, "tile_f32", False), (32768, "tile_f32", False), (32768, "tile_f16", False),
+                              (32768, "tile_f16", True), (131072, "tile_f32", False)):
         caches = []
         for layer in range(layers):
             pair = []
             for which in range(2):
                 X = torch_gaussian_matrix(tokens, kvh * d, 1.0, 7000 + 2 * layer + which, device=dev)
-                pair.append(L.quantize_ex(X, lattice="e8", tile=d, seed=7100 + 2 * layer + which, beta=BETA,
-                                          scale_format=fmt))
+                if dith:
+                    pair.append(L.quantize_dithered(X, lattice="e8", tile=d, seed=7100 + 2 * layer + which,
+                                                    dither_seed=7300 + 2 * layer + which, beta=BETA,
+                                                    scale_format=fmt))
+                else:
+                    pair.append(L.quantize_ex(X, lattice="e8", tile=d, seed=7100 + 2 * layer + which, beta=BETA,
+                                              scale_format=fmt))
                 del X
             caches.append(pair)
         q = [torch.randn((qh, d), device=dev, generator=torch.Generator(device=dev).manual_seed(7200 + i)
@@ -890,7 +897,11 @@ def kv_arm(args, ws, rank, local):
 
         def step():
             for i, ((kc, ks, kd), (vc, vs, vd)) in enumerate(caches):
-                L.lq_attention_decode_ex("e8", kc, ks, kd, vc, vs, vd, fmt, q[i], out[i], wsz)
+                if dith:
+                    L.lq_attention_decode_dithered("e8", kc, ks, kd, 7300 + 2 * i, vc, vs, vd, 7301 + 2 * i, fmt,
+                                                   q[i], out[i], wsz)
+                else:
+                    L.lq_attention_decode_ex("e8", kc, ks, kd, vc, vs, vd, fmt, q[i], out[i], wsz)
 
         torch.cuda.synchronize(dev)
         with torch.cuda.stream(stream):
@@ -904,7 +915,7 @@ def kv_arm(args, ws, rank, local):
         ms = _graph_ms(torch, g, stream, reps)
         sbytes = 2 if fmt == "tile_f16" else 4
         cache_bytes = layers * 2 * tokens * kvh * (d + sbytes)
-        key = f"ctx{tokens}" + ("_fp16_norms" if fmt == "tile_f16" else "")
+        key = f"ctx{tokens}" + ("_fp16_norms" if fmt == "tile_f16" else "") + ("_dithered" if dith else "")
         results[key] = {"ms_per_step": round(ms, 4), "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
                         "cache_bytes": cache_bytes, "compression_vs_bf16": round(2.0 * d / (d + sbytes), 3)}
         del caches, q, out, wsz, g

@@ -466,6 +466,43 @@ lq_status lq_attention_decode_ex(int lattice, const int8_t* k_codes_dev, const v
                                  int q_heads, int head_dim, const void* q_dev, int qdtype, float* out_dev,
                                  void* workspace_dev, size_t workspace_bytes, void* stream);
 
+/*
+ * ------------------------------------------------------------------------
+ * Subtractive Voronoi dither (HyperQuant page, "Key algorithmic ingredients":
+ * a subtractive dither keeps the KV cache's inner products unbiased; Zamir &
+ * Feder, "On lattice quantization noise", 1996: the reconstruction error is
+ * then uniform over the lattice cell and independent of the input).
+ * Element (r, k) of a [rows x cols] matrix draws w = (top 24 bits of SplitMix64
+ * output r * cols + k from state dither_seed) / 2^24; the draws of one lattice
+ * block, scaled to a box that tiles space under a sublattice (E8, D4: side 2;
+ * A2: 1 x sqrt 3; Z1: 1), are reduced into the Voronoi cell: u = z - Q(z).
+ * The codes are those of Q(y + u), y the scaled rotated tile; the reconstruction
+ * is s (p - u).  Codes and scales keep their layouts; scale_format is
+ * LQ_SCALE_TILE_F32 or LQ_SCALE_TILE_F16.  A tile with a zero scale keeps zero
+ * codes (no dither).
+ * ------------------------------------------------------------------------
+ */
+lq_status lq_quantize_dithered(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
+                               int64_t ldw, int tile, uint64_t seed, uint64_t dither_seed, float beta,
+                               int scale_format, int8_t* codes_dev, void* scales_dev, int8_t* signs_dev,
+                               int32_t* dev_status_dev, void* stream);
+
+/* W^ = D H (s (p - u)) / sqrt(tile) for codes made by lq_quantize_dithered. */
+lq_status lq_dequantize_dithered(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
+                                 const int8_t* signs_dev, uint64_t dither_seed, int64_t rows, int64_t cols,
+                                 int tile, void* What_dev, int out_dtype, void* stream);
+
+/* lq_attention_decode_ex over K and V caches made by lq_quantize_dithered with
+ * the given dither seeds (K^ = s (p - u) row by row, the same for V^); the
+ * dither draws are regenerated on chip, never stored. */
+lq_status lq_attention_decode_dithered(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
+                                       const int8_t* k_signs_dev, uint64_t k_dither_seed,
+                                       const int8_t* v_codes_dev, const void* v_scales_dev,
+                                       const int8_t* v_signs_dev, uint64_t v_dither_seed, int scale_format,
+                                       int64_t tokens, int kv_heads, int q_heads, int head_dim, const void* q_dev,
+                                       int qdtype, float* out_dev, void* workspace_dev, size_t workspace_bytes,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,6 +37,11 @@ SIGNATURES = {
     "lq_gemm_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
     "lq_attention_decode_ex": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P,
                                       _P, ctypes.c_size_t, _P]),
+    "lq_quantize_dithered": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _U64, _F32, _I32, _P, _P, _P,
+                                    _P, _P]),
+    "lq_dequantize_dithered": (_I32, [_I32, _P, _P, _I32, _P, _U64, _I64, _I64, _I32, _P, _I32, _P]),
+    "lq_attention_decode_dithered": (_I32, [_I32, _P, _P, _P, _U64, _P, _P, _P, _U64, _I32, _I64, _I32, _I32, _I32,
+                                            _P, _I32, _P, _P, ctypes.c_size_t, _P]),
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
     "lq_gemv": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
     "lq_gemv_noalloc": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P]),
@@ -410,6 +415,50 @@ def lq_attention_decode_ex(lattice, k_codes, k_scales, k_signs, v_codes, v_scale
         _lattice_id(lattice), _ptr(k_codes), _ptr(k_scales), _ptr(k_signs), _ptr(v_codes), _ptr(v_scales),
         _ptr(v_signs), _scale_format_id(scale_format), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q),
         _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lq_quantize_dithered(lattice, W, tile: int, seed: int, dither_seed: int, beta: float, scale_format, codes,
+                         scales, signs, dev_status=None, stream=None) -> None:
+    """lq_quantize with the subtractive Voronoi dither of seed `dither_seed`."""
+    rows, cols = W.shape
+    _check("lq_quantize_dithered", _get_lib().lq_quantize_dithered(
+        _lattice_id(lattice), _ptr(W), _dtype_id(W), rows, cols, _row_stride(W), int(tile),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, int(dither_seed) & 0xFFFFFFFFFFFFFFFF, float(beta),
+        _scale_format_id(scale_format), _ptr(codes), _ptr(scales), _ptr(signs), _ptr(dev_status), _stream(stream)))
+
+
+def quantize_dithered(W, lattice: str = "e8", tile: int = 128, seed: int = 0, dither_seed: int = 1,
+                      beta: float = 0.25, scale_format="tile_f32", dev_status=None, stream=None):
+    """Allocate outputs and call :func:`lq_quantize_dithered`; returns (codes, scales, signs)."""
+    import torch
+    rows, cols = W.shape
+    codes = torch.empty((rows, cols), dtype=torch.int8, device=W.device)
+    scales = scales_tensor(rows, cols, tile, scale_format, W.device)
+    signs = torch.empty((cols,), dtype=torch.int8, device=W.device)
+    lq_quantize_dithered(lattice, W, tile, seed, dither_seed, beta, scale_format, codes, scales, signs, dev_status,
+                         stream)
+    return codes, scales, signs
+
+
+def lq_dequantize_dithered(lattice, codes, scales, scale_format, signs, dither_seed: int, tile: int, W_hat,
+                           stream=None) -> None:
+    rows, cols = codes.shape
+    _check("lq_dequantize_dithered", _get_lib().lq_dequantize_dithered(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _scale_format_id(scale_format), _ptr(signs),
+        int(dither_seed) & 0xFFFFFFFFFFFFFFFF, rows, cols, int(tile), _ptr(W_hat), _dtype_id(W_hat),
+        _stream(stream)))
+
+
+def lq_attention_decode_dithered(lattice, k_codes, k_scales, k_signs, k_dither_seed: int, v_codes, v_scales,
+                                 v_signs, v_dither_seed: int, scale_format, q, out, workspace, stream=None) -> None:
+    tokens = k_codes.shape[0]
+    kv_heads = k_scales.shape[1]
+    q_heads, head_dim = q.shape
+    _check("lq_attention_decode_dithered", _get_lib().lq_attention_decode_dithered(
+        _lattice_id(lattice), _ptr(k_codes), _ptr(k_scales), _ptr(k_signs), int(k_dither_seed) & 0xFFFFFFFFFFFFFFFF,
+        _ptr(v_codes), _ptr(v_scales), _ptr(v_signs), int(v_dither_seed) & 0xFFFFFFFFFFFFFFFF,
+        _scale_format_id(scale_format), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lq_rotate_blocks(R, X, Y, transpose: bool = False, stream=None) -> None:

@@ -450,4 +450,63 @@ __device__ __forceinline__ void decode_lane(const float2 (&p)[32], uint32_t (&w)
   }
 }
 
+// ---------------------------------------------------------------- dither
+// Subtractive dither (Zamir & Feder, "On lattice quantization noise", 1996):
+// element (r, k) of a [rows x cols] matrix draws w = (top 24 bits of SplitMix64
+// output r * cols + k from state seed) / 2^24 -- the generator of the signs
+// (Steele, Lea & Flood 2014) -- and the draws of one lattice block, scaled to
+// a box that tiles space under a sublattice (E8, D4: side 2; A2: 1 x sqrt 3;
+// Z: 1), are reduced into the Voronoi cell: u = z - Q(z).
+__device__ __forceinline__ float dither_w(uint64_t seed, uint64_t counter) {
+  uint64_t z = seed + (counter + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return (float)(uint32_t)(z >> 40) * (1.0f / 16777216.0f);
+}
+
+__device__ __forceinline__ float code_byte(uint32_t w, int k) { return (float)(int8_t)(w >> (8 * k)); }
+
+// Dither u (point coordinates) of the 8 consecutive elements whose first has
+// counter c0 (one E8 block, two D4 blocks, four A2 pairs or eight Z values).
+template <int LAT>
+__device__ __forceinline__ void dither8(uint64_t seed, uint64_t c0, float (&u)[8]) {
+  float z[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) z[i] = dither_w(seed, c0 + (uint64_t)i);
+  bool unused = false;
+  if constexpr (LAT == LQ_E8) {
+    const float2 y[4] = {make_float2(2.f * z[0], 2.f * z[1]), make_float2(2.f * z[2], 2.f * z[3]),
+                         make_float2(2.f * z[4], 2.f * z[5]), make_float2(2.f * z[6], 2.f * z[7])};
+    const BlockCodes8 c = decode_e8<false>(y, unused);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u[i] = 2.f * z[i] - 0.5f * code_byte(i < 4 ? c.w0 : c.w1, i & 3);
+  } else if constexpr (LAT == LQ_D4) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const float2 y[2] = {make_float2(2.f * z[4 * b], 2.f * z[4 * b + 1]),
+                           make_float2(2.f * z[4 * b + 2], 2.f * z[4 * b + 3])};
+      const uint32_t c = decode_d4<false>(y, unused);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[4 * b + i] = 2.f * z[4 * b + i] - 0.5f * code_byte(c, i);
+    }
+  } else if constexpr (LAT == LQ_A2) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float2 y = make_float2(z[2 * b], 1.7320508075688772f * z[2 * b + 1]);
+      const uint32_t c = decode_a2_pair<false>(y, unused);
+      u[2 * b] = y.x - 0.5f * code_byte(c, 0);
+      u[2 * b + 1] = y.y - 0.8660254037844386f * code_byte(c, 1);
+    }
+  } else {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t c = decode_z1_quad<false>(make_float2(z[4 * b], z[4 * b + 1]),
+                                               make_float2(z[4 * b + 2], z[4 * b + 3]), unused);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) u[4 * b + i] = z[4 * b + i] - 0.5f * code_byte(c, i);
+    }
+  }
+}
+
 }  // namespace lq

@@ -39,6 +39,7 @@ struct AttnArgs {
   const void* vs;
   const int8_t* vsg;
   int sfmt;
+  uint64_t kdseed, vdseed;   // subtractive dither seeds (DLAT instantiations)
   const void* q;
   int qbf16;
   int64_t tokens;
@@ -79,11 +80,30 @@ __global__ void __launch_bounds__(D) rotate_query_kernel(AttnArgs a) {
   a.qrot[qi] = v[i] * (0.5f / (float)D) * ((a.a2 && (i & 1)) ? 1.7320508075688772f : 1.f);
 }
 
-template <int G, bool F16S>
+// Rows of the per-warp dither transpose (padded: conflict-free 16-byte
+// accesses both by token rows and by dimension columns).
+constexpr int kDvStride = D + 4;
+
+// Dither of one cached vector in the doubled code units the kernel uses
+// (2u; A2 odd coordinates 2u / sqrt 3): element (token, kvh * D + i) of the
+// [tokens x kv_heads * D] cache.
+template <int LAT>
+__device__ __forceinline__ void dither8_codes(uint64_t seed, uint64_t c0, float (&du)[8]) {
+  dither8<LAT>(seed, c0, du);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) du[i] *= (LAT == LQ_A2 && (i & 1)) ? 1.1547005383792515f : 2.f;
+}
+
+// DLAT = 0: caches without dither; otherwise the lattice of dithered caches,
+// whose reconstruction is s (p - u): each score loses q~ . u of its token and
+// the value sum the weighted dither of each token (transposed through shared
+// memory, dynamic: kWarps x 32 x kDvStride floats).
+template <int G, bool F16S, int DLAT>
 __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(AttnArgs a) {
   __shared__ __align__(16) float qr[G][D];         // rotated, scaled queries
   __shared__ float wm[kWarps][G], wl[kWarps][G];
   __shared__ __align__(16) float wacc[kWarps][G][D];
+  extern __shared__ __align__(16) float dv_smem[];
   const int kvh = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t ld = (int64_t)a.kv_heads * D;
@@ -150,6 +170,34 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(
         }
       }
     }
+    if constexpr (DLAT != 0) {
+      // this lane's token: scores lose q~ . u (K dither); the V dither goes to
+      // the warp's transpose buffer, row = lane
+      float* dvrow = dv_smem + ((size_t)warp * 32 + lane) * kDvStride;
+      const uint64_t cbase = (uint64_t)j * (uint64_t)ld + (uint64_t)kvh * D;
+#pragma unroll 1
+      for (int gb = 0; gb < D / 8; ++gb) {
+        float du[8], dvv[8];
+        if (ok) {
+          dither8_codes<DLAT>(a.kdseed, cbase + 8 * gb, du);
+          dither8_codes<DLAT>(a.vdseed, cbase + 8 * gb, dvv);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) du[i] = dvv[i] = 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float4 q0 = *reinterpret_cast<const float4*>(&qr[g][8 * gb]);
+          const float4 q1 = *reinterpret_cast<const float4*>(&qr[g][8 * gb + 4]);
+          float d = q0.x * du[0] + q0.y * du[1] + q0.z * du[2] + q0.w * du[3];
+          d += q1.x * du[4] + q1.y * du[5] + q1.z * du[6] + q1.w * du[7];
+          sc[g] -= d;
+        }
+        *reinterpret_cast<float4*>(dvrow + 8 * gb) = make_float4(dvv[0], dvv[1], dvv[2], dvv[3]);
+        *reinterpret_cast<float4*>(dvrow + 8 * gb + 4) = make_float4(dvv[4], dvv[5], dvv[6], dvv[7]);
+      }
+      __syncwarp();
+    }
     // online softmax over this chunk
     float p[G];
 #pragma unroll
@@ -171,7 +219,11 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(
 #pragma unroll
     for (int t = 0; t < 32; ++t) {
       const uint32_t w = vw[t];
-      const float v0 = code_f(w, 0), v1 = code_f(w, 1), v2 = code_f(w, 2), v3 = code_f(w, 3);
+      float v0 = code_f(w, 0), v1 = code_f(w, 1), v2 = code_f(w, 2), v3 = code_f(w, 3);
+      if constexpr (DLAT != 0) {
+        const float4 dq = *reinterpret_cast<const float4*>(dv_smem + ((size_t)warp * 32 + t) * kDvStride + 4 * lane);
+        v0 -= dq.x; v1 -= dq.y; v2 -= dq.z; v3 -= dq.w;
+      }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float pt = __shfl_sync(0xffffffffu, p[g], t);
@@ -181,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(
         acc[g][3] = fmaf(pt, v3, acc[g][3]);
       }
     }
+    if constexpr (DLAT != 0) __syncwarp();   // the next chunk rewrites the transpose buffer
   }
   // merge the four warps
 #pragma unroll
@@ -338,11 +391,38 @@ extern "C" size_t lq_attention_workspace_size(int64_t tokens, int kv_heads, int 
 
 namespace {
 
+constexpr size_t kDvSmem = (size_t)kWarps * 32 * kDvStride * sizeof(float);
+
+template <int G, bool H, int LAT>
+lq_status launch_partial_dithered_g(const AttnArgs& a, unsigned grid, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(attn_partial_kernel<G, H, LAT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kDvSmem) != cudaSuccess) {
+      cudaGetLastError();
+      return LQ_ERR_CUDA;
+    }
+    attr = true;
+  }
+  attn_partial_kernel<G, H, LAT><<<grid, kThreads, kDvSmem, s>>>(a);
+  return LQ_OK;
+}
+
+template <int LAT>
+lq_status launch_partial_dithered(const AttnArgs& a, int group, bool h, unsigned grid, cudaStream_t s) {
+  switch (group) {
+    case 1: return h ? launch_partial_dithered_g<1, true, LAT>(a, grid, s) : launch_partial_dithered_g<1, false, LAT>(a, grid, s);
+    case 2: return h ? launch_partial_dithered_g<2, true, LAT>(a, grid, s) : launch_partial_dithered_g<2, false, LAT>(a, grid, s);
+    case 4: return h ? launch_partial_dithered_g<4, true, LAT>(a, grid, s) : launch_partial_dithered_g<4, false, LAT>(a, grid, s);
+    default: return h ? launch_partial_dithered_g<8, true, LAT>(a, grid, s) : launch_partial_dithered_g<8, false, LAT>(a, grid, s);
+  }
+}
+
 lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
                         const int8_t* k_signs_dev, const int8_t* v_codes_dev, const void* v_scales_dev,
                         const int8_t* v_signs_dev, int sfmt, int64_t tokens, int kv_heads, int q_heads, int head_dim,
                         const void* q_dev, int qdtype, float* out_dev, void* workspace_dev, size_t workspace_bytes,
-                        void* stream) {
+                        void* stream, bool dither = false, uint64_t k_dither_seed = 0, uint64_t v_dither_seed = 0) {
   if (!valid_lattice(lattice)) return LQ_ERR_ARG;
   if (sfmt != LQ_SCALE_TILE_F32 && sfmt != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
   const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
@@ -365,6 +445,8 @@ lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_sc
   a.kc = k_codes_dev; a.ks = k_scales_dev; a.ksg = k_signs_dev;
   a.vc = v_codes_dev; a.vs = v_scales_dev; a.vsg = v_signs_dev;
   a.sfmt = sfmt;
+  a.kdseed = k_dither_seed;
+  a.vdseed = v_dither_seed;
   a.q = q_dev; a.qbf16 = (qdtype == LQ_BF16);
   a.tokens = tokens; a.kv_heads = kv_heads; a.group = group;
   a.splits = attn_splits(tokens, kv_heads);
@@ -377,17 +459,28 @@ lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_sc
   rotate_query_kernel<<<(unsigned)q_heads, D, 0, s>>>(a);
   const unsigned grid = (unsigned)(kv_heads * a.splits);
   const bool h = (sfmt == LQ_SCALE_TILE_F16);
-  switch (group) {
-    case 1: h ? attn_partial_kernel<1, true><<<grid, kThreads, 0, s>>>(a)
-              : attn_partial_kernel<1, false><<<grid, kThreads, 0, s>>>(a); break;
-    case 2: h ? attn_partial_kernel<2, true><<<grid, kThreads, 0, s>>>(a)
-              : attn_partial_kernel<2, false><<<grid, kThreads, 0, s>>>(a); break;
-    case 4: h ? attn_partial_kernel<4, true><<<grid, kThreads, 0, s>>>(a)
-              : attn_partial_kernel<4, false><<<grid, kThreads, 0, s>>>(a); break;
-    default: h ? attn_partial_kernel<8, true><<<grid, kThreads, 0, s>>>(a)
-               : attn_partial_kernel<8, false><<<grid, kThreads, 0, s>>>(a); break;
+  lq_status st = LQ_OK;
+  if (dither) {
+    switch (lattice) {
+      case LQ_E8: st = launch_partial_dithered<LQ_E8>(a, group, h, grid, s); break;
+      case LQ_D4: st = launch_partial_dithered<LQ_D4>(a, group, h, grid, s); break;
+      case LQ_A2: st = launch_partial_dithered<LQ_A2>(a, group, h, grid, s); break;
+      default:    st = launch_partial_dithered<LQ_Z1>(a, group, h, grid, s); break;
+    }
+    if (st != LQ_OK) return st;
+  } else {
+    switch (group) {
+      case 1: h ? attn_partial_kernel<1, true, 0><<<grid, kThreads, 0, s>>>(a)
+                : attn_partial_kernel<1, false, 0><<<grid, kThreads, 0, s>>>(a); break;
+      case 2: h ? attn_partial_kernel<2, true, 0><<<grid, kThreads, 0, s>>>(a)
+                : attn_partial_kernel<2, false, 0><<<grid, kThreads, 0, s>>>(a); break;
+      case 4: h ? attn_partial_kernel<4, true, 0><<<grid, kThreads, 0, s>>>(a)
+                : attn_partial_kernel<4, false, 0><<<grid, kThreads, 0, s>>>(a); break;
+      default: h ? attn_partial_kernel<8, true, 0><<<grid, kThreads, 0, s>>>(a)
+                 : attn_partial_kernel<8, false, 0><<<grid, kThreads, 0, s>>>(a); break;
+    }
   }
-  lq_status st = check_launch();
+  st = check_launch();
   if (st != LQ_OK) return st;
   attn_combine_kernel<<<(unsigned)q_heads, D, 0, s>>>(a, group);
   return check_launch();
@@ -417,6 +510,19 @@ extern "C" lq_status lq_attention_decode_ex(int lattice, const int8_t* k_codes_d
   return attention_fmt(lattice, k_codes_dev, k_scales_dev, k_signs_dev, v_codes_dev, v_scales_dev, v_signs_dev,
                        scale_format, tokens, kv_heads, q_heads, head_dim, q_dev, qdtype, out_dev, workspace_dev,
                        workspace_bytes, stream);
+}
+
+extern "C" lq_status lq_attention_decode_dithered(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
+                                                  const int8_t* k_signs_dev, uint64_t k_dither_seed,
+                                                  const int8_t* v_codes_dev, const void* v_scales_dev,
+                                                  const int8_t* v_signs_dev, uint64_t v_dither_seed, int scale_format,
+                                                  int64_t tokens, int kv_heads, int q_heads, int head_dim,
+                                                  const void* q_dev, int qdtype, float* out_dev, void* workspace_dev,
+                                                  size_t workspace_bytes, void* stream) {
+  LQ_NVTX_RANGE("lq_attention_decode_dithered");
+  return attention_fmt(lattice, k_codes_dev, k_scales_dev, k_signs_dev, v_codes_dev, v_scales_dev, v_signs_dev,
+                       scale_format, tokens, kv_heads, q_heads, head_dim, q_dev, qdtype, out_dev, workspace_dev,
+                       workspace_bytes, stream, true, k_dither_seed, v_dither_seed);
 }
 
 extern "C" lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, const void* X_dev,

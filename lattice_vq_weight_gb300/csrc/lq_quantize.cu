@@ -104,10 +104,13 @@ struct DequantArgs {
   float inv_2sqrt_tile;
   void* out;
   int64_t units;
+  int dither;             // subtract the subtractive dither of seed dither_seed
+  uint64_t dither_seed;
 };
 
 // W^ = D H (s p) / sqrt(T): codes -> (A2: odd coordinates x sqrt3) -> FWHT
-// (integer-exact for the doubled codes) -> x s / (2 sqrt T) -> signs.
+// (integer-exact for the doubled codes) -> x s / (2 sqrt T) -> signs; with a
+// dither, p - u replaces p (2u in the doubled code units).
 template <int LAT, bool OUT_BF16>
 __global__ void __launch_bounds__(256, 1) dequantize_kernel(DequantArgs a) {
   const int lane = threadIdx.x & 31;
@@ -139,6 +142,16 @@ __global__ void __launch_bounds__(256, 1) dequantize_kernel(DequantArgs a) {
           if constexpr (LAT == LQ_A2) v1 *= 1.7320508075688772f;
           p[(16 * q + 4 * h + c) >> 1] = make_float2(v0, v1);
         }
+      }
+    }
+    if (a.dither && active) {
+#pragma unroll
+      for (int gb = 0; gb < 8; ++gb) {
+        float du[8];
+        dither8<LAT>(a.dither_seed, (uint64_t)row * (uint64_t)a.cols + (uint64_t)(col0 + 8 * gb), du);
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          p[4 * gb + h] = sub2(p[4 * gb + h], make_float2(2.f * du[2 * h], 2.f * du[2 * h + 1]));
       }
     }
     fwht64_local(p);
@@ -216,7 +229,8 @@ extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_de
 }
 
 template <int LAT, bool BF16>
-static lq_status launch_quantize(QuantArgs& a, int sf, cudaStream_t st) {
+static lq_status launch_quantize(QuantArgs& a, int sf, bool dither, cudaStream_t st) {
+  if (dither) return launch_quantize_dithered(a, LAT, BF16, sf, st);
   if (a.n_mats > 1) return launch_quantize_walk<LAT, BF16, true, LQ_SCALE_TILE_F32>(a, st);
   if (sf != LQ_SCALE_TILE_F32) return launch_quantize_scaled16(a, LAT, BF16, sf, st);
   return launch_quantize_walk<LAT, BF16, false, LQ_SCALE_TILE_F32>(a, st);
@@ -256,9 +270,11 @@ lq_status validate_quantize(int lattice, const void* W_dev, int wdtype, int64_t 
 lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, const int64_t* rows,
                          const int64_t* cols, const int64_t* ldw, int tile, const uint64_t* seeds, float beta,
                          int8_t* const* codes, void* const* scales, int8_t* const* signs, int32_t* dev_status,
-                         int sf, bool make_signs_too, cudaStream_t s) {
+                         int sf, bool make_signs_too, cudaStream_t s, bool dither = false,
+                         uint64_t dither_seed = 0) {
   SignsArgs sa = {};
   QuantArgs a = {};
+  a.dither_seed = dither_seed;
   int64_t max_cols = 0, units = 0;
   int k = 0;
   for (int m = 0; m < n; ++m) {
@@ -290,10 +306,10 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
   a.cta_units = units;
   const bool bf = (wdtype == LQ_BF16);
   switch (lattice) {
-    case LQ_E8: return bf ? launch_quantize<LQ_E8, true>(a, sf, s) : launch_quantize<LQ_E8, false>(a, sf, s);
-    case LQ_D4: return bf ? launch_quantize<LQ_D4, true>(a, sf, s) : launch_quantize<LQ_D4, false>(a, sf, s);
-    case LQ_A2: return bf ? launch_quantize<LQ_A2, true>(a, sf, s) : launch_quantize<LQ_A2, false>(a, sf, s);
-    default:    return bf ? launch_quantize<LQ_Z1, true>(a, sf, s) : launch_quantize<LQ_Z1, false>(a, sf, s);
+    case LQ_E8: return bf ? launch_quantize<LQ_E8, true>(a, sf, dither, s) : launch_quantize<LQ_E8, false>(a, sf, dither, s);
+    case LQ_D4: return bf ? launch_quantize<LQ_D4, true>(a, sf, dither, s) : launch_quantize<LQ_D4, false>(a, sf, dither, s);
+    case LQ_A2: return bf ? launch_quantize<LQ_A2, true>(a, sf, dither, s) : launch_quantize<LQ_A2, false>(a, sf, dither, s);
+    default:    return bf ? launch_quantize<LQ_Z1, true>(a, sf, dither, s) : launch_quantize<LQ_Z1, false>(a, sf, dither, s);
   }
 }
 
@@ -356,6 +372,20 @@ extern "C" lq_status lq_quantize_ex(int lattice, const void* W_dev, int wdtype, 
   return LQ_OK;
 }
 
+extern "C" lq_status lq_quantize_dithered(int lattice, const void* W_dev, int wdtype, int64_t rows, int64_t cols,
+                                          int64_t ldw, int tile, uint64_t seed, uint64_t dither_seed, float beta,
+                                          int scale_format, int8_t* codes_dev, void* scales_dev, int8_t* signs_dev,
+                                          int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_quantize_dithered");
+  if (scale_format != LQ_SCALE_TILE_F32 && scale_format != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
+  const lq_status st = validate_quantize(lattice, W_dev, wdtype, rows, cols, ldw, tile, beta, codes_dev,
+                                         scales_dev, signs_dev, dev_status_dev, scale_format);
+  if (st != LQ_OK) return st;
+  return quantize_group(lattice, 1, &W_dev, wdtype, &rows, &cols, &ldw, tile, &seed, beta, &codes_dev,
+                        &scales_dev, &signs_dev, dev_status_dev, scale_format, true, (cudaStream_t)stream, true,
+                        dither_seed);
+}
+
 extern "C" lq_status lq_quantize_grouped(int lattice, int n, const void* const* W_dev, int wdtype,
                                          const int64_t* rows, const int64_t* cols, const int64_t* ldw, int tile,
                                          const uint64_t* seeds, float beta, int8_t* const* codes_dev,
@@ -391,7 +421,7 @@ namespace {
 
 lq_status dequantize_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev, int sfmt,
                          const int8_t* signs_dev, int64_t rows, int64_t cols, int tile, void* What_dev,
-                         int out_dtype, cudaStream_t s) {
+                         int out_dtype, cudaStream_t s, bool dither = false, uint64_t dither_seed = 0) {
   lq_status st = validate_common(lattice, rows, cols, tile);
   if (st != LQ_OK) return st;
   if (out_dtype != LQ_BF16 && out_dtype != LQ_F32) return LQ_ERR_DTYPE;
@@ -410,6 +440,8 @@ lq_status dequantize_fmt(int lattice, const int8_t* codes_dev, const void* scale
   a.inv_2sqrt_tile = (float)(0.5 / sqrt((double)tile));
   a.out = What_dev;
   a.units = rows * a.chunks_per_row;
+  a.dither = dither ? 1 : 0;
+  a.dither_seed = dither_seed;
   const bool ob = (out_dtype == LQ_BF16);
   switch (lattice) {
     case LQ_E8: return ob ? launch_dequant<LQ_E8, true>(a, s) : launch_dequant<LQ_E8, false>(a, s);
@@ -435,4 +467,14 @@ extern "C" lq_status lq_dequantize_ex(int lattice, const int8_t* codes_dev, cons
   LQ_NVTX_RANGE("lq_dequantize_ex");
   return dequantize_fmt(lattice, codes_dev, scales_dev, scale_format, signs_dev, rows, cols, tile, What_dev,
                         out_dtype, (cudaStream_t)stream);
+}
+
+extern "C" lq_status lq_dequantize_dithered(int lattice, const int8_t* codes_dev, const void* scales_dev,
+                                            int scale_format, const int8_t* signs_dev, uint64_t dither_seed,
+                                            int64_t rows, int64_t cols, int tile, void* What_dev, int out_dtype,
+                                            void* stream) {
+  LQ_NVTX_RANGE("lq_dequantize_dithered");
+  if (scale_format != LQ_SCALE_TILE_F32 && scale_format != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
+  return dequantize_fmt(lattice, codes_dev, scales_dev, scale_format, signs_dev, rows, cols, tile, What_dev,
+                        out_dtype, (cudaStream_t)stream, true, dither_seed);
 }

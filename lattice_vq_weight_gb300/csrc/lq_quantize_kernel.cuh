@@ -166,6 +166,7 @@ struct QuantArgs {
   float beta, sqrt_tile, inv_tile;
   int32_t* status;
   int64_t cta_units;  // CTA units of all matrices
+  uint64_t dither_seed;   // subtractive dither (DITHER instantiations only)
 };
 
 constexpr int kQuantThreads = 128;
@@ -254,9 +255,11 @@ __device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf
 // Residency: 4 CTAs per SM (128 registers) for the single-matrix walk, 3 (168
 // registers) for the grouped walk -- each measured faster than the other
 // choice for its walk.
-template <int LAT, bool BF16, int MP, bool GROUPED, int SF>
+// DITHER: subtractive dither (lq_device.cuh) added to y before the decode.
+template <int LAT, bool BF16, int MP, bool GROUPED, int SF, bool DITHER = false>
 __global__ void __launch_bounds__(kQuantThreads, GROUPED ? 3 : 4) quantize_kernel(QuantArgs a) {
   static_assert(!GROUPED || SF == LQ_SCALE_TILE_F32, "grouped calls store float32 tile scales");
+  static_assert(!(GROUPED && DITHER), "the dither runs on the single-matrix walk");
   using SM = QuantSmem<BF16>;
   extern __shared__ uint4 quant_smem[];
   const int lane = threadIdx.x & 31;
@@ -351,11 +354,28 @@ __global__ void __launch_bounds__(kQuantThreads, GROUPED ? 3 : 4) quantize_kerne
 #pragma unroll
     for (int j = 0; j < 32; ++j) p[j] = mul2(p[j], k2);
 
+    constexpr int Q = 1 << MP;
+    if constexpr (DITHER) {
+      // y + u for tiles with a scale (a zero scale keeps y = 0 and zero codes);
+      // register block g holds the 8 columns 8 q + 8 Q gx + 64 ga (see the store)
+      if (k > 0.f) {
+        const uint64_t c_row = (uint64_t)row * (uint64_t)M.cols + (uint64_t)chunk * kChunkCols +
+                               (uint64_t)((lane >> MP) * (64 * Q) + 8 * (lane & (Q - 1)));
+#pragma unroll
+        for (int gb = 0; gb < 8; ++gb) {
+          float u[8];
+          dither8<LAT>(a.dither_seed, c_row + (uint64_t)((gb >> MP) * (8 * Q) + 64 * (gb & (Q - 1))), u);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) p[4 * gb + h] = add2(p[4 * gb + h], make_float2(u[2 * h], u[2 * h + 1]));
+        }
+      }
+    }
     // every |y| of the lane below 62.5 keeps every code inside int8, and the
     // per-block range check is left out; the lane's sum of y^2 decides that
-    // for free in most cases, the lane maximum otherwise
+    // for free in most cases (not with a dither, which moves y), the lane
+    // maximum otherwise
     const float lane_y2 = (acc.x + acc.y) * (k * k);
-    bool small = lane_y2 < 3906.25f;
+    bool small = !DITHER && lane_y2 < 3906.25f;
     if (!small) {
       float mx = 0.f;
 #pragma unroll
@@ -372,7 +392,6 @@ __global__ void __launch_bounds__(kQuantThreads, GROUPED ? 3 : 4) quantize_kerne
       nonfinite |= !finite;
       // register block u holds tile columns 8 q + 8 Q ux + 64 a (q = lane bits,
       // ux = u >> MP, a = u & (Q - 1)) of the tile group G = lane >> MP
-      constexpr int Q = 1 << MP;
       int8_t* dst = M.codes + row * M.cols + (int64_t)chunk * kChunkCols + (lane >> MP) * (64 * Q) +
                     8 * (lane & (Q - 1));
 #pragma unroll
@@ -457,17 +476,17 @@ inline int64_t gcd64(int64_t x, int64_t y) {
   return x;
 }
 
-template <int LAT, bool BF16, int MP, bool GROUPED, int SF>
+template <int LAT, bool BF16, int MP, bool GROUPED, int SF, bool DITHER = false>
 inline lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
   constexpr size_t smem = (size_t)(kQuantThreads / 32) * QuantSmem<BF16>::kPerWarp * sizeof(uint4);
   static int per_sm = 0;
   if (per_sm == 0) {
-    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP, GROUPED, SF>,
+    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP, GROUPED, SF, DITHER>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
     }
-    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP, GROUPED, SF>, kQuantThreads, smem);
+    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP, GROUPED, SF, DITHER>, kQuantThreads, smem);
   }
   // a warp count that is a multiple of every matrix's chunks per row keeps
   // each warp on one chunk (one set of signs) within a matrix
@@ -490,7 +509,7 @@ inline lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP, GROUPED, SF>, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP, GROUPED, SF, DITHER>, a) != cudaSuccess) {
     cudaGetLastError();
     return LQ_ERR_CUDA;
   }
@@ -499,15 +518,19 @@ inline lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
 
 // MP = tile bits exchanged through shared memory: log2(tile / 64), at most 3.
 // A 128-column tile has a single cross-lane stage, cheaper as a shuffle (MP = 0).
-template <int LAT, bool BF16, bool GROUPED, int SF>
+template <int LAT, bool BF16, bool GROUPED, int SF, bool DITHER = false>
 inline lq_status launch_quantize_walk(QuantArgs& a, cudaStream_t st) {
-  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, GROUPED, SF>(a, st);
-  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, GROUPED, SF>(a, st);
-  return launch_quantize_mp<LAT, BF16, 3, GROUPED, SF>(a, st);
+  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, GROUPED, SF, DITHER>(a, st);
+  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, GROUPED, SF, DITHER>(a, st);
+  return launch_quantize_mp<LAT, BF16, 3, GROUPED, SF, DITHER>(a, st);
 }
 
 // Launch of the single-matrix walk with a 16-bit scale format
 // (LQ_SCALE_ROW_BF16 or LQ_SCALE_TILE_F16), defined in lq_quantize_fmt.cu.
 lq_status launch_quantize_scaled16(QuantArgs& a, int lattice, bool bf16, int sf, cudaStream_t st);
+
+// Launch of the single-matrix walk with the subtractive dither (scale format
+// LQ_SCALE_TILE_F32 or LQ_SCALE_TILE_F16), defined in lq_quantize_dither.cu.
+lq_status launch_quantize_dithered(QuantArgs& a, int lattice, bool bf16, int sf, cudaStream_t st);
 
 }  // namespace lq

@@ -122,6 +122,13 @@ def test_argument_errors_are_synchronous():
     # the KV attention takes float32 or fp16 tile scales only
     assert lib.lq_attention_decode_ex(8, good, good, good, good, good, good, L.LQ_SCALE_ROW_BF16, 16, 1, 1, 128,
                                       good, 1, good, good, ctypes.c_size_t(1 << 20), s) == L.LQ_ERR_ARG
+    # dithered calls take float32 or fp16 tile scales only
+    assert lib.lq_quantize_dithered(8, good, 1, 4, 256, 256, 256, 0, 1, 0.25, L.LQ_SCALE_ROW_BF16, good, good,
+                                    good, nul, s) == L.LQ_ERR_ARG
+    assert lib.lq_dequantize_dithered(8, good, good, L.LQ_SCALE_ROW_BF16, good, 1, 4, 256, 256, good, 0,
+                                      s) == L.LQ_ERR_ARG
+    assert lib.lq_attention_decode_dithered(8, good, good, good, 1, good, good, good, 2, L.LQ_SCALE_ROW_BF16, 16, 1,
+                                            1, 128, good, 1, good, good, ctypes.c_size_t(1 << 20), s) == L.LQ_ERR_ARG
     # Rice format: worst case 8 bits per symbol + parity bits + 3 bits per segment, 16 bytes of padding
     assert L.lq_rice_stream_bound("e8", 2, 256, 256) == ((2 * 3 + 2 * 256 * 8 + 2 * 32 + 31) // 32) * 4 + 16
     assert L.lq_rice_stream_bound("e8", 1 << 15, 1 << 14, 256) == 0          # more than 2^28 weights
