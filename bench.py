@@ -874,8 +874,10 @@ def kv_arm(args, ws, rank, local):
     reps = max(3, min(args.steps, 10))
     # float32 norms at every context; fp16 norms (the pages' cache layout) at 32 K
     # and the subtractive dither (fp16 norms, dither regenerated on chip) at 32 K
-    for tokens, fmt, dith in ((4096, "tile_f32", False), (32768, "tile_f32", False), (32768, "tile_f16", False),
-                              (32768, "tile_f16", True), (131072, "tile_f32", False)):
+    # and the Rice-coded cache (fp16 norms, decoded on chip) at 32 K
+    for tokens, fmt, dith, rice in ((4096, "tile_f32", False, False), (32768, "tile_f32", False, False),
+                                    (32768, "tile_f16", False, False), (32768, "tile_f16", True, False),
+                                    (32768, "tile_f16", False, True), (131072, "tile_f32", False, False)):
         caches = []
         for layer in range(layers):
             pair = []
@@ -890,12 +892,35 @@ def kv_arm(args, ws, rank, local):
                                               scale_format=fmt))
                 del X
             caches.append(pair)
+        stream_bytes = 0
+        if rice:
+            rcaches = []
+            for pair in caches:
+                rp = []
+                for (c, sc, sg) in pair:
+                    nb = L.lq_rice_stream_bound("e8", tokens, kvh * d, d)
+                    words = torch.empty(nb // 4, dtype=torch.int32, device=dev)
+                    offs = torch.empty((tokens, kvh), dtype=torch.int32, device=dev)
+                    tot = torch.empty(1, dtype=torch.int64, device=dev)
+                    rws = torch.empty(L.lq_rice_workspace_size(tokens, kvh * d, d), dtype=torch.uint8, device=dev)
+                    L.lq_rice_encode("e8", c, d, words, offs, tot, rws)
+                    torch.cuda.synchronize(dev)
+                    nw = (int(tot.item()) + 31) // 32 + 4
+                    stream_bytes += int(tot.item()) / 8.0
+                    rp.append((words[:nw].clone(), offs, sc, sg))
+                    del words, rws
+                rcaches.append(rp)
+            caches = rcaches
         q = [torch.randn((qh, d), device=dev, generator=torch.Generator(device=dev).manual_seed(7200 + i)
                          ).to(torch.bfloat16) for i in range(layers)]
         out = [torch.empty((qh, d), dtype=torch.float32, device=dev) for _ in range(layers)]
         wsz = torch.empty(L.lq_attention_workspace_size(tokens, kvh, qh, d), dtype=torch.uint8, device=dev)
 
         def step():
+            if rice:
+                for i, ((kw, ko, ks, kd), (vw, vo, vs, vd)) in enumerate(caches):
+                    L.lq_attention_decode_rice("e8", kw, ko, ks, kd, vw, vo, vs, vd, fmt, q[i], out[i], wsz)
+                return
             for i, ((kc, ks, kd), (vc, vs, vd)) in enumerate(caches):
                 if dith:
                     L.lq_attention_decode_dithered("e8", kc, ks, kd, 7300 + 2 * i, vc, vs, vd, 7301 + 2 * i, fmt,
@@ -915,9 +940,13 @@ def kv_arm(args, ws, rank, local):
         ms = _graph_ms(torch, g, stream, reps)
         sbytes = 2 if fmt == "tile_f16" else 4
         cache_bytes = layers * 2 * tokens * kvh * (d + sbytes)
-        key = f"ctx{tokens}" + ("_fp16_norms" if fmt == "tile_f16" else "") + ("_dithered" if dith else "")
+        if rice:   # stream + 32-bit segment offsets + norms
+            cache_bytes = int(stream_bytes + layers * 2 * tokens * kvh * (4 + sbytes))
+        key = (f"ctx{tokens}" + ("_fp16_norms" if fmt == "tile_f16" else "") + ("_dithered" if dith else "")
+               + ("_rice" if rice else ""))
         results[key] = {"ms_per_step": round(ms, 4), "cache_gbs": round(cache_bytes / (ms * 1e-3) / 1e9, 1),
-                        "cache_bytes": cache_bytes, "compression_vs_bf16": round(2.0 * d / (d + sbytes), 3)}
+                        "cache_bytes": cache_bytes,
+                        "compression_vs_bf16": round(layers * 2 * tokens * kvh * d * 2 / cache_bytes, 3)}
         del caches, q, out, wsz, g
         torch.cuda.empty_cache()
     peak, src = hbm_peak("burst")

@@ -503,6 +503,27 @@ lq_status lq_attention_decode_dithered(int lattice, const int8_t* k_codes_dev, c
                                        int qdtype, float* out_dev, void* workspace_dev, size_t workspace_bytes,
                                        void* stream);
 
+/*
+ * Decode attention over K and V caches held as Rice streams (HyperQuant page,
+ * KV-cache storage table: "Rice bitstream + fp16 norms", ~3.8x against bf16):
+ * each cache [tokens x kv_heads * head_dim] is quantized (lq_quantize_ex, tile
+ * = head_dim) and then coded with lq_rice_encode (rows = tokens, cols =
+ * kv_heads * head_dim, tile = head_dim), one segment per (token, kv head).  The
+ * kernel decodes every token's segments on chip and computes what
+ * lq_attention_decode_ex computes on the int8 codes.
+ *   k_stream_dev / v_stream_dev   the Rice words (k_stream_bytes, v_stream_bytes)
+ *   k_offsets_dev / v_offsets_dev uint32 [tokens x kv_heads] segment bit offsets
+ *   scales, signs, q, out, workspace, shapes: as in lq_attention_decode_ex
+ * At most 2^28 cached values per stream (the format's 32-bit bit offsets).
+ */
+lq_status lq_attention_decode_rice(int lattice, const uint32_t* k_stream_dev, size_t k_stream_bytes,
+                                   const uint32_t* k_offsets_dev, const void* k_scales_dev,
+                                   const int8_t* k_signs_dev, const uint32_t* v_stream_dev, size_t v_stream_bytes,
+                                   const uint32_t* v_offsets_dev, const void* v_scales_dev,
+                                   const int8_t* v_signs_dev, int scale_format, int64_t tokens, int kv_heads,
+                                   int q_heads, int head_dim, const void* q_dev, int qdtype, float* out_dev,
+                                   void* workspace_dev, size_t workspace_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,6 +40,8 @@ SIGNATURES = {
     "lq_quantize_dithered": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _U64, _F32, _I32, _P, _P, _P,
                                     _P, _P]),
     "lq_dequantize_dithered": (_I32, [_I32, _P, _P, _I32, _P, _U64, _I64, _I64, _I32, _P, _I32, _P]),
+    "lq_attention_decode_rice": (_I32, [_I32, _P, ctypes.c_size_t, _P, _P, _P, _P, ctypes.c_size_t, _P, _P, _P,
+                                        _I32, _I64, _I32, _I32, _I32, _P, _I32, _P, _P, ctypes.c_size_t, _P]),
     "lq_attention_decode_dithered": (_I32, [_I32, _P, _P, _P, _U64, _P, _P, _P, _U64, _I32, _I64, _I32, _I32, _I32,
                                             _P, _I32, _P, _P, ctypes.c_size_t, _P]),
     "lq_gemv_workspace_size": (ctypes.c_size_t, [_I32, _I64, _I32]),
@@ -459,6 +461,18 @@ def lq_attention_decode_dithered(lattice, k_codes, k_scales, k_signs, k_dither_s
         _ptr(v_codes), _ptr(v_scales), _ptr(v_signs), int(v_dither_seed) & 0xFFFFFFFFFFFFFFFF,
         _scale_format_id(scale_format), tokens, kv_heads, q_heads, head_dim, _ptr(q), _dtype_id(q), _ptr(out),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lq_attention_decode_rice(lattice, k_stream, k_offsets, k_scales, k_signs, v_stream, v_offsets, v_scales,
+                             v_signs, scale_format, q, out, workspace, stream=None) -> None:
+    """Decode attention over Rice-coded caches (streams and offsets from lq_rice_encode, tile = head_dim)."""
+    tokens, kv_heads = k_offsets.shape
+    q_heads, head_dim = q.shape
+    _check("lq_attention_decode_rice", _get_lib().lq_attention_decode_rice(
+        _lattice_id(lattice), _ptr(k_stream), k_stream.numel() * k_stream.element_size(), _ptr(k_offsets),
+        _ptr(k_scales), _ptr(k_signs), _ptr(v_stream), v_stream.numel() * v_stream.element_size(), _ptr(v_offsets),
+        _ptr(v_scales), _ptr(v_signs), _scale_format_id(scale_format), tokens, kv_heads, q_heads, head_dim, _ptr(q),
+        _dtype_id(q), _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def lq_rotate_blocks(R, X, Y, transpose: bool = False, stream=None) -> None:

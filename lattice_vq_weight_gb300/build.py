@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "liblq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ("lq_api.cu", "lq_quantize.cu", "lq_quantize_fmt.cu", "lq_quantize_dither.cu", "lq_gemv.cu", "lq_gemm.cu", "lq_rice.cu", "lq_calib.cu", "lq_kv.cu")
+SOURCES = ("lq_api.cu", "lq_quantize.cu", "lq_quantize_fmt.cu", "lq_quantize_dither.cu", "lq_gemv.cu", "lq_gemm.cu", "lq_rice.cu", "lq_calib.cu", "lq_kv.cu", "lq_kv_dither.cu", "lq_kv_rice.cu")
 
 
 def nvcc_path() -> str:

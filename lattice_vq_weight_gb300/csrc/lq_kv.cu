@@ -16,41 +16,10 @@
 // the scores (128 codes against the group's rotated queries), an online
 // softmax, then lane = 4 dimensions for the value sum over those 32 tokens.
 // Kernel 3 merges the ranges and rotates the result back.
-#include <cmath>
-
-#include <cuda_runtime.h>
-#include <cuda_bf16.h>
-
-#include "lq_device.cuh"
-#include "lq_host.h"
+#include "lq_kv_kernel.cuh"
 
 namespace lq {
 namespace kv {
-
-constexpr int D = 128;              // head_dim handled here
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-
-struct AttnArgs {
-  const int8_t* kc;
-  const void* ks;        // [tokens x kv_heads], format sfmt (LQ_SCALE_TILE_F32 / _F16)
-  const int8_t* ksg;
-  const int8_t* vc;
-  const void* vs;
-  const int8_t* vsg;
-  int sfmt;
-  uint64_t kdseed, vdseed;   // subtractive dither seeds (DLAT instantiations)
-  const void* q;
-  int qbf16;
-  int64_t tokens;
-  int kv_heads, group, splits;
-  int a2;
-  float* part;        // [kv_heads x splits x group x (2 + D)]: m, l, acc[D]
-  float* qrot;        // [q_heads x D]: rotated, scaled queries
-  float* out;         // [q_heads x D]
-};
-
-__device__ __forceinline__ float code_f(uint32_t w, int k) { return (float)(int8_t)(w >> (8 * k)); }
 
 // In-place unnormalised Walsh-Hadamard transform of v[0 .. D) in shared memory
 // (Sylvester order), all threads of the block.
@@ -78,194 +47,6 @@ __global__ void __launch_bounds__(D) rotate_query_kernel(AttnArgs a) {
   v[i] = x * (float)a.ksg[kvh * D + i];
   block_fwht(v);
   a.qrot[qi] = v[i] * (0.5f / (float)D) * ((a.a2 && (i & 1)) ? 1.7320508075688772f : 1.f);
-}
-
-// Rows of the per-warp dither transpose (padded: conflict-free 16-byte
-// accesses both by token rows and by dimension columns).
-constexpr int kDvStride = D + 4;
-
-// Dither of one cached vector in the doubled code units the kernel uses
-// (2u; A2 odd coordinates 2u / sqrt 3): element (token, kvh * D + i) of the
-// [tokens x kv_heads * D] cache.
-template <int LAT>
-__device__ __forceinline__ void dither8_codes(uint64_t seed, uint64_t c0, float (&du)[8]) {
-  dither8<LAT>(seed, c0, du);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) du[i] *= (LAT == LQ_A2 && (i & 1)) ? 1.1547005383792515f : 2.f;
-}
-
-// DLAT = 0: caches without dither; otherwise the lattice of dithered caches,
-// whose reconstruction is s (p - u): each score loses q~ . u of its token and
-// the value sum the weighted dither of each token (transposed through shared
-// memory, dynamic: kWarps x 32 x kDvStride floats).
-template <int G, bool F16S, int DLAT>
-__global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(AttnArgs a) {
-  __shared__ __align__(16) float qr[G][D];         // rotated, scaled queries
-  __shared__ float wm[kWarps][G], wl[kWarps][G];
-  __shared__ __align__(16) float wacc[kWarps][G][D];
-  extern __shared__ __align__(16) float dv_smem[];
-  const int kvh = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t ld = (int64_t)a.kv_heads * D;
-  const int64_t j0 = split * a.tokens / a.splits, j1 = (split + 1) * a.tokens / a.splits;
-
-  // the group's rotated queries
-  for (int e = threadIdx.x; e < G * D / 4; e += blockDim.x)
-    reinterpret_cast<float4*>(&qr[0][0])[e] =
-        reinterpret_cast<const float4*>(a.qrot + (int64_t)kvh * a.group * D)[e];
-  __syncthreads();
-
-  float m[G], l[G], acc[G][4];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) acc[g][k] = 0.f;
-  }
-
-  for (int64_t c0 = j0 + (int64_t)warp * 32; c0 < j1; c0 += kWarps * 32) {
-    // issue every load of the chunk first: this lane's token's 128 K codes and
-    // scales (lane = token), and its 4 V codes of each of the chunk's tokens
-    // (lane = dimensions 4 lane .. 4 lane + 3)
-    const int64_t j = c0 + lane;
-    const bool ok = j < j1;
-    const int nt = (j1 - c0) < 32 ? (int)(j1 - c0) : 32;
-    uint4 kw[D / 16];
-    float s_k = 0.f, s_v = 0.f;
-    if (ok) {
-      const uint4* kp = reinterpret_cast<const uint4*>(a.kc + j * ld + (int64_t)kvh * D);
-#pragma unroll
-      for (int q = 0; q < D / 16; ++q) kw[q] = __ldg(kp + q);
-      if constexpr (F16S) {
-        s_k = __half2float(__ldg(reinterpret_cast<const __half*>(a.ks) + j * a.kv_heads + kvh));
-        s_v = __half2float(__ldg(reinterpret_cast<const __half*>(a.vs) + j * a.kv_heads + kvh));
-      } else {
-        s_k = __ldg(reinterpret_cast<const float*>(a.ks) + j * a.kv_heads + kvh);
-        s_v = __ldg(reinterpret_cast<const float*>(a.vs) + j * a.kv_heads + kvh);
-      }
-    } else {
-#pragma unroll
-      for (int q = 0; q < D / 16; ++q) kw[q] = make_uint4(0, 0, 0, 0);
-    }
-    const uint32_t* vp = reinterpret_cast<const uint32_t*>(a.vc + c0 * ld + (int64_t)kvh * D) + lane;
-    uint32_t vw[32];
-#pragma unroll
-    for (int t = 0; t < 32; ++t) vw[t] = (t < nt) ? __ldg(vp + t * (ld / 4)) : 0u;
-
-    // scores
-    float sc[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) sc[g] = 0.f;
-#pragma unroll
-    for (int q = 0; q < D / 16; ++q) {
-      const uint32_t w[4] = {kw[q].x, kw[q].y, kw[q].z, kw[q].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float c0f = code_f(w[e], 0), c1f = code_f(w[e], 1), c2f = code_f(w[e], 2), c3f = code_f(w[e], 3);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qv = *reinterpret_cast<const float4*>(&qr[g][16 * q + 4 * e]);
-          sc[g] = fmaf(c0f, qv.x, fmaf(c1f, qv.y, fmaf(c2f, qv.z, fmaf(c3f, qv.w, sc[g]))));
-        }
-      }
-    }
-    if constexpr (DLAT != 0) {
-      // this lane's token: scores lose q~ . u (K dither); the V dither goes to
-      // the warp's transpose buffer, row = lane
-      float* dvrow = dv_smem + ((size_t)warp * 32 + lane) * kDvStride;
-      const uint64_t cbase = (uint64_t)j * (uint64_t)ld + (uint64_t)kvh * D;
-#pragma unroll 1
-      for (int gb = 0; gb < D / 8; ++gb) {
-        float du[8], dvv[8];
-        if (ok) {
-          dither8_codes<DLAT>(a.kdseed, cbase + 8 * gb, du);
-          dither8_codes<DLAT>(a.vdseed, cbase + 8 * gb, dvv);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) du[i] = dvv[i] = 0.f;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 q0 = *reinterpret_cast<const float4*>(&qr[g][8 * gb]);
-          const float4 q1 = *reinterpret_cast<const float4*>(&qr[g][8 * gb + 4]);
-          float d = q0.x * du[0] + q0.y * du[1] + q0.z * du[2] + q0.w * du[3];
-          d += q1.x * du[4] + q1.y * du[5] + q1.z * du[6] + q1.w * du[7];
-          sc[g] -= d;
-        }
-        *reinterpret_cast<float4*>(dvrow + 8 * gb) = make_float4(dvv[0], dvv[1], dvv[2], dvv[3]);
-        *reinterpret_cast<float4*>(dvrow + 8 * gb + 4) = make_float4(dvv[4], dvv[5], dvv[6], dvv[7]);
-      }
-      __syncwarp();
-    }
-    // online softmax over this chunk
-    float p[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float s = ok ? sc[g] * s_k : -INFINITY;
-      float cm = s;
-      for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-      const float mn = fmaxf(m[g], cm);
-      const float r = __expf(m[g] - mn);         // 0 when m was -inf
-      p[g] = ok ? __expf(s - mn) : 0.f;
-      l[g] = l[g] * r + p[g];                   // per-lane partial sum
-      m[g] = mn;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[g][k] *= r;
-      p[g] *= s_v;                              // the value scale of this lane's token
-    }
-    // values over the chunk's tokens (codes of missing tokens are zero, and so
-    // are their weights)
-#pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const uint32_t w = vw[t];
-      float v0 = code_f(w, 0), v1 = code_f(w, 1), v2 = code_f(w, 2), v3 = code_f(w, 3);
-      if constexpr (DLAT != 0) {
-        const float4 dq = *reinterpret_cast<const float4*>(dv_smem + ((size_t)warp * 32 + t) * kDvStride + 4 * lane);
-        v0 -= dq.x; v1 -= dq.y; v2 -= dq.z; v3 -= dq.w;
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pt = __shfl_sync(0xffffffffu, p[g], t);
-        acc[g][0] = fmaf(pt, v0, acc[g][0]);
-        acc[g][1] = fmaf(pt, v1, acc[g][1]);
-        acc[g][2] = fmaf(pt, v2, acc[g][2]);
-        acc[g][3] = fmaf(pt, v3, acc[g][3]);
-      }
-    }
-    if constexpr (DLAT != 0) __syncwarp();   // the next chunk rewrites the transpose buffer
-  }
-  // merge the four warps
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float ls = l[g];
-    for (int o = 16; o; o >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
-    if (lane == 0) {
-      wm[warp][g] = m[g];
-      wl[warp][g] = ls;
-    }
-    *reinterpret_cast<float4*>(&wacc[warp][g][4 * lane]) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-  }
-  __syncthreads();
-  for (int g = 0; g < G; ++g) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w][g]);
-    float* dst = a.part + (((int64_t)kvh * a.splits + split) * G + g) * (2 + D);
-    for (int i = threadIdx.x; i < D; i += blockDim.x) {
-      float s = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += (wm[w][g] == -INFINITY) ? 0.f : wacc[w][g][i] * __expf(wm[w][g] - M);
-      dst[2 + i] = s;
-    }
-    if (threadIdx.x == 0) {
-      float L = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) L += (wm[w][g] == -INFINITY) ? 0.f : wl[w][g] * __expf(wm[w][g] - M);
-      dst[0] = M;
-      dst[1] = L;
-    }
-  }
 }
 
 // One block per query head: merge the token ranges (weights exp(m_s - M) of
@@ -391,38 +172,22 @@ extern "C" size_t lq_attention_workspace_size(int64_t tokens, int kv_heads, int 
 
 namespace {
 
-constexpr size_t kDvSmem = (size_t)kWarps * 32 * kDvStride * sizeof(float);
-
-template <int G, bool H, int LAT>
-lq_status launch_partial_dithered_g(const AttnArgs& a, unsigned grid, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(attn_partial_kernel<G, H, LAT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kDvSmem) != cudaSuccess) {
-      cudaGetLastError();
-      return LQ_ERR_CUDA;
-    }
-    attr = true;
-  }
-  attn_partial_kernel<G, H, LAT><<<grid, kThreads, kDvSmem, s>>>(a);
-  return LQ_OK;
-}
-
-template <int LAT>
-lq_status launch_partial_dithered(const AttnArgs& a, int group, bool h, unsigned grid, cudaStream_t s) {
-  switch (group) {
-    case 1: return h ? launch_partial_dithered_g<1, true, LAT>(a, grid, s) : launch_partial_dithered_g<1, false, LAT>(a, grid, s);
-    case 2: return h ? launch_partial_dithered_g<2, true, LAT>(a, grid, s) : launch_partial_dithered_g<2, false, LAT>(a, grid, s);
-    case 4: return h ? launch_partial_dithered_g<4, true, LAT>(a, grid, s) : launch_partial_dithered_g<4, false, LAT>(a, grid, s);
-    default: return h ? launch_partial_dithered_g<8, true, LAT>(a, grid, s) : launch_partial_dithered_g<8, false, LAT>(a, grid, s);
-  }
-}
+// K and V caches held as Rice streams (lq_rice_encode with tile = head_dim).
+struct RiceKV {
+  const uint32_t* krs;
+  int64_t knw;
+  const uint32_t* koff;
+  const uint32_t* vrs;
+  int64_t vnw;
+  const uint32_t* voff;
+};
 
 lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_scales_dev,
                         const int8_t* k_signs_dev, const int8_t* v_codes_dev, const void* v_scales_dev,
                         const int8_t* v_signs_dev, int sfmt, int64_t tokens, int kv_heads, int q_heads, int head_dim,
                         const void* q_dev, int qdtype, float* out_dev, void* workspace_dev, size_t workspace_bytes,
-                        void* stream, bool dither = false, uint64_t k_dither_seed = 0, uint64_t v_dither_seed = 0) {
+                        void* stream, bool dither = false, uint64_t k_dither_seed = 0, uint64_t v_dither_seed = 0,
+                        const RiceKV* rice = nullptr) {
   if (!valid_lattice(lattice)) return LQ_ERR_ARG;
   if (sfmt != LQ_SCALE_TILE_F32 && sfmt != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
   const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
@@ -432,12 +197,18 @@ lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_sc
   const int group = q_heads / kv_heads;
   if (group != 1 && group != 2 && group != 4 && group != 8) return LQ_ERR_UNSUPPORTED;
   if (tokens > (int64_t(1) << 31)) return LQ_ERR_SHAPE;
-  if (k_codes_dev == nullptr || k_scales_dev == nullptr || k_signs_dev == nullptr || v_codes_dev == nullptr ||
-      v_scales_dev == nullptr || v_signs_dev == nullptr || q_dev == nullptr || out_dev == nullptr ||
-      workspace_dev == nullptr)
+  if (k_scales_dev == nullptr || k_signs_dev == nullptr || v_scales_dev == nullptr || v_signs_dev == nullptr ||
+      q_dev == nullptr || out_dev == nullptr || workspace_dev == nullptr)
     return LQ_ERR_ARG;
-  if (!aligned16(k_codes_dev) || !aligned16(v_codes_dev) || (reinterpret_cast<uintptr_t>(k_scales_dev) & salign) ||
-      (reinterpret_cast<uintptr_t>(v_scales_dev) & salign) ||
+  if (rice != nullptr) {
+    if (rice->krs == nullptr || rice->koff == nullptr || rice->vrs == nullptr || rice->voff == nullptr ||
+        !aligned4(rice->krs) || !aligned4(rice->koff) || !aligned4(rice->vrs) || !aligned4(rice->voff) ||
+        rice->knw <= 0 || rice->vnw <= 0)
+      return LQ_ERR_ARG;
+  } else if (k_codes_dev == nullptr || v_codes_dev == nullptr || !aligned16(k_codes_dev) || !aligned16(v_codes_dev)) {
+    return LQ_ERR_ARG;
+  }
+  if ((reinterpret_cast<uintptr_t>(k_scales_dev) & salign) || (reinterpret_cast<uintptr_t>(v_scales_dev) & salign) ||
       !aligned4(out_dev) || !aligned4(workspace_dev))
     return LQ_ERR_ARG;
   if (workspace_bytes < lq_attention_workspace_size(tokens, kv_heads, q_heads, head_dim)) return LQ_ERR_SHAPE;
@@ -447,6 +218,8 @@ lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_sc
   a.sfmt = sfmt;
   a.kdseed = k_dither_seed;
   a.vdseed = v_dither_seed;
+  a.krs = rice ? rice->krs : nullptr; a.knw = rice ? rice->knw : 0; a.koff = rice ? rice->koff : nullptr;
+  a.vrs = rice ? rice->vrs : nullptr; a.vnw = rice ? rice->vnw : 0; a.voff = rice ? rice->voff : nullptr;
   a.q = q_dev; a.qbf16 = (qdtype == LQ_BF16);
   a.tokens = tokens; a.kv_heads = kv_heads; a.group = group;
   a.splits = attn_splits(tokens, kv_heads);
@@ -460,26 +233,10 @@ lq_status attention_fmt(int lattice, const int8_t* k_codes_dev, const void* k_sc
   const unsigned grid = (unsigned)(kv_heads * a.splits);
   const bool h = (sfmt == LQ_SCALE_TILE_F16);
   lq_status st = LQ_OK;
-  if (dither) {
-    switch (lattice) {
-      case LQ_E8: st = launch_partial_dithered<LQ_E8>(a, group, h, grid, s); break;
-      case LQ_D4: st = launch_partial_dithered<LQ_D4>(a, group, h, grid, s); break;
-      case LQ_A2: st = launch_partial_dithered<LQ_A2>(a, group, h, grid, s); break;
-      default:    st = launch_partial_dithered<LQ_Z1>(a, group, h, grid, s); break;
-    }
-    if (st != LQ_OK) return st;
-  } else {
-    switch (group) {
-      case 1: h ? attn_partial_kernel<1, true, 0><<<grid, kThreads, 0, s>>>(a)
-                : attn_partial_kernel<1, false, 0><<<grid, kThreads, 0, s>>>(a); break;
-      case 2: h ? attn_partial_kernel<2, true, 0><<<grid, kThreads, 0, s>>>(a)
-                : attn_partial_kernel<2, false, 0><<<grid, kThreads, 0, s>>>(a); break;
-      case 4: h ? attn_partial_kernel<4, true, 0><<<grid, kThreads, 0, s>>>(a)
-                : attn_partial_kernel<4, false, 0><<<grid, kThreads, 0, s>>>(a); break;
-      default: h ? attn_partial_kernel<8, true, 0><<<grid, kThreads, 0, s>>>(a)
-                 : attn_partial_kernel<8, false, 0><<<grid, kThreads, 0, s>>>(a); break;
-    }
-  }
+  if (dither) st = launch_partial_dithered(a, lattice, group, h, grid, s);
+  else if (rice != nullptr) st = launch_partial_rice(a, lattice, group, h, grid, s);
+  else st = launch_partial_groups<0, 0>(a, group, h, grid, s);
+  if (st != LQ_OK) return st;
   st = check_launch();
   if (st != LQ_OK) return st;
   attn_combine_kernel<<<(unsigned)q_heads, D, 0, s>>>(a, group);
@@ -523,6 +280,25 @@ extern "C" lq_status lq_attention_decode_dithered(int lattice, const int8_t* k_c
   return attention_fmt(lattice, k_codes_dev, k_scales_dev, k_signs_dev, v_codes_dev, v_scales_dev, v_signs_dev,
                        scale_format, tokens, kv_heads, q_heads, head_dim, q_dev, qdtype, out_dev, workspace_dev,
                        workspace_bytes, stream, true, k_dither_seed, v_dither_seed);
+}
+
+extern "C" lq_status lq_attention_decode_rice(int lattice, const uint32_t* k_stream_dev, size_t k_stream_bytes,
+                                              const uint32_t* k_offsets_dev, const void* k_scales_dev,
+                                              const int8_t* k_signs_dev, const uint32_t* v_stream_dev,
+                                              size_t v_stream_bytes, const uint32_t* v_offsets_dev,
+                                              const void* v_scales_dev, const int8_t* v_signs_dev, int scale_format,
+                                              int64_t tokens, int kv_heads, int q_heads, int head_dim,
+                                              const void* q_dev, int qdtype, float* out_dev, void* workspace_dev,
+                                              size_t workspace_bytes, void* stream) {
+  LQ_NVTX_RANGE("lq_attention_decode_rice");
+  if (tokens > 0 && kv_heads > 0 && (uint64_t)tokens * (uint64_t)kv_heads * D > ((uint64_t)1 << 28))
+    return LQ_ERR_SHAPE;   // the format's 32-bit bit offsets cover at most 2^28 weights per stream
+  RiceKV r;
+  r.krs = k_stream_dev; r.knw = (int64_t)(k_stream_bytes / 4); r.koff = k_offsets_dev;
+  r.vrs = v_stream_dev; r.vnw = (int64_t)(v_stream_bytes / 4); r.voff = v_offsets_dev;
+  return attention_fmt(lattice, nullptr, k_scales_dev, k_signs_dev, nullptr, v_scales_dev, v_signs_dev, scale_format,
+                       tokens, kv_heads, q_heads, head_dim, q_dev, qdtype, out_dev, workspace_dev, workspace_bytes,
+                       stream, false, 0, 0, &r);
 }
 
 extern "C" lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, const void* X_dev,
