@@ -592,7 +592,7 @@ def gpu_arm(args, ws, rank, local):
         "parts": parts,
         "e2e": {"value": round(e2e_val, 1), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 3)},
-        "roofline": {"kernel": "quantize_kernel (all 7 matrices of the layer)", "bound": "hbm",
+        "roofline": {"kernel": "quantize_kernel (one grouped launch over the 7 matrices of the layer)", "bound": "hbm",
                      "achieved": round(roof_achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(roof_achieved / peak, 4), "peak_source": peak_src,
                      "traffic": traffic},
@@ -745,7 +745,7 @@ def stack_arm(args, ws, rank, local):
         "parts": {"quantize_gbs": round(qgbs, 1), "quantize_ms": round(ms_q, 3),
                   **{f"gemv_b{b}_gbs": round(gb[b] / (ms_g[b] * 1e-3) / 1e9, 1) for b in batches},
                   **{f"gemv_b{b}_ms": round(ms_g[b], 3) for b in batches}},
-        "roofline": {"kernel": "quantize_kernel (224 matrices)", "bound": "hbm", "achieved": round(qgbs, 1),
+        "roofline": {"kernel": "quantize_kernel (224 matrices, one grouped launch per layer)", "bound": "hbm", "achieved": round(qgbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(qgbs / peak, 4), "peak_source": src,
                      "traffic": None},
         "clocks": clk,
