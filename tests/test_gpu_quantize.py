@@ -253,3 +253,44 @@ def test_quantize_grouped_layer_matches_single_calls():
     q = O.quantize(Wd, "e8", 256, O.splitmix64_signs(seeds[6], 14336), 0.25)
     np.testing.assert_allclose(scales[6].cpu().numpy()[rows], q.scales, rtol=1e-6)
     compare_codes(codes[6].cpu().numpy()[rows], q, "e8")
+
+
+@pytest.mark.parametrize("tile", [256, 2048])
+def test_maximum_width_rows(tile):
+    """cols = 2^20, the widest row the ABI takes (512 chunks per row): quantize,
+    dequantize and the batch-16 GEMV against the oracle on the whole matrix."""
+    torch, L = cuda()
+    rows, cols = 3, 1 << 20
+    W = gaussian_matrix(rows, cols, 0.02, 610 + tile, outlier_frac=0.001, dtype="bf16")
+    codes, scales, signs, st = run_quantize(torch, L, W, "bf16", "e8", tile, 611, 0.25)
+    d = O.splitmix64_signs(611, cols)
+    q = O.quantize(W, "e8", tile, d, 0.25)
+    assert st == 0
+    np.testing.assert_allclose(scales, q.scales, rtol=1e-6)
+    compare_codes(codes, q, "e8")
+    What = L.dequantize(to_dev(torch, q.codes), to_dev(torch, q.scales), to_dev(torch, d), lattice="e8", tile=tile)
+    assert normwise_rel(What.cpu().numpy(), O.dequantize(q.codes, q.scales, d, tile, "e8")) < 1e-6
+    x = gaussian_vectors(16, cols, 612, dtype="bf16")
+    y = L.gemv(to_dev(torch, q.codes), to_dev(torch, q.scales), to_dev(torch, d), to_dev_bf16(torch, x),
+               lattice="e8", tile=tile)
+    torch.cuda.synchronize()
+    assert normwise_rel(y.cpu().numpy(), O.gemv(q.codes, q.scales, d, tile, "e8", x)) < 2e-3
+
+
+def test_quantize_grouped_with_a_maximum_width_matrix():
+    """A group whose chunks-per-row counts (512 and 2) have a least common
+    multiple above 64: the warps then change chunk from unit to unit (the
+    signs are reloaded); every matrix still equals the oracle."""
+    torch, L = cuda()
+    shapes = [(3, 1 << 20), (5, 4096), (2, 2048 * 3 + 256)]
+    seeds = [21, 22, 23]
+    Wn = [gaussian_matrix(r, c, 0.02, 620 + i, dtype="bf16") for i, (r, c) in enumerate(shapes)]
+    Ws = [to_dev_bf16(torch, W) for W in Wn]
+    codes, scales, signs, st = _grouped(torch, L, Ws, 256, seeds, 0.25, "e8")
+    assert st == 0
+    for m, W in enumerate(Wn):
+        d = O.splitmix64_signs(seeds[m], W.shape[1])
+        q = O.quantize(W, "e8", 256, d, 0.25)
+        np.testing.assert_array_equal(signs[m].cpu().numpy(), d)
+        np.testing.assert_allclose(scales[m].cpu().numpy(), q.scales, rtol=1e-6)
+        compare_codes(codes[m].cpu().numpy(), q, "e8")
