@@ -23,13 +23,16 @@ template <> struct Fmt<LQ_Z1> { static constexpr int n = 1; static constexpr boo
 __device__ __forceinline__ uint32_t zigzag(int u) { return ((uint32_t)u << 1) ^ (uint32_t)(u >> 31); }
 __device__ __forceinline__ int unzigzag(uint32_t z) { return (int)(z >> 1) ^ -(int)(z & 1u); }
 
-// Sequential reader over the stream, 64-bit window; words past `nwords` read as 0.
+// Sequential reader over the stream, 64-bit window; words past `nwords` read
+// as 0.  The next four words wait in registers (loaded four words before the
+// window needs them), so a refill never waits for memory in the decode chain.
 struct BitReader {
   const uint32_t* w;
   int64_t nwords;
   int64_t word;      // stream word of the window's low half
   uint64_t win;
   int b;             // next bit inside the window, 0 .. 31 between calls
+  uint32_t ahead[4]; // stream words word + 2 .. word + 5
 
   __device__ __forceinline__ uint32_t at(int64_t i) const { return i < nwords ? __ldg(w + i) : 0u; }
   __device__ __forceinline__ void init(const uint32_t* words, int64_t n, uint64_t pos) {
@@ -38,10 +41,16 @@ struct BitReader {
     word = (int64_t)(pos >> 5);
     b = (int)(pos & 31u);
     win = (uint64_t)at(word) | ((uint64_t)at(word + 1) << 32);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ahead[k] = at(word + 2 + k);
   }
   __device__ __forceinline__ void refill() {
     while (b >= 32) {
-      win = (win >> 32) | ((uint64_t)at(word + 2) << 32);
+      win = (win >> 32) | ((uint64_t)ahead[0] << 32);
+      ahead[0] = ahead[1];
+      ahead[1] = ahead[2];
+      ahead[2] = ahead[3];
+      ahead[3] = at(word + 6);
       ++word;
       b -= 32;
     }

@@ -6,6 +6,7 @@
     python -m lattice_vq_weight_gb300.profile_case gemv --batch 1 --gate-up   # one grouped call
     python -m lattice_vq_weight_gb300.profile_case gemm --M 256
     python -m lattice_vq_weight_gb300.profile_case kv --tokens 32768
+    python -m lattice_vq_weight_gb300.profile_case rice --batch 1   # GEMV from the gate matrix's Rice stream
 
 Each op runs `--reps` passes (default 2) after building inputs on the device;
 the second pass is the one to capture (`ncu -s <launches of one pass>`).
@@ -16,7 +17,8 @@ GEMM on the 8192 x 28672 Llama-3-70B up-like shape with X of M rows.  With
 --gate-up the GEMV is one grouped call over the gate and up matrices (as in
 the benchmark's layer step).  kv: one layer of a Llama-3-8B KV cache (8 kv
 heads, 32 query heads, head_dim 128, N(0, 1) K and V, E8, beta 0.25) and the
-decode attention over --tokens cached tokens.
+decode attention over --tokens cached tokens.  rice: the GEMV from the
+Rice stream of a gate-shaped E8 matrix (14336 x 4096, tile 256).
 """
 from __future__ import annotations
 
@@ -31,7 +33,7 @@ if ROOT not in sys.path:
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("op", choices=("quantize", "gemv", "gemm", "kv"))
+    ap.add_argument("op", choices=("quantize", "gemv", "gemm", "kv", "rice"))
     ap.add_argument("--tokens", type=int, default=32768)
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--M", type=int, default=256)
@@ -58,6 +60,23 @@ def main(argv=None):
         ws = torch.empty(L.lq_attention_workspace_size(args.tokens, 8, 32, 128), dtype=torch.uint8, device=dev)
         for _ in range(args.reps):
             L.lq_attention_decode("e8", kc, ks, kd, vc, vs, vd, q, out, ws)
+        torch.cuda.synchronize()
+        print("ok")
+        return
+    if args.op == "rice":
+        W = (torch.randn((14336, 4096), device=dev, generator=gen) * 0.02).to(torch.bfloat16)
+        codes, scales, signs = L.quantize(W, "e8", 256, 1, 0.25)
+        nb = L.lq_rice_stream_bound("e8", 14336, 4096, 256)
+        words = torch.empty(nb // 4, dtype=torch.int32, device=dev)
+        offs = torch.empty((14336, 16), dtype=torch.int32, device=dev)
+        tot = torch.empty(1, dtype=torch.int64, device=dev)
+        rws = torch.empty(L.lq_rice_workspace_size(14336, 4096, 256), dtype=torch.uint8, device=dev)
+        L.lq_rice_encode("e8", codes, 256, words, offs, tot, rws)
+        x = torch.randn((args.batch, 4096), device=dev, generator=gen).to(torch.bfloat16)
+        y = torch.empty((args.batch, 14336), dtype=torch.float32, device=dev)
+        ws = torch.empty(L.lq_gemv_workspace_size(args.batch, 4096, 256), dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            L.lq_gemv_rice("e8", words, offs, scales, signs, 256, x, y, ws)
         torch.cuda.synchronize()
         print("ok")
         return
