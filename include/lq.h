@@ -167,8 +167,8 @@ size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile);
  *   batch     1 .. 16
  *   y_dev     float32 [batch x rows] (overwritten)
  *   workspace_dev  lq_gemv_workspace_size(batch, cols, tile) bytes, 16-byte aligned
- *   dev_status_dev  int32 status word or NULL (LQ_DEV_RANGE if a rotated
- *             activation does not fit the fp16 split)
+ *   dev_status_dev  int32 status word or NULL (LQ_DEV_NONFINITE if an
+ *             activation row holds a non-finite value; y is then unspecified)
  * Two kernels run on `stream`: the activation rotation, then the product.
  */
 lq_status lq_gemv(int lattice, const int8_t* codes_dev, const float* scales_dev,

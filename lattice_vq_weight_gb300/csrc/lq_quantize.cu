@@ -104,14 +104,14 @@ struct DequantArgs {
   float inv_2sqrt_tile;
   void* out;
   int64_t units;
-  int dither;             // subtract the subtractive dither of seed dither_seed
+  int dither;             // subtract the subtractive dither of seed dither_seed (selects the DITHER kernel)
   uint64_t dither_seed;
 };
 
 // W^ = D H (s p) / sqrt(T): codes -> (A2: odd coordinates x sqrt3) -> FWHT
 // (integer-exact for the doubled codes) -> x s / (2 sqrt T) -> signs; with a
 // dither, p - u replaces p (2u in the doubled code units).
-template <int LAT, bool OUT_BF16>
+template <int LAT, bool OUT_BF16, bool DITHER>
 __global__ void __launch_bounds__(256, 1) dequantize_kernel(DequantArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(256, 1) dequantize_kernel(DequantArgs a) {
         }
       }
     }
-    if (a.dither && active) {
+    if (DITHER && active) {
 #pragma unroll
       for (int gb = 0; gb < 8; ++gb) {
         float du[8];
@@ -407,14 +407,19 @@ extern "C" lq_status lq_quantize_grouped(int lattice, int n, const void* const* 
                         dev_status_dev, LQ_SCALE_TILE_F32, true, (cudaStream_t)stream);
 }
 
-template <int LAT, bool OB>
-static lq_status launch_dequant(const DequantArgs& a, cudaStream_t st) {
+template <int LAT, bool OB, bool DITHER>
+static lq_status launch_dequant_d(const DequantArgs& a, cudaStream_t st) {
   static int per_sm = 0;
-  if (per_sm == 0) per_sm = occupancy_per_sm(dequantize_kernel<LAT, OB>, 256);
+  if (per_sm == 0) per_sm = occupancy_per_sm(dequantize_kernel<LAT, OB, DITHER>, 256);
   const int grid = persistent_grid(a.units, 8, 1, per_sm);
   if (grid <= 0) return LQ_ERR_CUDA;
-  dequantize_kernel<LAT, OB><<<grid, 256, 0, st>>>(a);
+  dequantize_kernel<LAT, OB, DITHER><<<grid, 256, 0, st>>>(a);
   return check_launch();
+}
+
+template <int LAT, bool OB>
+static lq_status launch_dequant(const DequantArgs& a, cudaStream_t st) {
+  return a.dither ? launch_dequant_d<LAT, OB, true>(a, st) : launch_dequant_d<LAT, OB, false>(a, st);
 }
 
 namespace {
