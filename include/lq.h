@@ -53,7 +53,7 @@ typedef enum {
     LQ_ERR_SHAPE = 2,       /* sizes inconsistent or out of the supported range */
     LQ_ERR_DTYPE = 3,       /* unsupported element type */
     LQ_ERR_CUDA = 4,        /* a CUDA runtime call failed (launch, attribute, ...) */
-    LQ_ERR_UNSUPPORTED = 5  /* valid request that this build does not implement */
+    LQ_ERR_UNSUPPORTED = 5  /* valid request that this library does not implement */
 } lq_status;
 
 /* Bits OR-ed into the device status word by the kernels. */

@@ -10,7 +10,7 @@ extern "C" const char* lq_status_string(int status) {
     case LQ_ERR_SHAPE: return "invalid or unsupported shape";
     case LQ_ERR_DTYPE: return "unsupported element type";
     case LQ_ERR_CUDA: return "CUDA runtime error";
-    case LQ_ERR_UNSUPPORTED: return "not supported by this build";
+    case LQ_ERR_UNSUPPORTED: return "not supported by this library";
     default: return "unknown status";
   }
 }
