@@ -62,6 +62,18 @@ struct BitReader {
     return v;
   }
   __device__ __forceinline__ uint32_t rice(int K) {
+    // common case: the run of ones, its closing zero and the K low bits all lie
+    // in the window's next 32 bits (b <= 31 between calls)
+    const uint32_t lo = (uint32_t)(win >> b);
+    if (~lo != 0u) {
+      const int t = __ffs((int)~lo) - 1;           // ones before the first zero
+      if (t + 1 + K <= 32) {
+        const uint32_t v = ((uint32_t)t << K) | ((uint32_t)((uint64_t)lo >> (t + 1)) & ((1u << K) - 1u));
+        b += t + 1 + K;
+        refill();
+        return v;
+      }
+    }
     uint32_t q = 0;
     while (true) {
       const uint64_t x = ~(win >> b);            // valid bits inverted; the vacated top bits read as 1
