@@ -44,6 +44,18 @@ struct BitReader {
 #pragma unroll
     for (int k = 0; k < 4; ++k) ahead[k] = at(word + 2 + k);
   }
+  // one refill step: enough whenever b < 64
+  __device__ __forceinline__ void refill1() {
+    if (b >= 32) {
+      win = (win >> 32) | ((uint64_t)ahead[0] << 32);
+      ahead[0] = ahead[1];
+      ahead[1] = ahead[2];
+      ahead[2] = ahead[3];
+      ahead[3] = at(word + 6);
+      ++word;
+      b -= 32;
+    }
+  }
   __device__ __forceinline__ void refill() {
     while (b >= 32) {
       win = (win >> 32) | ((uint64_t)ahead[0] << 32);
@@ -57,8 +69,8 @@ struct BitReader {
   }
   __device__ __forceinline__ uint32_t get(int nbits) {   // nbits <= 32
     const uint32_t v = (uint32_t)(win >> b) & (uint32_t)((1ull << nbits) - 1ull);
-    b += nbits;
-    refill();
+    b += nbits;   // at most 31 + 32
+    refill1();
     return v;
   }
   __device__ __forceinline__ uint32_t rice(int K) {
@@ -69,8 +81,8 @@ struct BitReader {
       const int t = __ffs((int)~lo) - 1;           // ones before the first zero
       if (t + 1 + K <= 32) {
         const uint32_t v = ((uint32_t)t << K) | ((uint32_t)((uint64_t)lo >> (t + 1)) & ((1u << K) - 1u));
-        b += t + 1 + K;
-        refill();
+        b += t + 1 + K;   // at most 31 + 32
+        refill1();
         return v;
       }
     }
