@@ -11,11 +11,13 @@
 //     sum_j p_j v^_j = D H (sum_j p_j s_j c~_j) / (2 sqrt d)
 //                                      (accumulate codes in the rotated domain,
 //                                       rotate back once per head)
-// Kernel 1 rotates the queries.  Kernel 2 (one CTA per kv head and token
-// range, four warps): each warp takes 32 tokens at a time -- lane = token for
-// the scores (128 codes against the group's rotated queries), an online
-// softmax, then lane = 4 dimensions for the value sum over those 32 tokens.
-// Kernel 3 merges the ranges and rotates the result back.
+// Kernel 1 rotates the queries.  Kernel 2 (attn_partial_kernel in
+// lq_kv_kernel.cuh; one CTA per kv head and token range, four warps): each
+// warp takes 32 tokens at a time -- lane = token for the scores (128 codes
+// against the group's rotated queries), an online softmax, then lane = 4
+// dimensions for the value sum over those 32 tokens; its variants subtract a
+// subtractive dither or decode Rice-coded caches on chip.  Kernel 3 merges
+// the ranges and rotates the result back.
 #include "lq_kv_kernel.cuh"
 
 namespace lq {
