@@ -129,6 +129,12 @@ def test_argument_errors_are_synchronous():
                                       s) == L.LQ_ERR_ARG
     assert lib.lq_attention_decode_dithered(8, good, good, good, 1, good, good, good, 2, L.LQ_SCALE_ROW_BF16, 16, 1,
                                             1, 128, good, 1, good, good, ctypes.c_size_t(1 << 20), s) == L.LQ_ERR_ARG
+    # Rice-coded caches: streams and offsets required; 2^28 values per stream at most
+    ar = lambda ks, tokens: lib.lq_attention_decode_rice(8, ks, ctypes.c_size_t(1024), good, good, good, good,
+                                                         ctypes.c_size_t(1024), good, good, good, 0, tokens, 1, 1,
+                                                         128, good, 1, good, good, ctypes.c_size_t(1 << 30), s)
+    assert ar(nul, 16) == L.LQ_ERR_ARG
+    assert ar(good, (1 << 21) + 1) == L.LQ_ERR_SHAPE
     # Rice format: worst case 8 bits per symbol + parity bits + 3 bits per segment, 16 bytes of padding
     assert L.lq_rice_stream_bound("e8", 2, 256, 256) == ((2 * 3 + 2 * 256 * 8 + 2 * 32 + 31) // 32) * 4 + 16
     assert L.lq_rice_stream_bound("e8", 1 << 15, 1 << 14, 256) == 0          # more than 2^28 weights
