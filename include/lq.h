@@ -6,9 +6,10 @@
  *
  * Method source: HyperQuant (github release page of moonmath-ai/HyperQuant),
  * sections "Key algorithmic ingredients" (per-tile RHT, E8/D4/A2/Z1 lattice VQ),
- * the mma="int8" paragraph (codes decoded into int8; RHT of the activation on
- * every forward; no bf16 weight written), the mma="bf16" paragraph (decode
- * straight into partial dot products) and "Hadamard block size" (tile rule).
+ * the mma="int8" paragraph (codes expanded to int8 on chip, the activation
+ * rotated at each forward, the weight never materialised in bf16), the
+ * mma="bf16" paragraph (the product accumulated from the codes as they are
+ * decoded) and "Hadamard block size" (tile rule).
  * Nearest-point algorithms: Conway & Sloane, Sphere Packings, Lattices and
  * Groups, ch. 20.
  *
@@ -159,8 +160,8 @@ size_t lq_gemv_workspace_size(int batch, int64_t cols, int tile);
 
 /*
  * Decode-side product y = W^ x from the codes (HyperQuant page, mma="bf16"
- * paragraph: decoding straight into partial dot products; mma="int8"
- * paragraph: the activation goes through the RHT on every forward):
+ * paragraph: the product is accumulated from the codes, no decoded weight is
+ * stored; mma="int8" paragraph: the activation is rotated at each forward):
  *     y[b, r] = sum_t s[r, t] * sum_i p[r, t, i] * x~[b, t, i],
  *     x~ = H D x / sqrt(tile) per tile.
  *   x_dev     [batch x cols] of type xdtype (LQ_BF16 or LQ_F32), row stride cols
@@ -263,8 +264,9 @@ lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
 /*
  * ------------------------------------------------------------------------
  * Rice format of the codes (HyperQuant page, "Key algorithmic ingredients":
- * lossless bit-stripping, then Rice entropy codes; mma="bf16" paragraph: the
- * weight kept as a ~4 bps bitstream that the GEMV decodes directly).  The
+ * the bits the lattice fixes are dropped, the rest Rice coded; mma="bf16"
+ * paragraph: the weight stored as that ~4 bps stream and read by the GEMV
+ * without an int8 copy).  The
  * pages fix no layout; this library's format is:
  *  - per block of n codes: E8 and A2 store the block's common parity as one raw
  *    bit, then the halved codes u_i = floor(c_i / 2); D4 and Z1 codes are even
@@ -328,9 +330,9 @@ lq_status lq_gemv_rice(int lattice, const uint32_t* stream_dev, size_t stream_by
 
 /*
  * ------------------------------------------------------------------------
- * Rate / SNR calibration (HyperQuant page, usage section and "bps" table: a
- * calibration sweep maps a target rate in bits per scalar to an SNR, and the
- * lattice scale follows from a target SNR).  SNR = 10 log10(sum w^2 /
+ * Rate / SNR calibration (HyperQuant page, usage section and "bps" table: rates
+ * in bits per scalar are related to SNRs by measurement, and the lattice
+ * scale is set from a target SNR).  SNR = 10 log10(sum w^2 /
  * sum (w - w^)^2) in dB.
  * ------------------------------------------------------------------------
  */
@@ -417,8 +419,8 @@ lq_status lq_rotate_blocks(const float* R_dev, int transpose, int head_dim, cons
  *   LQ_SCALE_TILE_F32  float32 [rows x cols/tile]: the format of the calls above.
  *   LQ_SCALE_ROW_BF16  bfloat16 [rows] (raw 16-bit patterns): one scale per row,
  *                      s_r = beta * RMS of the whole row (HyperQuant page,
- *                      mma="int8" paragraph: row-normalised weights stored
- *                      with a bf16 per-row scale).
+ *                      mma="int8" paragraph: each output row normalised by
+ *                      its own statistic, one bf16 scale stored per row).
  *   LQ_SCALE_TILE_F16  float16 [rows x cols/tile] (raw 16-bit patterns): the
  *                      per-tile scale in half precision (the page's KV cache:
  *                      int8 codes with fp16 norms).
@@ -469,7 +471,7 @@ lq_status lq_attention_decode_ex(int lattice, const int8_t* k_codes_dev, const v
 /*
  * ------------------------------------------------------------------------
  * Subtractive Voronoi dither (HyperQuant page, "Key algorithmic ingredients":
- * a subtractive dither keeps the KV cache's inner products unbiased; Zamir &
+ * one of two listed ways to keep the cache's inner products unbiased; Zamir &
  * Feder, "On lattice quantization noise", 1996: the reconstruction error is
  * then uniform over the lattice cell and independent of the input).
  * Element (r, k) of a [rows x cols] matrix draws w = (top 24 bits of SplitMix64

@@ -1,8 +1,8 @@
 // Rate / SNR calibration of the lattice quantizer.
 //
 // HyperQuant page, usage section and "bps" table: the quantizer runs on a
-// continuous bits-per-scalar axis; a calibration sweep maps a target rate to
-// the SNR it reaches, and the lattice scale follows from a target SNR.
+// continuous bits-per-scalar axis; rates are related to the SNRs they reach
+// by measurement, and the lattice scale is set from a target SNR.
 //
 //  - lq_beta_for_snr: high-resolution closed form.  The error per coordinate of
 //    a lattice quantizer with cell volume V and normalised second moment G at

@@ -1,8 +1,8 @@
 // Decode-side GEMV: y = W^ x computed from the lattice codes.
 //
-// HyperQuant page, mma="bf16" paragraph: the product decodes the stored weight
-// straight into partial dot products (no decoded weight in memory); mma="int8"
-// paragraph: the activation goes through the RHT on every forward.
+// HyperQuant page, mma="bf16" paragraph: the product is accumulated from the
+// codes as they are read (no decoded weight in memory); mma="int8" paragraph:
+// the activation is rotated at each forward.
 //
 //   y[b, r] = sum_t s[r, t] * sum_i p[r, t, i] * x~[b, t, i],  x~ = H D x / sqrt(T).
 //

@@ -1,10 +1,10 @@
 // Rice format of lattice codes: encoder, decoder and the GEMV that reads the
 // stream directly.
 //
-// HyperQuant page, "Key algorithmic ingredients": lossless bit-stripping of the
-// bits the lattice pins, then variable-length Rice codes over the unbounded
-// integers; mma="bf16" paragraph: the weight is kept as that bitstream (~4 bps)
-// and the GEMV decodes it straight into partial dot products.  Rice codes:
+// HyperQuant page, "Key algorithmic ingredients": the bits the lattice fixes
+// are dropped without loss and the remaining integers Rice coded; mma="bf16"
+// paragraph: the weight is stored as that stream (~4 bps) and the GEMV reads
+// it without an int8 copy.  Rice codes:
 // R. F. Rice, JPL Publication 79-22 (1979).
 //
 // Format (see include/lq.h): per (row, tile) one segment -- K in 3 bits, then

@@ -6,8 +6,8 @@ CUDA path.
 
 Source: HyperQuant (github release page of moonmath-ai/HyperQuant), usage
 section and "bps" table: the quantizer runs on a continuous bits-per-scalar
-axis; a calibration sweep maps a target rate (bps) to the SNR it reaches, and
-a lattice scale ("alpha") is derived from a target SNR.  The pages give the
+axis; rates (bps) are related to the SNRs they reach by measurement, and a
+lattice scale ("alpha") is set from a target SNR.  The pages give the
 calls, not the procedure; the readings taken here (also in the design notes):
 
 * SNR of a quantized matrix: 10 log10(sum w^2 / sum (w - w^)^2), in dB.

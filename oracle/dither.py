@@ -6,9 +6,9 @@ no code with the CUDA path.
 Sources, cited by page and section:
 
 * HyperQuant (github release page of moonmath-ai/HyperQuant), "Key algorithmic
-  ingredients", bias correction: a QJL rotation and/or a subtractive Voronoi
-  dither keep the KV cache's inner products unbiased; its file list names the
-  KV quantizer's rotation and dither.
+  ingredients": two ways, usable together, to keep the cache's inner products
+  unbiased -- a QJL rotation and a subtractive dither over the lattice cell;
+  its file list names the cache quantizer's rotation and dither.
 * Subtractive dither with a lattice (Zamir & Feder, "On lattice quantization
   noise", IEEE Trans. Inf. Theory 42, 1996): with u uniform over the Voronoi
   cell V of the lattice and independent of x, the error Q(x + u) - u - x is

@@ -18,8 +18,8 @@ readings taken (also listed in the design notes):
 * Decode attention of query head h (kv head h // group, group = q_heads /
   kv_heads): o_h = softmax(K^_h q_h / sqrt(head_dim)) V^_h over all tokens,
   with K^, V^ the dequantized caches -- the textbook definition, float64.
-* The "qjl" rotation (Haar-uniform, "strictly unbiased inner products on
-  average"): a Haar orthogonal matrix Q [d x d] drawn as the Q factor of a
+* The "qjl" rotation (a Haar-uniform rotation whose inner products are
+  unbiased on average, per the page): a Haar orthogonal matrix Q [d x d] drawn as the Q factor of a
   Gaussian matrix with the signs of R's diagonal folded in (Mezzadri, "How to
   generate random matrices from the classical compact groups", Notices AMS
   2007), applied to every head vector (x -> Q x) before the quantizer's own

@@ -396,8 +396,8 @@ def gemv(codes, scales, signs, T, lattice, x) -> np.ndarray:
     """y[b, r] = sum_t s32[r, t] * sum_i p[r, t, i] * x~[b, t, i]  (float64 [batch, rows]).
 
     The decode-side product computed from the codes, never materialising W^
-    (HyperQuant page, "mma='bf16'" paragraph: decoding straight into partial
-    dot products).
+    (HyperQuant page, "mma='bf16'" paragraph: the product is accumulated from
+    the codes; no decoded weight is stored).
     """
     return _tile_sum_product(codes, scales, signs, T, lattice, x)
 
