@@ -104,3 +104,21 @@ def test_attention_dithered(lattice, tokens, kv_heads, group, fmt):
     Vh = D.dequantize_dithered(vc.cpu().numpy(), vs.float().cpu().numpy(), dv, 128, lattice, 2222)
     ref = KV.attention_decode(q, Kh, Vh, kv_heads, 128)
     assert normwise_rel(out.cpu().numpy(), ref) < 2e-3
+
+
+def test_quantize_dithered_fp32_input():
+    """fp32 weights (the fp32 load path) with the dither, tile 256, E8 and D4."""
+    torch, L = cuda()
+    from tests.gpu_util import to_dev
+    W = gaussian_matrix(21, 1280, 0.02, 540, outlier_frac=0.002, dtype="fp32")
+    d = O.splitmix64_signs(63, 1280)
+    for lattice in ("e8", "d4"):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        codes, scales, signs = L.quantize_dithered(to_dev(torch, W.astype(np.float32)), lattice=lattice, tile=256,
+                                                   seed=63, dither_seed=77, beta=0.25, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        got_s = scales.cpu().numpy()
+        q = D.quantize_dithered(W, lattice, 256, d, 0.25, 77)
+        np.testing.assert_allclose(got_s, q.scales, rtol=1e-6, atol=0)
+        compare_codes(codes.cpu().numpy(), dithered_reference(W, lattice, 256, d, 77, got_s, "tile_f32"), lattice)
