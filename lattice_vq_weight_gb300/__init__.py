@@ -373,7 +373,7 @@ def lq_quantize_ex(lattice, W, tile: int, seed: int, beta: float, scale_format, 
 
 
 def quantize_ex(W, lattice: str = "e8", tile: int = 256, seed: int = 0, beta: float = 0.25,
-                scale_format="row_bf16", dev_status=None, stream=None):
+                scale_format="tile_f32", dev_status=None, stream=None):
     """Allocate outputs and call :func:`lq_quantize_ex`; returns (codes, scales, signs)."""
     import torch
     rows, cols = W.shape
