@@ -461,7 +461,8 @@ __device__ __forceinline__ float dither_w(uint64_t seed, uint64_t counter) {
   uint64_t z = seed + (counter + 1) * 0x9E3779B97F4A7C15ull;
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
   z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  z ^= z >> 31;
+  // the generator's last step, z ^= z >> 31, leaves bits 63 .. 40 unchanged
+  // (it only flips bits below 33), so the top 24 bits are read before it
   return (float)(uint32_t)(z >> 40) * (1.0f / 16777216.0f);
 }
 
