@@ -535,23 +535,33 @@ def gemm(codes, scales, signs, X, lattice: str = "e8", tile: int = 256, workspac
 CHECKPOINT_FORMAT = "lq-codes-v1"
 
 
-def save_quantized(path, codes, scales, signs, lattice: str, tile: int, seed: int, beta: float) -> None:
+def save_quantized(path, codes, scales, signs, lattice: str, tile: int, seed: int, beta: float,
+                   scale_format="tile_f32", dither_seed=None) -> None:
     """Write codes, scales and signs with the header needed to use them again
-    (lattice, tile, seed, beta, shape) in one torch.save file."""
+    (lattice, tile, seed, beta, shape, scale format, and the dither seed of a
+    dithered quantization or None) in one torch.save file."""
     import torch
+    fmt = {v: k for k, v in _SCALE_FORMATS.items()}.get(_scale_format_id(scale_format))
+    if fmt is None:
+        raise ValueError(f"unknown scale format {scale_format!r}")
     torch.save({"format": CHECKPOINT_FORMAT, "lattice": str(lattice), "tile": int(tile), "seed": int(seed),
-                "beta": float(beta), "shape": list(codes.shape), "codes": codes.detach().cpu(),
+                "beta": float(beta), "shape": list(codes.shape), "scale_format": fmt,
+                "dither_seed": None if dither_seed is None else int(dither_seed), "codes": codes.detach().cpu(),
                 "scales": scales.detach().cpu(), "signs": signs.detach().cpu()}, path)
 
 
 def load_quantized(path, device=None) -> dict:
-    """Read a file written by :func:`save_quantized`; tensors moved to `device` when given."""
+    """Read a file written by :func:`save_quantized`; tensors moved to `device` when given.
+    Files written before the scale formats existed read as float32 tile scales."""
     import torch
     d = torch.load(path, map_location="cpu", weights_only=True)
     if d.get("format") != CHECKPOINT_FORMAT:
         raise ValueError(f"{path}: not a {CHECKPOINT_FORMAT} file")
+    d.setdefault("scale_format", "tile_f32")
+    d.setdefault("dither_seed", None)
     rows, cols = d["shape"]
-    if tuple(d["codes"].shape) != (rows, cols) or tuple(d["scales"].shape) != (rows, cols // d["tile"]) \
+    want_scales = (rows,) if d["scale_format"] == "row_bf16" else (rows, cols // d["tile"])
+    if tuple(d["codes"].shape) != (rows, cols) or tuple(d["scales"].shape) != want_scales \
             or tuple(d["signs"].shape) != (cols,):
         raise ValueError(f"{path}: tensor shapes do not match the header")
     if device is not None:
