@@ -92,3 +92,29 @@ def test_rate_near_four_bits_at_beta_quarter():
     words, offs, total = R.encode(q.codes, "e8", 256)
     bps = R.bits_per_weight(total, 4, 2048)
     assert 3.6 < bps < 4.6, bps
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+def test_round_trip_on_arbitrary_lattice_codes(lattice):
+    """Random valid codes of any size (not only what the quantizer produces at
+    beta = 1/4: runs far longer than K, codes near the int8 ends) survive
+    encode -> decode, and every segment decodes from its own offset alone."""
+    rng = np.random.default_rng(11)
+    n = O.LATTICE_DIM[lattice]
+    rows, T = 5, 128
+    for scale in (0.3, 3.0, 30.0):
+        y = rng.standard_normal((rows, T * 3)) * scale
+        p = O.nearest_point(lattice, y.reshape(rows, -1, n)).reshape(rows, -1)
+        c = O.point_to_codes(lattice, p.reshape(rows, -1, n)).reshape(rows, -1)
+        c = np.clip(c, -127, 127)
+        ok = O.code_membership_ok(lattice, c.reshape(-1, n)).reshape(rows, -1).all(axis=1)
+        c = c[ok]                                   # rows whose clipping left them lattice codes
+        if len(c) == 0:
+            continue
+        words, offsets, total = R.encode(c.astype(np.int8), lattice, T)
+        back = R.decode(words, offsets, lattice, T)
+        np.testing.assert_array_equal(back, c)
+        for r in range(c.shape[0]):
+            for t in range(c.shape[1] // T):
+                seg = R.decode_segment(words, int(offsets[r, t]), lattice, T)
+                np.testing.assert_array_equal(seg, c[r, t * T:(t + 1) * T])
