@@ -446,7 +446,10 @@ def pick_tile(cols: int, requested: int, allowed=(256, 512, 1024, 2048)) -> int:
 
 
 def code_entropy_bits(codes: np.ndarray) -> float:
-    """Empirical zeroth-order entropy of the code values (bits per scalar)."""
+    """Empirical zeroth-order entropy of the code values (bits per scalar):
+    H = -sum_v p(v) log2 p(v) over the relative counts p(v) of each value
+    (Shannon 1948).  Pinned to hand-worked cases (tests/golden/
+    entropy_hand_cases.json) and to the bounds 0 <= H <= log2(#values)."""
     vals, counts = np.unique(np.asarray(codes).ravel(), return_counts=True)
     p = counts / counts.sum()
     return float(-(p * np.log2(p)).sum())

@@ -317,3 +317,29 @@ def test_tile_rule_matches_page(golden_dir):
     f = _load(golden_dir, "pages_figures.json")["hadamard_tile_sizes"]
     for c in f["cases"]:
         assert O.pick_tile(c["cols"], c["requested"], tuple(f["allowed"])) == c["expect"], c
+
+
+def test_code_entropy_matches_hand_worked_cases(golden_dir):
+    """code_entropy_bits against entropies worked out by hand from the counts
+    (tests/golden/entropy_hand_cases.json): a dropped minus sign, a natural log
+    in place of log2, or counting distinct values instead of occurrences each
+    fail one of them."""
+    with open(os.path.join(golden_dir, "entropy_hand_cases.json")) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        got = O.code_entropy_bits(np.asarray(case["codes"], dtype=np.int8))
+        assert abs(got - case["bits"]) < 1e-12, (case, got)
+
+
+def test_code_entropy_bounds_and_relabelling():
+    """0 <= H <= log2(number of distinct values), with equality for equal counts,
+    and H does not depend on which int8 values carry the counts."""
+    rng = np.random.default_rng(3)
+    c = rng.integers(-20, 21, size=5000).astype(np.int8)
+    h = O.code_entropy_bits(c)
+    assert 0.0 < h <= np.log2(len(np.unique(c))) + 1e-12
+    perm = rng.permutation(np.arange(-20, 21))
+    relabelled = perm[c.astype(np.int64) + 20].astype(np.int8)
+    assert abs(O.code_entropy_bits(relabelled) - h) < 1e-12
+    equal = np.repeat(np.arange(-16, 16), 7).astype(np.int8)
+    assert abs(O.code_entropy_bits(equal) - 5.0) < 1e-12

@@ -98,19 +98,23 @@ def test_rate_near_four_bits_at_beta_quarter():
 def test_round_trip_on_arbitrary_lattice_codes(lattice):
     """Random valid codes of any size (not only what the quantizer produces at
     beta = 1/4: runs far longer than K, codes near the int8 ends) survive
-    encode -> decode, and every segment decodes from its own offset alone."""
+    encode -> decode, and every segment decodes from its own offset alone.
+
+    The largest case scales y so that max |y| = 59: every code 2 p then stays
+    within |2 y| + 3 <= 121 < 127 (no clipping, so every row is a lattice code)
+    and reaches past 100 in magnitude."""
     rng = np.random.default_rng(11)
     n = O.LATTICE_DIM[lattice]
     rows, T = 5, 128
-    for scale in (0.3, 3.0, 30.0):
-        y = rng.standard_normal((rows, T * 3)) * scale
+    for case in ("small", "medium", "int8_ends"):
+        y = rng.standard_normal((rows, T * 3))
+        y *= {"small": 0.3, "medium": 3.0}.get(case, 59.0 / np.abs(y).max())
         p = O.nearest_point(lattice, y.reshape(rows, -1, n)).reshape(rows, -1)
         c = O.point_to_codes(lattice, p.reshape(rows, -1, n)).reshape(rows, -1)
-        c = np.clip(c, -127, 127)
-        ok = O.code_membership_ok(lattice, c.reshape(-1, n)).reshape(rows, -1).all(axis=1)
-        c = c[ok]                                   # rows whose clipping left them lattice codes
-        if len(c) == 0:
-            continue
+        assert np.abs(c).max() <= 127
+        assert O.code_membership_ok(lattice, c.reshape(-1, n)).all()
+        if case == "int8_ends":
+            assert np.abs(c).max() >= 100, np.abs(c).max()
         words, offsets, total = R.encode(c.astype(np.int8), lattice, T)
         back = R.decode(words, offsets, lattice, T)
         np.testing.assert_array_equal(back, c)
