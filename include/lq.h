@@ -215,10 +215,15 @@ lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* codes_dev,
  * a fixed array of LQ_GEMV_NOALLOC_MAX_WORKSPACE bytes inside the library's
  * device image: every GPU that loads the library holds it until the process
  * exits.  Requests whose lq_gemv_workspace_size(batch, cols, tile) exceeds that
- * size return LQ_ERR_SHAPE before anything is launched (for example batch 16
- * with cols up to 65536 fits).  The first call on a device looks the array's
- * device address up (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Nothing is allocated by this call.  All calls share the one
+ * size return LQ_ERR_SHAPE before anything is launched: a request fits when
+ * align256(batch * cols * 2) + align256(batch * (cols / tile) * 4) <=
+ * LQ_GEMV_NOALLOC_MAX_WORKSPACE (align256 rounds up to a multiple of 256), for
+ * example batch 16 with cols = 131072 at any tile >= 128.  The first call on a
+ * device looks the array's device address up (cudaGetSymbolAddress); make that
+ * first call before any stream capture.  The address is looked up again when
+ * the device's current context changes (after cudaDeviceReset the array may
+ * sit elsewhere); that call too should come before any stream capture.
+ * Nothing is allocated by this call.  All calls share the one
  * array, so calls that may overlap on the GPU (different streams without
  * ordering between them) race and must not be issued; calls on one stream are
  * ordered and safe.  The array keeps the previous call's contents; the call
@@ -231,16 +236,19 @@ lq_status lq_gemv_noalloc(int lattice, const int8_t* codes_dev, const float* sca
                           int32_t* dev_status_dev, void* stream);
 
 /*
- * Workspace bytes lq_gemm needs: the rotated activations X~ as fp16 [M x K],
- * one float per token row and one float per weight row.
+ * Workspace bytes lq_gemm needs for an output of type ydtype (LQ_F32 or
+ * LQ_BF16): the rotated activations X~ as fp16 [M x K], one float per token
+ * row and one per weight row, and for a bf16 output the float32 sums [M x N]
+ * that the K splits of the launch add into before the final rounding.
+ * 0 for an invalid ydtype or a non-positive size.
  */
-size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
+size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int ydtype);
 
 /*
  * Prefill product Y[M x N] = X W^T from the lattice codes of W [N x K]
  * (HyperQuant page, mma="int8" paragraph: tensor-core GEMM on the decoded
  * codes, the activation rotated on every forward, no decoded weight written
- * to memory; best for prefill / large batch):
+ * to memory, a bf16 result; best for prefill / large batch):
  *     Y[m, n] = sum_t s[n, t] * sum_i p[n, t, i] * X~[m, t, i],
  *     X~ = H D X / sqrt(tile) per tile.
  * On chip the decoded weights p s are formed in fp16 (times a per-row power of
@@ -248,18 +256,39 @@ size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K);
  * tcgen05 tensor cores accumulate in fp32.
  *   codes_dev int8 [N x K], scales_dev float32 [N x K/tile], signs_dev int8 [K]
  *   X_dev     bf16 [M x K] (raw 16-bit patterns), row stride K
- *   tile      128, 256, 512, 1024 or 2048;  N % 128 == 0;  K % tile == 0;  M >= 0
- *   Y_dev     float32 [M x N] (overwritten)
- *   workspace_dev  lq_gemm_workspace_size(M, N, K) bytes, 256-byte aligned
+ *   tile      128, 256, 512, 1024 or 2048;  K % tile == 0;  N >= 0 (any; the
+ *             last 128-row weight tile may be partial);  M >= 0
+ *   Y_dev     [M x N] of type ydtype (overwritten): LQ_F32 (the parity
+ *             output) or LQ_BF16 (the page's output type; the float32 result
+ *             rounded to nearest even)
+ *   workspace_dev  lq_gemm_workspace_size(M, N, K, ydtype) bytes, 256-byte aligned
  *   dev_status_dev  int32 status word or NULL (LQ_DEV_NONFINITE for a
  *             non-finite activation row, LQ_DEV_TIMEOUT if a pipeline wait
  *             gave up -- Y is then unspecified)
- * Two kernels run on `stream`: the activation rotation, then the GEMM.
+ * Two kernels run on `stream` (the activation rotation, then the GEMM), and a
+ * third for a bf16 output whose launch splits K across CTAs (the rounding of
+ * the float32 sums).  LQ_ERR_DTYPE for another ydtype.
  */
 lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
                   const int8_t* signs_dev, int64_t N, int64_t K, int tile,
-                  const uint16_t* X_dev, int64_t M, float* Y_dev,
+                  const uint16_t* X_dev, int64_t M, void* Y_dev, int ydtype,
                   void* workspace_dev, int32_t* dev_status_dev, void* stream);
+
+/*
+ * Self-test of the GEMM's bounded pipeline waits; not part of the method (the
+ * pages have no counterpart).  Same arguments and preconditions as lq_gemm,
+ * with dev_status_dev required.  It launches lq_gemm's kernel in a variant
+ * whose activation (X~) producer never fills its ring and whose waits give up
+ * after about 2e5 clock cycles (~0.1 ms) instead of about a second: the MMA
+ * issuer's wait for the first X~ tile expires, LQ_DEV_TIMEOUT is OR-ed into
+ * *dev_status_dev, the code producer waits for its copies in flight, the tensor
+ * memory is released, and the kernel returns.  Y is unspecified afterwards;
+ * the context stays usable and later calls on the stream run normally.
+ */
+lq_status lq_gemm_wait_expiry_test(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                                   const int8_t* signs_dev, int64_t N, int64_t K, int tile,
+                                   const uint16_t* X_dev, int64_t M, void* Y_dev, int ydtype,
+                                   void* workspace_dev, int32_t* dev_status_dev, void* stream);
 
 /*
  * ------------------------------------------------------------------------
@@ -455,10 +484,10 @@ lq_status lq_gemv_ex(int lattice, const int8_t* codes_dev, const void* scales_de
                      int xdtype, int batch, float* y_dev, void* workspace_dev, int32_t* dev_status_dev,
                      void* stream);
 
-/* lq_gemm reading scales_dev in scale_format (same workspace). */
+/* lq_gemm reading scales_dev in scale_format (same workspace and output types). */
 lq_status lq_gemm_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
                      const int8_t* signs_dev, int64_t N, int64_t K, int tile, const uint16_t* X_dev, int64_t M,
-                     float* Y_dev, void* workspace_dev, int32_t* dev_status_dev, void* stream);
+                     void* Y_dev, int ydtype, void* workspace_dev, int32_t* dev_status_dev, void* stream);
 
 /* lq_attention_decode with both caches' scales in scale_format
  * (LQ_SCALE_TILE_F32 or LQ_SCALE_TILE_F16, [tokens x kv_heads]). */

@@ -34,7 +34,7 @@ SIGNATURES = {
     "lq_quantize_ex": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _F32, _I32, _P, _P, _P, _P, _P]),
     "lq_dequantize_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I32, _P]),
     "lq_gemv_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
-    "lq_gemm_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
+    "lq_gemm_ex": (_I32, [_I32, _P, _P, _I32, _P, _I64, _I64, _I32, _P, _I64, _P, _I32, _P, _P, _P]),
     "lq_attention_decode_ex": (_I32, [_I32, _P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, _P, _I32, _P,
                                       _P, ctypes.c_size_t, _P]),
     "lq_quantize_dithered": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _U64, _U64, _F32, _I32, _P, _P, _P,
@@ -49,8 +49,9 @@ SIGNATURES = {
     "lq_gemv_noalloc": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I32, _I32, _P, _P, _P]),
     "lq_gemv_grouped_workspace_size": (ctypes.c_size_t, [_I32, _I32, _I64, _I32]),
     "lq_gemv_grouped": (_I32, [_I32, _I32, _P, _P, _P, _P, _I64, _I32, _P, _I32, _I32, _P, _P, _P, _P]),
-    "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64]),
-    "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _P, _P, _P]),
+    "lq_gemm_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I64, _I32]),
+    "lq_gemm": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _I32, _P, _P, _P]),
+    "lq_gemm_wait_expiry_test": (_I32, [_I32, _P, _P, _P, _I64, _I64, _I32, _P, _I64, _P, _I32, _P, _P, _P]),
     "lq_rice_stream_bound": (ctypes.c_size_t, [_I32, _I64, _I64, _I32]),
     "lq_rice_workspace_size": (ctypes.c_size_t, [_I64, _I64, _I32]),
     "lq_rice_encode": (_I32, [_I32, _P, _I64, _I64, _I32, _P, ctypes.c_size_t, _P, _P, _P, _P, _P]),
@@ -251,18 +252,28 @@ def lq_gemv_grouped(lattice, codes, scales, signs, tile: int, x, ys, workspace, 
         _stream(stream)))
 
 
-def lq_gemm_workspace_size(M: int, N: int, K: int) -> int:
-    return int(_get_lib().lq_gemm_workspace_size(int(M), int(N), int(K)))
+def lq_gemm_workspace_size(M: int, N: int, K: int, ydtype=LQ_F32) -> int:
+    yd = ydtype if isinstance(ydtype, int) else _dtype_id(ydtype)
+    return int(_get_lib().lq_gemm_workspace_size(int(M), int(N), int(K), yd))
 
 
 def lq_gemm(lattice, codes, scales, signs, tile: int, X, Y, workspace, dev_status=None,
             stream=None) -> None:
-    """Y [M x N] float32 = X~ . (s p)^T from the codes [N x K]; X bf16 [M x K]."""
+    """Y [M x N] (float32 or bf16, Y's dtype) = X~ . (s p)^T from the codes [N x K]; X bf16 [M x K]."""
     N, K = codes.shape
     M = X.shape[0]
     _check("lq_gemm", _get_lib().lq_gemm(
         _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), N, K, int(tile), _ptr(X), M,
-        _ptr(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+        _ptr(Y), _dtype_id(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+
+
+def lq_gemm_wait_expiry_test(lattice, codes, scales, signs, tile: int, X, Y, workspace, dev_status,
+                             stream=None) -> None:
+    """The GEMM's wait-expiry self-test (lq.h): raises LQ_DEV_TIMEOUT in dev_status."""
+    N, K = codes.shape
+    _check("lq_gemm_wait_expiry_test", _get_lib().lq_gemm_wait_expiry_test(
+        _lattice_id(lattice), _ptr(codes), _ptr(scales), _ptr(signs), N, K, int(tile), _ptr(X), X.shape[0],
+        _ptr(Y), _dtype_id(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
 
 
 def lq_rice_stream_bound(lattice, rows: int, cols: int, tile: int) -> int:
@@ -405,7 +416,8 @@ def lq_gemm_ex(lattice, codes, scales, scale_format, signs, tile: int, X, Y, wor
     N, K = codes.shape
     _check("lq_gemm_ex", _get_lib().lq_gemm_ex(
         _lattice_id(lattice), _ptr(codes), _ptr(scales), _scale_format_id(scale_format), _ptr(signs), N, K,
-        int(tile), _ptr(X), X.shape[0], _ptr(Y), _ptr(workspace), _ptr(dev_status), _stream(stream)))
+        int(tile), _ptr(X), X.shape[0], _ptr(Y), _dtype_id(Y), _ptr(workspace), _ptr(dev_status),
+        _stream(stream)))
 
 
 def lq_attention_decode_ex(lattice, k_codes, k_scales, k_signs, v_codes, v_scales, v_signs, scale_format, q, out,
@@ -520,13 +532,14 @@ def gemv(codes, scales, signs, x, lattice: str = "e8", tile: int = 256, workspac
 
 
 def gemm(codes, scales, signs, X, lattice: str = "e8", tile: int = 256, workspace=None,
-         dev_status=None, stream=None):
+         dev_status=None, stream=None, out_dtype=None):
     import torch
     N, K = codes.shape
     M = X.shape[0]
-    Y = torch.empty((M, N), dtype=torch.float32, device=codes.device)
+    Y = torch.empty((M, N), dtype=out_dtype or torch.float32, device=codes.device)
     if workspace is None:
-        workspace = torch.empty(lq_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=codes.device)
+        workspace = torch.empty(lq_gemm_workspace_size(M, N, K, _dtype_id(Y)), dtype=torch.uint8,
+                                device=codes.device)
     lq_gemm(lattice, codes, scales, signs, tile, X, Y, workspace, dev_status, stream)
     return Y
 

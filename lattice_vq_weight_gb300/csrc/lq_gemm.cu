@@ -28,6 +28,7 @@
 //   tile overlaps the main loop of the next.  Every mbarrier wait is bounded
 //   (about a second of clock cycles); on expiry the kernel records
 //   LQ_DEV_TIMEOUT and winds down.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -62,6 +63,8 @@ static_assert(kDecodePasses * kDecodeThreads * 16 == BM * BK, "decoders cover th
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
 constexpr long long kWaitCycles = 2000000000ll;  // about one second
+// Wait limit of the wait-expiry self-test instantiation (about 0.1 ms).
+constexpr long long kSelfTestWaitCycles = 200000ll;
 
 struct Smem {
   // stage buffers come first and are 1024-byte aligned (128-byte swizzle atoms)
@@ -89,7 +92,8 @@ struct Args {
   const void* scales;     // [N x K/T] or [N], in gemm_kernel's format SF
   const float* f;         // [N]   row factors 2^e
   const float* inv_g;     // [M]   1 / g_m
-  float* Y;               // [M x N]
+  float* Y32;             // [M x N] float32 output, or the float32 sums of the K splits
+  __nv_bfloat16* Ybf;     // [M x N] bf16 output written directly (one K split), else null
   int32_t* status;
 };
 
@@ -116,14 +120,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false when the limit expired (the caller records the timeout).
+// Bounded wait: false when the limit expired (the caller records the timeout)
+// or when another thread of the CTA already recorded one.
+template <long long LIMIT = kWaitCycles>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* timeout_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*timeout_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > LIMIT) {
       *timeout_flag = 1;
       return false;
     }
@@ -195,9 +201,14 @@ __device__ __forceinline__ float scale_value(const typename ScaleType<SF>::T* p)
 }
 
 // SF: the scale format (LQ_SCALE_*), fixed at compile time for the decode loop.
-template <int SF>
+// SELF_TEST: the wait-expiry self-test (lq_gemm_wait_expiry_test): the X~
+// producer issues no copies and every pipeline wait gives up after
+// kSelfTestWaitCycles, so the MMA issuer's first wait on an X~ tile expires and
+// the timeout path below runs.  Never instantiated for lq_gemm / lq_gemm_ex.
+template <int SF, bool SELF_TEST = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x, Args a) {
+  constexpr long long kLimit = SELF_TEST ? kSelfTestWaitCycles : kWaitCycles;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
@@ -261,11 +272,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
         int nt, mt, k0, k1;
         unit_range(u, nt, mt, k0, k1);
         for (int ks = k0; ks < k1; ++ks) {
-          if (!mbar_wait(&empty[s], ph ^ 1, timeout)) break;
-          mbar_arrive_expect_tx(&full[s], bytes);
-          if (codes_side) tma_load_2d(sm.codes[s], &map_codes, &full[s], ks * BK, nt * BM);
-          else tma_load_2d(sm.x[s], &map_x, &full[s], ks * BK, mt * BN);
-          ++issued;
+          if (!mbar_wait<kLimit>(&empty[s], ph ^ 1, timeout)) break;
+          if (SELF_TEST && !codes_side) {
+            // the self-test's X~ producer never fills its ring
+          } else {
+            mbar_arrive_expect_tx(&full[s], bytes);
+            if (codes_side) tma_load_2d(sm.codes[s], &map_codes, &full[s], ks * BK, nt * BM);
+            else tma_load_2d(sm.x[s], &map_x, &full[s], ks * BK, mt * BN);
+            ++issued;
+          }
           if (++s == depth) { s = 0; ph ^= 1; }
         }
       }
@@ -290,12 +305,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
         unit_range(u, nt, mt, k0, k1);
         const int acc = it & 1;
         const uint32_t acc_ph = (uint32_t)((it >> 1) & 1);
-        if (!mbar_wait(&sm.tmem_empty[acc], acc_ph ^ 1, timeout)) break;
+        if (!mbar_wait<kLimit>(&sm.tmem_empty[acc], acc_ph ^ 1, timeout)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
         bool ok = true;
         for (int ks = k0; ks < k1; ++ks) {
-          if (!mbar_wait(&sm.full_a[sa], pha, timeout) || !mbar_wait(&sm.full_x[sx], phx, timeout)) {
+          if (!mbar_wait<kLimit>(&sm.full_a[sa], pha, timeout) || !mbar_wait<kLimit>(&sm.full_x[sx], phx, timeout)) {
             ok = false;
             break;
           }
@@ -336,9 +351,12 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
       const ST* srow[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) {
+        // rows past N (a ragged last weight tile) decode the TMA's zero fill
+        // with a zero factor, reading the scales of row 0
         const int64_t row = (int64_t)nt * BM + kRowsPerPass * p + rsub;
-        fr[p] = 0.5f * __ldg(a.f + row);
-        srow[p] = reinterpret_cast<const ST*>(a.scales) + row * (kTileStep ? a.tiles_per_row : 1);
+        const bool in = row < a.N;
+        fr[p] = in ? 0.5f * __ldg(a.f + row) : 0.f;
+        srow[p] = reinterpret_cast<const ST*>(a.scales) + (in ? row : 0) * (kTileStep ? a.tiles_per_row : 1);
       }
       // scales of the current tile and (prefetched) of the next one
       float s_cur[P], s_nxt[P];
@@ -361,8 +379,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
             s_nxt[p] = (t + 1 < a.tiles_per_row) ? scale_value<SF>(srow[p] + kTileStep * (t + 1)) : 0.f;
           }
         }
-        if (!mbar_wait(&sm.full_c[sc], phc, timeout)) break;
-        if (!mbar_wait(&sm.empty_a[sa], pha ^ 1, timeout)) break;
+        if (!mbar_wait<kLimit>(&sm.full_c[sc], phc, timeout)) break;
+        if (!mbar_wait<kLimit>(&sm.empty_a[sa], pha ^ 1, timeout)) break;
         const uint8_t* cbase = sm.codes[sc];
         uint8_t* abase = sm.a[sa];
 #pragma unroll
@@ -399,24 +417,27 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
       unit_range(u, nt, mt, k0, k1);
       const int acc = it & 1;
       const uint32_t acc_ph = (uint32_t)((it >> 1) & 1);
-      const bool ready = mbar_wait(&sm.tmem_full[acc], acc_ph, timeout);
+      const bool ready = mbar_wait<kLimit>(&sm.tmem_full[acc], acc_ph, timeout);
       if (!__all_sync(0xffffffffu, ready)) break;
       tc_fence_after();
       const int64_t n = (int64_t)nt * BM + row_in_tile;
-      const float inv_f = 1.0f / __ldg(a.f + n);
+      const bool row_in = n < a.N;                 // false in a ragged last weight tile
+      const float inv_f = row_in ? 1.0f / __ldg(a.f + n) : 0.f;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
-      float* yrow = a.Y + n;
       const bool atomic = a.splits > 1;
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t r[16];
+        __syncwarp();                              // tcgen05.ld is warp-collective
         tmem_ld16(taddr + (uint32_t)c0, r);
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int64_t m = (int64_t)mt * BN + c0 + j;
-          if (m < a.M) {
+          if (row_in && m < a.M) {
             const float v = __uint_as_float(r[j]) * inv_f * __ldg(a.inv_g + m);
-            if (atomic) atomicAdd(yrow + m * a.N, v); else yrow[m * a.N] = v;
+            if (atomic) atomicAdd(a.Y32 + m * a.N + n, v);
+            else if (a.Ybf != nullptr) a.Ybf[m * a.N + n] = __float2bfloat16_rn(v);
+            else a.Y32[m * a.N + n] = v;
           }
         }
       }
@@ -564,6 +585,24 @@ __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
   }
 }
 
+// bf16 output of a K-split launch: Y = bf16(the float32 sums), nearest even.
+__global__ void __launch_bounds__(256) gemm_to_bf16_kernel(const float* __restrict__ src,
+                                                            __nv_bfloat16* __restrict__ dst, int64_t n) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; 4 * i < n; i += stride) {
+    if (4 * i + 4 <= n) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(src) + i);
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+      uint2 o;
+      o.x = *reinterpret_cast<const uint32_t*>(&lo);
+      o.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst + 4 * i) = o;
+    } else {
+      for (int64_t j = 4 * i; j < n; ++j) dst[j] = __float2bfloat16_rn(src[j]);
+    }
+  }
+}
+
 }  // namespace gemm
 }  // namespace lq
 
@@ -575,15 +614,18 @@ namespace {
 constexpr size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct GemmWorkspace {
-  size_t xt, inv_g, f, total;
+  size_t xt, inv_g, f, acc, total;
 };
 
-GemmWorkspace gemm_layout(int64_t M, int64_t N, int64_t K) {
+// X~ fp16 [M x K], 1/g [M], f [N], and for a bf16 output the float32 sums
+// [M x N] that the K splits add into.
+GemmWorkspace gemm_layout(int64_t M, int64_t N, int64_t K, bool bf16_out) {
   GemmWorkspace w;
   w.xt = 0;
   w.inv_g = align256((size_t)M * (size_t)K * 2);
   w.f = w.inv_g + align256((size_t)M * 4);
-  w.total = w.f + align256((size_t)N * 4);
+  w.acc = w.f + align256((size_t)N * 4);
+  w.total = w.acc + (bf16_out ? align256((size_t)M * (size_t)N * 4) : 0);
   return w;
 }
 
@@ -635,22 +677,24 @@ int choose_splits(int64_t tiles, int k_stages, int sms) {
 
 }  // namespace
 
-extern "C" size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return gemm_layout(M, N, K).total;
+extern "C" size_t lq_gemm_workspace_size(int64_t M, int64_t N, int64_t K, int ydtype) {
+  if (M <= 0 || N <= 0 || K <= 0 || (ydtype != LQ_F32 && ydtype != LQ_BF16)) return 0;
+  return gemm_layout(M, N, K, ydtype == LQ_BF16).total;
 }
 
 namespace {
 
 lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev, int sfmt, const int8_t* signs_dev,
-                   int64_t N, int64_t K, int tile, const uint16_t* X_dev, int64_t M, float* Y_dev,
-                   void* workspace_dev, int32_t* dev_status_dev, void* stream) {
+                   int64_t N, int64_t K, int tile, const uint16_t* X_dev, int64_t M, void* Y_dev, int ydtype,
+                   void* workspace_dev, int32_t* dev_status_dev, void* stream, bool self_test = false) {
   if (sfmt != LQ_SCALE_TILE_F32 && sfmt != LQ_SCALE_ROW_BF16 && sfmt != LQ_SCALE_TILE_F16) return LQ_ERR_ARG;
+  if (ydtype != LQ_F32 && ydtype != LQ_BF16) return LQ_ERR_DTYPE;
+  const bool bf16_out = ydtype == LQ_BF16;
   const uintptr_t salign = (sfmt == LQ_SCALE_TILE_F32) ? 3u : 1u;
   lq_status st = validate_common(lattice, N, K, tile);
   if (st != LQ_OK) return st;
   if (M < 0) return LQ_ERR_SHAPE;
-  if (N % BM != 0 || K % BK != 0) return LQ_ERR_SHAPE;
+  if (K % BK != 0) return LQ_ERR_SHAPE;       // implied by K % tile == 0
   if (M > (int64_t(1) << 31) || N > (int64_t(1) << 31)) return LQ_ERR_SHAPE;
   if (M == 0 || N == 0) return LQ_OK;
   if (codes_dev == nullptr || scales_dev == nullptr || signs_dev == nullptr || X_dev == nullptr ||
@@ -665,7 +709,7 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
   const int sms = device_sm_count();
   if (sms <= 0) return LQ_ERR_CUDA;
 
-  const GemmWorkspace lay = gemm_layout(M, N, K);
+  const GemmWorkspace lay = gemm_layout(M, N, K, bf16_out);
   char* ws = reinterpret_cast<char*>(workspace_dev);
   __half* Xt = reinterpret_cast<__half*>(ws + lay.xt);
   float* inv_g = reinterpret_cast<float*>(ws + lay.inv_g);
@@ -673,14 +717,20 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
 
   Args a;
   a.M = M; a.N = N; a.K = K; a.tile = tile; a.tiles_per_row = (int)(K / tile);
-  a.n_tiles = (int)(N / BM);
+  a.n_tiles = (int)((N + BM - 1) / BM);
   a.m_tiles = (int)((M + BN - 1) / BN);
   a.k_stages = (int)(K / BK);
   a.splits = choose_splits((int64_t)a.n_tiles * a.m_tiles, a.k_stages, sms);
   a.stages_per_split = (a.k_stages + a.splits - 1) / a.splits;
   a.splits = (a.k_stages + a.stages_per_split - 1) / a.stages_per_split;
   a.units = (int64_t)a.n_tiles * a.m_tiles * a.splits;
-  a.scales = scales_dev; a.f = f; a.inv_g = inv_g; a.Y = Y_dev; a.status = dev_status_dev;
+  a.scales = scales_dev; a.f = f; a.inv_g = inv_g; a.status = dev_status_dev;
+  // float32 output: the kernel writes (or, split along K, adds into) Y.  bf16
+  // output: one split writes bf16 directly; several add into float32 sums in
+  // the workspace that a last kernel rounds to bf16.
+  const bool via_acc = bf16_out && a.splits > 1;
+  a.Y32 = bf16_out ? (via_acc ? reinterpret_cast<float*>(ws + lay.acc) : nullptr) : reinterpret_cast<float*>(Y_dev);
+  a.Ybf = (bf16_out && !via_acc) ? reinterpret_cast<__nv_bfloat16*>(Y_dev) : nullptr;
 
   PrepArgs p;
   p.X = reinterpret_cast<const __nv_bfloat16*>(X_dev); p.signs = signs_dev; p.M = M; p.N = N; p.K = K;
@@ -688,7 +738,7 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
   p.chunks_per_row = (int)((K + kChunkCols - 1) / kChunkCols);
   p.inv_sqrt_tile = (float)(1.0 / sqrt((double)tile));
   p.a2 = (lattice == LQ_A2);
-  p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.sfmt = sfmt; p.f = f; p.Y = Y_dev; p.zero_y = a.splits > 1;
+  p.Xt = Xt; p.inv_g = inv_g; p.scales = scales_dev; p.sfmt = sfmt; p.f = f; p.Y = a.Y32; p.zero_y = a.splits > 1;
   p.status = dev_status_dev;
   const int64_t prep_blocks = M + (N + kPrepWarps - 1) / kPrepWarps;
   const int E = act_elems_for_tile(tile);
@@ -715,6 +765,8 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
         cudaFuncSetAttribute(gemm_kernel<LQ_SCALE_ROW_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
         cudaFuncSetAttribute(gemm_kernel<LQ_SCALE_TILE_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_kernel<LQ_SCALE_TILE_F32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
@@ -722,12 +774,19 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
     attr_set = true;
   }
   const int64_t grid = a.units < sms ? a.units : sms;
-  if (sfmt == LQ_SCALE_ROW_BF16)
+  if (self_test)
+    gemm_kernel<LQ_SCALE_TILE_F32, true><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
+  else if (sfmt == LQ_SCALE_ROW_BF16)
     gemm_kernel<LQ_SCALE_ROW_BF16><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
   else if (sfmt == LQ_SCALE_TILE_F16)
     gemm_kernel<LQ_SCALE_TILE_F16><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
   else
     gemm_kernel<LQ_SCALE_TILE_F32><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
+  st = check_launch();
+  if (st != LQ_OK || !via_acc) return st;
+  const int64_t n_out = M * N;
+  const int64_t cvt_blocks = std::min<int64_t>((n_out / 4 + 255) / 256 + 1, (int64_t)sms * 8);
+  gemm_to_bf16_kernel<<<(unsigned)cvt_blocks, 256, 0, s>>>(a.Y32, reinterpret_cast<__nv_bfloat16*>(Y_dev), n_out);
   return check_launch();
 }
 
@@ -735,18 +794,28 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
 
 extern "C" lq_status lq_gemm(int lattice, const int8_t* codes_dev, const float* scales_dev,
                              const int8_t* signs_dev, int64_t N, int64_t K, int tile,
-                             const uint16_t* X_dev, int64_t M, float* Y_dev, void* workspace_dev,
+                             const uint16_t* X_dev, int64_t M, void* Y_dev, int ydtype, void* workspace_dev,
                              int32_t* dev_status_dev, void* stream) {
   LQ_NVTX_RANGE("lq_gemm");
-  return gemm_fmt(lattice, codes_dev, scales_dev, LQ_SCALE_TILE_F32, signs_dev, N, K, tile, X_dev, M, Y_dev,
+  return gemm_fmt(lattice, codes_dev, scales_dev, LQ_SCALE_TILE_F32, signs_dev, N, K, tile, X_dev, M, Y_dev, ydtype,
                   workspace_dev, dev_status_dev, stream);
 }
 
 extern "C" lq_status lq_gemm_ex(int lattice, const int8_t* codes_dev, const void* scales_dev, int scale_format,
                                 const int8_t* signs_dev, int64_t N, int64_t K, int tile, const uint16_t* X_dev,
-                                int64_t M, float* Y_dev, void* workspace_dev, int32_t* dev_status_dev,
+                                int64_t M, void* Y_dev, int ydtype, void* workspace_dev, int32_t* dev_status_dev,
                                 void* stream) {
   LQ_NVTX_RANGE("lq_gemm_ex");
-  return gemm_fmt(lattice, codes_dev, scales_dev, scale_format, signs_dev, N, K, tile, X_dev, M, Y_dev,
+  return gemm_fmt(lattice, codes_dev, scales_dev, scale_format, signs_dev, N, K, tile, X_dev, M, Y_dev, ydtype,
                   workspace_dev, dev_status_dev, stream);
+}
+
+extern "C" lq_status lq_gemm_wait_expiry_test(int lattice, const int8_t* codes_dev, const float* scales_dev,
+                                              const int8_t* signs_dev, int64_t N, int64_t K, int tile,
+                                              const uint16_t* X_dev, int64_t M, void* Y_dev, int ydtype,
+                                              void* workspace_dev, int32_t* dev_status_dev, void* stream) {
+  LQ_NVTX_RANGE("lq_gemm_wait_expiry_test");
+  if (dev_status_dev == nullptr) return LQ_ERR_ARG;
+  return gemm_fmt(lattice, codes_dev, scales_dev, LQ_SCALE_TILE_F32, signs_dev, N, K, tile, X_dev, M, Y_dev, ydtype,
+                  workspace_dev, dev_status_dev, stream, true);
 }

@@ -23,6 +23,7 @@
 // its own signs, scales and output: one launch pair serves the whole group.
 #include <mutex>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -519,8 +520,10 @@ extern "C" lq_status lq_gemv_grouped(int lattice, int n, const int8_t* const* co
 // memory themselves.  Its workspace is a fixed array in this library's device
 // image (allocated once per GPU when the library's module is loaded and kept
 // until the process exits).  Host code must not use the array's name as a
-// device address; the address is looked up per device with
-// cudaGetSymbolAddress the first time a device is used.
+// device address; the address is looked up with cudaGetSymbolAddress the first
+// time a device is used, and again whenever the device's current context is no
+// longer the one the address was looked up in (after cudaDeviceReset the
+// module is loaded anew and the array may move).
 static __device__ __align__(256) unsigned char g_gemv_noalloc_scratch[LQ_GEMV_NOALLOC_MAX_WORKSPACE];
 
 namespace {
@@ -528,16 +531,41 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The driver's current context of the calling thread (nullptr if unknown).
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    else
+      cudaGetLastError();
+  });
+  CUcontext c = nullptr;
+  if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of the scratch array on the current device, looked up once
+// per device and context.
 lq_status noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return LQ_ERR_CUDA;
   }
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || ctx == nullptr || ctx != g_scratch_ctx[dev]) {
+    // the lookup also makes the device's primary context current if no
+    // context was current yet
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_gemv_noalloc_scratch);
     if (e != cudaSuccess || p == nullptr) {
@@ -545,6 +573,7 @@ lq_status noalloc_scratch(void** out) {
       return LQ_ERR_CUDA;
     }
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context();
   }
   *out = g_scratch_ptr[dev];
   return LQ_OK;

@@ -118,7 +118,19 @@ def test_argument_errors_are_synchronous():
     assert lib.lq_dequantize_ex(8, good, P(0x10001), L.LQ_SCALE_TILE_F16, good, 4, 256, 256, good, 0,
                                 s) == L.LQ_ERR_ARG
     assert lib.lq_gemv_ex(8, good, good, 5, good, 4, 256, 256, good, 1, 1, good, good, nul, s) == L.LQ_ERR_ARG
-    assert lib.lq_gemm_ex(8, good, good, 7, good, 128, 256, 256, good, 4, good, good, nul, s) == L.LQ_ERR_ARG
+    assert lib.lq_gemm_ex(8, good, good, 7, good, 128, 256, 256, good, 4, good, L.LQ_F32, good, nul,
+                          s) == L.LQ_ERR_ARG
+    # GEMM output type: float32 or bf16; the bf16 workspace adds the float32 sums [M x N]
+    assert lib.lq_gemm(8, good, good, good, 200, 256, 256, good, 4, good, 5, good, nul, s) == L.LQ_ERR_DTYPE
+    assert L.lq_gemm_workspace_size(4, 200, 256, 7) == 0
+    assert (L.lq_gemm_workspace_size(300, 200, 1024, L.LQ_BF16)
+            >= L.lq_gemm_workspace_size(300, 200, 1024, L.LQ_F32) + 300 * 200 * 4)
+    # the wait-expiry self-test needs a status word to report into
+    assert lib.lq_gemm_wait_expiry_test(8, good, good, good, 128, 256, 256, good, 4, good, L.LQ_F32, good, nul,
+                                        s) == L.LQ_ERR_ARG
+    # lq_gemv_noalloc: a request larger than its fixed scratch is refused before any pointer is looked at
+    assert lib.lq_gemv_noalloc(8, None, None, None, 4, 1 << 20, 256, None, L.LQ_BF16, 16, None, None,
+                               None) == L.LQ_ERR_SHAPE
     # the KV attention takes float32 or fp16 tile scales only
     assert lib.lq_attention_decode_ex(8, good, good, good, good, good, good, L.LQ_SCALE_ROW_BF16, 16, 1, 1, 128,
                                       good, 1, good, good, ctypes.c_size_t(1 << 20), s) == L.LQ_ERR_ARG
