@@ -450,6 +450,142 @@ __device__ __forceinline__ void decode_lane(const float2 (&p)[32], uint32_t (&w)
   }
 }
 
+// ---------------------------------------------------------------- pair decoders
+// The quantize kernel holds the 64 coordinates of a lane as float2 p[32] with
+// p[j].x = column j and p[j].y = column j + 32 (after its transform: two
+// different lattice blocks), so one f32x2 instruction works on coordinate i of
+// two blocks at once.  These decoders take u[i] = p[8 g + i] (i = 0..7) and
+// the scale k (y = u k): block P in the .x halves, block Q in the .y halves.
+//
+// Fast-path precondition: every |y| < 62.5.  Then rint(y) lies in [-62, 62]
+// and every code in [-127, 127], and the codes are built four to a word in
+// "offset binary" (code + 128 per byte, every byte in [1, 255] at every step),
+// so that 32-bit adds and subtracts never carry from one byte into the next;
+// one XOR with 0x80808080 at the end gives the int8 codes.
+
+// y + kRoundMagic64 (|y| < 2^22) rounds y to the nearest integer (ties to
+// even) and leaves rint(y) + 64 in the low byte of its bits.
+constexpr float kRoundMagic64 = 12582976.0f;   // 1.5 * 2^23 + 64
+
+// PTX prmt in its default mode: byte n of the result is byte (sel_n & 7) of
+// {b, a}, or, when bit 3 of the selector nibble sel_n is set, that byte's sign
+// bit replicated over all 8 bits.  (The __byte_perm intrinsic keeps only the
+// low three bits of each nibble, so the sign mode needs the instruction itself.)
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Bytes 0 of four words into one word.
+__device__ __forceinline__ uint32_t pack_low4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return prmt(prmt(a, b, 0x0040u), prmt(c, d, 0x0040u), 0x5410u);
+}
+// 0xFF in byte i where word i is negative (its sign bit replicated), else 0.
+__device__ __forceinline__ uint32_t pack_sign4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return prmt(prmt(a, b, 0x00FBu), prmt(c, d, 0x00FBu), 0x5410u);
+}
+
+// PRMT selectors that turn a word of per-coordinate fix bytes into the fix of
+// one coordinate as a signed 32-bit number: entry i (0..7) keeps byte i & 3 of
+// the fix word of code word i >> 2 at its place, zero below it and its sign
+// replicated above it (.x: selector for word 0, coordinates 0..3; .y: word 1,
+// coordinates 4..7; the other word gets zero); entry 8 is no fix at all.
+// Nibble 4 selects a zero byte (byte 0 of the zero operand), nibble p byte p,
+// nibble 8 | p the sign of byte p.
+__device__ __forceinline__ uint2 parity_fix_selector(int i) {
+  const int p = i & 3;
+  const uint32_t one = p == 0 ? 0x8880u : p == 1 ? 0x9914u : p == 2 ? 0xA244u : 0x3444u;
+  if (i >= 8) return make_uint2(0x4444u, 0x4444u);
+  return i < 4 ? make_uint2(one, 0x4444u) : make_uint2(0x4444u, one);
+}
+
+// Codes of one E8 block from its rounding bits t (rint(y) + 64 in byte 0),
+// residual bits e (y - rint(y)) and keys (|e| with the low three mantissa bits
+// replaced by 7 - i), with lhs = 2 - sum |e|.  E8 = D8 u (D8 + 1/2) decoded as
+// in decode_e8: the D8 point is f = rint(y) with the worst coordinate (largest
+// |e|, lowest index on ties) rounded the other way when sum f is odd; the
+// D8 + 1/2 point is floor(y) + 1/2 with its worst coordinate (smallest |e|)
+// moved across when sum floor(y) is odd.  Their squared distances minus sum e^2
+// are dA = [odd A] (1 - 2 max|e|) and dB = 2 - sum|e| + [odd B] 2 min|e|, and
+// D8 is kept when dA <= dB.  Per byte, in offset binary: D8 code 2F (F =
+// rint(y) + 64), D8 + 1/2 code 2F + 1 - 2[e < 0]; the parity fix adds +-2 at
+// the chosen coordinate (toward y: +2 - 4[e < 0] for D8, -2 + 4[e < 0] for
+// D8 + 1/2).
+__device__ __forceinline__ uint2 e8_block_codes(const uint32_t (&t)[8], const uint32_t (&e)[8],
+                                                const uint32_t (&key)[8], float lhs, const uint2* fixsel) {
+  const uint32_t kA = key_max3(key_max3(key[0], key[1], key[2]), key_max3(key[3], key[4], key[5]),
+                               __float_as_uint(fmaxf(__uint_as_float(key[6]), __uint_as_float(key[7]))));
+  const uint32_t kB = key_min3(key_min3(key[0], key[1], key[2]), key_min3(key[3], key[4], key[5]),
+                               __float_as_uint(fminf(__uint_as_float(key[6]), __uint_as_float(key[7]))));
+  const uint32_t F0 = pack_low4(t[0], t[1], t[2], t[3]), F1 = pack_low4(t[4], t[5], t[6], t[7]);
+  const uint32_t N0 = pack_sign4(e[0], e[1], e[2], e[3]), N1 = pack_sign4(e[4], e[5], e[6], e[7]);
+  // bit 0 of each byte: parity of F_i + F_(i+4); bit 4: of the two signs.  The
+  // byte sum (top byte of the product) then has the parity of sum F (= that of
+  // sum rint(y): 8 * 64 is even) in bit 0 and that of the count of negative
+  // residuals in bit 4.
+  const uint32_t par = imad(((F0 ^ F1) & 0x01010101u) | ((N0 ^ N1) & 0x10101010u), 0x01010101u, 0u) >> 24;
+  const bool oddA = (par & 1u) != 0;
+  const bool oddB = ((par ^ (par >> 4)) & 1u) != 0;
+  const float dA = oddA ? fmaf(-2.f, __uint_as_float(kA), 1.f) : 0.f;
+  const float dB = oddB ? fmaf(2.f, __uint_as_float(kB), lhs) : lhs;
+  const bool takeB = dB < dA;
+  const uint32_t kk = takeB ? kB : kA;
+  const bool fix = takeB ? oddB : oddA;
+  const uint2 sel = fixsel[fix ? 7 - (int)(kk & 7u) : 8];
+  const uint32_t bm = takeB ? 0xFFFFFFFFu : 0u;
+  const uint32_t fixbytes = 0x02020202u ^ (bm & 0xFCFCFCFCu);   // +2 (D8) or -2 (D8 + 1/2) where e >= 0
+  uint2 r;
+  r.x = ((F0 + F0 + (bm & 0x01010101u)) - (N0 & bm & 0x02020202u) +
+         prmt(fixbytes ^ (N0 & 0xFCFCFCFCu), 0u, sel.x)) ^ 0x80808080u;
+  r.y = ((F1 + F1 + (bm & 0x01010101u)) - (N1 & bm & 0x02020202u) +
+         prmt(fixbytes ^ (N1 & 0xFCFCFCFCu), 0u, sel.y)) ^ 0x80808080u;
+  return r;
+}
+
+// Fast E8 decode of two blocks side by side (see above): y = u k is never
+// formed; the rounding t = u k + magic and the residual e = u k - rint(y) are
+// each one fused multiply-add of the exact product.
+__device__ __forceinline__ void decode_e8_pair(const float2 (&u)[8], float2 k2, const uint2* fixsel, uint2& cP,
+                                               uint2& cQ) {
+  const float2 MG = make_float2(kRoundMagic64, kRoundMagic64);
+  uint32_t tP[8], tQ[8], eP[8], eQ[8], kP[8], kQ[8];
+  float2 kf[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 t = fma2(u[i], k2, MG);
+    const float2 e = fma2(u[i], k2, sub2(MG, t));   // MG - t = -rint(y), exact
+    tP[i] = __float_as_uint(t.x);
+    tQ[i] = __float_as_uint(t.y);
+    eP[i] = __float_as_uint(e.x);
+    eQ[i] = __float_as_uint(e.y);
+    kP[i] = (eP[i] & 0x7FFFFFF8u) | (uint32_t)(7 - i);
+    kQ[i] = (eQ[i] & 0x7FFFFFF8u) | (uint32_t)(7 - i);
+    kf[i] = make_float2(__uint_as_float(kP[i]), __uint_as_float(kQ[i]));
+  }
+  // sum |e| of each block from the keys (each within 7 ulps of |e|)
+  const float2 s = add2(add2(add2(kf[0], kf[1]), add2(kf[2], kf[3])), add2(add2(kf[4], kf[5]), add2(kf[6], kf[7])));
+  const float2 lhs = sub2(make_float2(2.f, 2.f), s);
+  cP = e8_block_codes(tP, eP, kP, lhs.x, fixsel);
+  cQ = e8_block_codes(tQ, eQ, kQ, lhs.y, fixsel);
+}
+
+// Fast Z1 decode of two 8-coordinate groups side by side: c = 2 rint(y).
+__device__ __forceinline__ void decode_z1_pair(const float2 (&u)[8], float2 k2, uint2& cP, uint2& cQ) {
+  const float2 MG = make_float2(kRoundMagic64, kRoundMagic64);
+  uint32_t tP[8], tQ[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 t = fma2(u[i], k2, MG);
+    tP[i] = __float_as_uint(t.x);
+    tQ[i] = __float_as_uint(t.y);
+  }
+  const uint32_t P0 = pack_low4(tP[0], tP[1], tP[2], tP[3]), P1 = pack_low4(tP[4], tP[5], tP[6], tP[7]);
+  const uint32_t Q0 = pack_low4(tQ[0], tQ[1], tQ[2], tQ[3]), Q1 = pack_low4(tQ[4], tQ[5], tQ[6], tQ[7]);
+  cP = make_uint2((P0 + P0) ^ 0x80808080u, (P1 + P1) ^ 0x80808080u);
+  cQ = make_uint2((Q0 + Q0) ^ 0x80808080u, (Q1 + Q1) ^ 0x80808080u);
+}
+
 // ---------------------------------------------------------------- dither
 // Subtractive dither (Zamir & Feder, "On lattice quantization noise", 1996):
 // element (r, k) of a [rows x cols] matrix draws w = (top 24 bits of SplitMix64

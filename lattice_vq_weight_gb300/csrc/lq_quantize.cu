@@ -231,9 +231,8 @@ extern "C" lq_status lq_make_signs(uint64_t seed, int64_t cols, int8_t* signs_de
 template <int LAT, bool BF16>
 static lq_status launch_quantize(QuantArgs& a, int sf, bool dither, cudaStream_t st) {
   if (dither) return launch_quantize_dithered(a, LAT, BF16, sf, st);
-  if (a.n_mats > 1) return launch_quantize_walk<LAT, BF16, true, LQ_SCALE_TILE_F32>(a, st);
   if (sf != LQ_SCALE_TILE_F32) return launch_quantize_scaled16(a, LAT, BF16, sf, st);
-  return launch_quantize_walk<LAT, BF16, false, LQ_SCALE_TILE_F32>(a, st);
+  return launch_quantize_walk<LAT, BF16, LQ_SCALE_TILE_F32>(a, st);
 }
 
 namespace {
@@ -277,20 +276,25 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
   a.dither_seed = dither_seed;
   int64_t max_cols = 0, units = 0;
   int k = 0;
+  const bool bf = (wdtype == LQ_BF16);
   for (int m = 0; m < n; ++m) {
     sa.seed[m] = seeds[m];
     sa.n[m] = cols[m];
     sa.out[m] = signs[m];
     if (cols[m] > max_cols) max_cols = cols[m];
     if (rows[m] == 0) continue;   // signs only
+    // the input as 128-byte lines, one warp unit (2048 columns of a row) per copy
+    if (!encode_row_lines_map(&a.maps[k], bf ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                              bf ? 2 : 4, W[m], rows[m], cols[m], ldw[m], bf ? 32 : 64))
+      return LQ_ERR_CUDA;
     QuantMat& M = a.mat[k++];
-    M.W = W[m]; M.codes = codes[m]; M.scales = reinterpret_cast<float*>(scales[m]); M.signs = signs[m];
-    M.rows = rows[m]; M.cols = cols[m]; M.ldw = ldw[m];
+    M.codes = codes[m]; M.scales = scales[m]; M.signs = signs[m];
+    M.rows = rows[m]; M.cols = cols[m];
     M.tiles_per_row = (int)(cols[m] / tile);
     M.chunks_per_row = (int)((cols[m] + kChunkCols - 1) / kChunkCols);
+    M.row_groups = (rows[m] + kQuantWarps - 1) / kQuantWarps;
     M.cta_begin = units;
-    M.cpr_recip = M.chunks_per_row == 1 ? 0 : ~0ull / (uint64_t)M.chunks_per_row + 1;
-    units += (rows[m] * M.chunks_per_row + kQuantThreads / 32 - 1) / (kQuantThreads / 32);
+    units += M.row_groups * M.chunks_per_row;
   }
   if (units >= ((int64_t)1 << 40)) return LQ_ERR_SHAPE;
   if (make_signs_too) {
@@ -304,7 +308,6 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
   a.beta = beta; a.sqrt_tile = sqrtf((float)tile); a.inv_tile = 1.0f / (float)tile;
   a.status = dev_status;
   a.cta_units = units;
-  const bool bf = (wdtype == LQ_BF16);
   switch (lattice) {
     case LQ_E8: return bf ? launch_quantize<LQ_E8, true>(a, sf, dither, s) : launch_quantize<LQ_E8, false>(a, sf, dither, s);
     case LQ_D4: return bf ? launch_quantize<LQ_D4, true>(a, sf, dither, s) : launch_quantize<LQ_D4, false>(a, sf, dither, s);

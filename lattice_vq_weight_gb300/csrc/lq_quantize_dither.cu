@@ -11,10 +11,10 @@ namespace {
 template <int LAT>
 lq_status dithered_for(QuantArgs& a, bool bf16, int sf, cudaStream_t st) {
   if (sf == LQ_SCALE_TILE_F16)
-    return bf16 ? launch_quantize_walk<LAT, true, false, LQ_SCALE_TILE_F16, true>(a, st)
-                : launch_quantize_walk<LAT, false, false, LQ_SCALE_TILE_F16, true>(a, st);
-  return bf16 ? launch_quantize_walk<LAT, true, false, LQ_SCALE_TILE_F32, true>(a, st)
-              : launch_quantize_walk<LAT, false, false, LQ_SCALE_TILE_F32, true>(a, st);
+    return bf16 ? launch_quantize_walk<LAT, true, LQ_SCALE_TILE_F16, true>(a, st)
+                : launch_quantize_walk<LAT, false, LQ_SCALE_TILE_F16, true>(a, st);
+  return bf16 ? launch_quantize_walk<LAT, true, LQ_SCALE_TILE_F32, true>(a, st)
+              : launch_quantize_walk<LAT, false, LQ_SCALE_TILE_F32, true>(a, st);
 }
 
 }  // namespace

@@ -12,10 +12,10 @@ namespace {
 template <int LAT>
 lq_status scaled16_for(QuantArgs& a, bool bf16, int sf, cudaStream_t st) {
   if (sf == LQ_SCALE_ROW_BF16)
-    return bf16 ? launch_quantize_walk<LAT, true, false, LQ_SCALE_ROW_BF16>(a, st)
-                : launch_quantize_walk<LAT, false, false, LQ_SCALE_ROW_BF16>(a, st);
-  return bf16 ? launch_quantize_walk<LAT, true, false, LQ_SCALE_TILE_F16>(a, st)
-              : launch_quantize_walk<LAT, false, false, LQ_SCALE_TILE_F16>(a, st);
+    return bf16 ? launch_quantize_walk<LAT, true, LQ_SCALE_ROW_BF16>(a, st)
+                : launch_quantize_walk<LAT, false, LQ_SCALE_ROW_BF16>(a, st);
+  return bf16 ? launch_quantize_walk<LAT, true, LQ_SCALE_TILE_F16>(a, st)
+              : launch_quantize_walk<LAT, false, LQ_SCALE_TILE_F16>(a, st);
 }
 
 }  // namespace

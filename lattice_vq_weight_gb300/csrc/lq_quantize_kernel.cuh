@@ -1,17 +1,35 @@
 // The quantize kernel (tile RHT + lattice nearest point) and its launch
 // templates, shared by the translation units that instantiate it
-// (lq_quantize.cu: float32 tile scales, single and grouped walks;
-// lq_quantize_fmt.cu: the 16-bit scale formats).
+// (lq_quantize.cu: float32 tile scales, one matrix or a group; lq_quantize_fmt.cu:
+// the 16-bit scale formats; lq_quantize_dither.cu: the subtractive dither).
 //
 // HyperQuant page, "Key algorithmic ingredients": per-tile randomized Hadamard
 // transform, then optimal low-dimensional lattice VQ (E8, D4, A2, Z1).
 // Conway & Sloane, Sphere Packings, Lattices and Groups, ch. 20: nearest-point
 // decoders.
 //
-// Work decomposition: a warp unit is one 2048-column chunk of one row; lane l
-// loads columns [64 l, 64 l + 64) of the chunk (see lq_device.cuh).  Units are
-// visited by a persistent grid of 4-warp CTAs, and each warp loads the raw
-// data of its next unit before working on the current one.
+// Work decomposition.  A warp unit is one 2048-column chunk of one row, and a
+// CTA unit the same chunk of four consecutive rows of one matrix (one per
+// warp), so the four warps of a CTA share the chunk's signs.  A persistent
+// grid strides over CTA units, numbered matrix by matrix, row group by row
+// group, chunk fastest; a grid that is a multiple of the chunks per row keeps
+// every CTA on one chunk of a matrix.
+//
+// Staging.  Each warp's input arrives by one TMA copy per unit (lane 0 issues
+// it, an mbarrier counts its bytes) into a two-stage ring: the matrix is read
+// as lines of 128 bytes with the 128-byte swizzle, one line per lane for bf16
+// (two for fp32), so each lane reads its own 64 columns back with
+// conflict-free 16-byte loads.  The copy of the next unit is in flight while
+// the current one is transformed.
+//
+// Registers.  Lane l holds columns [64 l, 64 l + 64) of the chunk as float2
+// p[32], p[j].x = column j and p[j].y = column j + 32: five butterfly stages
+// run as packed f32x2 pairs, the stage between the halves as scalars.  Tile
+// bits 6 and 7 (or 6 alone for 128-column tiles) sit in the lane index; one
+// pass through shared memory swaps them with register bits 3 and 4, so their
+// stages run in registers too, every 8-column block stays in one lane, and
+// .x / .y hold two different blocks for the decoders (lq_device.cuh); larger
+// tiles' remaining bits cross lanes with shuffles.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -20,195 +38,85 @@
 
 #include "lq_device.cuh"
 #include "lq_host.h"
+#include "lq_tma.cuh"
 
 namespace lq {
 
 constexpr int kQuantMaxMats = LQ_QUANTIZE_MAX_GROUP;
+constexpr int kQuantWarps = 4;
+constexpr int kQuantThreads = kQuantWarps * 32;
+constexpr long long kQuantWaitCycles = 2000000000ll;   // about a second: a TMA copy that never lands
 
-// ------------------------------------------------------------------ loading
-// Raw storage of one lane's 64 input columns.
-template <bool BF16> struct LaneRaw;
-template <> struct LaneRaw<true> { uint4 v[8]; };    // 64 bf16
-template <> struct LaneRaw<false> { uint4 v[16]; };  // 64 fp32
-
-template <bool BF16>
-__device__ __forceinline__ void load_raw(LaneRaw<BF16>& r, const void* base) {
-  const uint4* p = reinterpret_cast<const uint4*>(base);
-#pragma unroll
-  for (int i = 0; i < (BF16 ? 8 : 16); ++i) r.v[i] = __ldg(p + i);
-}
-
-// Sign masks of the lane's 64 columns.  bf16: one word per column pair with
-// bits 15 and 31 set where the sign is -1.  fp32: the 64 sign bits in 2 words.
-template <bool BF16> struct LaneSigns;
-template <> struct LaneSigns<true> { uint32_t m[32]; };
-template <> struct LaneSigns<false> { uint32_t bits[2]; };
-
-template <bool BF16>
-__device__ __forceinline__ void load_signs(LaneSigns<BF16>& s, const int8_t* signs_col0) {
-  const uint4* p = reinterpret_cast<const uint4*>(signs_col0);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = __ldg(p + q);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      // word w[h] holds the signs of columns 16q + 4h .. 16q + 4h + 3
-      if constexpr (BF16) {
-        s.m[8 * q + 2 * h] = __byte_perm(w[h], 0u, 0x1404) & 0x80008000u;
-        s.m[8 * q + 2 * h + 1] = __byte_perm(w[h], 0u, 0x3424) & 0x80008000u;
-      } else {
-        // bit 7 of each byte -> one bit per column
-        uint32_t b = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) b |= ((w[h] >> (8 * c + 7)) & 1u) << c;
-        const int col = 16 * q + 4 * h;
-        s.bits[col >> 5] |= b << (col & 31);
-      }
-    }
-  }
-}
-
-// bf16 pair masks of one lane kept in shared memory: uint4 q of lane l at
-// msk[q * 32 + l] holds the masks of column pairs 4q .. 4q+3 (conflict-free).
-__device__ __forceinline__ void store_sign_masks(uint4* msk, int lane, const int8_t* signs_col0) {
-  const uint4* p = reinterpret_cast<const uint4*>(signs_col0);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 v = __ldg(p + q);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      // sign words 2hh, 2hh+1 of this 16-byte run cover column pairs 8q + 4hh .. +3
-      const uint32_t a = w[2 * hh], b = w[2 * hh + 1];
-      msk[(2 * q + hh) * 32 + lane] = make_uint4(__byte_perm(a, 0u, 0x1404) & 0x80008000u,
-                                                 __byte_perm(a, 0u, 0x3424) & 0x80008000u,
-                                                 __byte_perm(b, 0u, 0x1404) & 0x80008000u,
-                                                 __byte_perm(b, 0u, 0x3424) & 0x80008000u);
-    }
-  }
-}
-
-__device__ __forceinline__ void unpack_bf16_smem_signs(const LaneRaw<true>& r, const uint4* msk, int lane,
-                                                       float2 (&p)[32]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 m = msk[i * 32 + lane];
-    const uint32_t w[4] = {r.v[i].x ^ m.x, r.v[i].y ^ m.y, r.v[i].z ^ m.z, r.v[i].w ^ m.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h)
-      p[4 * i + h] = make_float2(__uint_as_float(w[h] << 16), __uint_as_float(w[h] & 0xFFFF0000u));
-  }
-}
-
-// Unpack raw input to fp32 pairs with the signs applied (exact).
-template <bool BF16>
-__device__ __forceinline__ void unpack_signed(const LaneRaw<BF16>& r, const LaneSigns<BF16>& s,
-                                              float2 (&p)[32]) {
-  if constexpr (BF16) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const uint32_t x = w[h] ^ s.m[4 * i + h];
-        p[4 * i + h] = make_float2(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-      }
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t w[4] = {r.v[i].x, r.v[i].y, r.v[i].z, r.v[i].w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int col = 4 * i + h;
-        const uint32_t sb = ((s.bits[col >> 5] >> (col & 31)) & 1u) << 31;
-        const float v = __uint_as_float(w[h] ^ sb);
-        if (h & 1) p[col >> 1].y = v; else p[col >> 1].x = v;
-      }
-    }
-  }
-}
-
-// ------------------------------------------------------------------ staging
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// ------------------------------------------------------------------ quantize
-// One matrix of a quantize launch.  Its warp units (row, 2048-column chunk)
-// are numbered row * chunks_per_row + chunk and taken four at a time by the
-// four warps of a CTA: CTA unit k of the matrix (global CTA unit cta_begin + k)
-// holds warp units 4k .. 4k + 3, those past the matrix's end doing nothing.
-// The grid strides over CTA units, so every warp of a CTA is always in the
-// same matrix.  A warp unit's row is local / chunks_per_row, computed as the
-// high half of local * cpr_recip with cpr_recip = ceil(2^64 / chunks_per_row)
-// (exact for every local below 2^64 / chunks_per_row; 0 marks one chunk per
-// row), so the kernel divides nothing.
+// One matrix of a quantize launch.  Its CTA units are cta_begin ..
+// cta_begin + row_groups * chunks_per_row - 1.
 struct QuantMat {
-  const void* W;
   int8_t* codes;
-  float* scales;
+  void* scales;             // in the launch's scale format
   const int8_t* signs;
-  int64_t rows, cols, ldw;
-  int64_t cta_begin;
-  uint64_t cpr_recip;
+  int64_t rows, cols;
+  int64_t cta_begin, row_groups;
   int tiles_per_row, chunks_per_row;
 };
 
 struct QuantArgs {
+  CUtensorMap maps[kQuantMaxMats];   // the matrices' input, see encode_row_lines_map
   QuantMat mat[kQuantMaxMats];
   int n_mats;
   int tile, tile_shift, lanes_per_tile;
   float beta, sqrt_tile, inv_tile;
   int32_t* status;
-  int64_t cta_units;  // CTA units of all matrices
-  uint64_t dither_seed;   // subtractive dither (DITHER instantiations only)
+  int64_t cta_units;        // CTA units of all matrices
+  uint64_t dither_seed;     // subtractive dither (DITHER instantiations only)
 };
 
-constexpr int kQuantThreads = 128;
-
-// Shared memory per warp: two stages of raw input (each lane copies its own
-// 64 columns with cp.async and later reads back only its own copies) and, for
-// bf16, the lane's sign masks.  Once a stage has been read into registers it
-// doubles as the buffer of the butterfly exchange below, so a stage holds at
-// least the exchange's 284 16-byte slots.
+// Shared memory of a CTA: the chunk's sign masks, the parity-fix selectors,
+// the mbarriers and, per warp, two stages of raw input.  A stage also serves
+// as the buffer of the butterfly exchange once its input is in registers.
 template <bool BF16> struct QuantSmem {
-  static constexpr int kRawVec = BF16 ? 8 : 16;             // 16-byte vectors per lane per stage
-  static constexpr int kStageVec = BF16 ? 288 : 512;        // uint4 per warp per stage
-  static constexpr int kRawWords = 2 * kStageVec;           // uint4 per warp, both stages
-  static constexpr int kMaskWords = BF16 ? 8 * 32 : 0;      // uint4 per warp
-  static constexpr int kPerWarp = kRawWords + kMaskWords;
+  static constexpr int kBoxBytes = BF16 ? 4096 : 8192;               // one warp unit of input
+  static constexpr int kStageBytes = BF16 ? 5120 : 8192;             // >= the exchange's 280 16-byte slots
+  static constexpr int kMaskBytes = 16 * 32 * 16;                    // uint4 [16][32]
+  static constexpr int kSelOffset = kMaskBytes;                      // uint2 [9]
+  static constexpr int kBarOffset = kSelOffset + 128;                // uint64 [warps][2]
+  static constexpr int kStageOffset = 10240;                         // 1024-aligned
+  static constexpr int kBytes = kStageOffset + kQuantWarps * 2 * kStageBytes;
+  static constexpr int kDynamic = kBytes + 1024;                     // room to align the base
+  static_assert(kBarOffset + kQuantWarps * 2 * 8 <= kStageOffset, "layout");
+  static_assert(kStageBytes % 1024 == 0, "stages keep the 1024-byte alignment of the swizzle");
 };
 
-// Butterfly stages of tile bits 6 .. 6+MP-1 without shuffles.  After the six
-// register stages, lane bits 0 .. MP-1 of a lane hold tile bits 6 .. and its
-// register index bits 3 .. 3+MP-1 hold tile bits 3 ..; one pass through shared
-// memory swaps the two, so those stages run in registers as well and every
-// 8-coordinate block (tile bits 0 .. 2) stays in one lane.  The pass goes in
-// two halves (register bit 2) of 32 values per lane.  Slot of the value with
-// lane group G, spectator register bits ux, lane bits a and register bits c:
-//   (G >> (3 - MP)) * kBlk + ux * kUxSpan + (G & (X - 1)) * Q + a + 9 c,
+// ------------------------------------------------------------------ exchange
+// Swap of EX lane bits (tile bits 6, 7) with register bits 3, 4 of p (float2
+// index bits 3, 4) through shared memory, in two halves (float2 index bit 2)
+// of 8 16-byte slots per lane.  A slot holds p[j], p[j + 1] (j even) and is
+// named (u, h): xj<EX>(u, h) is its j; the low EX bits of u are the exchanged
+// register bits, the others spectators.  Slot of the value with lane group G,
+// spectator ux, lane bits a and register bits c:
+//   (G >> (3 - EX)) * kBlk + ux * kUxSpan + (G & (X - 1)) * Q + a + 9 c,
 // additive in a and c, so every access is a per-lane base plus a constant,
 // and conflict-free for 16-byte accesses both when a varies (writes) and when
 // c varies (reads): the slots of the 8 lanes of a phase differ modulo 8.
-template <int MP> struct Xchg {
-  static constexpr int Q = 1 << MP;          // lanes whose bits are swapped
-  static constexpr int X = 8 >> MP;          // spectator register values per half
+template <int EX> struct Xchg {
+  static constexpr int Q = 1 << EX;          // lanes whose bits are swapped
+  static constexpr int X = 8 >> EX;          // spectator values per half
   static constexpr int kUxSpan = 9 * Q - 1;
   static constexpr int kBlk = X * kUxSpan;
   static constexpr int kSlots = 4 * kBlk;
 };
-static_assert(Xchg<2>::kSlots <= 288 && Xchg<3>::kSlots <= 288, "exchange slots");
+static_assert(Xchg<1>::kSlots * 16 <= 5120 && Xchg<2>::kSlots * 16 <= 5120, "exchange slots fit a stage");
 
-template <int MP>
+template <int EX>
+__device__ __forceinline__ constexpr int xj(int u, int h) {
+  // EX = 2: u = (c3, c4, c1) low to high; EX = 1: u = (c3, c1, c4); h = c2
+  return EX == 2 ? (((u >> 2) << 1) | (h << 2) | ((u & 3) << 3))
+                 : ((((u >> 1) & 1) << 1) | (h << 2) | ((u & 1) << 3) | ((u >> 2) << 4));
+}
+
+template <int EX>
 __device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf, int lane) {
-  using XC = Xchg<MP>;
-  const int q = lane & (XC::Q - 1), G = lane >> MP;
-  const uint32_t g = (uint32_t)((G >> (3 - MP)) * XC::kBlk + (G & (XC::X - 1)) * XC::Q);
+  using XC = Xchg<EX>;
+  const int q = lane & (XC::Q - 1), G = lane >> EX;
+  const uint32_t g = (uint32_t)((G >> (3 - EX)) * XC::kBlk + (G & (XC::X - 1)) * XC::Q);
   const uint32_t wb = buf + (g + (uint32_t)q) * 16u;
   const uint32_t rb = buf + (g + 9u * (uint32_t)q) * 16u;
 #pragma unroll
@@ -216,26 +124,25 @@ __device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t off = (uint32_t)(((u >> MP) * XC::kUxSpan + 9 * (u & (XC::Q - 1))) * 16);
-      const float2 v0 = p[4 * u + 2 * h], v1 = p[4 * u + 2 * h + 1];
-      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(wb + off), "f"(v0.x), "f"(v0.y),
-                   "f"(v1.x), "f"(v1.y) : "memory");
+      const uint32_t off = (uint32_t)(((u >> EX) * XC::kUxSpan + 9 * (u & (XC::Q - 1))) * 16);
+      const int j = xj<EX>(u, h);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(wb + off), "f"(p[j].x), "f"(p[j].y),
+                   "f"(p[j + 1].x), "f"(p[j + 1].y) : "memory");
     }
     __syncwarp();
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-      const uint32_t off = (uint32_t)(((u >> MP) * XC::kUxSpan + (u & (XC::Q - 1))) * 16);
-      float2 v0, v1;
-      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v0.x), "=f"(v0.y), "=f"(v1.x), "=f"(v1.y)
+      const uint32_t off = (uint32_t)(((u >> EX) * XC::kUxSpan + (u & (XC::Q - 1))) * 16);
+      const int j = xj<EX>(u, h);
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                   : "=f"(p[j].x), "=f"(p[j].y), "=f"(p[j + 1].x), "=f"(p[j + 1].y)
                    : "r"(rb + off) : "memory");
-      p[4 * u + 2 * h] = v0;
-      p[4 * u + 2 * h + 1] = v1;
     }
   }
   __syncwarp();
-  // the swapped tile bits now sit in register index bits 3 .. 3+MP-1 (float2 bits 2 ..)
+  // the swapped tile bits now sit in float2 index bits 3 (and 4)
 #pragma unroll
-  for (int hp = 4; hp < (4 << MP); hp <<= 1) {
+  for (int hp = 8; hp < (8 << EX); hp <<= 1) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       if ((j & hp) == 0) {
@@ -247,256 +154,353 @@ __device__ __forceinline__ void exchange_tile_bits(float2 (&p)[32], uint32_t buf
   }
 }
 
-// GROUPED = false: one matrix (a.mat[0]); a warp takes warp units w, w + W,
-// w + 2W, ... (W = warps of the grid), advanced without divisions.
-// GROUPED = true: the CTA-unit walk over several matrices described above.
-// Both walks feed the same per-unit body; they are separate instantiations
-// because the single-matrix walk keeps fewer values live across the decode.
-// Residency: 4 CTAs per SM (128 registers) for the single-matrix walk, 3 (168
-// registers) for the grouped walk -- each measured faster than the other
-// choice for its walk.
+// Column (within the chunk) of coordinate 0 of register block (g, h) of a lane
+// after the exchange: p[8 g + i].x (h = 0) or .y (h = 1) is column
+// block_col + i.
+template <int EX>
+__device__ __forceinline__ int block_col(int lane, int g, int h) {
+  return EX == 2 ? 8 * (lane & 3) + 32 * h + 64 * ((lane & ~3) + g)
+                 : 8 * (lane & 1) + 64 * (lane & ~1) + 32 * h + 64 * (g & 1) + 16 * (g >> 1);
+}
+
+// Codes of one 8-coordinate register block (consecutive coordinates y) with
+// the scalar decoders of lq_device.cuh: one E8 block, two D4 blocks, four A2
+// blocks or eight Z1 values; CHECK adds the exact int8 range check.
+template <int LAT, bool CHECK>
+__device__ __forceinline__ uint2 decode_block8(const float2 (&y4)[4], bool& r) {
+  if constexpr (LAT == LQ_E8) {
+    const BlockCodes8 b = decode_e8<CHECK>(y4, r);
+    return make_uint2(b.w0, b.w1);
+  } else if constexpr (LAT == LQ_D4) {
+    const float2 a0[2] = {y4[0], y4[1]}, a1[2] = {y4[2], y4[3]};
+    return make_uint2(decode_d4<CHECK>(a0, r), decode_d4<CHECK>(a1, r));
+  } else if constexpr (LAT == LQ_A2) {
+    return make_uint2(decode_a2_pair<CHECK>(y4[0], r) | (decode_a2_pair<CHECK>(y4[1], r) << 16),
+                      decode_a2_pair<CHECK>(y4[2], r) | (decode_a2_pair<CHECK>(y4[3], r) << 16));
+  } else {
+    return make_uint2(decode_z1_quad<CHECK>(y4[0], y4[1], r), decode_z1_quad<CHECK>(y4[2], y4[3], r));
+  }
+}
+
+// ------------------------------------------------------------------ quantize
+// EX = tile bits exchanged through shared memory: 1 for 128-column tiles, 2
+// above.  XL: tiles of 512 ... 2048 columns, whose bits above 7 cross lanes
+// with shuffles (a separate instantiation: the shuffle loop's registers would
+// otherwise crowd the 128- and 256-column kernels).
 // DITHER: subtractive dither (lq_device.cuh) added to y before the decode.
-template <int LAT, bool BF16, int MP, bool GROUPED, int SF, bool DITHER = false>
-__global__ void __launch_bounds__(kQuantThreads, GROUPED ? 3 : 4) quantize_kernel(QuantArgs a) {
-  static_assert(!GROUPED || SF == LQ_SCALE_TILE_F32, "grouped calls store float32 tile scales");
-  static_assert(!(GROUPED && DITHER), "the dither runs on the single-matrix walk");
+template <int LAT, bool BF16, int EX, bool XL, int SF, bool DITHER = false>
+__global__ void __launch_bounds__(kQuantThreads, (BF16 && !XL) ? 4 : 3)
+    quantize_kernel(const __grid_constant__ QuantArgs a) {
   using SM = QuantSmem<BF16>;
-  extern __shared__ uint4 quant_smem[];
-  const int lane = threadIdx.x & 31;
-  uint4* wsm = quant_smem + (threadIdx.x >> 5) * SM::kPerWarp;
-  uint4* raw_sm = wsm;                          // [stage][vec][lane]
-  uint4* msk = wsm + SM::kRawWords;             // bf16 sign masks [q][lane]
-  const uint32_t raw_s = (uint32_t)__cvta_generic_to_shared(raw_sm);
-  constexpr int kElemBytes = BF16 ? 2 : 4;
+  extern __shared__ uint8_t quant_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(quant_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint4* mtab = reinterpret_cast<uint4*>(smem);                       // [16][32] sign masks
+  uint2* fixsel = reinterpret_cast<uint2*>(smem + SM::kSelOffset);    // [9]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::kBarOffset) + 2 * warp;
+  uint8_t* stage_base = smem + SM::kStageOffset + warp * 2 * SM::kStageBytes;
 
-  LaneSigns<false> sg;     // fp32 input keeps its 64 sign bits in registers
-  int cached_chunk = -1, cached_m = -1;
-  bool range = false, nonfinite = false;
+  if (threadIdx.x < 9) fixsel[threadIdx.x] = parity_fix_selector(threadIdx.x);
+  if (lane == 0) {
+    mbar_init1(&bar[0], 1);
+    mbar_init1(&bar[1], 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
 
-  // copy the lane's 64 input columns of unit (row, chunk) of M into stage st
-  auto stage_in = [&](bool valid, const QuantMat& M, int64_t row, int chunk, int st) {
-    const int64_t c = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    if (valid && row < M.rows && c < M.cols) {
-      const char* src = reinterpret_cast<const char*>(M.W) + (row * M.ldw + c) * kElemBytes;
-#pragma unroll
-      for (int i = 0; i < SM::kRawVec; ++i)
-        cp_async16(raw_s + (uint32_t)((st * SM::kStageVec + i * 32 + lane) * 16), src + 16 * i);
+  // (matrix, row, chunk) of CTA unit cu for this warp
+  struct Unit {
+    int m, chunk;
+    int64_t row;
+    bool valid;   // the unit exists and its row is inside the matrix
+  };
+  auto locate = [&](int64_t cu, Unit& u) {
+    u.valid = false;
+    if (cu >= a.cta_units) return;
+    while (u.m + 1 < a.n_mats && cu >= a.mat[u.m + 1].cta_begin) ++u.m;
+    const QuantMat& M = a.mat[u.m];
+    const int64_t local = cu - M.cta_begin;
+    const int64_t rg = local < 0x7FFFFFFF ? (int64_t)((uint32_t)local / (uint32_t)M.chunks_per_row)
+                                          : local / M.chunks_per_row;
+    u.chunk = (int)(local - rg * M.chunks_per_row);
+    u.row = rg * kQuantWarps + warp;
+    u.valid = u.row < M.rows;
+  };
+  auto issue = [&](const Unit& u, int st) {
+    if (lane == 0 && u.valid) {
+      mbar_expect_tx(&bar[st], SM::kBoxBytes);
+      tma_load_3d(stage_base + st * SM::kStageBytes, &a.maps[u.m], &bar[st], 0, u.chunk * (BF16 ? 32 : 64),
+                  (int)u.row);
     }
-    cp_async_commit();
   };
 
-  // quantize unit (row, chunk) of matrix m, whose input is in stage st
-  auto process = [&](const QuantMat& M, int m, int64_t row, int chunk, int st) {
-    const int64_t col0 = (int64_t)chunk * kChunkCols + (int64_t)lane * kLaneElems;
-    const bool active = col0 < M.cols;
-    if (chunk != cached_chunk || m != cached_m) {
-      if constexpr (BF16) {
-        if (active) store_sign_masks(msk, lane, M.signs + col0);
+  bool range = false, nonfinite = false, timed_out = false;
+  uint32_t phase = 0;          // bit s: parity of stage s's next completion
+  bool pending[2] = {false, false};
+  int key_m = -1, key_chunk = -1;
+  int st = 0;
+  int64_t cu = blockIdx.x;
+  Unit cur;
+  cur.m = 0;
+  locate(cu, cur);
+  issue(cur, 0);
+  pending[0] = cur.valid;
+  // the signs (and the per-row scales) come from the kernel launched before
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  for (; cu < a.cta_units; cu += gridDim.x) {
+    Unit nxt = cur;
+    locate(cu + gridDim.x, nxt);
+    // the other stage was read, and written by the exchange, for the previous
+    // unit: order those accesses before the copy that refills it
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (!timed_out) {
+      issue(nxt, st ^ 1);
+      pending[st ^ 1] = nxt.valid;
+    }
+
+    const QuantMat& M = a.mat[cur.m];
+    if (cur.m != key_m || cur.chunk != key_chunk) {
+      // sign masks of this chunk: entry (q, l) holds bit 31 set where the sign
+      // of column 64 l + 4 q + i (i = 0..3) is -1; for bf16 input these are the
+      // masks of the low and high halves of column pairs 2 q and 2 q + 1
+      __syncthreads();
+      for (int e = threadIdx.x; e < 16 * 32; e += kQuantThreads) {
+        const int q = e >> 5, l = e & 31;
+        const int64_t col = (int64_t)cur.chunk * kChunkCols + 64 * l + 4 * q;
+        uint32_t w = 0;
+        if (col < M.cols) w = *reinterpret_cast<const uint32_t*>(M.signs + col);
+        mtab[e] = make_uint4((w << 24) & 0x80000000u, (w << 16) & 0x80000000u, (w << 8) & 0x80000000u,
+                             w & 0x80000000u);
+      }
+      __syncthreads();
+      key_m = cur.m;
+      key_chunk = cur.chunk;
+    }
+
+    if (cur.valid && !timed_out) {
+      if (!mbar_wait_bounded(&bar[st], (phase >> st) & 1u, kQuantWaitCycles)) {
+        timed_out = true;
       } else {
-        sg.bits[0] = 0;
-        sg.bits[1] = 0;
-        if (active) load_signs<false>(sg, M.signs + col0);
-      }
-      cached_chunk = chunk;
-      cached_m = m;
-    }
-    cp_async_wait1();   // this unit's copies have landed
-
-    float2 p[32];
-    {
-      LaneRaw<BF16> raw;
-#pragma unroll
-      for (int i = 0; i < SM::kRawVec; ++i) raw.v[i] = raw_sm[st * SM::kStageVec + i * 32 + lane];
-      if constexpr (BF16) unpack_bf16_smem_signs(raw, msk, lane, p);
-      else unpack_signed<false>(raw, sg, p);
-    }
-    fwht64_local(p);
-    if constexpr (MP > 0) exchange_tile_bits<MP>(p, raw_s + (uint32_t)(st * SM::kStageVec * 16), lane);
-    // lane bits not exchanged (MP = 0: all of them; tiles of 1024 and 2048
-    // columns: tile bits 9 .. on lane bits 3 ..) cross lanes with shuffles
-    for (int mm = (MP == 0 ? 1 : 8); mm < a.lanes_per_tile; mm <<= 1) {
-      const float sgn = (lane & mm) ? -1.0f : 1.0f;
-      const float2 sg2 = make_float2(sgn, sgn);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float2 o;
-        o.x = __shfl_xor_sync(0xffffffffu, p[j].x, mm);
-        o.y = __shfl_xor_sync(0xffffffffu, p[j].y, mm);
-        p[j] = fma2(p[j], sg2, o);
+        phase ^= 1u << st;
+        pending[st] = false;
       }
     }
+    if (cur.valid && !timed_out) {
+      const uint8_t* raw = stage_base + st * SM::kStageBytes;
+      const int64_t col0 = (int64_t)cur.chunk * kChunkCols + (int64_t)lane * kLaneElems;
+      const bool active = col0 < M.cols;
 
-    // U = sum u^2 over the tile; s = beta sqrt(U) / T; y = u / (s sqrt(T))
-    float2 acc = make_float2(0.f, 0.f);
+      // ---- load, signs, bf16 -> fp32 (exact)
+      float2 p[32];
+      if constexpr (BF16) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) acc = fma2(p[j], p[j], acc);
-    const float U = tile_lane_sum(acc.x + acc.y, a.lanes_per_tile);
-    const bool finite = isfinite(U);
-    // s: the value of the stored scale (the codes are decoded against it)
-    float s;
-    bool over = false;
-    __half s16;
-    if constexpr (SF == LQ_SCALE_ROW_BF16) {
-      // written by the row-norm kernel that precedes this one
-      s = __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(M.scales)[row] << 16);
-    } else {
-      s = a.beta * sqrtf(U) * a.inv_tile;
-      if (!finite) s = 0.f;
-      if constexpr (SF == LQ_SCALE_TILE_F16) {
-        s16 = __float2half_rn(s);
-        s = __half2float(s16);
-        over = isinf(s);
-        if (over) s = 0.f;
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = *reinterpret_cast<const uint4*>(raw + 128 * lane + 16 * (i ^ (lane & 7)));
+          const uint4 m0 = mtab[(2 * i) * 32 + lane], m1 = mtab[(2 * i + 1) * 32 + lane];
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          const uint32_t ml[4] = {m0.x, m0.z, m1.x, m1.z}, mh[4] = {m0.y, m0.w, m1.y, m1.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            // word 4 i + h = columns c = 8 i + 2 h (low half) and c + 1
+            const float lo = __uint_as_float(imad(w[h], 65536u, ml[h]));
+            const float hi = __uint_as_float((w[h] & 0xFFFF0000u) ^ mh[h]);
+            const int c = 8 * i + 2 * h;
+            if (c < 32) { p[c].x = lo; p[c + 1].x = hi; }
+            else { p[c - 32].y = lo; p[c - 31].y = hi; }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int line = 2 * lane + (i >> 3);
+          const uint4 v = *reinterpret_cast<const uint4*>(raw + 128 * line + 16 * ((i & 7) ^ (line & 7)));
+          const uint4 m = mtab[i * 32 + lane];
+          const uint32_t w[4] = {v.x ^ m.x, v.y ^ m.y, v.z ^ m.z, v.w ^ m.w};
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int c = 4 * i + h;
+            if (c < 32) p[c].x = __uint_as_float(w[h]);
+            else p[c - 32].y = __uint_as_float(w[h]);
+          }
+        }
       }
-    }
-    const float k = (s > 0.f) ? 1.0f / (s * a.sqrt_tile) : 0.f;
-    const float2 k2 = make_float2(k, k);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) p[j] = mul2(p[j], k2);
 
-    constexpr int Q = 1 << MP;
-    if constexpr (DITHER) {
-      // y + u for tiles with a scale (a zero scale keeps y = 0 and zero codes);
-      // register block g holds the 8 columns 8 q + 8 Q gx + 64 ga (see the store)
-      if (k > 0.f) {
-        const uint64_t c_row = (uint64_t)row * (uint64_t)M.cols + (uint64_t)chunk * kChunkCols +
-                               (uint64_t)((lane >> MP) * (64 * Q) + 8 * (lane & (Q - 1)));
+      // ---- Hadamard: register bits 0..4 (packed), the halves, the exchanged bits, shuffles
 #pragma unroll
-        for (int gb = 0; gb < 8; ++gb) {
-          float u[8];
-          dither8<LAT>(a.dither_seed, c_row + (uint64_t)((gb >> MP) * (8 * Q) + 64 * (gb & (Q - 1))), u);
+      for (int hp = 1; hp < 32; hp <<= 1) {
 #pragma unroll
-          for (int h = 0; h < 4; ++h) p[4 * gb + h] = add2(p[4 * gb + h], make_float2(u[2 * h], u[2 * h + 1]));
+        for (int j = 0; j < 32; ++j) {
+          if ((j & hp) == 0) {
+            const float2 x0 = p[j], x1 = p[j + hp];
+            p[j] = add2(x0, x1);
+            p[j + hp] = sub2(x0, x1);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) p[j] = make_float2(p[j].x + p[j].y, p[j].x - p[j].y);
+      exchange_tile_bits<EX>(p, smem_addr(raw), lane);
+      if constexpr (XL) for (int mm = 1 << EX; mm < a.lanes_per_tile; mm <<= 1) {
+        const float sgn = (lane & mm) ? -1.0f : 1.0f;
+        const float2 sg2 = make_float2(sgn, sgn);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float2 o;
+          o.x = __shfl_xor_sync(0xffffffffu, p[j].x, mm);
+          o.y = __shfl_xor_sync(0xffffffffu, p[j].y, mm);
+          p[j] = fma2(p[j], sg2, o);
+        }
+      }
+
+      // ---- scale: U = sum u^2 over the tile; s = beta sqrt(U) / T; y = u / (s sqrt(T))
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc = fma2(p[j], p[j], acc);
+      const float lane_u2 = acc.x + acc.y;
+      const float U = tile_lane_sum(lane_u2, a.lanes_per_tile);
+      const bool finite = isfinite(U);
+      float s;
+      bool over = false;
+      __half s16;
+      if constexpr (SF == LQ_SCALE_ROW_BF16) {
+        s = __uint_as_float((uint32_t)reinterpret_cast<const unsigned short*>(M.scales)[cur.row] << 16);
+      } else {
+        s = a.beta * sqrtf(U) * a.inv_tile;
+        if (!finite) s = 0.f;
+        if constexpr (SF == LQ_SCALE_TILE_F16) {
+          s16 = __float2half_rn(s);
+          s = __half2float(s16);
+          over = isinf(s);
+          if (over) s = 0.f;
+        }
+      }
+      if (!finite) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) p[j] = make_float2(0.f, 0.f);   // the tile's codes are zeros
+      }
+      float k = (s > 0.f) ? 1.0f / (s * a.sqrt_tile) : 0.f;
+
+      int8_t* dst = M.codes + cur.row * M.cols + (int64_t)cur.chunk * kChunkCols;
+      if constexpr (DITHER) {
+        // y + u (u the dither draw of each element's counter row * cols + col)
+        // for tiles with a scale; the decoders then see y with k = 1
+        const float2 k2 = make_float2(k, k);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) p[j] = mul2(p[j], k2);
+        if (k > 0.f) {
+          const uint64_t c_row = (uint64_t)cur.row * (uint64_t)M.cols + (uint64_t)cur.chunk * kChunkCols;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              float u[8];
+              dither8<LAT>(a.dither_seed, c_row + (uint64_t)block_col<EX>(lane, g, h), u);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                if (h == 0) p[8 * g + i].x += u[i];
+                else p[8 * g + i].y += u[i];
+              }
+            }
+          }
+        }
+        k = 1.f;
+      }
+
+      // ---- decode.  Every |y| of the lane below 62.5 keeps every code inside
+      // int8 and allows the packed fast decoders; the lane's sum of y^2 decides
+      // that for free in most cases, the lane maximum otherwise.
+      bool small = !DITHER && lane_u2 * (k * k) < 3906.25f;
+      if (!small) {
+        float mx = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
+        small = mx * k < 62.5f;
+      }
+      const float2 k2 = make_float2(k, k);
+      bool r = false;
+      if ((LAT == LQ_E8 || LAT == LQ_Z1) && small) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float2 u[8] = {p[8 * g], p[8 * g + 1], p[8 * g + 2], p[8 * g + 3],
+                               p[8 * g + 4], p[8 * g + 5], p[8 * g + 6], p[8 * g + 7]};
+          uint2 cP, cQ;
+          if constexpr (LAT == LQ_E8) decode_e8_pair(u, k2, fixsel, cP, cQ);
+          else decode_z1_pair(u, k2, cP, cQ);
+          if (active) {
+            *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 0)) = cP;
+            *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 1)) = cQ;
+          }
+        }
+      } else {
+        // scalar decoders (with the exact int8 range check unless the lane is
+        // known to be small) on the blocks regrouped as consecutive pairs
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float y[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) y[i] = (h ? p[8 * g + i].y : p[8 * g + i].x) * k;
+            const float2 y4[4] = {make_float2(y[0], y[1]), make_float2(y[2], y[3]), make_float2(y[4], y[5]),
+                                  make_float2(y[6], y[7])};
+            uint2 w;
+            if (small) w = decode_block8<LAT, false>(y4, r);
+            else w = decode_block8<LAT, true>(y4, r);
+            if (active) *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, h)) = w;
+          }
+        }
+      }
+
+      if (active) {
+        range |= r | over;
+        nonfinite |= !finite;
+        if ((lane & (a.lanes_per_tile - 1)) == 0) {
+          const int64_t si = cur.row * M.tiles_per_row + (col0 >> a.tile_shift);
+          if constexpr (SF == LQ_SCALE_TILE_F32) reinterpret_cast<float*>(M.scales)[si] = s;
+          if constexpr (SF == LQ_SCALE_TILE_F16) reinterpret_cast<__half*>(M.scales)[si] = s16;
         }
       }
     }
-    // every |y| of the lane below 62.5 keeps every code inside int8, and the
-    // per-block range check is left out; the lane's sum of y^2 decides that
-    // for free in most cases (not with a dither, which moves y), the lane
-    // maximum otherwise
-    const float lane_y2 = (acc.x + acc.y) * (k * k);
-    bool small = !DITHER && lane_y2 < 3906.25f;
-    if (!small) {
-      float mx = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
-      small = mx < 62.5f;
-    }
-    uint32_t w[16];
-    bool r = false;
-    if (small) decode_lane<LAT, false>(p, w, r);
-    else decode_lane<LAT, true>(p, w, r);
-
-    if (active) {
-      range |= r | over;
-      nonfinite |= !finite;
-      // register block u holds tile columns 8 q + 8 Q ux + 64 a (q = lane bits,
-      // ux = u >> MP, a = u & (Q - 1)) of the tile group G = lane >> MP
-      int8_t* dst = M.codes + row * M.cols + (int64_t)chunk * kChunkCols + (lane >> MP) * (64 * Q) +
-                    8 * (lane & (Q - 1));
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint2*>(dst + (u >> MP) * (8 * Q) + 64 * (u & (Q - 1))) = make_uint2(w[2 * u], w[2 * u + 1]);
-      if ((lane & (a.lanes_per_tile - 1)) == 0) {
-        const int64_t si = row * M.tiles_per_row + (col0 >> a.tile_shift);
-        if constexpr (SF == LQ_SCALE_TILE_F32) M.scales[si] = s;
-        if constexpr (SF == LQ_SCALE_TILE_F16) reinterpret_cast<__half*>(M.scales)[si] = s16;
-      }
-    }
-  };
-
-  int stage = 0;
-  if constexpr (!GROUPED) {
-    const QuantMat& M = a.mat[0];
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    // unit u = row * chunks_per_row + chunk grows by nwarps per step
-    const int64_t d_row = nwarps / M.chunks_per_row;
-    const int d_chunk = (int)(nwarps % M.chunks_per_row);
-    int64_t row = warp0 / M.chunks_per_row;
-    int chunk = (int)(warp0 % M.chunks_per_row);
-    stage_in(true, M, row, chunk, 0);
-    // the signs come from the kernel launched just before this one
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    while (row < M.rows) {
-      int64_t nrow = row + d_row;
-      int nchunk = chunk + d_chunk;
-      if (nchunk >= M.chunks_per_row) { nchunk -= M.chunks_per_row; ++nrow; }
-      stage_in(true, M, nrow, nchunk, stage ^ 1);
-      process(M, 0, row, chunk, stage);
-      row = nrow;
-      chunk = nchunk;
-      stage ^= 1;
-    }
-  } else {
-    // (matrix, row, chunk) of a CTA unit's warp unit for this warp
-    struct Pos {
-      int m, chunk;
-      int64_t row;
-    };
-    const int wic = threadIdx.x >> 5;   // warp in the CTA
-    auto locate = [&](int64_t cu, Pos& p) {
-      while (p.m + 1 < a.n_mats && cu >= a.mat[p.m + 1].cta_begin) ++p.m;
-      const QuantMat& M = a.mat[p.m];
-      const uint64_t local = (uint64_t)(cu - M.cta_begin) * (kQuantThreads / 32) + (uint64_t)wic;
-      const uint64_t r = M.cpr_recip ? __umul64hi(local, M.cpr_recip) : local;
-      p.row = (int64_t)r;
-      p.chunk = (int)(local - r * (uint64_t)M.chunks_per_row);
-    };
-    int64_t cu = blockIdx.x;
-    Pos cur;
-    cur.m = 0;
-    cur.row = 0;
-    cur.chunk = 0;
-    if (cu < a.cta_units) locate(cu, cur);
-    stage_in(cu < a.cta_units, a.mat[cur.m], cur.row, cur.chunk, 0);
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (; cu < a.cta_units; cu += gridDim.x) {
-      const int64_t cn = cu + gridDim.x;
-      Pos nxt = cur;
-      if (cn < a.cta_units) locate(cn, nxt);
-      stage_in(cn < a.cta_units, a.mat[nxt.m], nxt.row, nxt.chunk, stage ^ 1);
-      const QuantMat& M = a.mat[cur.m];
-      if (cur.row < M.rows) process(M, cur.m, cur.row, cur.chunk, stage);   // else past the matrix's end
-      cur = nxt;
-      stage ^= 1;
-    }
+    cur = nxt;
+    st ^= 1;
   }
-  cp_async_wait0();
+  // copies still in flight (only after a timeout) land before the CTA exits
+  for (int s2 = 0; s2 < 2; ++s2)
+    if (pending[s2]) mbar_wait_bounded(&bar[s2], (phase >> s2) & 1u, kQuantWaitCycles);
   if (__any_sync(0xffffffffu, range) && lane == 0) raise_flag(a.status, LQ_DEV_RANGE);
   if (__any_sync(0xffffffffu, nonfinite) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
+  if (__any_sync(0xffffffffu, timed_out) && lane == 0) raise_flag(a.status, LQ_DEV_TIMEOUT);
 }
 
-inline int64_t gcd64(int64_t x, int64_t y) {
-  while (y) {
-    const int64_t t = x % y;
-    x = y;
-    y = t;
-  }
-  return x;
-}
-
-template <int LAT, bool BF16, int MP, bool GROUPED, int SF, bool DITHER = false>
-inline lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
-  constexpr size_t smem = (size_t)(kQuantThreads / 32) * QuantSmem<BF16>::kPerWarp * sizeof(uint4);
+template <int LAT, bool BF16, int EX, bool XL, int SF, bool DITHER = false>
+inline lq_status launch_quantize_ex(QuantArgs& a, cudaStream_t st) {
+  constexpr int smem = QuantSmem<BF16>::kDynamic;
   static int per_sm = 0;
   if (per_sm == 0) {
-    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, MP, GROUPED, SF, DITHER>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) {
+    if (cudaFuncSetAttribute(quantize_kernel<LAT, BF16, EX, XL, SF, DITHER>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
       cudaGetLastError();
       return LQ_ERR_CUDA;
     }
-    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, MP, GROUPED, SF, DITHER>, kQuantThreads, smem);
+    per_sm = occupancy_per_sm(quantize_kernel<LAT, BF16, EX, XL, SF, DITHER>, kQuantThreads, smem);
   }
-  // a warp count that is a multiple of every matrix's chunks per row keeps
-  // each warp on one chunk (one set of signs) within a matrix
+  // a CTA count that is a multiple of every matrix's chunks per row keeps
+  // each CTA on one chunk (one set of signs) within a matrix
   int64_t modulus = 1;
   for (int m = 0; m < a.n_mats; ++m) {
     const int64_t c = a.mat[m].chunks_per_row;
-    modulus = modulus / gcd64(modulus, c) * c;
+    int64_t x = modulus, y = c;
+    while (y) {
+      const int64_t t = x % y;
+      x = y;
+      y = t;
+    }
+    modulus = modulus / x * c;
     if (modulus > 64) { modulus = 1; break; }
   }
-  const int grid = persistent_grid(a.cta_units * (kQuantThreads / 32), kQuantThreads / 32, (int)modulus, per_sm);
+  const int grid = persistent_grid(a.cta_units, 1, (int)modulus, per_sm);
   if (grid <= 0) return LQ_ERR_CUDA;
   // programmatic dependent launch after the signs (or row-norm) kernel
   cudaLaunchConfig_t cfg = {};
@@ -509,28 +513,26 @@ inline lq_status launch_quantize_mp(QuantArgs& a, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, MP, GROUPED, SF, DITHER>, a) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, quantize_kernel<LAT, BF16, EX, XL, SF, DITHER>, a) != cudaSuccess) {
     cudaGetLastError();
     return LQ_ERR_CUDA;
   }
   return LQ_OK;
 }
 
-// MP = tile bits exchanged through shared memory: log2(tile / 64), at most 3.
-// A 128-column tile has a single cross-lane stage, cheaper as a shuffle (MP = 0).
-template <int LAT, bool BF16, bool GROUPED, int SF, bool DITHER = false>
+template <int LAT, bool BF16, int SF, bool DITHER = false>
 inline lq_status launch_quantize_walk(QuantArgs& a, cudaStream_t st) {
-  if (a.lanes_per_tile == 2) return launch_quantize_mp<LAT, BF16, 0, GROUPED, SF, DITHER>(a, st);
-  if (a.lanes_per_tile == 4) return launch_quantize_mp<LAT, BF16, 2, GROUPED, SF, DITHER>(a, st);
-  return launch_quantize_mp<LAT, BF16, 3, GROUPED, SF, DITHER>(a, st);
+  if (a.lanes_per_tile == 2) return launch_quantize_ex<LAT, BF16, 1, false, SF, DITHER>(a, st);
+  if (a.lanes_per_tile == 4) return launch_quantize_ex<LAT, BF16, 2, false, SF, DITHER>(a, st);
+  return launch_quantize_ex<LAT, BF16, 2, true, SF, DITHER>(a, st);
 }
 
-// Launch of the single-matrix walk with a 16-bit scale format
-// (LQ_SCALE_ROW_BF16 or LQ_SCALE_TILE_F16), defined in lq_quantize_fmt.cu.
+// Launch with a 16-bit scale format (LQ_SCALE_ROW_BF16 or LQ_SCALE_TILE_F16),
+// defined in lq_quantize_fmt.cu.
 lq_status launch_quantize_scaled16(QuantArgs& a, int lattice, bool bf16, int sf, cudaStream_t st);
 
-// Launch of the single-matrix walk with the subtractive dither (scale format
-// LQ_SCALE_TILE_F32 or LQ_SCALE_TILE_F16), defined in lq_quantize_dither.cu.
+// Launch with the subtractive dither (scale format LQ_SCALE_TILE_F32 or
+// LQ_SCALE_TILE_F16), defined in lq_quantize_dither.cu.
 lq_status launch_quantize_dithered(QuantArgs& a, int lattice, bool bf16, int sf, cudaStream_t st);
 
 }  // namespace lq
