@@ -31,11 +31,11 @@
 #include "lq_act.cuh"
 #include "lq_device.cuh"
 #include "lq_host.h"
+#include "lq_tma.cuh"
 
 namespace lq {
 
 struct GemvMat {
-  const int8_t* codes;
   const void* scales;    // in the launch's scale format (gemv_kernel's SF)
   float* y;
   int64_t rows;
@@ -44,6 +44,7 @@ struct GemvMat {
 };
 
 struct GemvArgs {
+  CUtensorMap maps[kGemvMaxMats];   // codes of each matrix, boxes of 64 columns x 16 RG rows
   GemvMat mat[kGemvMaxMats];
   int n_mats;
   int64_t cols;
@@ -52,53 +53,70 @@ struct GemvArgs {
   const float* xs;       // [n_mats x batch x tiles]
   int64_t steps;         // total steps (row group, 64-column slice) of all matrices
   int64_t warps;         // warps of the persistent grid
+  int32_t* status;       // LQ_DEV_TIMEOUT if a code copy never landed
 };
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+constexpr long long kGemvWaitCycles = 2000000000ll;   // about a second
 
 // Work: a step is one 64-column slice of one group of 16 RG rows; the steps of
-// all matrices are ordered matrix, row group, column.  Warp w of the
-// persistent grid takes the contiguous step range [w S / W, (w+1) S / W), so
+// all matrices are ordered matrix, row group, column.  Steps come in pairs
+// (a "box": 128 columns of the group, copied as one unit), and warp w of the
+// persistent grid takes the contiguous box range [w B / W, (w+1) B / W), so
 // every warp streams the same number of code bytes whatever the tile size or
 // the matrices' shapes.  The per-tile scale is applied when a tile ends or
 // the range ends (the tile sum splits linearly), and a warp flushes its
 // per-row sums whenever its range leaves a row group -- with plain stores
 // when it covered the whole row, else with fp32 atomics.
 //
-// Fragment mapping (g = lane/4, q4 = lane%4): within a step the thread loads
-// 16 code bytes of rows g and g+8 at columns 16 q4 .. 16 q4 + 15; MMA k-chunk
-// c uses bytes 4c .. 4c+3, i.e. k-slots (2 q4, 2 q4+1, 2 q4+8, 2 q4+9) hold
-// columns 16 q4 + 4c + (0, 1, 2, 3).  The activation fragment of column n = g
-// uses the same permutation, so the dot products are unchanged.
+// Fragment mapping (g = lane/4, q4 = lane%4): within a step the thread uses
+// 16 code bytes of rows rg and rg+8 of each 16-row block (rg a permutation of
+// g, see below) at columns 16 q4 .. 16 q4 + 15; MMA k-chunk c uses bytes 4c .. 4c+3, i.e. k-slots (2 q4, 2 q4+1,
+// 2 q4+8, 2 q4+9) hold columns 16 q4 + 4c + (0, 1, 2, 3).  The activation
+// fragment of column n = g uses the same permutation, so the dot products are
+// unchanged.
 //
-// Code loads go through a per-thread ring of S stages in shared memory filled
-// with cp.async (each thread reads back only what it copied, so the only wait
-// is cp.async.wait_group on its own copies).  The ring is filled before
-// griddepcontrol.wait: codes do not depend on the activation kernel that
-// precedes this one, so with programmatic dependent launch the code stream
-// starts while that kernel is still running.
+// Codes arrive by TMA: one 2-D box per box unit (128 columns x 16 RG rows,
+// a full 128-byte line of each row, 128-byte swizzle) into a ring of S stages
+// per warp, issued by lane 0 S - 1 boxes ahead and counted on the stage's
+// mbarrier; rows past the matrix read as zeros.  With the swizzle (16-byte
+// chunk c of row r at chunk c ^ (r & 7)) a quarter warp reads 8 distinct
+// chunk positions, so the 16-byte loads are conflict-free.  The ring is filled
+// before griddepcontrol.wait: codes do not depend on the activation kernel
+// that precedes this one, so with programmatic dependent launch the code
+// stream starts while that kernel is still running.
 template <int NB, int RG, int S, int SF>
-__global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) {
-  constexpr int kCode = RG * 2;        // 16-byte code slots per thread per stage
+__global__ void __launch_bounds__(128, NB == 1 ? 5 : 3) gemv_kernel(const __grid_constant__ GemvArgs a) {
+  constexpr int kBoxBytes = 16 * RG * 128;
+  constexpr int kWarps = 4;
   static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
-  extern __shared__ uint4 gemv_ring[];
+  extern __shared__ __align__(1024) uint8_t gemv_smem_raw[];
+  // 1024-byte alignment of every stage (the swizzle pattern repeats every 8 rows)
+  uint8_t* gemv_smem = gemv_smem_raw + ((1024u - (smem_addr(gemv_smem_raw) & 1023u)) & 1023u);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, q4 = lane & 3;
-  uint4* ring = gemv_ring + (size_t)warp * S * kCode * 32;
-  const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  // matrix row (within each 8-row half of a 16-row block) of MMA fragment row
+  // g: rows 2j and 2j + 1 of the fragment, read by one quarter warp, sit 4 rows
+  // apart, so that the swizzle puts their chunks on different banks
+  const int rg = (g >> 1) | ((g & 1) << 2);
+  uint8_t* ring = gemv_smem + warp * S * kBoxBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(gemv_smem + kWarps * S * kBoxBytes) + warp * S;
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-  const int64_t i0 = w * a.steps / a.warps;
-  const int64_t i1 = (w + 1) * a.steps / a.warps;
+  const int64_t boxes = a.steps >> 1;
+  const int64_t b0 = w * boxes / a.warps;
+  const int64_t b1 = (w + 1) * boxes / a.warps;
+  const int64_t i0 = 2 * b0;
+  const int64_t n_box = b1 - b0;
+  const int64_t n_it = 2 * n_box;
   const int steps = a.tile >> 6;                 // steps per tile (power of two)
-  const int64_t n_it = i1 - i0;
-  const int per_grp = a.tiles_per_row * steps;          // steps per row group
+  const int per_grp = a.tiles_per_row * steps;          // steps per row group (even)
+
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < S; ++i) mbar_init1(&bar[i], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
 
   const bool xok0 = g < a.batch;
   const bool xok1 = NB > 1 && 8 + g < a.batch;
@@ -122,53 +140,29 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
     c.s = (int)(local - (int64_t)c.grp * per_grp);
     return c;
   };
-  auto advance = [&](Cursor& c) {
-    if (++c.s == per_grp) {
+  auto advance = [&](Cursor& c, int by) {
+    c.s += by;
+    if (c.s == per_grp) {
       c.s = 0;
       if (++c.grp == a.mat[c.m].groups) { c.grp = 0; ++c.m; }
     }
   };
-  auto kof = [&](const Cursor& c) { return (int64_t)c.s * 64; };
-  Cursor ci = start_cursor();   // next step to issue
+  Cursor ci = start_cursor();   // next box to issue (always at an even step)
   Cursor cx = ci;               // next step whose activations to load
   Cursor cm = ci;               // step being computed
-  // row pointers of the row group the issue cursor is in (recomputed only
-  // when the cursor enters a new row group)
-  const int8_t* irow[RG][2];
-  bool iok[RG][2];
-  int igrp = -1, im = -1;
-  int istage = 0;                         // ring stage the next issue writes
-  auto issue = [&](int64_t it) {
-    if (it < n_it) {
-      if (ci.grp != igrp || ci.m != im) {
-        igrp = ci.grp;
-        im = ci.m;
-        const int8_t* codes = a.mat[im].codes;
-        const int64_t rows = a.mat[im].rows;
-#pragma unroll
-        for (int i = 0; i < RG; ++i)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t r = (int64_t)igrp * 16 * RG + 16 * i + 8 * h + g;
-            iok[i][h] = r < rows;
-            irow[i][h] = codes + (iok[i][h] ? r : 0) * a.cols + 16 * q4;
-          }
+  auto issue = [&](int64_t ib) {
+    if (ib < n_box) {
+      if (lane == 0) {
+        const int st = (int)(ib & (S - 1));
+        mbar_expect_tx(&bar[st], kBoxBytes);
+        tma_load_2d(ring + st * kBoxBytes, &a.maps[ci.m], &bar[st], ci.s * 64, ci.grp * 16 * RG);
       }
-      const int64_t k0 = kof(ci);
-      const uint32_t islot = ring_s + (uint32_t)((istage * kCode * 32 + lane) * 16);
-#pragma unroll
-      for (int i = 0; i < RG; ++i)
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          cp_async16(islot + (uint32_t)(((2 * i + h) * 32) * 16), irow[i][h] + k0, iok[i][h]);
-      istage = (istage + 1) & (S - 1);
-      advance(ci);
+      advance(ci, 2);
     }
-    cp_async_commit();
   };
   auto load_x = [&](int64_t it, uint4 (&h)[NB][2]) {
     if (it < n_it) {
-      const int64_t k0 = kof(cx) + (int64_t)cx.m * xmat;
+      const int64_t k0 = (int64_t)cx.s * 64 + (int64_t)cx.m * xmat;
       if (xok0) {
         h[0][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0));
         h[0][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0) + 1);
@@ -179,13 +173,13 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
           h[1][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0) + 1);
         }
       }
-      advance(cx);
+      advance(cx, 1);
     }
   };
 
   // code prefetch first (independent of the preceding kernel), then wait for it
 #pragma unroll
-  for (int it = 0; it < S - 1; ++it) issue(it);
+  for (int ib = 0; ib < S - 1; ++ib) issue(ib);
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   float yacc[RG][NB][4], acc[RG][NB][4];
@@ -200,6 +194,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
   for (int n = 0; n < NB; ++n) xhv[n][0] = xhv[n][1] = nxh[n][0] = nxh[n][1] = make_uint4(0, 0, 0, 0);
   load_x(0, xhv);
   int cur_grp = -1, cur_m = -1, steps_in_grp = 0;
+  bool timed_out = false;
 
   auto flush = [&]() {
     const bool whole_row = steps_in_grp == per_grp;
@@ -211,7 +206,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
       for (int n = 0; n < NB; ++n)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const int64_t r = (int64_t)cur_grp * 16 * RG + 16 * i + 8 * (c >> 1) + g;
+          const int64_t r = (int64_t)cur_grp * 16 * RG + 16 * i + 8 * (c >> 1) + rg;
           const int bb = n * 8 + 2 * q4 + (c & 1);
           if (r < rows && bb < a.batch) {
             float* dst = y + (int64_t)bb * rows + r;
@@ -221,89 +216,115 @@ __global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(GemvArgs a) 
         }
   };
 
-  for (int64_t it = 0; it < n_it; ++it) {
-    issue(it + S - 1);
-    load_x(it + 1, nxh);
-    const int grp = cm.grp;
-    const int m = cm.m;
-    const int t = cm.s >> steps_log2;
-    const bool tile_end = (cm.s & (steps - 1)) == steps - 1;
-    advance(cm);
-    if (grp != cur_grp || m != cur_m) {
-      if (cur_grp >= 0) flush();
-      cur_grp = grp;
-      cur_m = m;
-      steps_in_grp = 0;
+  // swizzled 16-byte chunk of the thread in rows 8 h + rg of a block: column
+  // chunk 4 sub + q4 sits at chunk (4 sub + q4) ^ rg (every block starts at a
+  // multiple of 8 rows)
+  const int off0 = 128 * rg + 16 * ((0 + q4) ^ rg);
+  const int off1 = 128 * rg + 16 * ((4 + q4) ^ rg);
+
+  int64_t ib = 0;
+  for (; ib < n_box; ++ib) {
+    // the stage refilled now was read for the previous box: order those reads
+    // before the copy that overwrites it
+    fence_proxy_async_smem();
+    __syncwarp();
+    issue(ib + S - 1);
+    const int st = (int)(ib & (S - 1));
+    if (!mbar_wait_bounded(&bar[st], (uint32_t)((ib / S) & 1), kGemvWaitCycles)) {
+      timed_out = true;
+      break;
     }
-    ++steps_in_grp;
-    cp_async_wait<S - 1>();
-    const uint4* slot = ring + (size_t)(it & (S - 1)) * kCode * 32 + lane;
-    uint4 cw[RG][2];
+    const uint8_t* box = ring + st * kBoxBytes;
 #pragma unroll
-    for (int i = 0; i < RG; ++i) {
-      cw[i][0] = slot[(2 * i) * 32];
-      cw[i][1] = slot[(2 * i + 1) * 32];
-    }
+    for (int sub = 0; sub < 2; ++sub) {
+      const int64_t it = 2 * ib + sub;
+      load_x(it + 1, nxh);
+      const int grp = cm.grp;
+      const int m = cm.m;
+      const int t = cm.s >> steps_log2;
+      const bool tile_end = (cm.s & (steps - 1)) == steps - 1;
+      advance(cm, 1);
+      if (grp != cur_grp || m != cur_m) {
+        if (cur_grp >= 0) flush();
+        cur_grp = grp;
+        cur_m = m;
+        steps_in_grp = 0;
+      }
+      ++steps_in_grp;
+      const uint8_t* slot = box + (sub ? off1 : off0);
+      uint4 cw[RG][2];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t bh[NB][2];
+      for (int i = 0; i < RG; ++i) {
+        cw[i][0] = *reinterpret_cast<const uint4*>(slot + 128 * (16 * i));
+        cw[i][1] = *reinterpret_cast<const uint4*>(slot + 128 * (16 * i + 8));
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t bh[NB][2];
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          const uint4& H = xhv[n][c >> 1];
+          bh[n][0] = (c & 1) ? H.z : H.x;
+          bh[n][1] = (c & 1) ? H.w : H.y;
+        }
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+          const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
+          const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
+          uint32_t a0, a2, a1, a3;
+          codes_to_f16x2(wa, a0, a2);
+          codes_to_f16x2(wb, a1, a3);
+#pragma unroll
+          for (int n = 0; n < NB; ++n) {
+            mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
+          }
+        }
+      }
+      if (tile_end || it == n_it - 1) {
+        // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
+        const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
+        const void* scales = a.mat[m].scales;
+        const int64_t rows = a.mat[m].rows;
+        float fx[NB][2];
+#pragma unroll
+        for (int n = 0; n < NB; ++n)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int bb = n * 8 + 2 * q4 + h;
+            fx[n][h] = (bb < a.batch) ? __ldg(xs + (int64_t)bb * a.tiles_per_row) : 0.f;
+          }
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+          float sr[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t r = (int64_t)grp * 16 * RG + 16 * i + 8 * h + rg;
+            sr[h] = (r < rows) ? load_scale_t<SF>(scales, r, t, a.tiles_per_row) : 0.f;
+          }
+#pragma unroll
+          for (int n = 0; n < NB; ++n) {
+            yacc[i][n][0] = fmaf(acc[i][n][0], sr[0] * fx[n][0], yacc[i][n][0]);
+            yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
+            yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
+            yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+          }
+        }
+      }
 #pragma unroll
       for (int n = 0; n < NB; ++n) {
-        const uint4& H = xhv[n][c >> 1];
-        bh[n][0] = (c & 1) ? H.z : H.x;
-        bh[n][1] = (c & 1) ? H.w : H.y;
+        xhv[n][0] = nxh[n][0]; xhv[n][1] = nxh[n][1];
       }
-#pragma unroll
-      for (int i = 0; i < RG; ++i) {
-        const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
-        const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
-        uint32_t a0, a2, a1, a3;
-        codes_to_f16x2(wa, a0, a2);
-        codes_to_f16x2(wb, a1, a3);
-#pragma unroll
-        for (int n = 0; n < NB; ++n) {
-          mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
-        }
-      }
-    }
-    if (tile_end || it == n_it - 1) {
-      // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
-      const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
-      const void* scales = a.mat[m].scales;
-      const int64_t rows = a.mat[m].rows;
-      float fx[NB][2];
-#pragma unroll
-      for (int n = 0; n < NB; ++n)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int bb = n * 8 + 2 * q4 + h;
-          fx[n][h] = (bb < a.batch) ? __ldg(xs + (int64_t)bb * a.tiles_per_row) : 0.f;
-        }
-#pragma unroll
-      for (int i = 0; i < RG; ++i) {
-        float sr[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t r = (int64_t)grp * 16 * RG + 16 * i + 8 * h + g;
-          sr[h] = (r < rows) ? load_scale_t<SF>(scales, r, t, a.tiles_per_row) : 0.f;
-        }
-#pragma unroll
-        for (int n = 0; n < NB; ++n) {
-          yacc[i][n][0] = fmaf(acc[i][n][0], sr[0] * fx[n][0], yacc[i][n][0]);
-          yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
-          yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
-          yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-        }
-      }
-    }
-#pragma unroll
-    for (int n = 0; n < NB; ++n) {
-      xhv[n][0] = nxh[n][0]; xhv[n][1] = nxh[n][1];
     }
   }
-  cp_async_wait<0>();
+  if (timed_out) {
+    // copies issued for boxes ib .. ib + S - 1 may still be in flight: let them land
+    for (int64_t j = ib; j < n_box && j < ib + S; ++j)
+      mbar_wait_bounded(&bar[j & (S - 1)], (uint32_t)((j / S) & 1), kGemvWaitCycles);
+    if (lane == 0) raise_flag(a.status, LQ_DEV_TIMEOUT);
+    return;
+  }
   if (cur_grp >= 0) flush();
 }
 
@@ -334,9 +355,9 @@ constexpr int64_t kMinStepsPerWarp = 4;
 
 template <int NB, int RG, int SF>
 lq_status launch_gemv(const GemvArgs& a0, cudaStream_t st) {
-  constexpr int S = 4;                       // ring stages per warp
+  constexpr int S = 2;                       // ring stages (boxes) per warp
   constexpr int kWarps = 4;
-  constexpr size_t smem = (size_t)kWarps * S * (RG * 2) * 32 * 16;
+  constexpr size_t smem = (size_t)kWarps * S * (16 * RG * 128) + (size_t)kWarps * S * 8 + 1024;
   GemvArgs a = a0;
   static int per_sm = 0;
   if (per_sm == 0) {
@@ -439,15 +460,16 @@ lq_status gemv_group(int lattice, int n, const int8_t* const* codes_dev, const v
   if (st != LQ_OK) return st;
 
   GemvArgs g = {};
+  constexpr int kRowsPerStep = 32;   // 16 RG rows (RG = 2 in every instantiation below)
   for (int j = 0; j < ne; ++j) {
-    g.mat[j].codes = codes_dev[idx[j]];
+    if (!encode_codes_map(&g.maps[j], codes_dev[idx[j]], rows[idx[j]], cols, kRowsPerStep)) return LQ_ERR_CUDA;
     g.mat[j].scales = scales_dev[idx[j]];
     g.mat[j].y = y_dev[idx[j]];
     g.mat[j].rows = rows[idx[j]];
   }
   g.n_mats = ne;
   g.cols = cols; g.tile = tile; g.tiles_per_row = (int)(cols / tile); g.batch = batch;
-  g.xh = r.xh; g.xs = r.xs;
+  g.xh = r.xh; g.xs = r.xs; g.status = dev_status_dev;
   if (sfmt == LQ_SCALE_ROW_BF16)
     return batch <= 8 ? launch_gemv<1, 2, LQ_SCALE_ROW_BF16>(g, s) : launch_gemv<2, 2, LQ_SCALE_ROW_BF16>(g, s);
   if (sfmt == LQ_SCALE_TILE_F16)

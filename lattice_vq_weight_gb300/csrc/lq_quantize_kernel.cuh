@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kQuantThreads, (BF16 && !XL) ? 4 : 3)
     quantize_kernel(const __grid_constant__ QuantArgs a) {
   using SM = QuantSmem<BF16>;
   extern __shared__ uint8_t quant_smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(quant_smem_raw) + 1023) & ~uintptr_t(1023));
+  // aligned by pointer arithmetic on the shared array, so that accesses stay
+  // known shared-memory accesses
+  uint8_t* smem = quant_smem_raw + ((1024u - (smem_addr(quant_smem_raw) & 1023u)) & 1023u);
   uint4* mtab = reinterpret_cast<uint4*>(smem);                       // [16][32] sign masks
   uint2* fixsel = reinterpret_cast<uint2*>(smem + SM::kSelOffset);    // [9]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -176,9 +176,17 @@ def test_gemm_bf16_output(N, K, M):
     gb = Yb[:, ridx].float().cpu().numpy()
     assert normwise_rel(gb, ref) < TOL + 2.0 ** -8
     yf = Yf.cpu().numpy()
+    yb = Yb.float().cpu().numpy()
     rounded = Yf.to(torch.bfloat16).float().cpu().numpy()
-    diff = np.abs(Yb.float().cpu().numpy() - rounded)
-    assert np.all(diff <= _bf16_ulp(yf) * 1.0001), float(diff.max())
+    diff = np.abs(yb - rounded)
+    # one bf16 step, measured in the larger binade where the two straddle a power of two;
+    # plus the float32 summation-order noise of a K-split launch (its partial sums are
+    # added by atomics in any order), which near a cancellation can exceed the bf16 step
+    # of a tiny result: 2^-20 of the output's scale bounds it with room to spare
+    step = _bf16_ulp(np.maximum(np.abs(yb), np.abs(rounded)))
+    noise = 2.0 ** -20 * np.max(np.abs(yf))
+    excess = diff - (step * 1.0001 + noise)
+    assert np.all(excess <= 0), (float(excess.max()), float(diff.max()))
 
 
 def test_gemm_wait_expiry_reports_timeout_and_recovers():
