@@ -85,7 +85,7 @@ constexpr long long kGemvWaitCycles = 2000000000ll;   // about a second
 // that precedes this one, so with programmatic dependent launch the code
 // stream starts while that kernel is still running.
 template <int NB, int RG, int S, int SF>
-__global__ void __launch_bounds__(128, NB == 1 ? 5 : 3) gemv_kernel(const __grid_constant__ GemvArgs a) {
+__global__ void __launch_bounds__(128, NB == 1 ? 4 : 3) gemv_kernel(const __grid_constant__ GemvArgs a) {
   constexpr int kBoxBytes = 16 * RG * 128;
   constexpr int kWarps = 4;
   static_assert((S & (S - 1)) == 0, "ring size must be a power of two");
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(128, NB == 1 ? 5 : 3) gemv_kernel(const __grid
     }
   };
   Cursor ci = start_cursor();   // next box to issue (always at an even step)
-  Cursor cx = ci;               // next step whose activations to load
+  Cursor cb = ci;               // next box whose activations to load
   Cursor cm = ci;               // step being computed
   auto issue = [&](int64_t ib) {
     if (ib < n_box) {
@@ -160,20 +160,24 @@ __global__ void __launch_bounds__(128, NB == 1 ? 5 : 3) gemv_kernel(const __grid
       advance(ci, 2);
     }
   };
-  auto load_x = [&](int64_t it, uint4 (&h)[NB][2]) {
-    if (it < n_it) {
-      const int64_t k0 = (int64_t)cx.s * 64 + (int64_t)cx.m * xmat;
-      if (xok0) {
-        h[0][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0));
-        h[0][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff0 + k0) + 1);
-      }
-      if constexpr (NB > 1) {
-        if (xok1) {
-          h[1][0] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0));
-          h[1][1] = __ldg(reinterpret_cast<const uint4*>(a.xh + xoff1 + k0) + 1);
+  // activations of both steps of box ib (loaded one box ahead of their use)
+  auto load_xbox = [&](int64_t ib, uint4 (&h)[2][NB][2]) {
+    if (ib < n_box) {
+      const __half* xb = a.xh + (int64_t)cb.m * xmat + (int64_t)cb.s * 64;
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub) {
+        if (xok0) {
+          h[sub][0][0] = __ldg(reinterpret_cast<const uint4*>(xb + xoff0 + 64 * sub));
+          h[sub][0][1] = __ldg(reinterpret_cast<const uint4*>(xb + xoff0 + 64 * sub) + 1);
+        }
+        if constexpr (NB > 1) {
+          if (xok1) {
+            h[sub][1][0] = __ldg(reinterpret_cast<const uint4*>(xb + xoff1 + 64 * sub));
+            h[sub][1][1] = __ldg(reinterpret_cast<const uint4*>(xb + xoff1 + 64 * sub) + 1);
+          }
         }
       }
-      advance(cx, 1);
+      advance(cb, 2);
     }
   };
 
@@ -189,12 +193,18 @@ __global__ void __launch_bounds__(128, NB == 1 ? 5 : 3) gemv_kernel(const __grid
     for (int n = 0; n < NB; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) yacc[i][n][c] = acc[i][n][c] = 0.f;
-  uint4 xhv[NB][2], nxh[NB][2];
+  uint4 xA[2][NB][2], xB[2][NB][2];
 #pragma unroll
-  for (int n = 0; n < NB; ++n) xhv[n][0] = xhv[n][1] = nxh[n][0] = nxh[n][1] = make_uint4(0, 0, 0, 0);
-  load_x(0, xhv);
+  for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+    for (int n = 0; n < NB; ++n)
+      xA[sub][n][0] = xA[sub][n][1] = xB[sub][n][0] = xB[sub][n][1] = make_uint4(0, 0, 0, 0);
+  load_xbox(0, xA);
   int cur_grp = -1, cur_m = -1, steps_in_grp = 0;
   bool timed_out = false;
+  // scales of the tile being accumulated: s[r, t] for the thread's rows and
+  // 2^-e[b, t] for its batch columns, loaded when the tile starts
+  float scur[RG][2], fcur[NB][2];
 
   auto flush = [&]() {
     const bool whole_row = steps_in_grp == per_grp;
@@ -222,101 +232,106 @@ __global__ void __launch_bounds__(128, NB == 1 ? 5 : 3) gemv_kernel(const __grid
   const int off0 = 128 * rg + 16 * ((0 + q4) ^ rg);
   const int off1 = 128 * rg + 16 * ((4 + q4) ^ rg);
 
-  int64_t ib = 0;
-  for (; ib < n_box; ++ib) {
+  // one 64-column step: codes of the box at sub-step `sub`, activations xh
+  auto do_step = [&](const uint8_t* box, int sub, const uint4 (&xh)[NB][2], int64_t it) {
+    const int grp = cm.grp;
+    const int m = cm.m;
+    const int t = cm.s >> steps_log2;
+    const bool tile_start = (cm.s & (steps - 1)) == 0 || it == 0;
+    const bool tile_end = (cm.s & (steps - 1)) == steps - 1 || it == n_it - 1;
+    advance(cm, 1);
+    if (grp != cur_grp || m != cur_m) {
+      if (cur_grp >= 0) flush();
+      cur_grp = grp;
+      cur_m = m;
+      steps_in_grp = 0;
+    }
+    ++steps_in_grp;
+    if (tile_start) {
+      const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
+      const void* scales = a.mat[m].scales;
+      const int64_t rows = a.mat[m].rows;
+#pragma unroll
+      for (int n = 0; n < NB; ++n)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int bb = n * 8 + 2 * q4 + h;
+          fcur[n][h] = (bb < a.batch) ? __ldg(xs + (int64_t)bb * a.tiles_per_row) : 0.f;
+        }
+#pragma unroll
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t r = (int64_t)grp * 16 * RG + 16 * i + 8 * h + rg;
+          scur[i][h] = (r < rows) ? load_scale_t<SF>(scales, r, t, a.tiles_per_row) : 0.f;
+        }
+    }
+    const uint8_t* slot = box + (sub ? off1 : off0);
+    uint4 cw[RG][2];
+#pragma unroll
+    for (int i = 0; i < RG; ++i) {
+      cw[i][0] = *reinterpret_cast<const uint4*>(slot + 128 * (16 * i));
+      cw[i][1] = *reinterpret_cast<const uint4*>(slot + 128 * (16 * i + 8));
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t bh[NB][2];
+#pragma unroll
+      for (int n = 0; n < NB; ++n) {
+        const uint4& H = xh[n][c >> 1];
+        bh[n][0] = (c & 1) ? H.z : H.x;
+        bh[n][1] = (c & 1) ? H.w : H.y;
+      }
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
+        const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
+        uint32_t a0, a2, a1, a3;
+        codes_to_f16x2(wa, a0, a2);
+        codes_to_f16x2(wb, a1, a3);
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
+        }
+      }
+    }
+    if (tile_end) {
+#pragma unroll
+      for (int i = 0; i < RG; ++i)
+#pragma unroll
+        for (int n = 0; n < NB; ++n) {
+          yacc[i][n][0] = fmaf(acc[i][n][0], scur[i][0] * fcur[n][0], yacc[i][n][0]);
+          yacc[i][n][1] = fmaf(acc[i][n][1], scur[i][0] * fcur[n][1], yacc[i][n][1]);
+          yacc[i][n][2] = fmaf(acc[i][n][2], scur[i][1] * fcur[n][0], yacc[i][n][2]);
+          yacc[i][n][3] = fmaf(acc[i][n][3], scur[i][1] * fcur[n][1], yacc[i][n][3]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
+        }
+    }
+  };
+
+  // one box: refill the ring, prefetch the next box's activations, compute
+  // both steps with the activations X (the next box's go to Xn)
+  auto do_box = [&](int64_t ib, const uint4 (&X)[2][NB][2], uint4 (&Xn)[2][NB][2]) -> bool {
     // the stage refilled now was read for the previous box: order those reads
     // before the copy that overwrites it
     fence_proxy_async_smem();
     __syncwarp();
     issue(ib + S - 1);
+    load_xbox(ib + 1, Xn);
     const int st = (int)(ib & (S - 1));
-    if (!mbar_wait_bounded(&bar[st], (uint32_t)((ib / S) & 1), kGemvWaitCycles)) {
-      timed_out = true;
-      break;
-    }
+    if (!mbar_wait_bounded(&bar[st], (uint32_t)((ib / S) & 1), kGemvWaitCycles)) return false;
     const uint8_t* box = ring + st * kBoxBytes;
-#pragma unroll
-    for (int sub = 0; sub < 2; ++sub) {
-      const int64_t it = 2 * ib + sub;
-      load_x(it + 1, nxh);
-      const int grp = cm.grp;
-      const int m = cm.m;
-      const int t = cm.s >> steps_log2;
-      const bool tile_end = (cm.s & (steps - 1)) == steps - 1;
-      advance(cm, 1);
-      if (grp != cur_grp || m != cur_m) {
-        if (cur_grp >= 0) flush();
-        cur_grp = grp;
-        cur_m = m;
-        steps_in_grp = 0;
-      }
-      ++steps_in_grp;
-      const uint8_t* slot = box + (sub ? off1 : off0);
-      uint4 cw[RG][2];
-#pragma unroll
-      for (int i = 0; i < RG; ++i) {
-        cw[i][0] = *reinterpret_cast<const uint4*>(slot + 128 * (16 * i));
-        cw[i][1] = *reinterpret_cast<const uint4*>(slot + 128 * (16 * i + 8));
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t bh[NB][2];
-#pragma unroll
-        for (int n = 0; n < NB; ++n) {
-          const uint4& H = xhv[n][c >> 1];
-          bh[n][0] = (c & 1) ? H.z : H.x;
-          bh[n][1] = (c & 1) ? H.w : H.y;
-        }
-#pragma unroll
-        for (int i = 0; i < RG; ++i) {
-          const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
-          const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
-          uint32_t a0, a2, a1, a3;
-          codes_to_f16x2(wa, a0, a2);
-          codes_to_f16x2(wb, a1, a3);
-#pragma unroll
-          for (int n = 0; n < NB; ++n) {
-            mma16816(acc[i][n], a0, a1, a2, a3, bh[n][0], bh[n][1]);
-          }
-        }
-      }
-      if (tile_end || it == n_it - 1) {
-        // per-tile scale: s[r, t] for rows (g, g+8) times 2^-e[b, t] for columns (2 q4, 2 q4 + 1)
-        const float* xs = a.xs + (int64_t)m * a.batch * a.tiles_per_row + t;
-        const void* scales = a.mat[m].scales;
-        const int64_t rows = a.mat[m].rows;
-        float fx[NB][2];
-#pragma unroll
-        for (int n = 0; n < NB; ++n)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int bb = n * 8 + 2 * q4 + h;
-            fx[n][h] = (bb < a.batch) ? __ldg(xs + (int64_t)bb * a.tiles_per_row) : 0.f;
-          }
-#pragma unroll
-        for (int i = 0; i < RG; ++i) {
-          float sr[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t r = (int64_t)grp * 16 * RG + 16 * i + 8 * h + rg;
-            sr[h] = (r < rows) ? load_scale_t<SF>(scales, r, t, a.tiles_per_row) : 0.f;
-          }
-#pragma unroll
-          for (int n = 0; n < NB; ++n) {
-            yacc[i][n][0] = fmaf(acc[i][n][0], sr[0] * fx[n][0], yacc[i][n][0]);
-            yacc[i][n][1] = fmaf(acc[i][n][1], sr[0] * fx[n][1], yacc[i][n][1]);
-            yacc[i][n][2] = fmaf(acc[i][n][2], sr[1] * fx[n][0], yacc[i][n][2]);
-            yacc[i][n][3] = fmaf(acc[i][n][3], sr[1] * fx[n][1], yacc[i][n][3]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) acc[i][n][c] = 0.f;
-          }
-        }
-      }
-#pragma unroll
-      for (int n = 0; n < NB; ++n) {
-        xhv[n][0] = nxh[n][0]; xhv[n][1] = nxh[n][1];
-      }
-    }
+    do_step(box, 0, X[0], 2 * ib);
+    do_step(box, 1, X[1], 2 * ib + 1);
+    return true;
+  };
+
+  int64_t ib = 0;
+  for (; ib < n_box; ib += 2) {
+    // boxes in pairs, so that the two activation register sets alternate
+    if (!do_box(ib, xA, xB)) { timed_out = true; break; }
+    if (ib + 1 < n_box && !do_box(ib + 1, xB, xA)) { ++ib; timed_out = true; break; }
   }
   if (timed_out) {
     // copies issued for boxes ib .. ib + S - 1 may still be in flight: let them land
