@@ -102,7 +102,10 @@ __global__ void __launch_bounds__(256) rotate_activation_kernel(RotateArgs a) {
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_flag(a.status, LQ_DEV_NONFINITE);
 }
 
-// int8 codes (4 per word) -> two f16x2 words holding the exact values.
+// int8 codes (4 per word) -> two f16x2 words holding the exact values: the
+// offset byte u = c + 128 under the fp16 exponent of 1024 (bits 0x6400 | u are
+// 1024 + u), minus 1152 -- the magic-number conversion of Kim et al. 2022
+// ("Who Says Elephants Can't Run").
 __device__ __forceinline__ void codes_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t u = w ^ 0x80808080u;  // c + 128 as unsigned bytes
   const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);

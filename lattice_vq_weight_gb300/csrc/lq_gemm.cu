@@ -181,7 +181,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// int8 codes (4 per word) -> f16x2 words (exact), then times the fp16 scale.
+// int8 codes (4 per word) -> f16x2 words (exact: the magic-number conversion of
+// Kim et al. 2022, "Who Says Elephants Can't Run"), then times the fp16 scale.
 __device__ __forceinline__ uint32_t code_pair_f16(uint32_t u, uint32_t sel, __half2 sf) {
   const uint32_t h = __byte_perm(u, 0x64646464u, sel);
   const __half2 off = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152

@@ -14,7 +14,9 @@
 //     the prefill GEMM's fp16 activations).  It also zeroes y.
 //  2. gemv_kernel: warps stream 16-row groups of int8 codes with 16-byte loads,
 //     turn them into exact fp16 values (magic-number conversion: the fp16 with
-//     bits 0x6400 | u is 1024 + u), and run m16n8k16 fp16 MMAs with fp32
+//     bits 0x6400 | u is 1024 + u for a byte u; the fast int8 -> fp16 conversion
+//     of Kim et al., "Who Says Elephants Can't Run: Bringing Large Scale MoE
+//     Models into Cloud Scale Production", 2022), and run m16n8k16 fp16 MMAs with fp32
 //     accumulation against the activation.  One accumulator per tile is scaled by
 //     s[r, t] * 2^-e[b, t] and summed; warps that split a row combine with
 //     fp32 atomics.
