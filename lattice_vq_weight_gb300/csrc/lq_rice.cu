@@ -15,8 +15,9 @@
 // Kernels: one thread per segment for the encoder passes (lengths, then bits
 // with atomicOr into the zeroed stream) and the decoder; a three-pass scan turns
 // lengths into offsets.  The GEMV gives each lane one row of a 32-row group:
-// the lane decodes its row 64 columns at a time into shared memory, in the
-// fragment layout of the int8-code GEMV, and the warp runs the same fp16 MMAs.
+// the lane decodes its row 64 columns at a time, from a shared-memory ring
+// that the warp fills with coalesced background copies of the rows' stream,
+// into the fragment layout of the int8-code GEMV, and the warp runs fp16 MMAs.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -330,19 +331,91 @@ struct GemvRiceArgs {
   int64_t warps;
 };
 
+// Per row of a warp's 32-row group, a ring of two 32-word chunks of the row's
+// part of the stream: the region starts at the 32-word line holding the row's
+// first segment, and word w of it (w from the region's start; s = the word of
+// the segment's first bit) sits at ring index (w - s) & 63, so that rows that
+// have decoded the same number of codes read distinct banks.  Index 64 holds a
+// copy of index 0, so that a two-word window read never wraps.  The odd row
+// stride (65 words) spreads the rows over the banks.
+constexpr int kRingWords = 65;
+
+// One 4-byte global -> shared copy in the background (`bytes` 4, or 0 to
+// write a zero without reading).
+__device__ __forceinline__ void cp_async4(uint32_t* dst, const uint32_t* src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Four zigzag values (plus kone each) in bytes -> four codes 2 u + k in bytes:
+// per byte u2 = v ^ (0 - (v & 1)) is twice the signed value, ORed with the
+// block's parity bit (kp: 0x01010101 or 0).
+__device__ __forceinline__ uint32_t codes_from_zigzag4(uint32_t vb0, uint32_t vb1, uint32_t vb2, uint32_t vb3,
+                                                       uint32_t kk, uint32_t kp) {
+  const uint32_t vw = ((vb3 * 256u + vb2) * 65536u + (vb1 * 256u + vb0)) - kk;
+  const uint32_t m = (vw & 0x01010101u) * 0xFFu;
+  return (vw ^ m) | kp;
+}
+
+// The last code of an even-sum block (E8, D4) in byte 3 of `w`: the format
+// stores half of its halved value; the halved value is 2 * that + the parity
+// of the sum of the block's other halved values.  `w0` is the block's other
+// code word for E8 (zero for D4).  Bit 1 of a code is the parity of its halved
+// value, so the parity of the sum is bit 1 of the XOR of the other codes,
+// summed into bit 25 by one multiply.
+template <bool TWO_WORDS>
+__device__ __forceinline__ uint32_t fix_last_code(uint32_t w0, uint32_t w) {
+  const uint32_t t = TWO_WORDS ? ((w0 ^ w) & 0x02020202u) : (w & 0x00020202u);
+  const uint32_t p = t * 0x01010101u;                 // bit 25: parity (E8: XOR bit 1 of code 7 too)
+  const uint32_t a = w << 1;                          // code 7 doubled in byte 3 (bit 24: junk)
+  const uint32_t sel = (w & 0x01FFFFFFu) | (a & 0xFE000000u);
+  const uint32_t q = TWO_WORDS ? (p ^ w ^ a) : (p ^ a);  // bit 25: the sum parity, less what sel holds
+  return sel ^ (q & 0x02000000u);
+}
+
 // Items are (32-row group, tile) pairs; warp w takes [w I / W, (w+1) I / W).
-// Lane l decodes row 32 grp + l: 64 codes per step, stored as four 16-byte
-// chunks at the shared-memory slots the int8-code GEMV fills with cp.async
-// (slot (2i + h) * 32 + 4 g + q holds columns 16 q .. 16 q + 15 of row
-// 16 i + 8 h + g), so the MMA part is the same.
+// Lane l decodes row 32 grp + l, 64 codes per step, into the shared-memory
+// slots of the int8-code GEMV's fragment layout (slot (2i + h) * 32 + 4 g + q
+// holds columns 16 q .. 16 q + 15 of row 16 i + 8 h + g; here chunk q of row
+// g is stored at q ^ (g >> 1), which makes both the decoder's 16-byte stores
+// and the fragment loads conflict-free), and the warp runs fp16 MMAs on them.
+//
+// The decoder takes two Rice symbols from one 32-bit window of the lane's
+// ring: a symbol's unary run and closing zero are counted as the popcount of
+// x ^ (x + 1), its K low bits follow, and the window is shifted on.  Four
+// decoded values are packed into one word and un-zigzagged bytewise.  A step
+// is redone from the stream in global memory with the sequential reader when a
+// pair of symbols (with a block's parity bit) does not fit in its window, or
+// when the step read words whose chunk had not landed.  Chunks are copied by
+// the whole warp, one row's 32 words per instruction, as the rows' positions
+// free ring slots.
 template <int LAT, int NB>
-__global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
+__global__ void __launch_bounds__(128, 4) gemv_rice_kernel(const GemvRiceArgs a) {
   constexpr int n = Fmt<LAT>::n;
+  __shared__ uint32_t rings[4][32 * kRingWords];
   __shared__ uint4 slots[4][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* ring = rings[warp];
+  uint32_t* myring = ring + lane * kRingWords;
   uint4* slot = slots[warp];
   const int g = lane >> 2, q4 = lane & 3;
   const int di = lane >> 4, dh = (lane >> 3) & 1, dg = lane & 7;   // the row this lane decodes
+  uint4* myslot = slot + (2 * di + dh) * 32 + 4 * dg;
+  const int mysw = dg >> 1;
+  const int rdsw = g >> 1;
+  // 8 codes (columns 8 j .. 8 j + 7 of this lane's row) as two words: chunk
+  // (j >> 1) ^ (g >> 1), half (j & 1) ^ h of the chunk -- the half swap makes
+  // the 8-byte stores of a half warp conflict-free; the reader undoes it.
+  auto store_half = [&](uint4* base, int j, uint32_t lo, uint32_t hi) {
+    reinterpret_cast<uint2*>(base + ((j >> 1) ^ mysw))[(j & 1) ^ dh] = make_uint2(lo, hi);
+  };
   const int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
   const int64_t i0 = w * a.items / a.warps, i1 = (w + 1) * a.items / a.warps;
   const int steps = a.tile >> 6;
@@ -365,6 +438,13 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
   int64_t cur_grp = -1;
   int tiles_in_grp = 0;
 
+  // The lane's region of the stream: base word wb (a multiple of 32), the
+  // segment's first word s (0..31) from wb, the bit position posr from word
+  // wb + s; chunks [0, ic) issued, [0, landed) landed.
+  uint32_t wb = 0, s = 0, posr = 0;
+  int ic = 0, landed = 0;
+  bool row_ok = false;
+
   auto flush = [&](int64_t fg, bool whole_row) {
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -382,17 +462,64 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
         }
   };
 
+  // Issue the chunks each row's position has room for: [ic, chunk + 2), one
+  // or two per row, one warp-wide copy instruction per chunk.
+  auto issue = [&]() {
+    __syncwarp();
+    const int want = row_ok ? (int)(((posr >> 5) + s) >> 5) + 2 : 0;
+    const int nc = min(max(want - ic, 0), 2);
+    unsigned m = __ballot_sync(0xFFFFFFFFu, nc > 0);
+    const unsigned m2 = __ballot_sync(0xFFFFFFFFu, nc > 1);
+    const uint32_t my_gw = wb + 32u * (uint32_t)ic;                  // the first chunk's first stream word
+    const uint32_t my_ix = (32u * (uint32_t)ic - s) & 63u;          // its ring index
+    while (m != 0u) {
+      const int r = __ffs((int)m) - 1;
+      m &= m - 1u;
+      const uint32_t gw = __shfl_sync(0xFFFFFFFFu, my_gw, r) + (uint32_t)lane;
+      const uint32_t ix = (__shfl_sync(0xFFFFFFFFu, my_ix, r) + (uint32_t)lane) & 63u;
+      uint32_t* rrow = ring + r * kRingWords;
+      const bool in = (int64_t)gw < a.nwords;
+      const uint32_t* src = a.stream + (in ? gw : 0u);
+      cp_async4(rrow + ix, src, in ? 4u : 0u);
+      if (ix == 0u) cp_async4(rrow + 64, src, in ? 4u : 0u);
+      if ((m2 >> r) & 1u) {   // the next chunk too: ring index + 32
+        const uint32_t gw2 = gw + 32u;
+        const uint32_t ix2 = ix ^ 32u;
+        const bool in2 = (int64_t)gw2 < a.nwords;
+        const uint32_t* src2 = a.stream + (in2 ? gw2 : 0u);
+        cp_async4(rrow + ix2, src2, in2 ? 4u : 0u);
+        if (ix2 == 0u) cp_async4(rrow + 64, src2, in2 ? 4u : 0u);
+      }
+    }
+    ic += nc;
+  };
+
   for (int64_t it = i0; it < i1; ++it) {
-    if (grp != cur_grp) {
+    const bool newgrp = grp != cur_grp;
+    if (newgrp) {
       if (cur_grp >= 0) flush(cur_grp, tiles_in_grp == a.tiles_per_row);
       cur_grp = grp;
       tiles_in_grp = 0;
     }
     const int64_t my_row = grp * 32 + lane;
-    const bool ok = my_row < a.rows;
-    BitReader rd;
-    rd.init(a.stream, a.nwords, ok ? a.off[my_row * a.tiles_per_row + t] : 0ull);
-    const int K = ok ? (int)rd.get(kKBits) : 0;
+    row_ok = my_row < a.rows;
+    const uint32_t o = row_ok ? __ldg(a.off + my_row * a.tiles_per_row + t) : 0u;
+    // a segment that does not start where the lane stands restarts its region
+    const bool restart = newgrp || (row_ok && o != (wb + s) * 32u + posr);
+    if (restart) {
+      wb = (o >> 5) & ~31u;
+      s = (o >> 5) & 31u;
+      posr = o & 31u;
+      ic = 0;
+    }
+    if (__any_sync(0xFFFFFFFFu, restart)) {
+      issue();
+      cp_async_commit();
+      cp_async_wait<0>();
+      __syncwarp();
+      landed = ic;
+    }
+    uint32_t K = 0, kone = 1, kmask = 0, kk = 0x01010101u;
     float acc[2][NB][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -402,28 +529,6 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
         for (int c = 0; c < 4; ++c) acc[i][nb][c] = 0.f;
 
     for (int st = 0; st < steps; ++st) {
-      // decode 64 codes of this lane's row straight into its 64 contiguous bytes
-      // of the slot array (chunks (2 di + dh) * 32 + 4 dg + 0..3)
-      __syncwarp();
-      uint8_t* row_bytes = reinterpret_cast<uint8_t*>(slot + (2 * di + dh) * 32 + 4 * dg);
-      if (ok) {
-#pragma unroll 1
-        for (int j = 0; j < 64 / n; ++j) {
-          int c[n];
-          decode_block<LAT>(rd, K, c);
-          store_block<n>(row_bytes + j * n, c);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(row_bytes)[q] = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-      uint4 cw[2][2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        cw[i][0] = slot[(2 * i) * 32 + lane];
-        cw[i][1] = slot[(2 * i + 1) * 32 + lane];
-      }
       const int64_t k0 = (int64_t)t * a.tile + st * 64;
       uint4 xhv[NB][2];
 #pragma unroll
@@ -438,6 +543,103 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
           xhv[1][1] = __ldg(reinterpret_cast<const uint4*>(xh1 + k0) + 1);
         }
       }
+      cp_async_wait<1>();
+      __syncwarp();
+
+      // ---- decode 64 codes of this lane's row
+      const uint32_t posr0 = posr;
+      if (st == 0) {   // the segment's K
+        const uint32_t* p = myring + ((posr >> 5) & 63u);
+        K = __funnelshift_r(p[0], p[1], posr) & 7u;
+        kone = 1u << K;
+        kmask = kone - 1u;
+        kk = kone * 0x01010101u;
+        posr += kKBits;
+      }
+      {
+        uint32_t vb[4];
+        uint32_t x = 0, pw = 0, umax = 0, kp = 0, prev = 0, half_lo = 0;
+#pragma unroll
+        for (int sy = 0; sy < 64; ++sy) {
+          const int i = sy % n;
+          if ((sy & 1) == 0) {
+            const uint32_t* p = myring + ((posr >> 5) & 63u);
+            x = __funnelshift_r(p[0], p[1], posr);
+            pw = posr;
+            if (Fmt<LAT>::parity && i == 0) {
+              // the block's parity bit in each of its code bytes (A2: two blocks per word)
+              if constexpr (n >= 4) {
+                kp = (x & 1u) * 0x01010101u;
+              } else {
+                const uint32_t kb = (x & 1u) * (0x0101u << (8 * (sy & 3)));
+                kp = (sy & 3) == 0 ? kb : (kp | kb);
+              }
+              x >>= 1;
+              posr += 1;
+            }
+          }
+          const uint32_t p1 = __popc(x ^ (x + 1u));          // run of ones + its closing zero
+          const uint32_t y1 = __funnelshift_rc(x, 0u, p1);   // x >> p1 (0 when p1 = 32)
+          vb[sy & 3] = p1 * kone + (y1 & kmask);             // zigzag value + kone
+          x = y1 >> K;
+          posr += p1 + K;
+          if ((sy & 1) == 1) umax = max(umax, posr - pw);
+          if ((sy & 3) == 3) {
+            uint32_t cword = codes_from_zigzag4(vb[0], vb[1], vb[2], vb[3], kk, kp);
+            if constexpr (LAT == LQ_E8) {
+              if ((sy & 7) == 7) cword = fix_last_code<true>(prev, cword);
+            } else if constexpr (LAT == LQ_D4) {
+              cword = fix_last_code<false>(0u, cword);
+            }
+            if ((sy & 7) == 3) {
+              half_lo = cword;
+            } else {
+              // columns 8 j .. 8 j + 7 (j = sy >> 3): 16-byte chunk j >> 1, half (j & 1) ^ dh
+              store_half(myslot, sy >> 3, half_lo, cword);
+            }
+            prev = cword;
+          }
+        }
+        const uint32_t last_word = (posr >> 5) + s + 1u;   // highest stream word (from wb) the windows read
+        const bool bad = row_ok && (umax > 31u || last_word >= (uint32_t)landed * 32u);
+        if (!row_ok) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) store_half(myslot, j, 0u, 0u);
+        }
+        if (bad) {
+          // the sequential reader on the stream in global memory
+          BitReader rd;
+          rd.init(a.stream, a.nwords, (uint64_t)(wb + s) * 32u + posr0);
+          if (st == 0) {
+            K = rd.get(kKBits);
+            kone = 1u << K;
+            kmask = kone - 1u;
+            kk = kone * 0x01010101u;
+          }
+#pragma unroll 1
+          for (int j = 0; j < 64 / n; ++j) {
+            int c[n];
+            decode_block<LAT>(rd, (int)K, c);
+#pragma unroll
+            for (int e = 0; e < n; ++e) {
+              const int col = j * n + e;
+              reinterpret_cast<uint8_t*>(myslot + (((col >> 4) ^ mysw)))[(8 * (((col >> 3) & 1) ^ dh)) + (col & 7)] =
+                  (uint8_t)c[e];
+            }
+          }
+          posr = (uint32_t)((uint64_t)rd.word * 32u + (uint64_t)rd.b - (uint64_t)(wb + s) * 32u);
+        }
+      }
+      __syncwarp();
+
+      // ---- MMA on the 32 x 64 codes
+      uint4 cwv[2][2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        cwv[i][0] = slot[(2 * i) * 32 + 4 * g + (q4 ^ rdsw)];
+        const uint4 sw = slot[(2 * i + 1) * 32 + 4 * g + (q4 ^ rdsw)];
+        cwv[i][1] = make_uint4(sw.z, sw.w, sw.x, sw.y);   // rows 8 + g: halves stored swapped
+      }
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t bh[NB][2];
@@ -449,17 +651,21 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
         }
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          const uint32_t wa = (c == 0) ? cw[i][0].x : (c == 1) ? cw[i][0].y : (c == 2) ? cw[i][0].z : cw[i][0].w;
-          const uint32_t wb = (c == 0) ? cw[i][1].x : (c == 1) ? cw[i][1].y : (c == 2) ? cw[i][1].z : cw[i][1].w;
+          const uint32_t wa = (c == 0) ? cwv[i][0].x : (c == 1) ? cwv[i][0].y : (c == 2) ? cwv[i][0].z : cwv[i][0].w;
+          const uint32_t wbw = (c == 0) ? cwv[i][1].x : (c == 1) ? cwv[i][1].y : (c == 2) ? cwv[i][1].z : cwv[i][1].w;
           uint32_t a0, a2, a1, a3;
           codes_to_f16x2(wa, a0, a2);
-          codes_to_f16x2(wb, a1, a3);
+          codes_to_f16x2(wbw, a1, a3);
 #pragma unroll
           for (int nb = 0; nb < NB; ++nb) {
             mma16816(acc[i][nb], a0, a1, a2, a3, bh[nb][0], bh[nb][1]);
           }
         }
       }
+      // next chunks for the rows that have room
+      landed = ic;
+      issue();
+      cp_async_commit();
     }
     // per-tile scale
     float fx[NB][2];
@@ -490,6 +696,7 @@ __global__ void __launch_bounds__(128) gemv_rice_kernel(GemvRiceArgs a) {
     if (++t == a.tiles_per_row) { t = 0; ++grp; }
   }
   if (cur_grp >= 0) flush(cur_grp, tiles_in_grp == a.tiles_per_row);
+  cp_async_wait<0>();
 }
 
 }  // namespace rice

@@ -80,6 +80,61 @@ def test_gemv_rice_parity(lattice, tile, batch):
     assert normwise_rel(y.cpu().numpy(), ref) < 2e-3
 
 
+def _crafted_codes(lattice, rows, cols, seed):
+    """Codes with the pinned bits of the lattice: most blocks in {-1, 0, 1}
+    halves (a small Rice parameter), 5 % of the blocks with halves up to +-62
+    (unary runs far longer than a 32-bit word), and every fourth row made only
+    of the large blocks, so that rows advance through the stream at very
+    different rates."""
+    n = {"e8": 8, "d4": 4, "a2": 2, "z1": 1}[lattice]
+    parity = lattice in ("e8", "a2")
+    even = lattice in ("e8", "d4")
+    rng = np.random.default_rng(seed)
+    C = np.zeros((rows, cols), np.int64)
+    for r in range(rows):
+        frac = 1.0 if r % 4 == 3 else 0.05
+        for b0 in range(0, cols, n):
+            k = int(rng.integers(0, 2)) if parity else 0
+            if rng.random() < frac:
+                u = rng.integers(-62, 62, n)
+            else:
+                u = rng.integers(-1, 2, n)
+            if even and u.sum() % 2:
+                u[-1] += 1 if u[-1] < 60 else -1
+            C[r, b0:b0 + n] = 2 * u + k
+    return C
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+@pytest.mark.parametrize("tile,batch", [(128, 1), (256, 9), (512, 3)])
+def test_gemv_rice_long_runs_and_uneven_rows(lattice, tile, batch):
+    """Unary runs longer than the decoder's 32-bit window and rows of very
+    different stream rates: the stream decodes back to the codes and the GEMV
+    from the stream matches the oracle's GEMV of the codes."""
+    torch, L = cuda()
+    rows, cols = 70, 3 * tile
+    codes = _crafted_codes(lattice, rows, cols, 900 + tile)
+    assert np.abs(codes).max() >= 100
+    rng = np.random.default_rng(901)
+    scales = rng.uniform(0.5, 2.0, (rows, cols // tile)).astype(np.float32)
+    d = O.splitmix64_signs(13, cols)
+    words, offs, _ = gpu_encode(torch, L, to_dev(torch, codes.astype(np.int8)), lattice, tile)
+    out = torch.empty((rows, cols), dtype=torch.int8, device="cuda")
+    L.lq_rice_decode(lattice, words, offs, tile, out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), codes.astype(np.int8))
+    x = gaussian_vectors(batch, cols, 902 + batch, dtype="bf16")
+    y = torch.full((batch, rows), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(L.lq_gemv_workspace_size(batch, cols, tile), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.lq_gemv_rice(lattice, words, offs, to_dev(torch, scales), to_dev(torch, d), tile,
+                   to_dev_bf16(torch, x), y, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = O.gemv(codes, scales, d, tile, lattice, x)
+    assert normwise_rel(y.cpu().numpy(), ref) < 2e-3
+
+
 def test_format_flag_on_codes_without_pinned_bits():
     """E8 blocks of mixed parity cannot be stripped: the encoder flags them."""
     torch, L = cuda()
