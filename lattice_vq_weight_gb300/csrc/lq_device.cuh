@@ -500,26 +500,21 @@ __device__ __forceinline__ uint2 parity_fix_selector(int i) {
   return i < 4 ? make_uint2(one, 0x4444u) : make_uint2(0x4444u, one);
 }
 
-// Codes of one E8 block from its rounding bits t (rint(y) + 64 in byte 0),
-// residual bits e (y - rint(y)) and keys (|e| with the low three mantissa bits
-// replaced by 7 - i), with lhs = 2 - sum |e|.  E8 = D8 u (D8 + 1/2) decoded as
-// in decode_e8: the D8 point is f = rint(y) with the worst coordinate (largest
-// |e|, lowest index on ties) rounded the other way when sum f is odd; the
-// D8 + 1/2 point is floor(y) + 1/2 with its worst coordinate (smallest |e|)
-// moved across when sum floor(y) is odd.  Their squared distances minus sum e^2
-// are dA = [odd A] (1 - 2 max|e|) and dB = 2 - sum|e| + [odd B] 2 min|e|, and
-// D8 is kept when dA <= dB.  Per byte, in offset binary: D8 code 2F (F =
-// rint(y) + 64), D8 + 1/2 code 2F + 1 - 2[e < 0]; the parity fix adds +-2 at
-// the chosen coordinate (toward y: +2 - 4[e < 0] for D8, -2 + 4[e < 0] for
+// Codes of one E8 block from its packed rounding bytes F0, F1 (rint(y) + 64 of
+// coordinates 0..3 and 4..7), packed residual signs N0, N1 (0xFF where
+// y < rint(y)), the largest and smallest key (|e| with the low three mantissa
+// bits replaced by 7 - i) and lhs = 2 - sum |e|.  E8 = D8 u (D8 + 1/2) decoded
+// as in decode_e8: the D8 point is f = rint(y) with the worst coordinate
+// (largest |e|, lowest index on ties) rounded the other way when sum f is odd;
+// the D8 + 1/2 point is floor(y) + 1/2 with its worst coordinate (smallest |e|)
+// moved across when sum floor(y) is odd.  Their squared distances minus
+// sum e^2 are dA = [odd A] (1 - 2 max|e|) and dB = 2 - sum|e| + [odd B] 2 min|e|,
+// and D8 is kept when dA <= dB.  Per byte, in offset binary: D8 code 2F
+// (F = rint(y) + 64), D8 + 1/2 code 2F + 1 - 2[e < 0]; the parity fix adds +-2
+// at the chosen coordinate (toward y: +2 - 4[e < 0] for D8, -2 + 4[e < 0] for
 // D8 + 1/2).
-__device__ __forceinline__ uint2 e8_block_codes(const uint32_t (&t)[8], const uint32_t (&e)[8],
-                                                const uint32_t (&key)[8], float lhs, const uint2* fixsel) {
-  const uint32_t kA = key_max3(key_max3(key[0], key[1], key[2]), key_max3(key[3], key[4], key[5]),
-                               __float_as_uint(fmaxf(__uint_as_float(key[6]), __uint_as_float(key[7]))));
-  const uint32_t kB = key_min3(key_min3(key[0], key[1], key[2]), key_min3(key[3], key[4], key[5]),
-                               __float_as_uint(fminf(__uint_as_float(key[6]), __uint_as_float(key[7]))));
-  const uint32_t F0 = pack_low4(t[0], t[1], t[2], t[3]), F1 = pack_low4(t[4], t[5], t[6], t[7]);
-  const uint32_t N0 = pack_sign4(e[0], e[1], e[2], e[3]), N1 = pack_sign4(e[4], e[5], e[6], e[7]);
+__device__ __forceinline__ uint2 e8_block_codes(uint32_t F0, uint32_t F1, uint32_t N0, uint32_t N1, uint32_t kA,
+                                                uint32_t kB, float lhs, const uint2* fixsel) {
   // bit 0 of each byte: parity of F_i + F_(i+4); bit 4: of the two signs.  The
   // byte sum (top byte of the product) then has the parity of sum F (= that of
   // sum rint(y): 8 * 64 is even) in bit 0 and that of the count of negative
@@ -543,31 +538,68 @@ __device__ __forceinline__ uint2 e8_block_codes(const uint32_t (&t)[8], const ui
   return r;
 }
 
-// Fast E8 decode of two blocks side by side (see above): y = u k is never
-// formed; the rounding t = u k + magic and the residual e = u k - rint(y) are
-// each one fused multiply-add of the exact product.
+// Rounding bits, residual bits and key of coordinate i of two blocks side by
+// side (.x block P, .y block Q): t = u k + magic and e = u k - rint(y) are each
+// one fused multiply-add of the exact product.
+struct E8Coord {
+  uint32_t tP, tQ, eP, eQ, kP, kQ;
+};
+__device__ __forceinline__ E8Coord e8_coord(float2 u, float2 k2, int i) {
+  const float2 MG = make_float2(kRoundMagic64, kRoundMagic64);
+  const float2 t = fma2(u, k2, MG);
+  const float2 e = fma2(u, k2, sub2(MG, t));   // MG - t = -rint(y), exact
+  E8Coord c;
+  c.tP = __float_as_uint(t.x);
+  c.tQ = __float_as_uint(t.y);
+  c.eP = __float_as_uint(e.x);
+  c.eQ = __float_as_uint(e.y);
+  c.kP = (c.eP & 0x7FFFFFF8u) | (uint32_t)(7 - i);
+  c.kQ = (c.eQ & 0x7FFFFFF8u) | (uint32_t)(7 - i);
+  return c;
+}
+__device__ __forceinline__ float2 key_pair(const E8Coord& c) {
+  return make_float2(__uint_as_float(c.kP), __uint_as_float(c.kQ));
+}
+
+// Fast E8 decode of two blocks side by side (see above), y = u k never formed.
+// The coordinates are taken four at a time and reduced at once (packed bytes,
+// partial key extremes and sums), which keeps few temporaries alive.
 __device__ __forceinline__ void decode_e8_pair(const float2 (&u)[8], float2 k2, const uint2* fixsel, uint2& cP,
                                                uint2& cQ) {
-  const float2 MG = make_float2(kRoundMagic64, kRoundMagic64);
-  uint32_t tP[8], tQ[8], eP[8], eQ[8], kP[8], kQ[8];
-  float2 kf[8];
+  uint32_t FP[2], FQ[2], NP[2], NQ[2];
+  uint32_t mxP = 0, mxQ = 0, mnP = 0, mnQ = 0;
+  float2 s = make_float2(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float2 t = fma2(u[i], k2, MG);
-    const float2 e = fma2(u[i], k2, sub2(MG, t));   // MG - t = -rint(y), exact
-    tP[i] = __float_as_uint(t.x);
-    tQ[i] = __float_as_uint(t.y);
-    eP[i] = __float_as_uint(e.x);
-    eQ[i] = __float_as_uint(e.y);
-    kP[i] = (eP[i] & 0x7FFFFFF8u) | (uint32_t)(7 - i);
-    kQ[i] = (eQ[i] & 0x7FFFFFF8u) | (uint32_t)(7 - i);
-    kf[i] = make_float2(__uint_as_float(kP[i]), __uint_as_float(kQ[i]));
+  for (int h = 0; h < 2; ++h) {
+    const E8Coord c0 = e8_coord(u[4 * h], k2, 4 * h), c1 = e8_coord(u[4 * h + 1], k2, 4 * h + 1);
+    const E8Coord c2 = e8_coord(u[4 * h + 2], k2, 4 * h + 2), c3 = e8_coord(u[4 * h + 3], k2, 4 * h + 3);
+    FP[h] = pack_low4(c0.tP, c1.tP, c2.tP, c3.tP);
+    FQ[h] = pack_low4(c0.tQ, c1.tQ, c2.tQ, c3.tQ);
+    NP[h] = pack_sign4(c0.eP, c1.eP, c2.eP, c3.eP);
+    NQ[h] = pack_sign4(c0.eQ, c1.eQ, c2.eQ, c3.eQ);
+    // sum |e| of each block from the keys (each within 7 ulps of |e|)
+    const float2 sh = add2(add2(key_pair(c0), key_pair(c1)), add2(key_pair(c2), key_pair(c3)));
+    if (h == 0) {
+      s = sh;
+      mxP = key_max3(c0.kP, c1.kP, c2.kP);
+      mxQ = key_max3(c0.kQ, c1.kQ, c2.kQ);
+      mnP = key_min3(c0.kP, c1.kP, c2.kP);
+      mnQ = key_min3(c0.kQ, c1.kQ, c2.kQ);
+      mxP = __float_as_uint(fmaxf(__uint_as_float(mxP), __uint_as_float(c3.kP)));
+      mxQ = __float_as_uint(fmaxf(__uint_as_float(mxQ), __uint_as_float(c3.kQ)));
+      mnP = __float_as_uint(fminf(__uint_as_float(mnP), __uint_as_float(c3.kP)));
+      mnQ = __float_as_uint(fminf(__uint_as_float(mnQ), __uint_as_float(c3.kQ)));
+    } else {
+      s = add2(s, sh);
+      mxP = key_max3(key_max3(mxP, c0.kP, c1.kP), c2.kP, c3.kP);
+      mxQ = key_max3(key_max3(mxQ, c0.kQ, c1.kQ), c2.kQ, c3.kQ);
+      mnP = key_min3(key_min3(mnP, c0.kP, c1.kP), c2.kP, c3.kP);
+      mnQ = key_min3(key_min3(mnQ, c0.kQ, c1.kQ), c2.kQ, c3.kQ);
+    }
   }
-  // sum |e| of each block from the keys (each within 7 ulps of |e|)
-  const float2 s = add2(add2(add2(kf[0], kf[1]), add2(kf[2], kf[3])), add2(add2(kf[4], kf[5]), add2(kf[6], kf[7])));
   const float2 lhs = sub2(make_float2(2.f, 2.f), s);
-  cP = e8_block_codes(tP, eP, kP, lhs.x, fixsel);
-  cQ = e8_block_codes(tQ, eQ, kQ, lhs.y, fixsel);
+  cP = e8_block_codes(FP[0], FP[1], NP[0], NP[1], mxP, mnP, lhs.x, fixsel);
+  cQ = e8_block_codes(FQ[0], FQ[1], NQ[0], NQ[1], mxQ, mnQ, lhs.y, fixsel);
 }
 
 // Fast Z1 decode of two 8-coordinate groups side by side: c = 2 rint(y).

@@ -182,6 +182,29 @@ __device__ __forceinline__ uint2 decode_block8(const float2 (&y4)[4], bool& r) {
   }
 }
 
+// The scalar decoders with the exact int8 range check over a lane's 64
+// values (blocks regrouped as consecutive 8-coordinate pairs), out of line: for
+// E8 and Z1 it only runs for a lane holding a value of 62.5 or more (an outlier
+// that survived the transform), so its registers are kept out of the fast
+// path's allocation.
+template <int LAT, int EX>
+__device__ __noinline__ void decode_lane_checked(const float2 (&p)[32], float k, int lane, int8_t* dst, bool active,
+                                                 bool& r) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float y[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) y[i] = (h ? p[8 * g + i].y : p[8 * g + i].x) * k;
+      const float2 y4[4] = {make_float2(y[0], y[1]), make_float2(y[2], y[3]), make_float2(y[4], y[5]),
+                            make_float2(y[6], y[7])};
+      const uint2 w = decode_block8<LAT, true>(y4, r);
+      if (active) *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, h)) = w;
+    }
+  }
+}
+
 // ------------------------------------------------------------------ quantize
 // EX = tile bits exchanged through shared memory: 1 for 128-column tiles, 2
 // above.  XL: tiles of 512 ... 2048 columns, whose bits above 7 cross lanes
@@ -422,22 +445,29 @@ __global__ void __launch_bounds__(kQuantThreads, (BF16 && !XL) ? 4 : 3)
       }
       const float2 k2 = make_float2(k, k);
       bool r = false;
-      if ((LAT == LQ_E8 || LAT == LQ_Z1) && small) {
+      if constexpr (LAT == LQ_E8 || LAT == LQ_Z1) {
+        if (small) {
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float2 u[8] = {p[8 * g], p[8 * g + 1], p[8 * g + 2], p[8 * g + 3],
-                               p[8 * g + 4], p[8 * g + 5], p[8 * g + 6], p[8 * g + 7]};
-          uint2 cP, cQ;
-          if constexpr (LAT == LQ_E8) decode_e8_pair(u, k2, fixsel, cP, cQ);
-          else decode_z1_pair(u, k2, cP, cQ);
-          if (active) {
-            *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 0)) = cP;
-            *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 1)) = cQ;
+          for (int g = 0; g < 4; ++g) {
+            const float2 u[8] = {p[8 * g], p[8 * g + 1], p[8 * g + 2], p[8 * g + 3],
+                                 p[8 * g + 4], p[8 * g + 5], p[8 * g + 6], p[8 * g + 7]};
+            uint2 cP, cQ;
+            if constexpr (LAT == LQ_E8) decode_e8_pair(u, k2, fixsel, cP, cQ);
+            else decode_z1_pair(u, k2, cP, cQ);
+            if (active) {
+              *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 0)) = cP;
+              *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 1)) = cQ;
+            }
           }
+        } else {
+          float2 pc[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pc[j] = p[j];
+          decode_lane_checked<LAT, EX>(pc, k, lane, dst, active, r);
         }
       } else {
-        // scalar decoders (with the exact int8 range check unless the lane is
-        // known to be small) on the blocks regrouped as consecutive pairs
+        // D4, A2: the scalar decoders, with the exact int8 range check unless
+        // the lane is known to be small
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
 #pragma unroll
