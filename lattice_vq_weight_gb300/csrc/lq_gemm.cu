@@ -181,6 +181,20 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 consecutive accumulator columns of this warp's 32 TMEM lanes, without
+// waiting (tmem_wait_ld waits for every load the thread has issued).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // int8 codes (4 per word) -> f16x2 words (exact: the magic-number conversion of
 // Kim et al. 2022, "Who Says Elephants Can't Run"), then times the fp16 scale.
 __device__ __forceinline__ uint32_t code_pair_f16(uint32_t u, uint32_t sel, __half2 sf) {
@@ -219,19 +233,19 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < kCodeStages; ++i) {
       mbar_init(&sm.full_c[i], 1);
-      mbar_init(&sm.empty_c[i], kDecodeThreads);
+      mbar_init(&sm.empty_c[i], kDecodeWarps);   // one arrival per decoder warp
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(&sm.full_x[i], 1);
       mbar_init(&sm.empty_x[i], 1);
     }
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&sm.full_a[i], kDecodeThreads);
+      mbar_init(&sm.full_a[i], kDecodeWarps);
       mbar_init(&sm.empty_a[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tmem_full[i], 1);
-      mbar_init(&sm.tmem_empty[i], kEpiThreads);
+      mbar_init(&sm.tmem_empty[i], kEpiThreads / 32);   // one arrival per epilogue warp
     }
     mbar_init(&sm.drain, 1);
     sm.timeout = 0;
@@ -380,8 +394,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
             s_nxt[p] = (t + 1 < a.tiles_per_row) ? scale_value<SF>(srow[p] + kTileStep * (t + 1)) : 0.f;
           }
         }
-        if (!mbar_wait<kLimit>(&sm.full_c[sc], phc, timeout)) break;
-        if (!mbar_wait<kLimit>(&sm.empty_a[sa], pha ^ 1, timeout)) break;
+        // warp-uniform waits: the warp arrives once per barrier below
+        if (!__all_sync(0xffffffffu, mbar_wait<kLimit>(&sm.full_c[sc], phc, timeout))) break;
+        if (!__all_sync(0xffffffffu, mbar_wait<kLimit>(&sm.empty_a[sa], pha ^ 1, timeout))) break;
         const uint8_t* cbase = sm.codes[sc];
         uint8_t* abase = sm.a[sa];
 #pragma unroll
@@ -400,9 +415,15 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
           *reinterpret_cast<uint4*>(abase + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<uint4*>(abase + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        mbar_arrive(&sm.empty_c[sc]);             // code tile consumed
+        // each thread orders its A writes before the tensor cores' reads; one
+        // arrival per warp (256 single-thread arrivals on one barrier cost
+        // hundreds of cycles per stage on the MMA's critical path)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive(&sm.full_a[sa]);              // A tile ready for the tensor cores
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.empty_c[sc]);           // this warp's code reads are done
+          mbar_arrive(&sm.full_a[sa]);            // its part of the A tile is written
+        }
         if (++sc == kCodeStages) { sc = 0; phc ^= 1; }
         if (++sa == kAStages) { sa = 0; pha ^= 1; }
       }
@@ -426,24 +447,43 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
       const float inv_f = row_in ? 1.0f / __ldg(a.f + n) : 0.f;
       const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN);
       const bool atomic = a.splits > 1;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        __syncwarp();                              // tcgen05.ld is warp-collective
-        tmem_ld16(taddr + (uint32_t)c0, r);
+      // 32 columns per TMEM load, the next load in flight while a chunk is
+      // written out; 1/g_m of the chunk's tokens loaded once per lane and
+      // broadcast by shuffles
+      const int64_t m_base = (int64_t)mt * BN;
+      auto write_chunk = [&](const uint32_t (&r)[32], int c0, float g_lane) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int64_t m = (int64_t)mt * BN + c0 + j;
+        for (int j = 0; j < 32; ++j) {
+          const int64_t m = m_base + c0 + j;
+          const float g = __shfl_sync(0xffffffffu, g_lane, j);
           if (row_in && m < a.M) {
-            const float v = __uint_as_float(r[j]) * inv_f * __ldg(a.inv_g + m);
+            const float v = __uint_as_float(r[j]) * inv_f * g;
             if (atomic) atomicAdd(a.Y32 + m * a.N + n, v);
             else if (a.Ybf != nullptr) a.Ybf[m * a.N + n] = __float2bfloat16_rn(v);
             else a.Y32[m * a.N + n] = v;
           }
         }
+      };
+      auto g_of = [&](int c0) {
+        const int64_t m = m_base + c0 + lane;
+        return m < a.M ? __ldg(a.inv_g + m) : 0.f;
+      };
+      uint32_t ra[32], rb[32];
+      __syncwarp();                                // tcgen05.ld is warp-collective
+      tmem_ld32(taddr, ra);
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        const float ga = g_of(c0), gb = g_of(c0 + 32);
+        tmem_wait_ld();                            // columns c0 .. c0 + 31 in ra
+        tmem_ld32(taddr + (uint32_t)(c0 + 32), rb);
+        write_chunk(ra, c0, ga);
+        tmem_wait_ld();                            // columns c0 + 32 .. c0 + 63 in rb
+        if (c0 + 64 < BN) tmem_ld32(taddr + (uint32_t)(c0 + 64), ra);
+        write_chunk(rb, c0 + 32, gb);
       }
       tc_fence_before();
-      mbar_arrive(&sm.tmem_empty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tmem_empty[acc]);
     }
   }
 
