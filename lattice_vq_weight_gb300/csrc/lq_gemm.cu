@@ -18,10 +18,11 @@
 //                 codes come from HBM, so this ring is the deep one)
 //     warp 14     TMA producer of X~ tiles [256 x 64] (4-stage ring, mostly L2)
 //     warp 1      allocates TMEM, one lane issues the MMAs
-//     warps 2..9  decoders (two per SM sub-partition; two 16-code chunks per
-//                 thread per stage): codes -> fp16 (c * s[n,t] * f_n / 2)
-//                 written to a 2-stage ring of A tiles in the 128-byte-swizzled
-//                 K-major layout
+//     warps 2..9  decoders in two groups of four warps taking alternate K
+//                 stages (four 16-code chunks per thread per stage): codes ->
+//                 fp16 (c * s[n,t] * f_n / 2) written to a 2-stage ring of A
+//                 tiles in the 128-byte-swizzled K-major layout, group g
+//                 always into slot g
 //     warps 10..13 epilogue: tcgen05.ld of the accumulator, Y = D / (f_n g_m)
 //   Each ring has its own full/empty mbarriers, so code loads run far ahead of
 //   the MMAs.  TMEM holds two 256-column accumulators so the epilogue of one
@@ -58,8 +59,12 @@ constexpr int kDecodeThreads = kDecodeWarps * 32;   // warps 2 .. 2 + kDecodeWar
 constexpr int kEpiWarp0 = 2 + kDecodeWarps;         // four epilogue warps
 constexpr int kXWarp = kEpiWarp0 + 4;               // X~ producer
 constexpr int kThreads = (kXWarp + 1) * 32;
-constexpr int kDecodePasses = BM * BK / 16 / kDecodeThreads;  // 16-code chunks per thread per stage
-static_assert(kDecodePasses * kDecodeThreads * 16 == BM * BK, "decoders cover the code tile");
+constexpr int kDecodeGroups = 2;                    // decoder groups taking alternate K stages
+constexpr int kGroupWarps = kDecodeWarps / kDecodeGroups;
+constexpr int kGroupThreads = kGroupWarps * 32;
+constexpr int kDecodePasses = BM * BK / 16 / kGroupThreads;  // 16-code chunks per thread per stage
+static_assert(kDecodePasses * kGroupThreads * 16 == BM * BK, "a decoder group covers the code tile");
+static_assert(kAStages % kDecodeGroups == 0, "each decoder group keeps to its own A slots");
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;          // two 256-column fp32 accumulators
 constexpr long long kWaitCycles = 2000000000ll;  // about one second
@@ -233,14 +238,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < kCodeStages; ++i) {
       mbar_init(&sm.full_c[i], 1);
-      mbar_init(&sm.empty_c[i], kDecodeWarps);   // one arrival per decoder warp
+      mbar_init(&sm.empty_c[i], kGroupWarps);    // one arrival per warp of the decoder group
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(&sm.full_x[i], 1);
       mbar_init(&sm.empty_x[i], 1);
     }
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&sm.full_a[i], kDecodeWarps);
+      mbar_init(&sm.full_a[i], kGroupWarps);
       mbar_init(&sm.empty_a[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -348,17 +353,20 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ decoders
-    const int d = threadIdx.x - 64;          // 0 .. kDecodeThreads - 1
+    // Two groups of four warps take alternate K stages (group g the stages
+    // whose CTA-wide index is g mod 2, which use A slot g), so each group has
+    // two MMA stage times to decode its tile and the two overlap.
+    const int dgrp = (warp - 2) / kGroupWarps;
+    const int d = threadIdx.x - 64 - dgrp * kGroupThreads;   // 0 .. kGroupThreads - 1
     const int rsub = d >> 2;                 // row within a pass
     const int c4 = d & 3;                    // 16-code chunk within the 64-code stage row
     const int stages_per_t = a.tile / BK;
-    int sc = 0, sa = 0;
-    uint32_t phc = 0, pha = 0;
+    int64_t i = 0;                           // CTA-wide stage index
     for (int64_t u = blockIdx.x; u < a.units && !*timeout; u += gridDim.x) {
       int nt, mt, k0, k1;
       unit_range(u, nt, mt, k0, k1);
       constexpr int P = kDecodePasses;
-      constexpr int kRowsPerPass = kDecodeThreads / 4;
+      constexpr int kRowsPerPass = kGroupThreads / 4;
       // per pass: the row's first tile scale (the row's scale for the per-row format)
       using ST = typename ScaleType<SF>::T;
       constexpr int kTileStep = (SF == LQ_SCALE_ROW_BF16) ? 0 : 1;
@@ -384,9 +392,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
       __half2 sf[P];
 #pragma unroll
       for (int p = 0; p < P; ++p) sf[p] = __float2half2_rn(s_cur[p] * fr[p]);
-      for (int ks = k0; ks < k1; ++ks) {
+      for (int ks = k0; ks < k1; ++ks, ++i) {
+        if ((int)(i & 1) != dgrp) continue;    // the other group's stage
         const int t = ks / stages_per_t;
         if (t != t_cur) {
+          // a group's stages advance by two at most, less than the stages of a tile
           t_cur = t;
 #pragma unroll
           for (int p = 0; p < P; ++p) {
@@ -394,6 +404,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
             s_nxt[p] = (t + 1 < a.tiles_per_row) ? scale_value<SF>(srow[p] + kTileStep * (t + 1)) : 0.f;
           }
         }
+        const int sc = (int)(i % kCodeStages), sa = (int)(i % kAStages);
+        const uint32_t phc = (uint32_t)((i / kCodeStages) & 1), pha = (uint32_t)((i / kAStages) & 1);
         // warp-uniform waits: the warp arrives once per barrier below
         if (!__all_sync(0xffffffffu, mbar_wait<kLimit>(&sm.full_c[sc], phc, timeout))) break;
         if (!__all_sync(0xffffffffu, mbar_wait<kLimit>(&sm.empty_a[sa], pha ^ 1, timeout))) break;
@@ -415,17 +427,14 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
           *reinterpret_cast<uint4*>(abase + r * 128 + ((j0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
           *reinterpret_cast<uint4*>(abase + r * 128 + ((j1 ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
-        // each thread orders its A writes before the tensor cores' reads; one
-        // arrival per warp (256 single-thread arrivals on one barrier cost
-        // hundreds of cycles per stage on the MMA's critical path)
+        // each thread orders its A writes before the tensor cores' reads; the
+        // warp then arrives once on each barrier
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sm.empty_c[sc]);           // this warp's code reads are done
           mbar_arrive(&sm.full_a[sa]);            // its part of the A tile is written
         }
-        if (++sc == kCodeStages) { sc = 0; phc ^= 1; }
-        if (++sa == kAStages) { sa = 0; pha ^= 1; }
       }
     }
   } else {
