@@ -55,7 +55,6 @@ constexpr int kCodeBytes = BM * BK;          // int8 codes per stage:   8 KB
 constexpr int kABytes = BM * BK * 2;         // fp16 decoded weights:   16 KB
 constexpr int kXBytes = BN * BK * 2;         // fp16 activations:       32 KB
 constexpr int kDecodeWarps = 8;
-constexpr int kDecodeThreads = kDecodeWarps * 32;   // warps 2 .. 2 + kDecodeWarps - 1
 constexpr int kEpiWarp0 = 2 + kDecodeWarps;         // four epilogue warps
 constexpr int kXWarp = kEpiWarp0 + 4;               // X~ producer
 constexpr int kThreads = (kXWarp + 1) * 32;
@@ -353,9 +352,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
     }
   } else if (warp < kEpiWarp0) {
     // ------------------------------------------------------------ decoders
-    // Two groups of four warps take alternate K stages (group g the stages
-    // whose CTA-wide index is g mod 2, which use A slot g), so each group has
-    // two MMA stage times to decode its tile and the two overlap.
+    // kDecodeGroups groups of warps take turns over the K stages (group g the
+    // stages whose CTA-wide index is g modulo the group count, which use the A
+    // slots congruent to g), so each group has several MMA stage times to
+    // decode its tile and the groups overlap.
     const int dgrp = (warp - 2) / kGroupWarps;
     const int d = threadIdx.x - 64 - dgrp * kGroupThreads;   // 0 .. kGroupThreads - 1
     const int rsub = d >> 2;                 // row within a pass
@@ -393,16 +393,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
 #pragma unroll
       for (int p = 0; p < P; ++p) sf[p] = __float2half2_rn(s_cur[p] * fr[p]);
       for (int ks = k0; ks < k1; ++ks, ++i) {
-        if ((int)(i & 1) != dgrp) continue;    // the other group's stage
+        if ((int)(i % kDecodeGroups) != dgrp) continue;    // another group's stage
         const int t = ks / stages_per_t;
         if (t != t_cur) {
-          // a group's stages advance by two at most, less than the stages of a tile
-          t_cur = t;
+          // the next tile's scales were loaded ahead; a group that skipped a
+          // whole tile loads them now
 #pragma unroll
           for (int p = 0; p < P; ++p) {
-            sf[p] = __float2half2_rn(s_nxt[p] * fr[p]);
+            const float sv = (t == t_cur + 1) ? s_nxt[p] : scale_value<SF>(srow[p] + kTileStep * t);
+            sf[p] = __float2half2_rn(sv * fr[p]);
             s_nxt[p] = (t + 1 < a.tiles_per_row) ? scale_value<SF>(srow[p] + kTileStep * (t + 1)) : 0.f;
           }
+          t_cur = t;
         }
         const int sc = (int)(i % kCodeStages), sa = (int)(i % kAStages);
         const uint32_t phc = (uint32_t)((i / kCodeStages) & 1), pha = (uint32_t)((i / kAStages) & 1);
