@@ -64,14 +64,20 @@ __device__ __forceinline__ void dither8_codes(uint64_t seed, uint64_t c0, float 
   for (int i = 0; i < 8; ++i) du[i] *= (LAT == LQ_A2 && (i & 1)) ? 1.1547005383792515f : 2.f;
 }
 
-// Rows of the per-warp Rice decode buffers: 32 words of codes plus one of
-// padding (conflict-free 4-byte accesses by rows and by columns).
+// Per-warp Rice buffers, rows of 33 words (conflict-free 4-byte accesses by
+// rows and by columns): the first 32 stream words of the chunk's K and of its
+// V segments, word k of token t at k * 33 + t (33 rows: a window read at word
+// 31 touches row 32), and the decoded V code words, word q of token t at
+// t * 33 + q.
 constexpr int kRiceStride = D / 4 + 1;
+constexpr int kRiceStageWords = 33 * kRiceStride;
+constexpr int kRiceWarpWords = 2 * kRiceStageWords + 32 * kRiceStride;
 constexpr size_t kDvSmem = (size_t)kWarps * 32 * kDvStride * sizeof(float);
-constexpr size_t kRiceSmem = (size_t)2 * kWarps * 32 * kRiceStride * sizeof(uint32_t);
+constexpr size_t kRiceSmem = (size_t)kWarps * kRiceWarpWords * sizeof(uint32_t);
 
-// Decode the Rice segment at bit `pos` (D codes) into 32 code words at row.
-template <int LAT>
+// Decode the Rice segment at bit `pos` (D codes) into 32 code words at row,
+// word q at row[q * STRIDE].
+template <int LAT, int STRIDE = 1>
 __device__ __forceinline__ void decode_segment(const uint32_t* stream, int64_t nwords, uint64_t pos, uint32_t* row) {
   constexpr int n = rice::Fmt<LAT>::n;
   rice::BitReader rd;
@@ -88,7 +94,7 @@ __device__ __forceinline__ void decode_segment(const uint32_t* stream, int64_t n
       for (int e = 0; e < n; ++e) wv[(j + e) >> 2] |= ((uint32_t)c[e] & 0xFFu) << (8 * ((j + e) & 3));
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) row[4 * q + e] = wv[e];
+    for (int e = 0; e < 4; ++e) row[(4 * q + e) * STRIDE] = wv[e];
   }
 }
 
@@ -97,9 +103,9 @@ __device__ __forceinline__ void decode_segment(const uint32_t* stream, int64_t n
 // the value sum the weighted dither of each token (transposed through shared
 // memory, dynamic: kWarps x 32 x kDvStride floats).
 // RLAT = 0: int8 codes; otherwise the lattice of Rice-coded caches: each lane
-// decodes its token's K and V segments into per-warp shared-memory rows (dynamic:
-// 2 x kWarps x 32 x kRiceStride words), read back by the same lane for the
-// scores and by dimension for the value sum.
+// decodes its token's K and V segments from per-warp staging buffers (dynamic:
+// kWarps x kRiceWarpWords words), K into registers for the scores and V into a
+// shared-memory row read back by dimension for the value sum.
 template <int G, bool F16S, int DLAT, int RLAT>
 __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(AttnArgs a) {
   static_assert(DLAT == 0 || RLAT == 0, "dither and Rice caches are separate variants");
@@ -136,24 +142,69 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(
     const int nt = (j1 - c0) < 32 ? (int)(j1 - c0) : 32;
     uint4 kw[D / 16];
     float s_k = 0.f, s_v = 0.f;
-    uint32_t* krow = nullptr;
+    uint32_t kcw[RLAT != 0 ? D / 4 : 1];
+    uint32_t* vrows = nullptr;
     if constexpr (RLAT != 0) {
-      krow = reinterpret_cast<uint32_t*>(dv_smem) + ((size_t)warp * 32 + lane) * kRiceStride;
-      uint32_t* vrow = reinterpret_cast<uint32_t*>(dv_smem) + ((size_t)(kWarps + warp) * 32 + lane) * kRiceStride;
+      // stage the first 32 words of every token's K and V segments (one
+      // coalesced copy per token and cache), then each lane decodes its own
+      // token's segments with the two-symbol decoder: K into registers, V into
+      // its row of vrows; a lane whose segment does not decode within the
+      // staged words (or overflows a window) falls back to the sequential
+      // reader on the stream in global memory
+      uint32_t* kst = reinterpret_cast<uint32_t*>(dv_smem) + (size_t)warp * kRiceWarpWords;
+      uint32_t* vst = kst + kRiceStageWords;
+      vrows = vst + kRiceStageWords;
+      const int64_t seg = j * a.kv_heads + kvh;
+      const uint32_t ko = ok ? __ldg(a.koff + seg) : 0u, vo = ok ? __ldg(a.voff + seg) : 0u;
+      __syncwarp();                                  // the previous chunk's reads of the buffers are done
+#pragma unroll 1
+      for (int t = 0; t < nt; ++t) {
+        const uint32_t gk = __shfl_sync(0xffffffffu, ko >> 5, t) + (uint32_t)lane;
+        const uint32_t gv = __shfl_sync(0xffffffffu, vo >> 5, t) + (uint32_t)lane;
+        const bool ik = (int64_t)gk < a.knw, iv = (int64_t)gv < a.vnw;
+        rice::cp_async4(kst + lane * kRiceStride + t, a.krs + (ik ? gk : 0u), ik ? 4u : 0u);
+        rice::cp_async4(vst + lane * kRiceStride + t, a.vrs + (iv ? gv : 0u), iv ? 4u : 0u);
+      }
+      rice::cp_async_commit();
+      rice::cp_async_wait<0>();
+      __syncwarp();
+      uint32_t* vrow = vrows + lane * kRiceStride;
       if (ok) {
-        const int64_t seg = j * a.kv_heads + kvh;
-        decode_segment<RLAT>(a.krs, a.knw, __ldg(a.koff + seg), krow);
-        decode_segment<RLAT>(a.vrs, a.vnw, __ldg(a.voff + seg), vrow);
+        auto kwin = [&](uint32_t pos) {
+          const uint32_t w = min(pos >> 5, 31u);
+          return __funnelshift_r(kst[w * kRiceStride + lane], kst[(w + 1) * kRiceStride + lane], pos);
+        };
+        auto vwin = [&](uint32_t pos) {
+          const uint32_t w = min(pos >> 5, 31u);
+          return __funnelshift_r(vst[w * kRiceStride + lane], vst[(w + 1) * kRiceStride + lane], pos);
+        };
+        // V first (into its row), then K into registers: the two decodes do
+        // not hold their outputs in registers at the same time
+        uint32_t pos = vo & 31u;
+        const rice::RiceK rv = rice::rice_k(vwin(pos) & 7u);
+        pos += rice::kKBits;
+        uint32_t um = rice::decode_codes_fast<RLAT, D>(vwin, pos, rv, [&](int q, uint32_t w) { vrow[q] = w; });
+        if (um > 31u || (pos >> 5) + 1u > 31u) decode_segment<RLAT>(a.vrs, a.vnw, vo, vrow);
+        pos = ko & 31u;
+        const rice::RiceK rk = rice::rice_k(kwin(pos) & 7u);
+        pos += rice::kKBits;
+        um = rice::decode_codes_fast<RLAT, D>(kwin, pos, rk, [&](int q, uint32_t w) { kcw[q] = w; });
+        if (um > 31u || (pos >> 5) + 1u > 31u) {
+          // this lane's staged K column is free now: the sequential reader's scratch
+          decode_segment<RLAT, kRiceStride>(a.krs, a.knw, ko, kst + lane);
+#pragma unroll
+          for (int q = 0; q < D / 4; ++q) kcw[q] = kst[q * kRiceStride + lane];
+        }
       } else {
 #pragma unroll
-        for (int e = 0; e < D / 4; ++e) krow[e] = vrow[e] = 0u;
+        for (int q = 0; q < D / 4; ++q) vrow[q] = 0u;
       }
       __syncwarp();
     }
     if (ok) {
       if constexpr (RLAT != 0) {
 #pragma unroll
-        for (int q = 0; q < D / 16; ++q) kw[q] = make_uint4(krow[4 * q], krow[4 * q + 1], krow[4 * q + 2], krow[4 * q + 3]);
+        for (int q = 0; q < D / 16; ++q) kw[q] = make_uint4(kcw[4 * q], kcw[4 * q + 1], kcw[4 * q + 2], kcw[4 * q + 3]);
       } else {
         const uint4* kp = reinterpret_cast<const uint4*>(a.kc + j * ld + (int64_t)kvh * D);
 #pragma unroll
@@ -172,9 +223,8 @@ __global__ void __launch_bounds__(kThreads, G <= 4 ? 4 : 2) attn_partial_kernel(
     }
     uint32_t vw[32];
     if constexpr (RLAT != 0) {
-      const uint32_t* vb = reinterpret_cast<const uint32_t*>(dv_smem) + (size_t)(kWarps + warp) * 32 * kRiceStride + lane;
 #pragma unroll
-      for (int t = 0; t < 32; ++t) vw[t] = vb[t * kRiceStride];
+      for (int t = 0; t < 32; ++t) vw[t] = vrows[t * kRiceStride + lane];
     } else {
       const uint32_t* vp = reinterpret_cast<const uint32_t*>(a.vc + c0 * ld + (int64_t)kvh * D) + lane;
 #pragma unroll

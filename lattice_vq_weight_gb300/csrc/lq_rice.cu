@@ -340,46 +340,6 @@ struct GemvRiceArgs {
 // stride (65 words) spreads the rows over the banks.
 constexpr int kRingWords = 65;
 
-// One 4-byte global -> shared copy in the background (`bytes` 4, or 0 to
-// write a zero without reading).
-__device__ __forceinline__ void cp_async4(uint32_t* dst, const uint32_t* src, uint32_t bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
-               "l"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// Four zigzag values (plus kone each) in bytes -> four codes 2 u + k in bytes:
-// per byte u2 = v ^ (0 - (v & 1)) is twice the signed value, ORed with the
-// block's parity bit (kp: 0x01010101 or 0).
-__device__ __forceinline__ uint32_t codes_from_zigzag4(uint32_t vb0, uint32_t vb1, uint32_t vb2, uint32_t vb3,
-                                                       uint32_t kk, uint32_t kp) {
-  const uint32_t vw = ((vb3 * 256u + vb2) * 65536u + (vb1 * 256u + vb0)) - kk;
-  const uint32_t m = (vw & 0x01010101u) * 0xFFu;
-  return (vw ^ m) | kp;
-}
-
-// The last code of an even-sum block (E8, D4) in byte 3 of `w`: the format
-// stores half of its halved value; the halved value is 2 * that + the parity
-// of the sum of the block's other halved values.  `w0` is the block's other
-// code word for E8 (zero for D4).  Bit 1 of a code is the parity of its halved
-// value, so the parity of the sum is bit 1 of the XOR of the other codes,
-// summed into bit 25 by one multiply.
-template <bool TWO_WORDS>
-__device__ __forceinline__ uint32_t fix_last_code(uint32_t w0, uint32_t w) {
-  const uint32_t t = TWO_WORDS ? ((w0 ^ w) & 0x02020202u) : (w & 0x00020202u);
-  const uint32_t p = t * 0x01010101u;                 // bit 25: parity (E8: XOR bit 1 of code 7 too)
-  const uint32_t a = w << 1;                          // code 7 doubled in byte 3 (bit 24: junk)
-  const uint32_t sel = (w & 0x01FFFFFFu) | (a & 0xFE000000u);
-  const uint32_t q = TWO_WORDS ? (p ^ w ^ a) : (p ^ a);  // bit 25: the sum parity, less what sel holds
-  return sel ^ (q & 0x02000000u);
-}
-
 // Items are (32-row group, tile) pairs; warp w takes [w I / W, (w+1) I / W).
 // Lane l decodes row 32 grp + l, 64 codes per step, into the shared-memory
 // slots of the int8-code GEMV's fragment layout (slot (2i + h) * 32 + 4 g + q
@@ -519,7 +479,7 @@ __global__ void __launch_bounds__(128, 4) gemv_rice_kernel(const GemvRiceArgs a)
       __syncwarp();
       landed = ic;
     }
-    uint32_t K = 0, kone = 1, kmask = 0, kk = 0x01010101u;
+    RiceK rk = rice_k(0);
     float acc[2][NB][4];
 #pragma unroll
     for (int i = 0; i < 2; ++i)
@@ -548,58 +508,21 @@ __global__ void __launch_bounds__(128, 4) gemv_rice_kernel(const GemvRiceArgs a)
 
       // ---- decode 64 codes of this lane's row
       const uint32_t posr0 = posr;
+      auto window = [&](uint32_t pos) {
+        const uint32_t* p = myring + ((pos >> 5) & 63u);
+        return __funnelshift_r(p[0], p[1], pos);
+      };
       if (st == 0) {   // the segment's K
-        const uint32_t* p = myring + ((posr >> 5) & 63u);
-        K = __funnelshift_r(p[0], p[1], posr) & 7u;
-        kone = 1u << K;
-        kmask = kone - 1u;
-        kk = kone * 0x01010101u;
+        rk = rice_k(window(posr) & 7u);
         posr += kKBits;
       }
       {
-        uint32_t vb[4];
-        uint32_t x = 0, pw = 0, umax = 0, kp = 0, prev = 0, half_lo = 0;
-#pragma unroll
-        for (int sy = 0; sy < 64; ++sy) {
-          const int i = sy % n;
-          if ((sy & 1) == 0) {
-            const uint32_t* p = myring + ((posr >> 5) & 63u);
-            x = __funnelshift_r(p[0], p[1], posr);
-            pw = posr;
-            if (Fmt<LAT>::parity && i == 0) {
-              // the block's parity bit in each of its code bytes (A2: two blocks per word)
-              if constexpr (n >= 4) {
-                kp = (x & 1u) * 0x01010101u;
-              } else {
-                const uint32_t kb = (x & 1u) * (0x0101u << (8 * (sy & 3)));
-                kp = (sy & 3) == 0 ? kb : (kp | kb);
-              }
-              x >>= 1;
-              posr += 1;
-            }
-          }
-          const uint32_t p1 = __popc(x ^ (x + 1u));          // run of ones + its closing zero
-          const uint32_t y1 = __funnelshift_rc(x, 0u, p1);   // x >> p1 (0 when p1 = 32)
-          vb[sy & 3] = p1 * kone + (y1 & kmask);             // zigzag value + kone
-          x = y1 >> K;
-          posr += p1 + K;
-          if ((sy & 1) == 1) umax = max(umax, posr - pw);
-          if ((sy & 3) == 3) {
-            uint32_t cword = codes_from_zigzag4(vb[0], vb[1], vb[2], vb[3], kk, kp);
-            if constexpr (LAT == LQ_E8) {
-              if ((sy & 7) == 7) cword = fix_last_code<true>(prev, cword);
-            } else if constexpr (LAT == LQ_D4) {
-              cword = fix_last_code<false>(0u, cword);
-            }
-            if ((sy & 7) == 3) {
-              half_lo = cword;
-            } else {
-              // columns 8 j .. 8 j + 7 (j = sy >> 3): 16-byte chunk j >> 1, half (j & 1) ^ dh
-              store_half(myslot, sy >> 3, half_lo, cword);
-            }
-            prev = cword;
-          }
-        }
+        uint32_t half_lo = 0;
+        // columns 8 j .. 8 j + 7 (code words 2 j, 2 j + 1): 16-byte chunk j >> 1, half (j & 1) ^ dh
+        const uint32_t umax = decode_codes_fast<LAT, 64>(window, posr, rk, [&](int q, uint32_t w) {
+          if ((q & 1) == 0) half_lo = w;
+          else store_half(myslot, q >> 1, half_lo, w);
+        });
         const uint32_t last_word = (posr >> 5) + s + 1u;   // highest stream word (from wb) the windows read
         const bool bad = row_ok && (umax > 31u || last_word >= (uint32_t)landed * 32u);
         if (!row_ok) {
@@ -610,16 +533,11 @@ __global__ void __launch_bounds__(128, 4) gemv_rice_kernel(const GemvRiceArgs a)
           // the sequential reader on the stream in global memory
           BitReader rd;
           rd.init(a.stream, a.nwords, (uint64_t)(wb + s) * 32u + posr0);
-          if (st == 0) {
-            K = rd.get(kKBits);
-            kone = 1u << K;
-            kmask = kone - 1u;
-            kk = kone * 0x01010101u;
-          }
+          if (st == 0) rk = rice_k(rd.get(kKBits));
 #pragma unroll 1
           for (int j = 0; j < 64 / n; ++j) {
             int c[n];
-            decode_block<LAT>(rd, (int)K, c);
+            decode_block<LAT>(rd, (int)rk.K, c);
 #pragma unroll
             for (int e = 0; e < n; ++e) {
               const int col = j * n + e;

@@ -1,6 +1,7 @@
-// Rice format of lattice codes: the format constants and the sequential
-// decoder, shared by the stream kernels (lq_rice.cu) and the decode attention
-// over a Rice-coded KV cache (lq_kv.cu).  Format: see include/lq.h.
+// Rice format of lattice codes: the format constants, the sequential decoder
+// and the two-symbol fast decoder, shared by the stream kernels (lq_rice.cu)
+// and the decode attention over a Rice-coded KV cache (lq_kv_kernel.cuh).
+// Format: see include/lq.h.
 // R. F. Rice, JPL Publication 79-22 (1979).
 #pragma once
 
@@ -119,6 +120,115 @@ __device__ __forceinline__ void decode_block(BitReader& rd, int K, int (&c)[Fmt<
   if constexpr (Fmt<LAT>::even_sum) u[n - 1] = 2 * u[n - 1] + (sum & 1);
 #pragma unroll
   for (int i = 0; i < n; ++i) c[i] = 2 * u[i] + k;
+}
+
+// One 4-byte global -> shared copy in the background (`bytes` 4, or 0 to
+// write a zero without reading).
+__device__ __forceinline__ void cp_async4(uint32_t* dst, const uint32_t* src, uint32_t bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------- fast decode
+// The Rice parameter of a segment and the constants the fast decoder derives
+// from it.
+struct RiceK {
+  uint32_t K, kone, kmask, kk;   // K, 2^K, 2^K - 1, 2^K in each byte
+};
+__device__ __forceinline__ RiceK rice_k(uint32_t K) {
+  RiceK r;
+  r.K = K;
+  r.kone = 1u << K;
+  r.kmask = r.kone - 1u;
+  r.kk = r.kone * 0x01010101u;
+  return r;
+}
+
+// Four zigzag values (plus kone each) in bytes -> four codes 2 u + k in bytes:
+// per byte u2 = v ^ (0 - (v & 1)) is twice the signed value, ORed with the
+// block's parity bit (kp: 0x01 in each byte of a block with odd codes).
+__device__ __forceinline__ uint32_t codes_from_zigzag4(uint32_t vb0, uint32_t vb1, uint32_t vb2, uint32_t vb3,
+                                                       uint32_t kk, uint32_t kp) {
+  const uint32_t vw = ((vb3 * 256u + vb2) * 65536u + (vb1 * 256u + vb0)) - kk;
+  const uint32_t m = (vw & 0x01010101u) * 0xFFu;
+  return (vw ^ m) | kp;
+}
+
+// The last code of an even-sum block (E8, D4) in byte 3 of `w`: the format
+// stores half of its halved value; the halved value is 2 * that + the parity
+// of the sum of the block's other halved values.  `w0` is the block's other
+// code word for E8 (zero for D4).  Bit 1 of a code is the parity of its halved
+// value, so the parity of the sum is bit 1 of the XOR of the other codes,
+// summed into bit 25 by one multiply.
+template <bool TWO_WORDS>
+__device__ __forceinline__ uint32_t fix_last_code(uint32_t w0, uint32_t w) {
+  const uint32_t t = TWO_WORDS ? ((w0 ^ w) & 0x02020202u) : (w & 0x00020202u);
+  const uint32_t p = t * 0x01010101u;                 // bit 25: parity (E8: XOR bit 1 of code 7 too)
+  const uint32_t a = w << 1;                          // code 7 doubled in byte 3 (bit 24: junk)
+  const uint32_t sel = (w & 0x01FFFFFFu) | (a & 0xFE000000u);
+  const uint32_t q = TWO_WORDS ? (p ^ w ^ a) : (p ^ a);  // bit 25: the sum parity, less what sel holds
+  return sel ^ (q & 0x02000000u);
+}
+
+// Fast decode of NCODES codes (whole blocks) starting at bit `pos` of a
+// segment, two Rice symbols per 32-bit window: a symbol's unary run and
+// closing zero are counted as the popcount of x ^ (x + 1), its K low bits
+// follow, and the window shifts on; four values are packed into one word and
+// un-zigzagged bytewise.  window(pos) returns the 32 stream bits from pos;
+// emit(q, w) receives code word q (codes 4 q .. 4 q + 3 as bytes).  Returns
+// the most bits one window gave: above 31 a pair (with a block's parity bit)
+// did not fit its window and the codes are invalid (the caller decodes again
+// with the sequential reader).
+template <int LAT, int NCODES, class Win, class Emit>
+__device__ __forceinline__ uint32_t decode_codes_fast(const Win& window, uint32_t& pos, const RiceK& rk,
+                                                      const Emit& emit) {
+  constexpr int n = Fmt<LAT>::n;
+  static_assert(NCODES % 8 == 0, "whole blocks, whole code words");
+  uint32_t vb[4];
+  uint32_t x = 0, pw = 0, umax = 0, kp = 0, prev = 0;
+#pragma unroll
+  for (int sy = 0; sy < NCODES; ++sy) {
+    const int i = sy % n;
+    if ((sy & 1) == 0) {
+      x = window(pos);
+      pw = pos;
+      if (Fmt<LAT>::parity && i == 0) {
+        // the block's parity bit in each of its code bytes (A2: two blocks per word)
+        if constexpr (n >= 4) {
+          kp = (x & 1u) * 0x01010101u;
+        } else {
+          const uint32_t kb = (x & 1u) * (0x0101u << (8 * (sy & 3)));
+          kp = (sy & 3) == 0 ? kb : (kp | kb);
+        }
+        x >>= 1;
+        pos += 1;
+      }
+    }
+    const uint32_t p1 = __popc(x ^ (x + 1u));          // run of ones + its closing zero
+    const uint32_t y1 = __funnelshift_rc(x, 0u, p1);   // x >> p1 (0 when p1 = 32)
+    vb[sy & 3] = p1 * rk.kone + (y1 & rk.kmask);       // zigzag value + kone
+    x = y1 >> rk.K;
+    pos += p1 + rk.K;
+    if ((sy & 1) == 1) umax = max(umax, pos - pw);
+    if ((sy & 3) == 3) {
+      uint32_t cword = codes_from_zigzag4(vb[0], vb[1], vb[2], vb[3], rk.kk, kp);
+      if constexpr (LAT == LQ_E8) {
+        if ((sy & 7) == 7) cword = fix_last_code<true>(prev, cword);
+      } else if constexpr (LAT == LQ_D4) {
+        cword = fix_last_code<false>(0u, cword);
+      }
+      emit(sy >> 2, cword);
+      prev = cword;
+    }
+  }
+  return umax;
 }
 
 }  // namespace rice

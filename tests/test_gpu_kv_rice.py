@@ -58,3 +58,40 @@ def test_attention_rice(lattice, tokens, kv_heads, group, fmt):
         # stream + 16-bit norms: about 4 bits per cached value, ~3.8x against bf16 on the pages
         bits = (kbits + vbits + 2 * 16 * tokens * kv_heads) / (2 * tokens * cols)
         assert 3.5 < 16.0 / bits < 4.5
+
+
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+def test_attention_rice_long_runs(lattice):
+    """Codes whose Rice segments have unary runs longer than the decoder's
+    32-bit window and segments longer than the 32 stream words each token
+    stages (every fourth token made only of large blocks): the attention from
+    the stream equals the attention from the same int8 codes."""
+    from tests.test_gpu_rice import _crafted_codes
+    torch, L = cuda()
+    tokens, kv_heads, group = 300, 2, 4
+    cols = kv_heads * 128
+    kc_np = _crafted_codes(lattice, tokens, cols, 950).astype(np.int8)
+    vc_np = _crafted_codes(lattice, tokens, cols, 951).astype(np.int8)
+    assert np.abs(kc_np.astype(np.int64)).max() >= 100
+    rng = np.random.default_rng(952)
+    ks = torch.from_numpy(rng.uniform(0.002, 0.004, (tokens, kv_heads)).astype(np.float32)).cuda()
+    vs = torch.from_numpy(rng.uniform(0.002, 0.004, (tokens, kv_heads)).astype(np.float32)).cuda()
+    kg = torch.from_numpy(O.splitmix64_signs(81, cols)).cuda()
+    vg = torch.from_numpy(O.splitmix64_signs(82, cols)).cuda()
+    kc, vc = torch.from_numpy(kc_np).cuda(), torch.from_numpy(vc_np).cuda()
+    kw, ko, _ = rice_cache(torch, L, lattice, kc)
+    vw, vo, _ = rice_cache(torch, L, lattice, vc)
+    q = to_dev_bf16(torch, gaussian_vectors(kv_heads * group, 128, 953, dtype="bf16"))
+    ws = torch.empty(L.lq_attention_workspace_size(tokens, kv_heads, kv_heads * group, 128), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty((kv_heads * group, 128), dtype=torch.float32, device="cuda")
+    L.lq_attention_decode_rice(lattice, kw, ko, ks, kg, vw, vo, vs, vg, "tile_f32", q, out, ws)
+    ref8 = torch.empty_like(out)
+    L.lq_attention_decode_ex(lattice, kc, ks, kg, vc, vs, vg, "tile_f32", q, ref8, ws)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert normwise_rel(got, ref8.cpu().numpy()) < 1e-6
+    ref = KV.attention_from_codes(q.float().cpu().numpy(), kc_np, ks.cpu().numpy(), kg.cpu().numpy(), vc_np,
+                                  vs.cpu().numpy(), vg.cpu().numpy(), kv_heads, 128, lattice)
+    assert normwise_rel(got, ref) < 2e-3
