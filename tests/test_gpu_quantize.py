@@ -117,6 +117,32 @@ def test_nonfinite_and_range_flags():
     assert st == 0
 
 
+@pytest.mark.parametrize("lattice", ["e8", "d4", "a2", "z1"])
+def test_large_values_take_the_checked_decoder(lattice):
+    """bf16 unit spikes at beta = 1/63 give |y| = 63 at every coordinate of their
+    tile: every lane leaves the packed fast decoders for the range-checked scalar
+    ones, the codes still fit int8 and equal the oracle's; at beta = 1/64 the
+    codes would be 128 and the range flag is raised."""
+    torch, L = cuda()
+    S = np.zeros((4, 512), dtype=np.float32)      # one spike per tile; row 3 stays zero
+    S[0, 3] = 1.0
+    S[1, 300] = -1.0
+    S[2, 17] = 1.0
+    S[2, 400] = 1.0
+    d = O.splitmix64_signs(0, 512)
+    codes, scales, signs, st = run_quantize(torch, L, S, "bf16", lattice, 256, 0, 1.0 / 63.0)
+    assert st == 0
+    q = O.quantize(S, lattice, 256, d, 1.0 / 63.0)
+    assert not q.range_error
+    assert np.abs(q.codes).max() >= 120
+    np.testing.assert_allclose(scales, q.scales, rtol=1e-6, atol=0)
+    # these tiles are exactly symmetric (every |y| equal), so A2 meets exact
+    # ties in many blocks: each differing block must be a certified tie
+    compare_codes(codes, q, lattice, max_fraction=1.0)
+    _, _, _, st = run_quantize(torch, L, S, "bf16", lattice, 256, 0, 1.0 / 64.0)
+    assert st & L.LQ_DEV_RANGE
+
+
 def test_empty_rows_is_noop():
     torch, L = cuda()
     W = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
