@@ -289,6 +289,7 @@ lq_status quantize_group(int lattice, int n, const void* const* W, int wdtype, c
       return LQ_ERR_CUDA;
     QuantMat& M = a.mat[k++];
     M.codes = codes[m]; M.scales = scales[m]; M.signs = signs[m];
+    M.W = W[m]; M.ldw = ldw[m];
     M.rows = rows[m]; M.cols = cols[m];
     M.tiles_per_row = (int)(cols[m] / tile);
     M.chunks_per_row = (int)((cols[m] + kChunkCols - 1) / kChunkCols);

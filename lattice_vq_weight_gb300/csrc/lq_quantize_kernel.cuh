@@ -53,6 +53,8 @@ struct QuantMat {
   int8_t* codes;
   void* scales;             // in the launch's scale format
   const int8_t* signs;
+  const void* W;            // the input (read by the fix-up of deferred tiles)
+  int64_t ldw;              // its row stride in elements
   int64_t rows, cols;
   int64_t cta_begin, row_groups;
   int tiles_per_row, chunks_per_row;
@@ -184,9 +186,9 @@ __device__ __forceinline__ uint2 decode_block8(const float2 (&y4)[4], bool& r) {
 
 // The scalar decoders with the exact int8 range check over a lane's 64
 // values (blocks regrouped as consecutive 8-coordinate pairs), out of line: for
-// E8 and Z1 it only runs for a lane holding a value of 62.5 or more (an outlier
-// that survived the transform), so its registers are kept out of the fast
-// path's allocation.
+// E8 and Z1 with 16-bit scales or the dither it only runs for a lane holding a
+// value of 62.5 or more (an outlier that survived the transform), so its
+// registers are kept out of the fast path's allocation.
 template <int LAT, int EX>
 __device__ __noinline__ void decode_lane_checked(const float2 (&p)[32], float k, int lane, int8_t* dst, bool active,
                                                  bool& r) {
@@ -201,6 +203,75 @@ __device__ __noinline__ void decode_lane_checked(const float2 (&p)[32], float k,
                             make_float2(y[6], y[7])};
       const uint2 w = decode_block8<LAT, true>(y4, r);
       if (active) *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, h)) = w;
+    }
+  }
+}
+
+// Instantiations that defer the tiles their packed decoders cannot take (a
+// value of 62.5 or more in a lane) to fix_deferred at the end of the warp's
+// unit: E8 and Z1 with float32 tile scales and no dither.
+template <int LAT, int SF, bool DITHER>
+constexpr bool kDeferTiles = (LAT == LQ_E8 || LAT == LQ_Z1) && SF == LQ_SCALE_TILE_F32 && !DITHER;
+
+__device__ __forceinline__ bool tile_lane_any(bool v, int lanes_per_tile) {
+  uint32_t x = v ? 1u : 0u;
+  for (int m = 1; m < lanes_per_tile; m <<= 1) x |= __shfl_xor_sync(0xffffffffu, x, m);
+  return x != 0u;
+}
+
+// One deferred tile (row, t) of matrix M again from its input (an L2 hit: the
+// unit was just copied in): signs, the Walsh-Hadamard transform (E columns per
+// lane over T / E lanes), the scale and the range-checked scalar decoders.
+template <int LAT, bool BF16, int E>
+__device__ __forceinline__ void fix_tile(const QuantArgs& a, const QuantMat& M, int64_t row, int t, int lane,
+                                         bool& range) {
+  const int lpt = a.tile / E;
+  const bool act = lane < lpt;
+  const int64_t col0 = (int64_t)t * a.tile + (int64_t)lane * E;
+  float v[E];
+  if (act) {
+    if constexpr (BF16) load_bf16_signed<E>(reinterpret_cast<const __nv_bfloat16*>(M.W) + row * M.ldw + col0,
+                                            M.signs + col0, v);
+    else load_f32_signed<E>(reinterpret_cast<const float*>(M.W) + row * M.ldw + col0, M.signs + col0, v);
+  } else {
+#pragma unroll
+    for (int c = 0; c < E; ++c) v[c] = 0.f;
+  }
+  fwht_tile<E>(v, lpt, lane);
+  float u2 = 0.f;
+#pragma unroll
+  for (int c = 0; c < E; ++c) u2 = fmaf(v[c], v[c], u2);
+  for (int o = 16; o; o >>= 1) u2 += __shfl_xor_sync(0xffffffffu, u2, o);
+  const bool finite = isfinite(u2);
+  float s = finite ? a.beta * sqrtf(u2) * a.inv_tile : 0.f;
+  const float k = (s > 0.f) ? 1.0f / (s * a.sqrt_tile) : 0.f;
+  bool r = false;
+#pragma unroll
+  for (int b = 0; b < E / 8; ++b) {
+    float2 y4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y4[i] = make_float2(v[8 * b + 2 * i] * k, v[8 * b + 2 * i + 1] * k);
+    const uint2 w = finite ? decode_block8<LAT, true>(y4, r) : make_uint2(0u, 0u);
+    if (act) *reinterpret_cast<uint2*>(M.codes + row * M.cols + col0 + 8 * b) = w;
+  }
+  if (lane == 0) reinterpret_cast<float*>(M.scales)[row * M.tiles_per_row + t] = s;
+  range |= r;
+}
+
+// The deferred tiles of a warp's unit (row, chunk): bit l of dm is set for the
+// first lane l of each.
+template <int LAT, bool BF16, bool XL>
+__device__ __forceinline__ void fix_deferred(const QuantArgs& a, const QuantMat& M, int64_t row, int chunk,
+                                             unsigned dm, int lane, bool& range) {
+  const int E = XL ? act_elems_for_tile(a.tile) : 16;
+  while (dm != 0u) {
+    const int src = __ffs((int)dm) - 1;
+    dm &= dm - 1u;
+    const int t = (int)(((int64_t)chunk * kChunkCols + (int64_t)src * kLaneElems) >> a.tile_shift);
+    if (E == 16) fix_tile<LAT, BF16, 16>(a, M, row, t, lane, range);
+    else if constexpr (XL) {
+      if (E == 32) fix_tile<LAT, BF16, 32>(a, M, row, t, lane, range);
+      else fix_tile<LAT, BF16, 64>(a, M, row, t, lane, range);
     }
   }
 }
@@ -445,6 +516,15 @@ __global__ void __launch_bounds__(kQuantThreads, (BF16 && !XL) ? 4 : 3)
       }
       const float2 k2 = make_float2(k, k);
       bool r = false;
+      // Deferred tiles (float32 scales, no dither): a tile with a lane that
+      // cannot use the packed decoders gets no codes here; fix_deferred redoes
+      // it after the unit, from the input, with the range-checked decoders.
+      // Called there, with the unit's registers dead, that decoder costs the
+      // fast path nothing (inline in the decode it cost about 6 %).
+      bool tile_deferred = false;
+      if constexpr (kDeferTiles<LAT, SF, DITHER>) {
+        if (__any_sync(0xffffffffu, !small)) tile_deferred = tile_lane_any(!small, a.lanes_per_tile);
+      }
       if constexpr (LAT == LQ_E8 || LAT == LQ_Z1) {
         if (small) {
 #pragma unroll
@@ -459,7 +539,7 @@ __global__ void __launch_bounds__(kQuantThreads, (BF16 && !XL) ? 4 : 3)
               *reinterpret_cast<uint2*>(dst + block_col<EX>(lane, g, 1)) = cQ;
             }
           }
-        } else {
+        } else if constexpr (!kDeferTiles<LAT, SF, DITHER>) {
           float2 pc[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) pc[j] = p[j];
@@ -490,9 +570,16 @@ __global__ void __launch_bounds__(kQuantThreads, (BF16 && !XL) ? 4 : 3)
         nonfinite |= !finite;
         if ((lane & (a.lanes_per_tile - 1)) == 0) {
           const int64_t si = cur.row * M.tiles_per_row + (col0 >> a.tile_shift);
-          if constexpr (SF == LQ_SCALE_TILE_F32) reinterpret_cast<float*>(M.scales)[si] = s;
+          if constexpr (SF == LQ_SCALE_TILE_F32) {
+            if (!tile_deferred) reinterpret_cast<float*>(M.scales)[si] = s;
+          }
           if constexpr (SF == LQ_SCALE_TILE_F16) reinterpret_cast<__half*>(M.scales)[si] = s16;
         }
+      }
+      if constexpr (kDeferTiles<LAT, SF, DITHER>) {
+        const unsigned dm =
+            __ballot_sync(0xffffffffu, tile_deferred && active && (lane & (a.lanes_per_tile - 1)) == 0);
+        if (dm != 0u) fix_deferred<LAT, BF16, XL>(a, M, cur.row, cur.chunk, dm, lane, range);
       }
     }
     cur = nxt;
@@ -554,9 +641,12 @@ inline lq_status launch_quantize_ex(QuantArgs& a, cudaStream_t st) {
 
 template <int LAT, bool BF16, int SF, bool DITHER = false>
 inline lq_status launch_quantize_walk(QuantArgs& a, cudaStream_t st) {
-  if (a.lanes_per_tile == 2) return launch_quantize_ex<LAT, BF16, 1, false, SF, DITHER>(a, st);
-  if (a.lanes_per_tile == 4) return launch_quantize_ex<LAT, BF16, 2, false, SF, DITHER>(a, st);
-  return launch_quantize_ex<LAT, BF16, 2, true, SF, DITHER>(a, st);
+  lq_status r;
+  if (a.lanes_per_tile == 2) r = launch_quantize_ex<LAT, BF16, 1, false, SF, DITHER>(a, st);
+  else if (a.lanes_per_tile == 4) r = launch_quantize_ex<LAT, BF16, 2, false, SF, DITHER>(a, st);
+  else r = launch_quantize_ex<LAT, BF16, 2, true, SF, DITHER>(a, st);
+
+  return r;
 }
 
 // Launch with a 16-bit scale format (LQ_SCALE_ROW_BF16 or LQ_SCALE_TILE_F16),

@@ -143,6 +143,45 @@ def test_large_values_take_the_checked_decoder(lattice):
     assert st & L.LQ_DEV_RANGE
 
 
+@pytest.mark.parametrize("lattice", ["e8", "z1", "d4"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("tile", [128, 1024, 2048])
+def test_large_value_tiles_among_zero_tiles_grouped(lattice, dtype, tile):
+    """Single spikes of assorted sizes at beta = 1/63 (|y| = 63 over their tile)
+    scattered among all-zero tiles of three matrices in one grouped launch, one
+    with a padded row stride: the spike tiles go through the range-checked
+    decoders, the zero tiles do not, and every matrix equals the oracle with no
+    range flag."""
+    torch, L = cuda()
+    rng = np.random.default_rng(tile)
+    shapes = [(9, 3 * tile), (3, 2048 + 2 * tile), (17, 4 * tile)]
+    seeds = [5, 6, 7]
+    beta = 1.0 / 63.0
+    Ws, Wn = [], []
+    for i, (r, c) in enumerate(shapes):
+        W = np.zeros((r, c), dtype=np.float32)
+        nt = c // tile
+        for row in range(r):
+            for t in range(nt):
+                if rng.random() < 0.4:
+                    W[row, t * tile + rng.integers(tile)] = rng.choice([1.0, -1.0, 3.0, -0.5, 96.0])
+        pad = 16 if i == 1 else 0
+        full = np.zeros((r, c + pad), dtype=np.float32)
+        full[:, :c] = W
+        Wd = to_dev_bf16(torch, full) if dtype == "bf16" else to_dev(torch, full)
+        Ws.append(Wd[:, :c])
+        Wn.append(W)
+    codes, scales, signs, st = _grouped(torch, L, Ws, tile, seeds, beta, lattice)
+    assert st == 0
+    for m, W in enumerate(Wn):
+        d = O.splitmix64_signs(seeds[m], W.shape[1])
+        q = O.quantize(W, lattice, tile, d, beta)
+        assert not q.range_error
+        np.testing.assert_allclose(scales[m].cpu().numpy(), q.scales, rtol=1e-6, atol=0)
+        compare_codes(codes[m].cpu().numpy(), q, lattice, max_fraction=1.0)
+        assert np.abs(codes[m].cpu().numpy()).max() >= 120
+
+
 def test_empty_rows_is_noop():
     torch, L = cuda()
     W = torch.empty((0, 512), dtype=torch.bfloat16, device="cuda")
