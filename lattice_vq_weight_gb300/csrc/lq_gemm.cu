@@ -256,6 +256,10 @@ gemm_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // launched as a programmatic dependent of the prep kernel: everything but
+  // the code stream (written before the prep kernel started) waits for its
+  // X~, factors and zeroed Y; the code producer fills its ring meanwhile
+  if (warp != 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // unit u -> (n tile, m tile, K split) and its K-stage range
   auto unit_range = [&](int64_t u, int& nt, int& mt, int& k0, int& k1) {
@@ -536,6 +540,8 @@ template <int E>
 __global__ void __launch_bounds__(kPrepThreads) gemm_prep_kernel(PrepArgs a) {
   __shared__ float red[kPrepWarps];
   __shared__ float row_g;
+  // the GEMM may be scheduled now (it waits for this grid's results)
+  asm volatile("griddepcontrol.launch_dependents;");
   if (blockIdx.x >= a.M) {
     const int64_t n = (int64_t)(blockIdx.x - a.M) * kPrepWarps + (threadIdx.x >> 5);
     const int ln = threadIdx.x & 31;
@@ -818,16 +824,26 @@ lq_status gemm_fmt(int lattice, const int8_t* codes_dev, const void* scales_dev,
     attr_set = true;
   }
   const int64_t grid = a.units < sms ? a.units : sms;
-  if (self_test)
-    gemm_kernel<LQ_SCALE_TILE_F32, true><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
-  else if (sfmt == LQ_SCALE_ROW_BF16)
-    gemm_kernel<LQ_SCALE_ROW_BF16><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
-  else if (sfmt == LQ_SCALE_TILE_F16)
-    gemm_kernel<LQ_SCALE_TILE_F16><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
-  else
-    gemm_kernel<LQ_SCALE_TILE_F32><<<(unsigned)grid, kThreads, smem, s>>>(map_codes, map_x, a);
-  st = check_launch();
-  if (st != LQ_OK || !via_acc) return st;
+  // programmatic dependent launch behind the prep kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  auto kern = self_test                       ? gemm_kernel<LQ_SCALE_TILE_F32, true>
+              : (sfmt == LQ_SCALE_ROW_BF16) ? gemm_kernel<LQ_SCALE_ROW_BF16>
+              : (sfmt == LQ_SCALE_TILE_F16) ? gemm_kernel<LQ_SCALE_TILE_F16>
+                                            : gemm_kernel<LQ_SCALE_TILE_F32>;
+  if (cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, a) != cudaSuccess) {
+    cudaGetLastError();
+    return LQ_ERR_CUDA;
+  }
+  if (!via_acc) return LQ_OK;
   const int64_t n_out = M * N;
   const int64_t cvt_blocks = std::min<int64_t>((n_out / 4 + 255) / 256 + 1, (int64_t)sms * 8);
   gemm_to_bf16_kernel<<<(unsigned)cvt_blocks, 256, 0, s>>>(a.Y32, reinterpret_cast<__nv_bfloat16*>(Y_dev), n_out);
