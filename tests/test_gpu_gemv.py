@@ -152,3 +152,39 @@ def test_grouped_gemv_matches_single_calls():
     torch.cuda.synchronize()
     for y, y1 in zip(ys, singles):
         assert normwise_rel(y.cpu().numpy(), y1.cpu().numpy()) < 1e-6
+
+
+@pytest.mark.parametrize("batch", [1, 5, 16])
+def test_chained_calls_read_the_previous_results(batch):
+    """Back-to-back calls on one stream, no synchronisation between them: the
+    weights of the second product are quantized right before it, and its
+    activation is the first product's output (fp32).  The activation rotation
+    of each call waits for the grid before it, so the second product sees the
+    finished y1 and codes; checked over repeated chains against the float64
+    oracle on the codes and y1 the GPU produced."""
+    torch, L = cuda()
+    tile = 256
+    WA = gaussian_matrix(1024, 2048, 0.02, 61, dtype="bf16")
+    dA = O.splitmix64_signs(61, 2048)
+    qA = O.quantize(WA, "e8", tile, dA, 0.25)
+    cA, sA, gA = to_dev(torch, qA.codes), to_dev(torch, qA.scales), to_dev(torch, dA)
+    WB = to_dev_bf16(torch, gaussian_matrix(768, 1024, 0.02, 62, dtype="bf16"))
+    x0 = gaussian_vectors(batch, 2048, 63, dtype="bf16")
+    x0d = to_dev_bf16(torch, x0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    runs = []
+    for it in range(6):
+        y1 = L.gemv(cA, sA, gA, x0d, lattice="e8", tile=tile, dev_status=status)
+        cB, sB, gB = L.quantize(WB, lattice="e8", tile=tile, seed=64 + it, beta=0.25, dev_status=status)
+        y2 = L.gemv(cB, sB, gB, y1, lattice="e8", tile=tile, dev_status=status)
+        runs.append((y1, cB, sB, gB, y2))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref1 = O.gemv(qA.codes, qA.scales, dA, tile, "e8", x0)
+    for it, (y1, cB, sB, gB, y2) in enumerate(runs):
+        y1h = y1.cpu().numpy()
+        assert normwise_rel(y1h, ref1) < TOL
+        np.testing.assert_array_equal(gB.cpu().numpy(), O.splitmix64_signs(64 + it, 1024))
+        ref2 = O.gemv(cB.cpu().numpy(), sB.cpu().numpy(), gB.cpu().numpy(), tile, "e8", y1h)
+        rel = normwise_rel(y2.cpu().numpy(), ref2)
+        assert rel < TOL, (it, rel)
