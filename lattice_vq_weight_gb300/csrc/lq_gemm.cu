@@ -29,6 +29,9 @@
 //   tile overlaps the main loop of the next.  Every mbarrier wait is bounded
 //   (about a second of clock cycles); on expiry the kernel records
 //   LQ_DEV_TIMEOUT and winds down.
+// The GEMM is a programmatic dependent launch of the prep kernel: its
+// prologue and the code producer run while the prep finishes, every other
+// warp waits for the prep's results first.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>

@@ -23,6 +23,9 @@
 // Both kernels take a group of up to kGemvMaxMats matrices that share the
 // activation x (for example the q, k and v projections of a layer), each with
 // its own signs, scales and output: one launch pair serves the whole group.
+// Both are programmatic dependent launches: the rotation waits for the grid
+// before it (whose output x may be), the GEMV prefetches codes during the
+// rotation and waits for x~ before reading it.
 #include <mutex>
 
 #include <cuda.h>
