@@ -22,6 +22,12 @@
  *   never allocates, frees or retains them.  Device pointers must be 16-byte
  *   aligned.  `stream` is a cudaStream_t passed as void* (NULL = legacy
  *   default stream).  Every call only enqueues work on `stream` and returns.
+ *   That work is stream-ordered: it reads its inputs after everything
+ *   enqueued before it has finished, and what follows it sees its results.
+ *   Within a call, and from one product call to the next, kernels are
+ *   programmatic dependent launches: a kernel may be scheduled while the one
+ *   before it ends, and waits for that grid before it touches data the
+ *   earlier work may write.
  * - Argument errors are returned synchronously, before anything is launched.
  *   Data-dependent problems (non-finite input, a code outside int8, a wait
  *   that gave up) are OR-ed as LQ_DEV_* bits into the caller's int32 status
