@@ -19,7 +19,12 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "liblq.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ("lq_api.cu", "lq_quantize.cu", "lq_quantize_fmt.cu", "lq_quantize_dither.cu", "lq_gemv.cu", "lq_gemm.cu", "lq_rice.cu", "lq_calib.cu", "lq_kv.cu", "lq_kv_dither.cu", "lq_kv_rice.cu")
+SOURCES = ("lq_api.cu", "lq_quantize.cu", "lq_quantize_fmt.cu", "lq_quantize_dither.cu", "lq_gemv.cu", "lq_gemm.cu",
+           "lq_rice.cu", "lq_calib.cu", "lq_kv.cu", "lq_kv_dither.cu", "lq_kv_rice.cu")
+# Objects: one per source, except lq_kv_rice.cu, compiled once per (lattice,
+# norm format) pair so that its slow instantiations build in parallel.
+UNITS = tuple((s, s.replace(".cu", ".o"), ()) for s in SOURCES if s != "lq_kv_rice.cu") + tuple(
+    ("lq_kv_rice.cu", f"lq_kv_rice_{p}.o", (f"-DLQ_KV_RICE_PART={p}",)) for p in range(8))
 
 
 def nvcc_path() -> str:
@@ -59,12 +64,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     nvcc = nvcc_path()
     os.makedirs(BUILD_DIR, exist_ok=True)
     objs = []
-    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+    # the slowest units first, so that they start before the pool fills
+    order = sorted(UNITS, key=lambda u: (u[0] != "lq_kv_rice.cu", u[1]))
+    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
         futs = {}
-        for s in SOURCES:
-            obj = os.path.join(BUILD_DIR, s.replace(".cu", ".o"))
+        for s, o, defs in order:
+            obj = os.path.join(BUILD_DIR, o)
             objs.append(obj)
-            futs[ex.submit(_compile, nvcc, os.path.join(CSRC, s), obj, list(extra_flags))] = s
+            futs[ex.submit(_compile, nvcc, os.path.join(CSRC, s), obj, list(defs) + list(extra_flags))] = o
         for f in cf.as_completed(futs):
             log = f.result()
             if verbose and log:

@@ -138,6 +138,21 @@ __global__ void __launch_bounds__(256) rotate_blocks_kernel(RotArgs a) {
   }
 }
 
+// The Rice-coded caches' partial attention of one lattice and norm format
+// (the instantiations live in the objects built from lq_kv_rice.cu).
+lq_status launch_partial_rice(const AttnArgs& a, int lattice, int group, bool h, unsigned grid, cudaStream_t s) {
+  switch (lattice) {
+    case LQ_E8: return h ? launch_partial_rice_lh<LQ_E8, true>(a, group, grid, s)
+                         : launch_partial_rice_lh<LQ_E8, false>(a, group, grid, s);
+    case LQ_D4: return h ? launch_partial_rice_lh<LQ_D4, true>(a, group, grid, s)
+                         : launch_partial_rice_lh<LQ_D4, false>(a, group, grid, s);
+    case LQ_A2: return h ? launch_partial_rice_lh<LQ_A2, true>(a, group, grid, s)
+                         : launch_partial_rice_lh<LQ_A2, false>(a, group, grid, s);
+    default:    return h ? launch_partial_rice_lh<LQ_Z1, true>(a, group, grid, s)
+                         : launch_partial_rice_lh<LQ_Z1, false>(a, group, grid, s);
+  }
+}
+
 }  // namespace kv
 }  // namespace lq
 

@@ -376,9 +376,14 @@ lq_status launch_partial_groups(const AttnArgs& a, int group, bool h, unsigned g
   }
 }
 
-// The dithered (lq_kv_dither.cu) and Rice-coded (lq_kv_rice.cu) variants, each
-// instantiated in its own translation unit.
+// The dithered (lq_kv_dither.cu) and Rice-coded (lq_kv_rice.cu) variants,
+// instantiated in translation units of their own.
 lq_status launch_partial_dithered(const AttnArgs& a, int lattice, int group, bool h, unsigned grid, cudaStream_t s);
+// Rice-coded caches of lattice RLAT with fp16 (H) or fp32 norms: explicitly
+// instantiated in lq_kv_rice.cu, which is compiled once per (lattice, norm
+// format) pair; launch_partial_rice (lq_kv.cu) picks the instantiation.
+template <int RLAT, bool H>
+lq_status launch_partial_rice_lh(const AttnArgs& a, int group, unsigned grid, cudaStream_t s);
 lq_status launch_partial_rice(const AttnArgs& a, int lattice, int group, bool h, unsigned grid, cudaStream_t s);
 
 }  // namespace kv
