@@ -145,7 +145,7 @@ def test_large_values_take_the_checked_decoder(lattice):
 
 @pytest.mark.parametrize("lattice", ["e8", "z1", "d4"])
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
-@pytest.mark.parametrize("tile", [128, 1024, 2048])
+@pytest.mark.parametrize("tile", [128, 512, 1024, 2048])
 def test_large_value_tiles_among_zero_tiles_grouped(lattice, dtype, tile):
     """Single spikes of assorted sizes at beta = 1/63 (|y| = 63 over their tile)
     scattered among all-zero tiles of three matrices in one grouped launch, one
